@@ -1,0 +1,70 @@
+// Device binding, SM count and the library's own device status word.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "dt_internal.h"
+
+namespace dt {
+
+// Status word for calls made with d_status == NULL (static device memory:
+// nothing is allocated at run time).
+__device__ int32_t g_dt_status_word;
+
+dt_status bind_device_of(const void* device_ptr) {
+  if (!device_ptr) return DT_OK;
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, device_ptr);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DT_ERR_CUDA, "cudaPointerGetAttributes: %s", cudaGetErrorString(e));
+  }
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+    return fail(DT_ERR_INVALID_ARG, "operand is not device memory");
+  int cur = -1;
+  cudaGetDevice(&cur);
+  if (cur != attr.device) {
+    e = cudaSetDevice(attr.device);
+    if (e != cudaSuccess) return fail(DT_ERR_CUDA, "cudaSetDevice: %s", cudaGetErrorString(e));
+  }
+  return DT_OK;
+}
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
+}
+
+int32_t* device_status_word(int32_t* user) {
+  if (user) return user;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_dt_status_word) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return static_cast<int32_t*>(p);
+}
+
+}  // namespace dt
+
+using namespace dt;
+
+extern "C" dt_status dt_read_device_status(int32_t* bits, int32_t clear) {
+  if (!bits) return fail(DT_ERR_INVALID_ARG, "bits is NULL");
+  cudaError_t e = cudaMemcpyFromSymbol(bits, g_dt_status_word, sizeof(int32_t));
+  if (e != cudaSuccess) return fail(DT_ERR_CUDA, "reading the status word: %s", cudaGetErrorString(e));
+  if (clear) {
+    int32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_dt_status_word, &zero, sizeof(int32_t));
+    if (e != cudaSuccess) return fail(DT_ERR_CUDA, "clearing the status word: %s", cudaGetErrorString(e));
+  }
+  return DT_OK;
+}

@@ -1,0 +1,393 @@
+// Lowering of batched GEMM groups to a launch: TMA descriptors (cached on
+// the host), tile counts, and the choice between the tcgen05 kernel and the
+// CUDA-core kernel (fp32 operands, or bf16 operands whose pitches TMA
+// cannot describe).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "gemm_plan.h"
+#include "gemm_sm103.cuh"
+
+namespace dt {
+namespace gemm {
+namespace {
+
+// ------------------------------------------------------------ TMA descriptors
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+struct MapKey {
+  uintptr_t ptr;
+  int64_t rows, cols, ld;
+  int32_t box_rows;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && rows == o.rows && cols == o.cols && ld == o.ld && box_rows == o.box_rows;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    size_t h = std::hash<uintptr_t>()(k.ptr);
+    h ^= std::hash<int64_t>()(k.rows) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+    h ^= std::hash<int64_t>()(k.cols) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+    h ^= std::hash<int64_t>()(k.ld) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+    h ^= std::hash<int32_t>()(k.box_rows) + (h << 6);
+    return h;
+  }
+};
+
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
+// 2-D bf16 map over a row-major [rows, cols] matrix with pitch ld elements:
+// box of 64 columns (128 bytes, the swizzle width) by box_rows rows, 128-byte
+// swizzle, zero fill outside the matrix.
+dt_status encode_map(const Mat& m, int box_rows, CUtensorMap* out) {
+  MapKey key{reinterpret_cast<uintptr_t>(m.ptr), m.rows, m.cols, m.ld, box_rows};
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    auto it = g_maps.find(key);
+    if (it != g_maps.end()) {
+      *out = it->second;
+      return DT_OK;
+    }
+  }
+  auto fn = encode_fn();
+  if (!fn) return fail(DT_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  CUtensorMap map;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(m.cols), static_cast<cuuint64_t>(m.rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(m.ld) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, m.ptr, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DT_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    if (g_maps.size() > 8192) g_maps.clear();
+    g_maps.emplace(key, map);
+  }
+  *out = map;
+  return DT_OK;
+}
+
+bool tma_ok(const Mat& m) {
+  return m.dtype == DT_BF16 && m.rows > 0 && m.cols > 0 && (reinterpret_cast<uintptr_t>(m.ptr) % 16) == 0 &&
+         (m.ld * 2) % 16 == 0 && m.ld >= m.cols && m.rows < (1ll << 31) && m.cols < (1ll << 31);
+}
+
+// ------------------------------------------------------------ CUDA-core kernel
+
+constexpr int S_TILE = 64, S_BK = 16, S_THREADS = 256;
+
+struct SSeg {
+  const char* a;
+  const char* b;
+  int64_t lda, ldb;
+  int32_t k, dtype;
+};
+
+struct SGroup {
+  int64_t m, n;
+  int32_t seg_begin, seg_count, m_tiles, n_tiles, tile_begin, out_dtype, nout, bias_dtype;
+  const void* bias;
+  int64_t row_begin[MAX_OUT + 1];
+  char* out_ptr[MAX_OUT];
+  int64_t out_ld[MAX_OUT];
+};
+
+struct SParams {
+  SSeg segs[MAX_SEGS];
+  SGroup groups[MAX_GROUPS];
+  int32_t ngroups, total_tiles;
+};
+
+__device__ __forceinline__ float load_elem(const char* base, int64_t idx, int dtype) {
+  if (dtype == DT_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx]);
+  return reinterpret_cast<const float*>(base)[idx];
+}
+
+// 64 x 64 output tile per block, 4 x 4 per thread; each output sums its
+// segments in order, k ascending, with fp32 fused multiply-adds.
+__global__ void __launch_bounds__(S_THREADS) simt_gemm_kernel(const __grid_constant__ SParams p) {
+  __shared__ float As[S_BK][S_TILE + 4];
+  __shared__ float Bs[S_BK][S_TILE + 4];
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+    int g = 0;
+    while (g + 1 < p.ngroups && p.groups[g + 1].tile_begin <= t) ++g;
+    const SGroup& G = p.groups[g];
+    const int local = t - G.tile_begin;
+    const int64_t m0 = (int64_t)(local / G.n_tiles) * S_TILE;
+    const int64_t n0 = (int64_t)(local % G.n_tiles) * S_TILE;
+    float acc[4][4] = {};
+    for (int si = G.seg_begin; si < G.seg_begin + G.seg_count; ++si) {
+      const SSeg& S = p.segs[si];
+      for (int k0 = 0; k0 < S.k; k0 += S_BK) {
+        for (int e = threadIdx.x; e < S_TILE * S_BK; e += S_THREADS) {
+          const int kk = e % S_BK, rr = e / S_BK;
+          const int64_t row = m0 + rr, k = k0 + kk;
+          As[kk][rr] = (row < G.m && k < S.k) ? load_elem(S.a, row * S.lda + k, S.dtype) : 0.f;
+          const int cc = e % S_TILE, kb = e / S_TILE;
+          const int64_t col = n0 + cc, kr = k0 + kb;
+          Bs[kb][cc] = (col < G.n && kr < S.k) ? load_elem(S.b, kr * S.ldb + col, S.dtype) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < S_BK; ++kk) {
+          float a[4], b[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t r = m0 + ty * 4 + i;
+      if (r >= G.m) continue;
+      int j = 0;
+      while (j + 1 < G.nout && G.row_begin[j + 1] <= r) ++j;
+      const int esize = G.out_dtype == DT_BF16 ? 2 : 4;
+      char* row_ptr = G.out_ptr[j] + (r - G.row_begin[j]) * G.out_ld[j] * esize;
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int64_t c = n0 + tx * 4 + jj;
+        if (c >= G.n) continue;
+        float v = acc[i][jj];
+        if (G.bias_dtype >= 0) v += load_elem(static_cast<const char*>(G.bias), c, G.bias_dtype);
+        if (G.out_dtype == DT_BF16) reinterpret_cast<__nv_bfloat16*>(row_ptr)[c] = __float2bfloat16_rn(v);
+        else reinterpret_cast<float*>(row_ptr)[c] = v;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------ lowering
+
+bool out_vec_ok(const HostGroup& g) {
+  const int esize = g.out_dtype == DT_BF16 ? 2 : 4;
+  for (size_t j = 0; j < g.out_ptr.size(); ++j) {
+    if (reinterpret_cast<uintptr_t>(g.out_ptr[j]) % 16) return false;
+    if ((g.out_ld[j] * esize) % 16) return false;
+  }
+  return true;
+}
+
+// Tile width choice: fewer, wider tiles unless the last wave of 256-wide
+// tiles leaves enough SMs idle that 128-wide tiles finish sooner.
+int choose_bn(const std::vector<HostGroup>& groups, size_t g0, size_t g1, int sms) {
+  double best_cost = 1e300;
+  int best = 256;
+  for (int bn : {256, 128}) {
+    int64_t tiles = 0;
+    for (size_t i = g0; i < g1; ++i) {
+      if (groups[i].dual) return 128;
+      tiles += ((groups[i].m + BM - 1) / BM) * ((groups[i].n + bn - 1) / bn);
+    }
+    const int64_t waves = (tiles + sms - 1) / sms;
+    const double cost = (double)waves * bn * (bn == 128 ? 1.12 : 1.0);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStream_t stream) {
+  static thread_local Params p;
+  const int sms = device_sm_count();
+  size_t gi = 0;
+  while (gi < groups.size()) {
+    // pack as many groups as fit one parameter block
+    size_t g_end = gi;
+    int nmaps = 0, nsegs = 0;
+    while (g_end < groups.size()) {
+      const HostGroup& G = groups[g_end];
+      const int need_segs = (int)G.segs.size();
+      const int need_maps = need_segs * (G.dual ? 3 : 2);
+      if ((int)(g_end - gi) + 1 > MAX_GROUPS || nsegs + need_segs > MAX_SEGS || nmaps + need_maps > MAX_MAPS) break;
+      nsegs += need_segs;
+      nmaps += need_maps;
+      ++g_end;
+    }
+    if (g_end == gi) return fail(DT_ERR_CAPACITY, "one GEMM group needs more than %d segments", MAX_SEGS);
+    const int bn = choose_bn(groups, gi, g_end, sms);
+    int map_i = 0, seg_i = 0, tiles = 0;
+    p.ngroups = 0;
+    for (size_t g = gi; g < g_end; ++g) {
+      const HostGroup& H = groups[g];
+      Group& G = p.groups[p.ngroups++];
+      G.m = (int32_t)H.m;
+      G.n = (int32_t)H.n;
+      G.bn = H.dual ? 128 : bn;
+      G.m_tiles = (int32_t)((H.m + BM - 1) / BM);
+      G.n_tiles = (int32_t)((H.n + G.bn - 1) / G.bn);
+      G.tile_begin = tiles;
+      tiles += G.m_tiles * G.n_tiles;
+      G.seg_begin = seg_i;
+      G.seg_count = (int32_t)H.segs.size();
+      G.dual = H.dual ? 1 : 0;
+      G.out_dtype = H.out_dtype;
+      G.nout = (int32_t)H.out_ptr.size();
+      for (int j = 0; j < G.nout; ++j) {
+        G.out_row_begin[j] = H.row_begin[j];
+        G.out_ptr[j] = H.out_ptr[j];
+        G.out_ld[j] = H.out_ld[j];
+      }
+      G.out_row_begin[G.nout] = H.m;
+      G.bias = H.bias;
+      G.bias_dtype = H.bias ? H.bias_dtype : -1;
+      G.out_vec = out_vec_ok(H) ? 1 : 0;
+      for (const HostSeg& s : H.segs) {
+        Seg& S = p.segs[seg_i++];
+        S.k_tiles = (int32_t)((s.a.cols + BK - 1) / BK);
+        S.a_map = map_i;
+        dt_status st = encode_map(s.a, BM, &p.maps[map_i++]);
+        if (st != DT_OK) return st;
+        S.b_map = map_i;
+        st = encode_map(s.b, BK, &p.maps[map_i++]);
+        if (st != DT_OK) return st;
+        S.b_map2 = S.b_map;
+        if (H.dual) {
+          S.b_map2 = map_i;
+          st = encode_map(s.b2, BK, &p.maps[map_i++]);
+          if (st != DT_OK) return st;
+        }
+      }
+    }
+    p.total_tiles = tiles;
+    p.status = status;
+    if (tiles > 0) {
+      const int grid = std::min(tiles, sms);
+      cudaError_t e = launch_tcgen05(p, grid, stream);
+      if (e != cudaSuccess) return fail(DT_ERR_CUDA, "tcgen05 GEMM launch: %s", cudaGetErrorString(e));
+    }
+    gi = g_end;
+  }
+  return DT_OK;
+}
+
+dt_status run_simt(std::vector<HostGroup>& groups, cudaStream_t stream) {
+  static thread_local SParams p;
+  const int sms = device_sm_count();
+  size_t gi = 0;
+  while (gi < groups.size()) {
+    size_t g_end = gi;
+    int nsegs = 0;
+    while (g_end < groups.size() && (int)(g_end - gi) < MAX_GROUPS &&
+           nsegs + (int)groups[g_end].segs.size() <= MAX_SEGS) {
+      nsegs += (int)groups[g_end].segs.size();
+      ++g_end;
+    }
+    if (g_end == gi) return fail(DT_ERR_CAPACITY, "one GEMM group needs more than %d segments", MAX_SEGS);
+    int seg_i = 0, tiles = 0;
+    p.ngroups = 0;
+    for (size_t g = gi; g < g_end; ++g) {
+      const HostGroup& H = groups[g];
+      if (H.dual) return fail(DT_ERR_ALIGNMENT, "the gated MLP needs TMA-compatible bf16 operands");
+      SGroup& G = p.groups[p.ngroups++];
+      G.m = H.m;
+      G.n = H.n;
+      G.m_tiles = (int32_t)((H.m + S_TILE - 1) / S_TILE);
+      G.n_tiles = (int32_t)((H.n + S_TILE - 1) / S_TILE);
+      G.tile_begin = tiles;
+      tiles += G.m_tiles * G.n_tiles;
+      G.seg_begin = seg_i;
+      G.seg_count = (int32_t)H.segs.size();
+      G.out_dtype = H.out_dtype;
+      G.nout = (int32_t)H.out_ptr.size();
+      for (int j = 0; j < G.nout; ++j) {
+        G.row_begin[j] = H.row_begin[j];
+        G.out_ptr[j] = H.out_ptr[j];
+        G.out_ld[j] = H.out_ld[j];
+      }
+      G.row_begin[G.nout] = H.m;
+      G.bias = H.bias;
+      G.bias_dtype = H.bias ? H.bias_dtype : -1;
+      for (const HostSeg& s : H.segs) {
+        SSeg& S = p.segs[seg_i++];
+        S.a = s.a.ptr;
+        S.b = s.b.ptr;
+        S.lda = s.a.ld;
+        S.ldb = s.b.ld;
+        S.k = (int32_t)s.a.cols;
+        S.dtype = s.a.dtype;
+      }
+    }
+    p.total_tiles = tiles;
+    if (tiles > 0) {
+      const int grid = std::min(tiles, sms * 8);
+      simt_gemm_kernel<<<grid, S_THREADS, 0, stream>>>(p);
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return fail(DT_ERR_CUDA, "CUDA-core GEMM launch: %s", cudaGetErrorString(e));
+    }
+    gi = g_end;
+  }
+  return DT_OK;
+}
+
+}  // namespace
+
+dt_status run_groups(std::vector<HostGroup>& groups, int32_t* d_status, cudaStream_t stream) {
+  // drop groups with no output; a group with no K contributes bias (or zeros)
+  std::vector<HostGroup> live;
+  live.reserve(groups.size());
+  for (auto& g : groups) {
+    if (g.m <= 0 || g.n <= 0) continue;
+    std::vector<HostSeg> segs;
+    for (auto& s : g.segs)
+      if (s.a.cols > 0) segs.push_back(s);
+    g.segs.swap(segs);
+    live.push_back(std::move(g));
+  }
+  if (live.empty()) return DT_OK;
+  for (auto& g : live)
+    if (g.out_ptr.size() > (size_t)MAX_OUT) return fail(DT_ERR_CAPACITY, "more than %d output row blocks", MAX_OUT);
+  bool tc = true;
+  for (const auto& g : live) {
+    if (g.segs.empty()) tc = false;
+    for (const auto& s : g.segs) {
+      if (!tma_ok(s.a) || !tma_ok(s.b) || (g.dual && !tma_ok(s.b2))) tc = false;
+    }
+  }
+  if (tc) {
+    int32_t* status = device_status_word(d_status);
+    if (!status) return fail(DT_ERR_CUDA, "no device status word");
+    return run_tcgen05(live, status, stream);
+  }
+  return run_simt(live, stream);
+}
+
+}  // namespace gemm
+}  // namespace dt
+
+extern "C" dt_status dt_clear_cache(void) {
+  std::lock_guard<std::mutex> lk(dt::gemm::g_map_mu);
+  dt::gemm::g_maps.clear();
+  return DT_OK;
+}

@@ -1,0 +1,334 @@
+// Persistent warp-specialised tcgen05 GEMM (see gemm_sm103.cuh for the
+// roles and the problem description) and its launcher.
+#include "gemm_sm103.cuh"
+#include "gemm_plan.h"
+
+namespace dt {
+namespace gemm {
+
+struct TileCoord {
+  int g, m0, n0;
+};
+
+__device__ __forceinline__ TileCoord decode_tile(const Params& p, int t) {
+  int g = 0;
+  while (g + 1 < p.ngroups && p.groups[g + 1].tile_begin <= t) ++g;
+  const Group& G = p.groups[g];
+  const int local = t - G.tile_begin;
+  const int span = GROUP_M * G.n_tiles;
+  const int first_m = (local / span) * GROUP_M;
+  const int gm = min(GROUP_M, G.m_tiles - first_m);
+  const int r = local % span;
+  return TileCoord{g, (first_m + r % gm) * BM, (r / gm) * G.bn};
+}
+
+// MMA width of a tile: the gated MLP always uses both 128-column halves;
+// otherwise the tile's remaining columns rounded up to the MMA's N step of 16.
+__device__ __forceinline__ int tile_mma_n(const Group& G, int n0) {
+  if (G.dual) return 256;
+  int rem = G.n - n0;
+  rem = (rem + 15) & ~15;
+  return rem < G.bn ? rem : G.bn;
+}
+
+__device__ __forceinline__ float bias_at(const Group& G, int col) {
+  if (G.bias_dtype == DT_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(G.bias)[col]);
+  return reinterpret_cast<const float*>(G.bias)[col];
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Store 32 fp32 values of one output row at columns [col0, col0 + 32).
+__device__ __forceinline__ void store_row32(const Group& G, char* row_ptr, int col0, const float (&v)[32]) {
+  const int valid = min(32, G.n - col0);
+  if (valid <= 0) return;
+  if (G.out_dtype == DT_BF16) {
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(row_ptr) + col0;
+    if (valid == 32 && G.out_vec) {
+      uint4* o4 = reinterpret_cast<uint4*>(o);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        o4[q] = make_uint4(pack2(v[8 * q + 0], v[8 * q + 1]), pack2(v[8 * q + 2], v[8 * q + 3]),
+                           pack2(v[8 * q + 4], v[8 * q + 5]), pack2(v[8 * q + 6], v[8 * q + 7]));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < valid) o[i] = __float2bfloat16_rn(v[i]);
+    }
+  } else {
+    float* o = reinterpret_cast<float*>(row_ptr) + col0;
+    if (valid == 32 && G.out_vec) {
+      float4* o4 = reinterpret_cast<float4*>(o);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) o4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < valid) o[i] = v[i];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  bool aborted = false;
+  int8_t issued_parity[STAGES];
+#pragma unroll
+  for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      for (int i = 0; i < p.ngroups; ++i) {
+        const Group& G = p.groups[i];
+        for (int s = G.seg_begin; s < G.seg_begin + G.seg_count && s < G.seg_begin + 2; ++s) {
+          prefetch_map(&p.maps[p.segs[s].a_map]);
+          prefetch_map(&p.maps[p.segs[s].b_map]);
+        }
+      }
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
+        const TileCoord tc = decode_tile(p, t);
+        const Group& G = p.groups[tc.g];
+        const int nmma = tile_mma_n(G, tc.n0);
+        const int nchunks = (nmma + 63) / 64;
+        const uint32_t bytes = A_TILE_BYTES + nchunks * B_CHUNK_BYTES;
+        for (int si = G.seg_begin; si < G.seg_begin + G.seg_count && !aborted; ++si) {
+          const Seg& S = p.segs[si];
+          for (int kt = 0; kt < S.k_tiles; ++kt) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+              aborted = true;
+              *abort_flag = 1;
+              break;
+            }
+            mbar_expect_tx(&full[stage], bytes);
+            uint8_t* a = smem + stage * STAGE_BYTES;
+            uint8_t* b = a + A_TILE_BYTES;
+            tma_load_2d(a, &p.maps[S.a_map], kt * BK, tc.m0, &full[stage]);
+            if (!G.dual) {
+              for (int c = 0; c < nchunks; ++c)
+                tma_load_2d(b + c * B_CHUNK_BYTES, &p.maps[S.b_map], tc.n0 + 64 * c, kt * BK, &full[stage]);
+            } else {
+              for (int c = 0; c < 2; ++c) {
+                tma_load_2d(b + c * B_CHUNK_BYTES, &p.maps[S.b_map], tc.n0 + 64 * c, kt * BK, &full[stage]);
+                tma_load_2d(b + (2 + c) * B_CHUNK_BYTES, &p.maps[S.b_map2], tc.n0 + 64 * c, kt * BK, &full[stage]);
+              }
+            }
+            issued_parity[stage] = static_cast<int8_t>(phase);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int buf = 0;
+      uint32_t tphase = 0;
+      const uint32_t a_base = smem_u32(smem);
+      for (int t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
+        const TileCoord tc = decode_tile(p, t);
+        const Group& G = p.groups[tc.g];
+        const uint32_t idesc = instr_desc(BM, tile_mma_n(G, tc.n0));
+        if (!mbar_wait(&tempty[buf], tphase ^ 1u, abort_flag)) {
+          aborted = true;
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN_MAX);
+        uint32_t acc = 0;
+        for (int si = G.seg_begin; si < G.seg_begin + G.seg_count && !aborted; ++si) {
+          const int kts = p.segs[si].k_tiles;
+          for (int kt = 0; kt < kts; ++kt) {
+            if (!mbar_wait(&full[stage], phase, abort_flag)) {
+              aborted = true;
+              *abort_flag = 1;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = a_base + stage * STAGE_BYTES;
+            const uint32_t b_addr = a_addr + A_TILE_BYTES;
+#pragma unroll
+            for (int j = 0; j < BK / 16; ++j) {
+              // A: K-major, 128 B rows, 8-row groups 1024 B apart; a K step of 16
+              //    elements moves 32 B inside the swizzled row.
+              // B: MN-major, 64-column chunks 8 KiB apart (LBO), 8-row K groups
+              //    1024 B apart (SBO); a K step of 16 rows moves 2 KiB.
+              const uint64_t adesc = smem_desc(a_addr + j * 32, 16, 1024);
+              const uint64_t bdesc = smem_desc(b_addr + j * 2048, B_CHUNK_BYTES, 1024);
+              mma_bf16(d_tmem, adesc, bdesc, idesc, acc);
+              acc = 1;
+            }
+            mma_commit(&empty[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        if (aborted) break;
+        mma_commit(&tfull[buf]);
+        if (++buf == 2) {
+          buf = 0;
+          tphase ^= 1u;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int row_in_tile = quarter * 32 + lane;
+    int buf = 0;
+    uint32_t tphase = 0;
+    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+      const TileCoord tc = decode_tile(p, t);
+      const Group& G = p.groups[tc.g];
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&tfull[buf], tphase, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);  // tcgen05.ld below is warp-collective
+      if (!ok) {
+        aborted = true;
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int64_t r = tc.m0 + row_in_tile;
+      char* row_ptr = nullptr;
+      if (r < G.m) {
+        int j = 0;
+        while (j + 1 < G.nout && G.out_row_begin[j + 1] <= r) ++j;
+        const int esize = G.out_dtype == DT_BF16 ? 2 : 4;
+        row_ptr = G.out_ptr[j] + (r - G.out_row_begin[j]) * G.out_ld[j] * esize;
+      }
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN_MAX);
+      if (!G.dual) {
+        const int nmma = tile_mma_n(G, tc.n0);
+        for (int c = 0; c < nmma; c += 32) {
+          uint32_t raw[32];
+          tmem_ld32(tbase + c, raw);
+          tmem_ld_wait();
+          if (row_ptr) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(raw[i]);
+            if (G.bias_dtype >= 0) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int col = tc.n0 + c + i;
+                if (col < G.n) v[i] += bias_at(G, col);
+              }
+            }
+            store_row32(G, row_ptr, tc.n0 + c, v);
+          }
+        }
+      } else {
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(tbase + c, g);
+          tmem_ld32(tbase + 128 + c, u);
+          tmem_ld_wait();
+          if (row_ptr) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float gv = __uint_as_float(g[i]);
+              const float uv = __uint_as_float(u[i]);
+              v[i] = gv / (1.0f + __expf(-gv)) * uv;  // SiLU(g) * u in fp32
+            }
+            store_row32(G, row_ptr, tc.n0 + c, v);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (++buf == 2) {
+        buf = 0;
+        tphase ^= 1u;
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  if (aborted && lane == 0) {
+    atomicOr(p.status, DT_DEV_ERR_TIMEOUT);
+  }
+  if (warp == 0 && lane == 0 && aborted) {
+    // let copies already in flight land before the CTA's smem is released
+    for (int s = 0; s < STAGES; ++s) {
+      if (issued_parity[s] < 0) continue;
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(&full[s], static_cast<uint32_t>(issued_parity[s])) && globaltimer() - t0 < 100000000ull) {
+      }
+    }
+  }
+  if (warp == 1 && lane == 0) {
+    // every MMA this CTA issued has completed before TMEM is freed
+    mma_commit(drain);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < 100000000ull) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+cudaError_t launch_tcgen05(const Params& p, int grid, cudaStream_t stream) {
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(tcgen05_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  tcgen05_gemm_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace gemm
+}  // namespace dt

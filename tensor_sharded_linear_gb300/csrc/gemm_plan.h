@@ -1,0 +1,49 @@
+// Host-side description of one batched GEMM call: independent output groups,
+// each summing a list of (A, B) K segments in order.  Built by the linear
+// entry points, lowered either to the tcgen05 kernel or to the CUDA-core
+// kernel.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <vector>
+
+#include "dt_internal.h"
+
+namespace dt {
+namespace gemm {
+
+// Row-major matrix view: element (r, c) at ptr + (r * ld + c) * esize.
+struct Mat {
+  char* ptr = nullptr;
+  int64_t rows = 0, cols = 0, ld = 0;
+  int dtype = DT_BF16;
+};
+
+struct HostSeg {
+  Mat a;   // [M, K_s]
+  Mat b;   // [K_s, N]
+  Mat b2;  // [K_s, N], gated MLP "up" operand (dual groups only)
+};
+
+struct HostGroup {
+  int64_t m = 0, n = 0;
+  std::vector<HostSeg> segs;
+  bool dual = false;  // out = SiLU(A B) * (A B2)
+  int out_dtype = DT_BF16;
+  // rows [row_begin[j], row_begin[j+1]) go to out_ptr[j] with leading dim out_ld[j]
+  std::vector<int64_t> row_begin;
+  std::vector<char*> out_ptr;
+  std::vector<int64_t> out_ld;
+  const void* bias = nullptr;  // [n], added before the cast
+  int bias_dtype = -1;
+};
+
+// Run every group; returns a host-detected error or DT_OK.
+dt_status run_groups(std::vector<HostGroup>& groups, int32_t* d_status, cudaStream_t stream);
+
+struct Params;
+cudaError_t launch_tcgen05(const Params& p, int grid, cudaStream_t stream);
+
+}  // namespace gemm
+}  // namespace dt

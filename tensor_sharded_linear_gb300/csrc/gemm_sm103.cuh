@@ -1,0 +1,219 @@
+// Device side of the tensor-parallel GEMM for sm_103a: tcgen05 MMA with the
+// accumulator in tensor memory (TMEM), operands staged in shared memory by
+// TMA, one persistent CTA per SM with warp-specialised roles.
+//
+//   warp 0      TMA producer  (one lane): fills a STAGES-deep smem ring
+//   warp 1      MMA issuer    (one lane): tcgen05.mma into a double-buffered
+//                                         TMEM accumulator; owns TMEM
+//   warps 2..5  epilogue      (128 threads, one accumulator row each):
+//                                         tcgen05.ld, bias / SiLU*mul, cast, store
+//
+// Problem description: a list of GROUPS, each an independent output tile
+// grid, and per group a list of K SEGMENTS, each one (A, B) pair of TMA
+// descriptors.  A tile accumulates every segment of its group, in order, in
+// fp32 in TMEM.  This one shape covers
+//   column parallel  (wineandchord "Column parallel", Y_i = X W_i):
+//                    one group per shard, one segment each;
+//   row parallel     (wineandchord "Row parallel", Y = sum_i X_i W_i):
+//                    one group, one segment per shard -- the Partial sum
+//                    never leaves the accumulator;
+//   gated MLP        two B descriptors per segment (gate, up) whose tiles sit
+//                    side by side in smem, so one N=256 MMA fills both halves
+//                    of the accumulator and the epilogue forms SiLU(g) * u.
+//
+// Operand layouts: A is K-major (row-major [M, K] activations), B is
+// MN-major (row-major [K, N] weights, the [in, out] convention), both with
+// the 128-byte swizzle that TMA writes and the MMA reads.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dt {
+namespace gemm {
+
+constexpr int BM = 128;                       // accumulator rows = TMEM lanes
+constexpr int BN_MAX = 256;                   // accumulator columns per buffer
+constexpr int BK = 64;                        // 64 bf16 = one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int A_TILE_BYTES = BM * BK * 2;     // 16 KiB
+constexpr int B_CHUNK_BYTES = 64 * BK * 2;    // 8 KiB: 64 N columns x 64 K rows
+constexpr int B_TILE_BYTES = BN_MAX * BK * 2; // 32 KiB
+constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 512;                // two 256-column accumulators
+constexpr int GROUP_M = 8;                    // tile raster: 8 M tiles per band
+constexpr int MAX_MAPS = 48;
+constexpr int MAX_SEGS = 96;
+constexpr int MAX_GROUPS = 32;
+constexpr int MAX_OUT = 8;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
+
+struct Seg {
+  int32_t a_map, b_map, b_map2, k_tiles;
+};
+
+struct Group {
+  int32_t m, n, m_tiles, n_tiles;
+  int32_t tile_begin, seg_begin, seg_count, bn;  // bn: output columns per tile
+  int32_t dual, out_dtype, nout, bias_dtype;     // bias_dtype < 0: no bias
+  int32_t out_vec, pad0, pad1, pad2;             // out_vec: 16-byte stores allowed
+  const void* bias;
+  int64_t out_row_begin[MAX_OUT + 1];  // output row blocks: rows [begin[j], begin[j+1]) -> out j
+  char* out_ptr[MAX_OUT];
+  int64_t out_ld[MAX_OUT];  // elements
+};
+
+struct Params {  // CUtensorMap carries its own 128-byte alignment
+  CUtensorMap maps[MAX_MAPS];
+  Seg segs[MAX_SEGS];
+  Group groups[MAX_GROUPS];
+  int32_t ngroups, total_tiles;
+  int32_t* status;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of parity `parity` to complete.  Gives up (and
+// returns false) when another role has raised the CTA's abort flag or after
+// WAIT_LIMIT_NS; the caller then records DT_DEV_ERR_TIMEOUT and unwinds.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  uint32_t spins = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++spins & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > WAIT_LIMIT_NS) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem], bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread issued so far completes.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 32 consecutive fp32 accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading and
+// stride byte offsets (all >> 4), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;  // version
+  d |= 2ull << 61;  // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 D, bf16 A and B, A K-major,
+// B MN-major, shape M x N.
+__host__ __device__ constexpr uint32_t instr_desc(int m, int n) {
+  return (1u << 4)                                 // D format: f32
+         | (1u << 7)                               // A format: bf16
+         | (1u << 10)                              // B format: bf16
+         | (0u << 15)                              // A K-major
+         | (1u << 16)                              // B MN-major
+         | (static_cast<uint32_t>(n >> 3) << 17)   // N / 8
+         | (static_cast<uint32_t>(m >> 4) << 24);  // M / 16
+}
+
+}  // namespace gemm
+}  // namespace dt

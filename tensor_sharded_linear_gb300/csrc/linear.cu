@@ -1,0 +1,580 @@
+// Tensor-parallel linear entry points: placement checks and the lowering of
+// every rank's local product to GEMM groups.
+//
+// DTorch user guide, "Module parallel", section 3: tp_shard_type "col" keeps
+// the weight sharded on output features and requires a Replicate input on
+// tp; "row" shards the weight on input features and requires a
+// Shard(ndim - 1) input; the row bias is Partial so it is added once; every
+// mesh dim other than tp keeps weights and biases Replicate.
+// Model parallelism (wineandchord), "Tensor Parallel": Y_i = X W_i and
+// Y = sum_i X_i W_i, weights [in, out].
+// nanotron tutorial ch. 5, 5.1: ALL_REDUCE / REDUCE_SCATTER row outputs.
+#include <algorithm>
+#include <cstring>
+#include <set>
+#include <tuple>
+#include <vector>
+
+#include "gemm_plan.h"
+
+namespace dt {
+namespace {
+
+using gemm::HostGroup;
+using gemm::HostSeg;
+using gemm::Mat;
+
+// Matrix view of a slot: leading dims flattened to rows, last dim = cols.
+dt_status slot_matrix(const SlotView& v, int ndim, int dtype, Mat* out, const char* what) {
+  Mat m;
+  m.ptr = v.ptr;
+  m.dtype = dtype;
+  m.cols = v.shape[ndim - 1];
+  m.rows = 1;
+  for (int d = 0; d < ndim - 1; ++d) m.rows *= v.shape[d];
+  if (m.cols > 1 && v.stride[ndim - 1] != 1) return fail(DT_ERR_UNSUPPORTED, "%s: inner stride must be 1", what);
+  if (ndim >= 2) {
+    m.ld = v.stride[ndim - 2];
+    for (int d = ndim - 3; d >= 0; --d)
+      if (v.shape[d] > 1 && v.stride[d] != v.stride[d + 1] * v.shape[d + 1])
+        return fail(DT_ERR_UNSUPPORTED, "%s: leading dims must be collapsible", what);
+    if (m.rows <= 1) m.ld = std::max<int64_t>(m.ld, m.cols);
+  } else {
+    m.ld = m.cols;
+  }
+  if (m.rows > 1 && m.ld < m.cols) return fail(DT_ERR_UNSUPPORTED, "%s: rows overlap", what);
+  *out = m;
+  return DT_OK;
+}
+
+bool same_mesh(const Layout& a, const Layout& b) {
+  if (a.mesh_ndim != b.mesh_ndim) return false;
+  for (int m = 0; m < a.mesh_ndim; ++m)
+    if (a.mesh[m] != b.mesh[m]) return false;
+  return true;
+}
+
+bool same_placement(const Layout& a, int ma, const Layout& b, int mb) {
+  if (a.kind[ma] != b.kind[mb]) return false;
+  return a.kind[ma] != DT_SHARD || a.dim[ma] == b.dim[mb];
+}
+
+const char* pname(const Layout& l, int m) {
+  switch (l.kind[m]) {
+    case DT_REPLICATE: return "Replicate";
+    case DT_SHARD: return "Shard";
+    default: return "Partial";
+  }
+}
+
+dt_status check_tp(int tp, const Layout& l) {
+  if (tp >= l.mesh_ndim) return fail(DT_ERR_INVALID_ARG, "tp_mesh_dim %d outside a %d-D mesh", tp, l.mesh_ndim);
+  return DT_OK;
+}
+
+int tp_size(const Layout& l, int tp) { return tp >= 0 ? l.mesh[tp] : 1; }
+
+// Rows of the first local dim, scaled to flattened rows.
+int64_t rows_per_dim0(const SlotView& v, int ndim) {
+  int64_t r = 1;
+  for (int d = 1; d < ndim - 1; ++d) r *= v.shape[d];
+  return r;
+}
+
+struct ColumnSpec {
+  const DTensor* w;
+  const DTensor* bias;  // nullptr: none
+  const DTensor* y;
+};
+
+// Checks shared by the column layers: x [.., K] Replicate on tp, w [K, N]
+// Shard(1) on tp, bias [N] Shard(0) on tp, y [.., N] Shard(-1) on tp; off tp
+// weights/bias Replicate and x, y placed alike.
+dt_status check_column(const DTensor& X, const ColumnSpec& c, int tp, bool allow_partial_x) {
+  const Layout& lx = X.layout;
+  const Layout& lw = c.w->layout;
+  const Layout& ly = c.y->layout;
+  if (!same_mesh(lx, lw) || !same_mesh(lx, ly) || (c.bias && !same_mesh(lx, c.bias->layout)))
+    return fail(DT_ERR_SHAPE, "operands live on different meshes");
+  if (lw.ndim != 2) return fail(DT_ERR_SHAPE, "weight must be 2-D [in, out]");
+  if (lx.dtype != lw.dtype) return fail(DT_ERR_INVALID_ARG, "x and w dtypes differ");
+  if (lx.dtype == DT_INT32 || ly.dtype == DT_INT32) return fail(DT_ERR_INVALID_ARG, "int32 linear");
+  if (ly.ndim != lx.ndim) return fail(DT_ERR_SHAPE, "y rank must equal x rank");
+  const int nd = lx.ndim;
+  if (lx.gshape[nd - 1] != lw.gshape[0]) return fail(DT_ERR_SHAPE, "x last dim %lld != w rows %lld",
+                                                     (long long)lx.gshape[nd - 1], (long long)lw.gshape[0]);
+  for (int d = 0; d < nd - 1; ++d)
+    if (ly.gshape[d] != lx.gshape[d]) return fail(DT_ERR_SHAPE, "y leading dims differ from x");
+  if (ly.gshape[nd - 1] != lw.gshape[1]) return fail(DT_ERR_SHAPE, "y last dim != w cols");
+  if (c.bias) {
+    const Layout& lb = c.bias->layout;
+    if (lb.ndim != 1 || lb.gshape[0] != lw.gshape[1]) return fail(DT_ERR_SHAPE, "bias must be [out]");
+    if (lb.dtype == DT_INT32) return fail(DT_ERR_INVALID_ARG, "bias dtype");
+  }
+  for (int m = 0; m < lx.mesh_ndim; ++m) {
+    if (m == tp) {
+      if (!lx.is_replicate(m)) return fail(DT_ERR_PLACEMENT, "column-parallel input must be Replicate on tp, got %s", pname(lx, m));
+      if (!lw.is_shard(m, 1)) return fail(DT_ERR_PLACEMENT, "column-parallel weight [in, out] must be Shard(1) on tp");
+      if (!ly.is_shard(m, nd - 1)) return fail(DT_ERR_PLACEMENT, "column-parallel output must be Shard(-1) on tp");
+      if (c.bias && !c.bias->layout.is_shard(m, 0)) return fail(DT_ERR_PLACEMENT, "column-parallel bias must be Shard(0) on tp");
+    } else {
+      if (!lw.is_replicate(m)) return fail(DT_ERR_PLACEMENT, "weight must be Replicate off tp");
+      if (c.bias && !c.bias->layout.is_replicate(m)) return fail(DT_ERR_PLACEMENT, "bias must be Replicate off tp");
+      if (!same_placement(lx, m, ly, m)) return fail(DT_ERR_PLACEMENT, "x and y must be placed alike off tp");
+      if (lx.kind[m] == DT_SHARD && lx.dim[m] == nd - 1) return fail(DT_ERR_PLACEMENT, "x may not be sharded on its last dim off tp");
+      if (lx.is_partial(m) && (!allow_partial_x || c.bias)) return fail(DT_ERR_PLACEMENT, "Partial input with a bias");
+    }
+  }
+  return DT_OK;
+}
+
+dt_status add_column_groups(const DTensor& X, const ColumnSpec& c, std::vector<HostGroup>* groups,
+                            std::set<std::pair<const void*, int>>* done) {
+  const Layout& lx = X.layout;
+  const int nd = lx.ndim;
+  int coords[DT_MAX_MESH_DIMS];
+  for (int r = 0; r < lx.mesh_size; ++r) {
+    lx.rank_coords(r, coords);
+    const int ys = c.y->layout.slot_of_coords(coords);
+    if (!done->insert({c.y, ys}).second) continue;
+    const SlotView& xv = X.slots[lx.slot_of_coords(coords)];
+    const SlotView& wv = c.w->slots[c.w->layout.slot_of_coords(coords)];
+    const SlotView& yv = c.y->slots[ys];
+    HostGroup g;
+    Mat a, b, y;
+    dt_status st = slot_matrix(xv, nd, lx.dtype, &a, "x");
+    if (st != DT_OK) return st;
+    st = slot_matrix(wv, 2, c.w->layout.dtype, &b, "w");
+    if (st != DT_OK) return st;
+    st = slot_matrix(yv, nd, c.y->layout.dtype, &y, "y");
+    if (st != DT_OK) return st;
+    if (y.rows != a.rows || y.cols != b.cols || a.cols != b.rows)
+      return fail(DT_ERR_SHAPE, "local shapes disagree: x [%lld, %lld] w [%lld, %lld] y [%lld, %lld]",
+                  (long long)a.rows, (long long)a.cols, (long long)b.rows, (long long)b.cols, (long long)y.rows,
+                  (long long)y.cols);
+    g.m = y.rows;
+    g.n = y.cols;
+    g.segs.push_back(HostSeg{a, b, Mat()});
+    g.out_dtype = c.y->layout.dtype;
+    g.row_begin = {0};
+    g.out_ptr = {y.ptr};
+    g.out_ld = {y.ld};
+    if (c.bias) {
+      const SlotView& bv = c.bias->slots[c.bias->layout.slot_of_coords(coords)];
+      if (bv.shape[0] != y.cols) return fail(DT_ERR_SHAPE, "bias shard width differs from the output shard");
+      if (bv.shape[0] > 1 && bv.stride[0] != 1) return fail(DT_ERR_UNSUPPORTED, "bias must be contiguous");
+      g.bias = bv.ptr;
+      g.bias_dtype = c.bias->layout.dtype;
+    }
+    groups->push_back(std::move(g));
+  }
+  return DT_OK;
+}
+
+dt_status column_multi(const dt_dtensor* x, int32_t n, const dt_dtensor* w, const dt_dtensor* bias,
+                       const dt_dtensor* y, int32_t tp, int32_t* d_status, dt_stream_t stream) {
+  clear_error();
+  if (n < 1 || !w || !y) return fail(DT_ERR_INVALID_ARG, "need n >= 1 weights and outputs");
+  DTensor X;
+  dt_status st = parse_dtensor(x, &X, "x");
+  if (st != DT_OK) return st;
+  st = check_tp(tp, X.layout);
+  if (st != DT_OK) return st;
+  std::vector<DTensor> W(n), Y(n), B(n);
+  std::vector<bool> has_bias(n, false);
+  for (int j = 0; j < n; ++j) {
+    if ((st = parse_dtensor(&w[j], &W[j], "w")) != DT_OK) return st;
+    if ((st = parse_dtensor(&y[j], &Y[j], "y")) != DT_OK) return st;
+    if (bias && bias[j].nslots > 0) {
+      if ((st = parse_dtensor(&bias[j], &B[j], "bias")) != DT_OK) return st;
+      has_bias[j] = true;
+    }
+    ColumnSpec c{&W[j], has_bias[j] ? &B[j] : nullptr, &Y[j]};
+    if ((st = check_column(X, c, tp, true)) != DT_OK) return st;
+  }
+  std::vector<HostGroup> groups;
+  std::set<std::pair<const void*, int>> done;
+  for (int j = 0; j < n; ++j) {
+    ColumnSpec c{&W[j], has_bias[j] ? &B[j] : nullptr, &Y[j]};
+    if ((st = add_column_groups(X, c, &groups, &done)) != DT_OK) return st;
+  }
+  if (groups.empty()) return DT_OK;
+  const void* any = groups[0].out_ptr[0];
+  if ((st = bind_device_of(any)) != DT_OK) return st;
+  return gemm::run_groups(groups, d_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Row-parallel groups for one (x, w, y) triple; `x_override` replaces the x
+// slots by explicit matrices (the MLP's H views) when non-null.
+dt_status row_groups(const Layout& lx, const std::vector<Mat>* x_mats, const DTensor* X, const DTensor& W,
+                     const DTensor* Bias, const DTensor& Y, int mode, int tp, std::vector<HostGroup>* groups) {
+  const Layout& lw = W.layout;
+  const Layout& ly = Y.layout;
+  const int nd = lx.ndim;
+  const int P = tp_size(lx, tp);
+  std::set<int> done;
+  int c0[DT_MAX_MESH_DIMS], cj[DT_MAX_MESH_DIMS];
+  for (int r = 0; r < lx.mesh_size; ++r) {
+    lx.rank_coords(r, c0);
+    if (tp >= 0 && c0[tp] != 0) continue;
+    // the P ranks of this tp group, in tp order
+    std::vector<HostSeg> segs;
+    std::vector<int> yslots;
+    Mat xm0;
+    int64_t x_row0 = 0;
+    for (int j = 0; j < P; ++j) {
+      std::copy(c0, c0 + DT_MAX_MESH_DIMS, cj);
+      if (tp >= 0) cj[tp] = j;
+      Mat a, b;
+      dt_status st;
+      const int xs = lx.slot_of_coords(cj);
+      if (x_mats) {
+        a = (*x_mats)[xs];
+      } else {
+        const SlotView& xv = X->slots[xs];
+        if ((st = slot_matrix(xv, nd, lx.dtype, &a, "x")) != DT_OK) return st;
+      }
+      x_row0 = lx.slot_box(xs).off[0];
+      const SlotView& wv = W.slots[lw.slot_of_coords(cj)];
+      if ((st = slot_matrix(wv, 2, lw.dtype, &b, "w")) != DT_OK) return st;
+      if (a.cols != b.rows) return fail(DT_ERR_SHAPE, "x shard width %lld != w shard rows %lld", (long long)a.cols, (long long)b.rows);
+      if (j == 0) xm0 = a;
+      if (a.rows != xm0.rows) return fail(DT_ERR_SHAPE, "x shards have different row counts");
+      segs.push_back(HostSeg{a, b, Mat()});
+      yslots.push_back(ly.slot_of_coords(cj));
+    }
+    const int64_t M = xm0.rows, N = lw.gshape[1];
+    const void* bias_ptr = nullptr;
+    int bias_dtype = -1;
+    if (Bias) {
+      const SlotView& bv = Bias->slots[Bias->layout.slot_of_coords(c0)];
+      if (bv.shape[0] > 1 && bv.stride[0] != 1) return fail(DT_ERR_UNSUPPORTED, "bias must be contiguous");
+      bias_ptr = bv.ptr;
+      bias_dtype = Bias->layout.dtype;
+    }
+    if (mode == DT_TP_ALL_REDUCE) {
+      for (int j = 0; j < P; ++j) {
+        if (!done.insert(yslots[j]).second) continue;
+        Mat y;
+        dt_status st = slot_matrix(Y.slots[yslots[j]], nd, ly.dtype, &y, "y");
+        if (st != DT_OK) return st;
+        if (y.rows != M || y.cols != N) return fail(DT_ERR_SHAPE, "ALL_REDUCE output slot shape");
+        HostGroup g;
+        g.m = M;
+        g.n = N;
+        g.segs = segs;
+        g.out_dtype = ly.dtype;
+        g.row_begin = {0};
+        g.out_ptr = {y.ptr};
+        g.out_ld = {y.ld};
+        g.bias = bias_ptr;
+        g.bias_dtype = bias_dtype;
+        groups->push_back(std::move(g));
+      }
+    } else if (mode == DT_TP_REDUCE_SCATTER) {
+      if (!done.insert(yslots[0]).second) continue;
+      HostGroup g;
+      g.m = M;
+      g.n = N;
+      g.segs = segs;
+      g.out_dtype = ly.dtype;
+      g.bias = bias_ptr;
+      g.bias_dtype = bias_dtype;
+      int64_t next = 0;
+      for (int j = 0; j < P; ++j) {
+        const SlotView& yv = Y.slots[yslots[j]];
+        Mat y;
+        dt_status st = slot_matrix(yv, nd, ly.dtype, &y, "y");
+        if (st != DT_OK) return st;
+        if (y.rows == 0) continue;
+        const int64_t begin = (yv.goff[0] - x_row0) * rows_per_dim0(yv, nd);
+        if (begin != next || y.cols != N) return fail(DT_ERR_SHAPE, "REDUCE_SCATTER output blocks do not tile the rows");
+        g.row_begin.push_back(begin);
+        g.out_ptr.push_back(y.ptr);
+        g.out_ld.push_back(y.ld);
+        next = begin + y.rows;
+      }
+      if (next != M) return fail(DT_ERR_SHAPE, "REDUCE_SCATTER output blocks cover %lld of %lld rows", (long long)next, (long long)M);
+      groups->push_back(std::move(g));
+    } else {  // DT_TP_PARTIAL
+      for (int j = 0; j < P; ++j) {
+        if (!done.insert(yslots[j]).second) continue;
+        Mat y;
+        dt_status st = slot_matrix(Y.slots[yslots[j]], nd, ly.dtype, &y, "y");
+        if (st != DT_OK) return st;
+        if (y.rows != M || y.cols != N) return fail(DT_ERR_SHAPE, "PARTIAL output slot shape");
+        HostGroup g;
+        g.m = M;
+        g.n = N;
+        g.segs = {segs[j]};
+        g.out_dtype = ly.dtype;
+        g.row_begin = {0};
+        g.out_ptr = {y.ptr};
+        g.out_ld = {y.ld};
+        if (j == 0) {  // the parts sum to X W + b: the bias rides on part 0
+          g.bias = bias_ptr;
+          g.bias_dtype = bias_dtype;
+        }
+        groups->push_back(std::move(g));
+      }
+    }
+  }
+  return DT_OK;
+}
+
+// Checks of the row layer: x [.., K] Shard(-1) on tp, w [K, N] Shard(0) on
+// tp, bias [N] Replicate, y per mode; off tp weights/bias Replicate and x, y
+// placed alike.
+dt_status check_row(const Layout& lx, const Layout& lw, const Layout* lb, const Layout& ly, int mode, int tp) {
+  if (!same_mesh(lx, lw) || !same_mesh(lx, ly) || (lb && !same_mesh(lx, *lb)))
+    return fail(DT_ERR_SHAPE, "operands live on different meshes");
+  if (mode != DT_TP_ALL_REDUCE && mode != DT_TP_REDUCE_SCATTER && mode != DT_TP_PARTIAL)
+    return fail(DT_ERR_INVALID_ARG, "mode %d", mode);
+  if (lw.ndim != 2) return fail(DT_ERR_SHAPE, "weight must be 2-D [in, out]");
+  if (lx.dtype != lw.dtype) return fail(DT_ERR_INVALID_ARG, "x and w dtypes differ");
+  if (lx.dtype == DT_INT32 || ly.dtype == DT_INT32) return fail(DT_ERR_INVALID_ARG, "int32 linear");
+  const int nd = lx.ndim;
+  if (ly.ndim != nd) return fail(DT_ERR_SHAPE, "y rank must equal x rank");
+  if (lx.gshape[nd - 1] != lw.gshape[0]) return fail(DT_ERR_SHAPE, "x last dim != w rows");
+  for (int d = 0; d < nd - 1; ++d)
+    if (ly.gshape[d] != lx.gshape[d]) return fail(DT_ERR_SHAPE, "y leading dims differ from x");
+  if (ly.gshape[nd - 1] != lw.gshape[1]) return fail(DT_ERR_SHAPE, "y last dim != w cols");
+  if (lb) {
+    if (lb->ndim != 1 || lb->gshape[0] != lw.gshape[1]) return fail(DT_ERR_SHAPE, "bias must be [out]");
+    if (lb->dtype == DT_INT32) return fail(DT_ERR_INVALID_ARG, "bias dtype");
+  }
+  for (int m = 0; m < lx.mesh_ndim; ++m) {
+    if (m == tp) {
+      if (!lx.is_shard(m, nd - 1)) return fail(DT_ERR_PLACEMENT, "row-parallel input must be Shard(-1) on tp, got %s", pname(lx, m));
+      if (!lw.is_shard(m, 0)) return fail(DT_ERR_PLACEMENT, "row-parallel weight [in, out] must be Shard(0) on tp");
+      if (lb && !lb->is_replicate(m)) return fail(DT_ERR_PLACEMENT, "row-parallel bias is passed reduced (Replicate)");
+      if (mode == DT_TP_ALL_REDUCE && !ly.is_replicate(m)) return fail(DT_ERR_PLACEMENT, "ALL_REDUCE output must be Replicate on tp");
+      if (mode == DT_TP_REDUCE_SCATTER && !ly.is_shard(m, 0)) return fail(DT_ERR_PLACEMENT, "REDUCE_SCATTER output must be Shard(0) on tp");
+      if (mode == DT_TP_REDUCE_SCATTER && nd < 2) return fail(DT_ERR_SHAPE, "REDUCE_SCATTER needs a leading dim");
+      if (mode == DT_TP_PARTIAL && !ly.is_partial(m)) return fail(DT_ERR_PLACEMENT, "PARTIAL output must be Partial on tp");
+    } else {
+      if (!lw.is_replicate(m)) return fail(DT_ERR_PLACEMENT, "weight must be Replicate off tp");
+      if (lb && !lb->is_replicate(m)) return fail(DT_ERR_PLACEMENT, "bias must be Replicate off tp");
+      if (!same_placement(lx, m, ly, m)) return fail(DT_ERR_PLACEMENT, "x and y must be placed alike off tp");
+      if (lx.kind[m] == DT_SHARD && lx.dim[m] == nd - 1) return fail(DT_ERR_PLACEMENT, "x may be sharded on its last dim only on tp");
+      if (lx.is_partial(m) && lb) return fail(DT_ERR_PLACEMENT, "Partial input with a bias");
+      if (mode == DT_TP_REDUCE_SCATTER && lx.kind[m] == DT_SHARD && lx.dim[m] == 0 && m > tp)
+        return fail(DT_ERR_UNSUPPORTED, "dim 0 sharded by a mesh dim inside tp");
+    }
+  }
+  return DT_OK;
+}
+
+}  // namespace
+}  // namespace dt
+
+using namespace dt;
+
+extern "C" {
+
+dt_status dt_column_parallel_linear(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* bias,
+                                    const dt_dtensor* y, int32_t tp_mesh_dim, int32_t* d_status,
+                                    dt_stream_t stream) {
+  return column_multi(x, 1, w, bias, y, tp_mesh_dim, d_status, stream);
+}
+
+dt_status dt_column_parallel_linear_multi(const dt_dtensor* x, int32_t n, const dt_dtensor* w,
+                                          const dt_dtensor* bias, const dt_dtensor* y, int32_t tp_mesh_dim,
+                                          int32_t* d_status, dt_stream_t stream) {
+  return column_multi(x, n, w, bias, y, tp_mesh_dim, d_status, stream);
+}
+
+dt_status dt_row_parallel_linear(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* bias,
+                                 const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim, int32_t* d_status,
+                                 dt_stream_t stream) {
+  clear_error();
+  DTensor X, W, B, Y;
+  dt_status st;
+  if ((st = parse_dtensor(x, &X, "x")) != DT_OK) return st;
+  if ((st = parse_dtensor(w, &W, "w")) != DT_OK) return st;
+  if ((st = parse_dtensor(y, &Y, "y")) != DT_OK) return st;
+  const bool has_bias = bias && bias->nslots > 0;
+  if (has_bias && (st = parse_dtensor(bias, &B, "bias")) != DT_OK) return st;
+  if ((st = check_tp(tp_mesh_dim, X.layout)) != DT_OK) return st;
+  if (tp_mesh_dim < 0 && mode != DT_TP_ALL_REDUCE)
+    return fail(DT_ERR_INVALID_ARG, "without tp only ALL_REDUCE (a plain linear) is defined");
+  if ((st = check_row(X.layout, W.layout, has_bias ? &B.layout : nullptr, Y.layout, mode, tp_mesh_dim)) != DT_OK)
+    return st;
+  std::vector<gemm::HostGroup> groups;
+  if ((st = row_groups(X.layout, nullptr, &X, W, has_bias ? &B : nullptr, Y, mode, tp_mesh_dim, &groups)) != DT_OK)
+    return st;
+  if (groups.empty()) return DT_OK;
+  if ((st = bind_device_of(groups[0].out_ptr[0])) != DT_OK) return st;
+  return gemm::run_groups(groups, d_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ---- TP MLP -------------------------------------------------------------
+
+namespace {
+
+struct MlpPlan {
+  std::vector<int> x_slots;        // distinct x slots (one H block each)
+  std::vector<int64_t> h_offset;   // byte offset of each H block
+  std::vector<int64_t> h_rows;
+  int64_t F = 0;
+  size_t bytes = 0;
+};
+
+dt_status mlp_plan(const DTensor& X, const DTensor& Wg, int tp, MlpPlan* plan) {
+  const Layout& lx = X.layout;
+  if (lx.ndim < 1) return fail(DT_ERR_SHAPE, "x rank");
+  plan->F = Wg.layout.gshape[1];
+  std::set<int> seen;
+  int c[DT_MAX_MESH_DIMS];
+  size_t off = 0;
+  for (int r = 0; r < lx.mesh_size; ++r) {
+    lx.rank_coords(r, c);
+    const int s = lx.slot_of_coords(c);
+    if (!seen.insert(s).second) continue;
+    const SlotView& v = X.slots[s];
+    int64_t rows = 1;
+    for (int d = 0; d < lx.ndim - 1; ++d) rows *= v.shape[d];
+    plan->x_slots.push_back(s);
+    plan->h_offset.push_back((int64_t)off);
+    plan->h_rows.push_back(rows);
+    off += ((size_t)rows * (size_t)plan->F * 2 + 255) & ~size_t(255);
+  }
+  plan->bytes = off;
+  (void)tp;
+  return DT_OK;
+}
+
+}  // namespace
+
+dt_status dt_tp_mlp_workspace_size(const dt_dtensor* x, const dt_dtensor* w_gate, int32_t tp_mesh_dim,
+                                   size_t* bytes) {
+  clear_error();
+  if (!bytes) return fail(DT_ERR_INVALID_ARG, "bytes is NULL");
+  DTensor X, Wg;
+  dt_status st;
+  if ((st = parse_dtensor(x, &X, "x")) != DT_OK) return st;
+  if ((st = parse_dtensor(w_gate, &Wg, "w_gate")) != DT_OK) return st;
+  MlpPlan plan;
+  if ((st = mlp_plan(X, Wg, tp_mesh_dim, &plan)) != DT_OK) return st;
+  *bytes = plan.bytes;
+  return DT_OK;
+}
+
+dt_status dt_tp_mlp(const dt_dtensor* x, const dt_dtensor* w_gate, const dt_dtensor* w_up, const dt_dtensor* w_down,
+                    const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim, void* workspace, size_t workspace_bytes,
+                    int32_t* d_status, dt_stream_t stream) {
+  clear_error();
+  DTensor X, Wg, Wu, Wd, Y;
+  dt_status st;
+  if ((st = parse_dtensor(x, &X, "x")) != DT_OK) return st;
+  if ((st = parse_dtensor(w_gate, &Wg, "w_gate")) != DT_OK) return st;
+  if ((st = parse_dtensor(w_up, &Wu, "w_up")) != DT_OK) return st;
+  if ((st = parse_dtensor(w_down, &Wd, "w_down")) != DT_OK) return st;
+  if ((st = parse_dtensor(y, &Y, "y")) != DT_OK) return st;
+  const int tp = tp_mesh_dim;
+  if ((st = check_tp(tp, X.layout)) != DT_OK) return st;
+  const Layout& lx = X.layout;
+  if (lx.dtype != DT_BF16 || Wg.layout.dtype != DT_BF16 || Wu.layout.dtype != DT_BF16 || Wd.layout.dtype != DT_BF16)
+    return fail(DT_ERR_INVALID_ARG, "the TP MLP runs bf16 operands");
+  // gate and up: column-parallel with the same placement and shape
+  if (Wg.layout.ndim != 2 || Wu.layout.ndim != 2 || Wg.layout.gshape[0] != Wu.layout.gshape[0] ||
+      Wg.layout.gshape[1] != Wu.layout.gshape[1])
+    return fail(DT_ERR_SHAPE, "gate and up weights must have one shape");
+  for (int m = 0; m < lx.mesh_ndim; ++m)
+    if (!same_placement(Wg.layout, m, Wu.layout, m)) return fail(DT_ERR_PLACEMENT, "gate and up weights placed differently");
+  for (int m = 0; m < lx.mesh_ndim; ++m) {
+    if (m == tp) {
+      if (!lx.is_replicate(m)) return fail(DT_ERR_PLACEMENT, "MLP input must be Replicate on tp");
+      if (!Wg.layout.is_shard(m, 1)) return fail(DT_ERR_PLACEMENT, "gate/up weights [in, out] must be Shard(1) on tp");
+    } else if (!Wg.layout.is_replicate(m)) {
+      return fail(DT_ERR_PLACEMENT, "weights must be Replicate off tp");
+    } else if (lx.is_partial(m)) {
+      return fail(DT_ERR_PLACEMENT, "the MLP is not linear in a Partial input");
+    } else if (lx.kind[m] == DT_SHARD && lx.dim[m] == lx.ndim - 1) {
+      return fail(DT_ERR_PLACEMENT, "x may not be sharded on its last dim");
+    }
+  }
+  const int nd = lx.ndim;
+  if (lx.gshape[nd - 1] != Wg.layout.gshape[0]) return fail(DT_ERR_SHAPE, "x last dim != w_gate rows");
+  if (Wd.layout.ndim != 2 || Wd.layout.gshape[0] != Wg.layout.gshape[1]) return fail(DT_ERR_SHAPE, "w_down must be [ffn, out]");
+  MlpPlan plan;
+  if ((st = mlp_plan(X, Wg, tp, &plan)) != DT_OK) return st;
+  if (!workspace || workspace_bytes < plan.bytes)
+    return fail(DT_ERR_INVALID_ARG, "workspace of %zu bytes needed", plan.bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) % 256) return fail(DT_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  const int64_t F = plan.F;
+  if ((F * 2) % 16) return fail(DT_ERR_ALIGNMENT, "ffn width must be a multiple of 8");
+
+  // H as a layout: x's placements with the last dim of size F, Shard(-1) on tp.
+  dt_layout hl;
+  std::memset(&hl, 0, sizeof(hl));
+  hl.mesh_ndim = lx.mesh_ndim;
+  for (int m = 0; m < lx.mesh_ndim; ++m) {
+    hl.mesh_shape[m] = lx.mesh[m];
+    hl.placements[m].kind = lx.kind[m];
+    hl.placements[m].dim = lx.dim[m];
+    if (m == tp) {
+      hl.placements[m].kind = DT_SHARD;
+      hl.placements[m].dim = nd - 1;
+    }
+  }
+  hl.ndim = nd;
+  for (int d = 0; d < nd; ++d) hl.gshape[d] = lx.gshape[d];
+  hl.gshape[nd - 1] = F;
+  hl.dtype = DT_BF16;
+  Layout LH;
+  if ((st = parse_layout(&hl, &LH)) != DT_OK) return st;
+  // every H slot is a column block of its x slot's [rows, F] H block
+  std::vector<Mat> hmats(LH.nslots);
+  int c[DT_MAX_MESH_DIMS];
+  for (int s = 0; s < LH.nslots; ++s) {
+    LH.slot_coords(s, c);
+    const int xs = lx.slot_of_coords(c);
+    size_t bi = 0;
+    while (bi < plan.x_slots.size() && plan.x_slots[bi] != xs) ++bi;
+    const Box hb = LH.slot_box(s);
+    Mat m;
+    m.ptr = static_cast<char*>(workspace) + plan.h_offset[bi] + hb.off[nd - 1] * 2;
+    m.rows = plan.h_rows[bi];
+    m.cols = hb.size[nd - 1];
+    m.ld = F;
+    m.dtype = DT_BF16;
+    hmats[s] = m;
+  }
+  // 1) gate/up: one dual group per (x slot, tp shard)
+  std::vector<gemm::HostGroup> up_groups;
+  std::set<int> done;
+  for (int r = 0; r < lx.mesh_size; ++r) {
+    lx.rank_coords(r, c);
+    const int hs = LH.slot_of_coords(c);
+    if (!done.insert(hs).second) continue;
+    Mat a, bg, bu;
+    if ((st = slot_matrix(X.slots[lx.slot_of_coords(c)], nd, DT_BF16, &a, "x")) != DT_OK) return st;
+    if ((st = slot_matrix(Wg.slots[Wg.layout.slot_of_coords(c)], 2, DT_BF16, &bg, "w_gate")) != DT_OK) return st;
+    if ((st = slot_matrix(Wu.slots[Wu.layout.slot_of_coords(c)], 2, DT_BF16, &bu, "w_up")) != DT_OK) return st;
+    const Mat& h = hmats[hs];
+    if (bg.cols != h.cols || bu.cols != h.cols || a.cols != bg.rows || a.rows != h.rows)
+      return fail(DT_ERR_SHAPE, "gate/up local shapes disagree");
+    gemm::HostGroup g;
+    g.m = h.rows;
+    g.n = h.cols;
+    g.dual = true;
+    g.segs.push_back(gemm::HostSeg{a, bg, bu});
+    g.out_dtype = DT_BF16;
+    g.row_begin = {0};
+    g.out_ptr = {h.ptr};
+    g.out_ld = {h.ld};
+    up_groups.push_back(std::move(g));
+  }
+  // 2) down: row-parallel over the H shards
+  if ((st = check_row(LH, Wd.layout, nullptr, Y.layout, mode, tp)) != DT_OK) return st;
+  std::vector<gemm::HostGroup> down_groups;
+  if ((st = row_groups(LH, &hmats, nullptr, Wd, nullptr, Y, mode, tp, &down_groups)) != DT_OK) return st;
+  if (up_groups.empty()) return DT_OK;
+  if ((st = bind_device_of(workspace)) != DT_OK) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = gemm::run_groups(up_groups, d_status, s)) != DT_OK) return st;
+  return gemm::run_groups(down_groups, d_status, s);
+}
+
+}  // extern "C"

@@ -24,3 +24,11 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def lib():
+    """Build (if needed) and load libdt.so."""
+    from tensor_sharded_linear_gb300 import _lib, build
+    build.build()
+    return _lib.load()

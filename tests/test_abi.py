@@ -1,0 +1,152 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+symbol ``include/dt.h`` declares, answers layout queries like the oracle, and
+rejects bad calls on the host before any launch."""
+import ctypes as C
+import os
+import random
+import re
+
+import pytest
+
+from oracle import placement as opl
+from tensor_sharded_linear_gb300 import _lib as L
+
+from test_oracle_placement import random_layout
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "dt.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^DT_API\s+[\w\s\*]+?\b(dt_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(L.EXPORTS)
+
+
+def abi_layout(lay: opl.Layout, dtype=L.BF16):
+    a = L.Layout()
+    a.mesh_ndim = len(lay.mesh_shape)
+    for m, s in enumerate(lay.mesh_shape):
+        a.mesh_shape[m] = s
+    for m, p in enumerate(lay.placements):
+        if isinstance(p, opl.Shard):
+            a.placements[m].kind, a.placements[m].dim = L.SHARD, p.dim
+        elif isinstance(p, opl.Replicate):
+            a.placements[m].kind = L.REPLICATE
+        else:
+            a.placements[m].kind = L.PARTIAL
+    a.ndim = len(lay.gshape)
+    for d, s in enumerate(lay.gshape):
+        a.gshape[d] = s
+    a.dtype = dtype
+    a.materialize_replicas = int(lay.materialize_replicas)
+    return a
+
+
+def test_layout_queries_match_oracle(lib):
+    rng = random.Random(3)
+    for _ in range(400):
+        lay = random_layout(rng)
+        a = abi_layout(lay)
+        n = C.c_int32()
+        assert lib.dt_layout_nslots(C.byref(a), C.byref(n)) == L.OK
+        assert n.value == lay.nslots
+        for r in range(opl.mesh_size(lay.mesh_shape)):
+            s = C.c_int32()
+            assert lib.dt_layout_slot_of_rank(C.byref(a), r, C.byref(s)) == L.OK
+            assert s.value == lay.slot_of_rank(r)
+        for s in range(lay.nslots):
+            ls = (C.c_int64 * 4)()
+            go = (C.c_int64 * 4)()
+            assert lib.dt_layout_slot_box(C.byref(a), s, ls, go) == L.OK
+            box = lay.box(s)
+            nd = len(lay.gshape)
+            assert tuple(ls[:nd]) == tuple(sz for _, sz in box)
+            assert tuple(go[:nd]) == tuple(o for o, _ in box)
+
+
+def test_malformed_layouts_are_rejected(lib):
+    a = abi_layout(opl.Layout((2, 2), [opl.Shard(0), opl.Replicate()], (4, 4)))
+    a.placements[0].dim = 5
+    n = C.c_int32()
+    assert lib.dt_layout_nslots(C.byref(a), C.byref(n)) == L.ERR_INVALID_ARG
+    assert b"Shard(5)" in lib.dt_last_error()
+    a = abi_layout(opl.Layout((2,), [opl.Shard(0)], (4,)))
+    a.mesh_shape[0] = 0
+    assert lib.dt_layout_nslots(C.byref(a), C.byref(n)) == L.ERR_INVALID_ARG
+    a = abi_layout(opl.Layout((2,), [opl.Shard(0)], (4,)))
+    a.dtype = 9
+    assert lib.dt_layout_nslots(C.byref(a), C.byref(n)) == L.ERR_INVALID_ARG
+    s = C.c_int32()
+    a = abi_layout(opl.Layout((2,), [opl.Shard(0)], (4,)))
+    assert lib.dt_layout_slot_of_rank(C.byref(a), 2, C.byref(s)) == L.ERR_INVALID_ARG
+
+
+_FAKE = 0x7F0000000000  # never dereferenced: every call below fails on the host
+
+
+def fake_desc(lay: opl.Layout, dtype=L.BF16):
+    d = L.DTensorDesc()
+    d.layout = abi_layout(lay, dtype)
+    d.nslots = lay.nslots
+    ptrs = (C.c_void_p * lay.nslots)(*[_FAKE + 4096 * i for i in range(lay.nslots)])
+    d.slots = C.cast(ptrs, C.POINTER(C.c_void_p))
+    d.strides = None
+    d._keep = ptrs
+    return d
+
+
+def test_host_rejections_before_launch(lib):
+    mesh = (4,)
+    R, S0, S1, P = opl.Replicate(), opl.Shard(0), opl.Shard(1), opl.Partial()
+    # Shard -> Partial is not defined
+    src = fake_desc(opl.Layout(mesh, [S0], (8, 8)))
+    dst = fake_desc(opl.Layout(mesh, [P], (8, 8)))
+    assert lib.dt_redistribute(C.byref(src), C.byref(dst), None, None) == L.ERR_UNSUPPORTED
+    # global shapes must agree
+    dst = fake_desc(opl.Layout(mesh, [R], (8, 9)))
+    assert lib.dt_redistribute(C.byref(src), C.byref(dst), None, None) == L.ERR_SHAPE
+    # wrong slot count
+    bad = fake_desc(opl.Layout(mesh, [S0], (8, 8)))
+    bad.nslots = 3
+    assert lib.dt_redistribute(C.byref(bad), C.byref(src), None, None) == L.ERR_INVALID_ARG
+    # column-parallel input must be Replicate on tp (DTorch check_placement)
+    x = fake_desc(opl.Layout(mesh, [S1], (16, 32)))
+    w = fake_desc(opl.Layout(mesh, [S1], (32, 64)))
+    y = fake_desc(opl.Layout(mesh, [S1], (16, 64)))
+    assert lib.dt_column_parallel_linear(C.byref(x), C.byref(w), None, C.byref(y), 0, None, None) == L.ERR_PLACEMENT
+    assert b"Replicate" in lib.dt_last_error()
+    # row-parallel input must be Shard(-1) on tp
+    xr = fake_desc(opl.Layout(mesh, [R], (16, 32)))
+    wr = fake_desc(opl.Layout(mesh, [S0], (32, 64)))
+    yr = fake_desc(opl.Layout(mesh, [R], (16, 64)))
+    assert lib.dt_row_parallel_linear(C.byref(xr), C.byref(wr), None, C.byref(yr), L.TP_ALL_REDUCE, 0, None,
+                                      None) == L.ERR_PLACEMENT
+    # REDUCE_SCATTER output must be Shard(0)
+    xs = fake_desc(opl.Layout(mesh, [S1], (16, 32)))
+    assert lib.dt_row_parallel_linear(C.byref(xs), C.byref(wr), None, C.byref(yr), L.TP_REDUCE_SCATTER, 0, None,
+                                      None) == L.ERR_PLACEMENT
+    # shape mismatch: w rows != x cols
+    w_bad = fake_desc(opl.Layout(mesh, [S0], (31, 64)))
+    assert lib.dt_row_parallel_linear(C.byref(xs), C.byref(w_bad), None, C.byref(yr), L.TP_ALL_REDUCE, 0, None,
+                                      None) == L.ERR_SHAPE
+    # bad mode
+    assert lib.dt_row_parallel_linear(C.byref(xs), C.byref(wr), None, C.byref(yr), 7, 0, None, None) \
+        == L.ERR_INVALID_ARG
+    # embedding: table must be Shard(1) on tp
+    ids = fake_desc(opl.Layout(mesh, [R], (2, 3)), L.INT32)
+    table = fake_desc(opl.Layout(mesh, [S0], (100, 16)))
+    out = fake_desc(opl.Layout(mesh, [R], (2, 3, 16)))
+    assert lib.dt_tp_embedding(C.byref(ids), C.byref(table), C.byref(out), 0, None, None) == L.ERR_PLACEMENT
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.dt_status_string(s)
+    assert lib.dt_version() >= 100

@@ -1,0 +1,221 @@
+"""GPU parity of the tensor-parallel linears against the fp64 oracle.
+
+Tolerance (bf16 inputs, fp32 accumulation, unit-scale outputs), on the
+fp32-output variant of every kernel: max |y - y_oracle| <= 2e-3 and
+||y - y_oracle||_F / ||y_oracle||_F <= 1e-3.  The bf16-output variant of the
+same launch is checked two ways: it equals the round-to-nearest-even bf16 of
+the fp32 output bit for bit (one cast in the epilogue), and
+|y_bf16 - y_oracle| <= 2e-3 + 2^-8 |y_oracle| (half a bf16 ulp on top).
+"""
+import numpy as np
+import pytest
+import torch
+
+import tensor_sharded_linear_gb300 as tsl
+from oracle import bf16
+from oracle import linear as olin
+from oracle.placement import chunk_bounds
+from tensor_sharded_linear_gb300 import workloads
+
+from helpers import to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+ABS_TOL = 2e-3
+REL_FRO_TOL = 1e-3
+
+
+def check_fp32(got: np.ndarray, expect: np.ndarray, what=""):
+    got = got.astype(np.float64)
+    err = np.abs(got - expect)
+    assert np.isfinite(got).all(), what
+    mx = float(err.max()) if err.size else 0.0
+    fro = float(np.linalg.norm(got - expect) / max(np.linalg.norm(expect), 1e-30)) if err.size else 0.0
+    assert mx <= ABS_TOL, f"{what}: max abs err {mx}"
+    assert fro <= REL_FRO_TOL, f"{what}: rel Frobenius err {fro}"
+
+
+def check_bf16(got_bits: np.ndarray, fp32_out: np.ndarray, expect: np.ndarray, what=""):
+    np.testing.assert_array_equal(got_bits, bf16.round_rne(fp32_out), err_msg=f"{what}: bf16 != RNE(fp32)")
+    g = bf16.widen64(got_bits)
+    assert (np.abs(g - expect) <= ABS_TOL + 2.0 ** -8 * np.abs(expect)).all(), what
+
+
+def mesh1(p):
+    return tsl.DeviceMesh((p,), ("tp",))
+
+
+def col_dtensor(w_bits, p, dtype="bf16", views=False):
+    """[K, N] weight, Shard(1) over p: separate slots, or column views of one parent."""
+    K, N = w_bits.shape
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    if views:
+        parent = to_dev(w_bits, dtype)
+        slots = [parent[:, o:o + s] for o, s in chunk_bounds(N, p)]
+    else:
+        slots = [to_dev(np.ascontiguousarray(w_bits[:, o:o + s]), dtype) for o, s in chunk_bounds(N, p)]
+    return tsl.DTensor(slots, mesh1(p), [tsl.Shard(1)], (K, N), td)
+
+
+def row_dtensor(w_bits, p, dtype="bf16"):
+    K, N = w_bits.shape
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    slots = [to_dev(np.ascontiguousarray(w_bits[o:o + s]), dtype) for o, s in chunk_bounds(K, p)]
+    return tsl.DTensor(slots, mesh1(p), [tsl.Shard(0)], (K, N), td)
+
+
+def x_rep(x_bits, p, dtype="bf16"):
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    return tsl.DTensor([to_dev(x_bits, dtype)], mesh1(p), [tsl.Replicate()], x_bits.shape, td)
+
+
+def x_shard(x_bits, p, dtype="bf16"):
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    K = x_bits.shape[-1]
+    slots = [to_dev(np.ascontiguousarray(x_bits[..., o:o + s]), dtype) for o, s in chunk_bounds(K, p)]
+    return tsl.DTensor(slots, mesh1(p), [tsl.Shard(x_bits.ndim - 1)], x_bits.shape, td)
+
+
+def w64(bits):
+    return bf16.widen64(bits)
+
+
+# ---------------------------------------------------------------- worked example
+
+def test_worked_example_fp32(lib):
+    """x[3, 8] @ W[8, 12], 4 parts, seed 0: column and row equal dense x @ W."""
+    x, w = workloads.worked_example()
+    p = 4
+    xd = x_rep(x, p, "fp32")
+    y = tsl.column_parallel_linear(xd, col_dtensor(w, p, "fp32"))
+    got = np.concatenate([to_host(t, "fp32") for t in y.slots], axis=-1)
+    dense = x.astype(np.float64) @ w.astype(np.float64)
+    assert got.shape == (3, 12)
+    torch.testing.assert_close(torch.from_numpy(got), torch.from_numpy(dense.astype(np.float32)))
+    yr = tsl.row_parallel_linear(x_shard(x, p, "fp32"), row_dtensor(w, p, "fp32"), mode=tsl.ALL_REDUCE)
+    torch.testing.assert_close(torch.from_numpy(to_host(yr.slots[0], "fp32")), torch.from_numpy(dense.astype(np.float32)))
+
+
+# ---------------------------------------------------------------- column parallel
+
+@pytest.mark.parametrize("M,K,N,p,views", [(300, 200, 1056, 4, False), (128, 64, 256, 1, False),
+                                           (517, 328, 8 * 136, 8, True), (64, 1024, 4 * 264, 4, True)])
+def test_column_parallel(lib, M, K, N, p, views):
+    x = workloads.randn_bf16((M, K), 11)
+    w = workloads.randn_bf16((K, N), 12, (1.0 / K) ** 0.5)
+    b = workloads.randn_bf16((N,), 13, 0.5)
+    xd = x_rep(x, p)
+    wd = col_dtensor(w, p, views=views)
+    bd = tsl.DTensor([to_dev(np.ascontiguousarray(b[o:o + s]), "bf16") for o, s in chunk_bounds(N, p)], mesh1(p),
+                     [tsl.Shard(0)], (N,), torch.bfloat16)
+    y32 = tsl.column_parallel_linear(xd, wd, bd, out_dtype=torch.float32)
+    y16 = tsl.column_parallel_linear(xd, wd, bd)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    expect = olin.column_parallel(w64(x), [w64(w[:, o:o + s]) for o, s in chunk_bounds(N, p)],
+                                  [w64(b[o:o + s]) for o, s in chunk_bounds(N, p)])
+    for i in range(p):
+        f = to_host(y32.slots[i], "fp32")
+        check_fp32(f, expect[i], f"shard {i}")
+        check_bf16(to_host(y16.slots[i], "bf16"), f, expect[i], f"shard {i}")
+
+
+def test_column_parallel_multi_qkv_small(lib):
+    M, K, p = 384, 256, 4
+    x = workloads.randn_bf16((M, K), 21)
+    ws = [workloads.randn_bf16((K, K), 22 + j, (1.0 / K) ** 0.5) for j in range(3)]
+    xd = x_rep(x, p)
+    ys = tsl.column_parallel_linear_multi(xd, [col_dtensor(w, p) for w in ws], out_dtype=torch.float32)
+    for j, w in enumerate(ws):
+        expect = olin.column_parallel(w64(x), [w64(w[:, o:o + s]) for o, s in chunk_bounds(K, p)])
+        for i in range(p):
+            check_fp32(to_host(ys[j].slots[i], "fp32"), expect[i], f"w{j} shard {i}")
+
+
+def test_unaligned_shapes_use_cuda_cores(lib):
+    """Shard pitches TMA cannot describe (odd widths) run on the CUDA-core kernel."""
+    M, K, N, p = 33, 50, 30, 4
+    x = workloads.randn_bf16((M, K), 31)
+    w = workloads.randn_bf16((K, N), 32, (1.0 / K) ** 0.5)
+    y = tsl.column_parallel_linear(x_rep(x, p), col_dtensor(w, p), out_dtype=torch.float32)
+    expect = olin.column_parallel(w64(x), [w64(w[:, o:o + s]) for o, s in chunk_bounds(N, p)])
+    for i in range(p):
+        check_fp32(to_host(y.slots[i], "fp32"), expect[i], f"shard {i}")
+
+
+# ---------------------------------------------------------------- row parallel
+
+@pytest.mark.parametrize("mode", [tsl.ALL_REDUCE, tsl.REDUCE_SCATTER, tsl.PARTIAL])
+@pytest.mark.parametrize("M,K,N,p", [(300, 288, 320, 4), (256, 512, 512, 8), (130, 4 * 136, 200, 4)])
+def test_row_parallel(lib, mode, M, K, N, p):
+    x = workloads.randn_bf16((M, K), 41)
+    w = workloads.randn_bf16((K, N), 42, (1.0 / K) ** 0.5)
+    b = workloads.randn_bf16((N,), 43, 0.5)
+    bd = tsl.DTensor([to_dev(b, "bf16")], mesh1(p), [tsl.Replicate()], (N,), torch.bfloat16)
+    xd, wd = x_shard(x, p), row_dtensor(w, p)
+    y32 = tsl.row_parallel_linear(xd, wd, bd, mode=mode, out_dtype=torch.float32)
+    y16 = tsl.row_parallel_linear(xd, wd, bd, mode=mode)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    omode = {tsl.ALL_REDUCE: olin.ALL_REDUCE, tsl.REDUCE_SCATTER: olin.REDUCE_SCATTER, tsl.PARTIAL: olin.PARTIAL}[mode]
+    expect = olin.row_parallel([w64(x[:, o:o + s]) for o, s in chunk_bounds(K, p)],
+                               [w64(w[o:o + s]) for o, s in chunk_bounds(K, p)], w64(b), omode, parts=p)
+    assert len(expect) == len(y32.slots)
+    for i, e in enumerate(expect):
+        f = to_host(y32.slots[i], "fp32")
+        check_fp32(f, e, f"{mode} out {i}")
+        check_bf16(to_host(y16.slots[i], "bf16"), f, e, f"{mode} out {i}")
+
+
+def test_row_parallel_3d_reduce_scatter_on_batch(lib):
+    """x [B, S, K] Shard(-1): REDUCE_SCATTER splits dim 0 (batch) into row blocks of S rows."""
+    B, S_, K, N, p = 4, 96, 256, 192, 4
+    x = workloads.randn_bf16((B, S_, K), 51)
+    w = workloads.randn_bf16((K, N), 52, (1.0 / K) ** 0.5)
+    y = tsl.row_parallel_linear(x_shard(x, p), row_dtensor(w, p), mode=tsl.REDUCE_SCATTER, out_dtype=torch.float32)
+    dense = olin.row_sum([w64(x[..., o:o + s]) for o, s in chunk_bounds(K, p)],
+                         [w64(w[o:o + s]) for o, s in chunk_bounds(K, p)])
+    for i, (o, s) in enumerate(chunk_bounds(B, p)):
+        check_fp32(to_host(y.slots[i], "fp32"), dense[o:o + s], f"block {i}")
+
+
+# ---------------------------------------------------------------- MLP / attention
+
+@pytest.mark.parametrize("M,K,F,N,p,mode", [(256, 256, 8 * 136, 384, 8, tsl.ALL_REDUCE),
+                                            (200, 192, 4 * 96, 320, 4, tsl.REDUCE_SCATTER)])
+def test_tp_mlp_small(lib, M, K, F, N, p, mode):
+    x, wg, wu, wd = workloads.mlp_inputs(M, K, F, seed_base=600)
+    wd = workloads.randn_bf16((F, N), 604, (1.0 / F) ** 0.5)
+    xd = x_rep(x, p)
+    ws = torch.empty(tsl.tp_mlp_workspace_bytes(xd, col_dtensor(wg, p)), dtype=torch.uint8, device="cuda")
+    y = tsl.tp_mlp(xd, col_dtensor(wg, p), col_dtensor(wu, p), row_dtensor(wd, p), mode=mode,
+                   out_dtype=torch.float32, workspace=ws)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    omode = olin.ALL_REDUCE if mode == tsl.ALL_REDUCE else olin.REDUCE_SCATTER
+    cols = chunk_bounds(F, p)
+    expect, hs = olin.tp_mlp(w64(x), [w64(wg[:, o:o + s]) for o, s in cols], [w64(wu[:, o:o + s]) for o, s in cols],
+                             [w64(wd[o:o + s]) for o, s in cols], omode)
+    # H: bf16 of SiLU(g) * u, allowed one bf16 ulp where fp32 and fp64 round apart
+    h_gpu = bf16.widen64(to_host(tsl.api.mlp_hidden_view(xd, col_dtensor(wg, p), ws), "bf16"))
+    h_ref = bf16.widen64(np.concatenate(hs, axis=-1))
+    assert (np.abs(h_gpu - h_ref) <= 2.0 ** -7 * np.abs(h_ref) + 1e-6).all()
+    for i, e in enumerate(expect):
+        check_fp32(to_host(y.slots[i], "fp32"), e, f"mlp out {i}")
+
+
+def test_attention_projections_small(lib):
+    T, H, p = 512, 256, 4
+    x, wq, wk, wv, wo = workloads.attention_inputs(T, H, seed_base=650)
+    xd = x_rep(x, p)
+    o, q, k, v = tsl.tp_attention_projections(xd, col_dtensor(wq, p), col_dtensor(wk, p), col_dtensor(wv, p),
+                                              row_dtensor(wo, p), mode=tsl.REDUCE_SCATTER, out_dtype=torch.float32)
+    cols = chunk_bounds(H, p)
+    eo, eq, ek, ev = olin.attention_projections(w64(x), *[[w64(w[:, a:a + s]) for a, s in cols] for w in (wq, wk, wv)],
+                                                [w64(wo[a:a + s]) for a, s in cols], olin.REDUCE_SCATTER)
+    for i in range(p):
+        for got, ref in ((q, eq), (k, ek), (v, ev)):
+            g = bf16.widen64(to_host(got.slots[i], "bf16"))
+            r = bf16.widen64(ref[i])
+            assert (np.abs(g - r) <= 2.0 ** -7 * np.abs(r) + 1e-6).all()  # one bf16 ulp
+        check_fp32(to_host(o.slots[i], "fp32"), eo[i], f"o block {i}")
