@@ -253,6 +253,10 @@ DT_API dt_status dt_read_device_status(int32_t* bits, int32_t clear);
 /* Drop host-side caches (TMA descriptors, planned launches). */
 DT_API dt_status dt_clear_cache(void);
 
+/* Number of kernels this library has launched in this process so far
+ * (every successful launch on any stream counts once). */
+DT_API uint64_t dt_launch_count(void);
+
 /* Library version, as major * 10000 + minor * 100 + patch. */
 DT_API int32_t dt_version(void);
 

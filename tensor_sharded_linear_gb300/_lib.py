@@ -54,7 +54,7 @@ EXPORTS = [
     "dt_layout_nslots", "dt_layout_slot_of_rank", "dt_layout_slot_box", "dt_redistribute",
     "dt_tp_embedding", "dt_column_parallel_linear", "dt_column_parallel_linear_multi",
     "dt_row_parallel_linear", "dt_tp_mlp_workspace_size", "dt_tp_mlp", "dt_status_string",
-    "dt_last_error", "dt_read_device_status", "dt_clear_cache", "dt_version",
+    "dt_last_error", "dt_read_device_status", "dt_clear_cache", "dt_version", "dt_launch_count",
 ]
 
 _lib = None
@@ -97,6 +97,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
             "dt_read_device_status": (st, [P(C.c_int32), C.c_int32]),
             "dt_clear_cache": (st, []),
             "dt_version": (C.c_int32, []),
+            "dt_launch_count": (C.c_uint64, []),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)

@@ -1,6 +1,7 @@
 // Device binding, SM count and the library's own device status word.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "dt_internal.h"
@@ -43,6 +44,10 @@ int device_sm_count() {
   return cached[dev];
 }
 
+static std::atomic<uint64_t> g_launches{0};
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 int32_t* device_status_word(int32_t* user) {
   if (user) return user;
   void* p = nullptr;
@@ -56,6 +61,8 @@ int32_t* device_status_word(int32_t* user) {
 }  // namespace dt
 
 using namespace dt;
+
+extern "C" uint64_t dt_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 extern "C" dt_status dt_read_device_status(int32_t* bits, int32_t clear) {
   if (!bits) return fail(DT_ERR_INVALID_ARG, "bits is NULL");

@@ -100,5 +100,6 @@ dt_status parse_dtensor(const dt_dtensor* in, DTensor* out, const char* what);
 dt_status bind_device_of(const void* device_ptr);
 int device_sm_count();
 int32_t* device_status_word(int32_t* user);  // user if non-null, else the library word
+void count_launch();
 
 }  // namespace dt

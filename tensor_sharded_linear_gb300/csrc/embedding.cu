@@ -178,5 +178,6 @@ extern "C" dt_status dt_tp_embedding(const dt_dtensor* ids, const dt_dtensor* ta
   embedding_kernel<<<(int)blocks, EMB_THREADS, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(DT_ERR_CUDA, "embedding launch: %s", cudaGetErrorString(e));
+  count_launch();
   return DT_OK;
 }

@@ -286,6 +286,7 @@ dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStrea
       const int grid = std::min(tiles, sms);
       cudaError_t e = launch_tcgen05(p, grid, stream);
       if (e != cudaSuccess) return fail(DT_ERR_CUDA, "tcgen05 GEMM launch: %s", cudaGetErrorString(e));
+      count_launch();
     }
     gi = g_end;
   }
@@ -345,6 +346,7 @@ dt_status run_simt(std::vector<HostGroup>& groups, cudaStream_t stream) {
       simt_gemm_kernel<<<grid, S_THREADS, 0, stream>>>(p);
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return fail(DT_ERR_CUDA, "CUDA-core GEMM launch: %s", cudaGetErrorString(e));
+      count_launch();
     }
     gi = g_end;
   }

@@ -515,6 +515,7 @@ extern "C" dt_status dt_redistribute(const dt_dtensor* src, const dt_dtensor* ds
       rd_kernel<false><<<grid, RD_THREADS, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(DT_ERR_CUDA, "redistribute launch: %s", cudaGetErrorString(e));
+    count_launch();
   }
   return DT_OK;
   };
