@@ -32,6 +32,8 @@ constexpr int RD_MAX_REFS = 256;
 constexpr int RD_MAX_SRC = 16;
 constexpr int RD_THREADS = 256;
 constexpr int RD_WARPS = RD_THREADS / 32;
+constexpr int COPY_SEG_BYTES = 4096;  // one warp moves up to 4 KiB of a row per work item
+constexpr int SUM_SEG_BYTES = 2048;   // of the destination, for Partial sums
 
 struct RdSlot {
   char* ptr;
@@ -39,15 +41,18 @@ struct RdSlot {
 };
 
 // One box: `ext` elements per (padded) dim, taken from `nsrc` sources (rank
-// order) and written to one destination slot.  nsrc == 0 writes zeros.
+// order) and written to one destination slot; nsrc == 0 writes zeros.  The
+// box is cut into work items of (row, segment): rows are the outer three
+// padded dims, a segment is `seg_elems` consecutive elements of a row.
 struct RdTask {
   int64_t ext[4];
   int64_t dst_off;
-  int64_t chunk_begin;
+  int64_t item_begin;
+  int64_t seg_elems;
   int32_t dst_slot;
   int32_t nsrc;
   int32_t ref_begin;
-  int32_t rows_per_chunk;
+  int32_t segs_per_row;
 };
 
 struct RdRef {
@@ -61,7 +66,7 @@ struct RdParams {
   RdSlot src[DT_MAX_SLOTS];
   RdTask task[RD_MAX_TASKS];
   RdRef ref[RD_MAX_REFS];
-  int64_t nchunks;
+  int64_t nitems;
   int32_t ntasks;
   int32_t dtype;
   int32_t esize;
@@ -73,40 +78,6 @@ struct RdParams {
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(uint4* p, uint4 v) { __stcs(p, v); }
 
-// Byte copy of one row with unit inner strides.  Both ends are moved in the
-// widest unit U (16, 8, 4 or the element size) for which source and
-// destination share their misalignment; the head up to the first U-aligned
-// destination byte and the tail are moved element by element.
-template <int U>
-__device__ __forceinline__ void copy_body(char* d, const char* s, int64_t nunits, int lane) {
-  if constexpr (U == 16) {
-    uint4* dv = reinterpret_cast<uint4*>(d);
-    const uint4* sv = reinterpret_cast<const uint4*>(s);
-    int64_t i = lane;
-    for (; i + 96 < nunits; i += 128) {
-      uint4 a = ld_stream(sv + i), b = ld_stream(sv + i + 32), c = ld_stream(sv + i + 64), e = ld_stream(sv + i + 96);
-      st_stream(dv + i, a);
-      st_stream(dv + i + 32, b);
-      st_stream(dv + i + 64, c);
-      st_stream(dv + i + 96, e);
-    }
-    for (; i < nunits; i += 32) st_stream(dv + i, ld_stream(sv + i));
-  } else {
-    using T = typename std::conditional<U == 8, uint2, typename std::conditional<U == 4, uint32_t, uint16_t>::type>::type;
-    T* dv = reinterpret_cast<T*>(d);
-    const T* sv = reinterpret_cast<const T*>(s);
-    int64_t i = lane;
-    for (; i + 96 < nunits; i += 128) {
-      T a = sv[i], b = sv[i + 32], c = sv[i + 64], e = sv[i + 96];
-      dv[i] = a;
-      dv[i + 32] = b;
-      dv[i + 64] = c;
-      dv[i + 96] = e;
-    }
-    for (; i < nunits; i += 32) dv[i] = sv[i];
-  }
-}
-
 __device__ __forceinline__ void copy_elems(char* d, const char* s, int64_t n, int esize, int lane) {
   if (esize == 2) {
     for (int64_t i = lane; i < n; i += 32) reinterpret_cast<uint16_t*>(d)[i] = reinterpret_cast<const uint16_t*>(s)[i];
@@ -115,31 +86,95 @@ __device__ __forceinline__ void copy_elems(char* d, const char* s, int64_t n, in
   }
 }
 
-__device__ void copy_row(char* d, const char* s, int64_t n, int esize, int lane) {
+// 16-byte vectors, source and destination equally aligned: every lane keeps
+// up to 8 loads in flight before storing.
+__device__ __forceinline__ void copy_vec_aligned(uint4* dv, const uint4* sv, int64_t nvec, int lane) {
+  int64_t i = lane;
+  for (; i + 7 * 32 < nvec; i += 8 * 32) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = ld_stream(sv + i + 32 * u);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) st_stream(dv + i + 32 * u, v[u]);
+  }
+  for (; i < nvec; i += 32) st_stream(dv + i, ld_stream(sv + i));
+}
+
+// Bytes [delta, delta + 16) of the 32-byte pair (a, b).
+__device__ __forceinline__ uint4 realign(const uint4& a, const uint4& b, int delta) {
+  const uint32_t sh = (delta & 3) * 8;
+  const uint32_t c0 = a.x, c1 = a.y, c2 = a.z, c3 = a.w, c4 = b.x, c5 = b.y, c6 = b.z, c7 = b.w;
+  switch (delta >> 2) {
+    case 0:
+      return make_uint4(__funnelshift_r(c0, c1, sh), __funnelshift_r(c1, c2, sh), __funnelshift_r(c2, c3, sh),
+                        __funnelshift_r(c3, c4, sh));
+    case 1:
+      return make_uint4(__funnelshift_r(c1, c2, sh), __funnelshift_r(c2, c3, sh), __funnelshift_r(c3, c4, sh),
+                        __funnelshift_r(c4, c5, sh));
+    case 2:
+      return make_uint4(__funnelshift_r(c2, c3, sh), __funnelshift_r(c3, c4, sh), __funnelshift_r(c4, c5, sh),
+                        __funnelshift_r(c5, c6, sh));
+    default:
+      return make_uint4(__funnelshift_r(c3, c4, sh), __funnelshift_r(c4, c5, sh), __funnelshift_r(c5, c6, sh),
+                        __funnelshift_r(c6, c7, sh));
+  }
+}
+
+__device__ __forceinline__ uint4 shfl_down_vec(const uint4& v) {
+  return make_uint4(__shfl_down_sync(0xffffffffu, v.x, 1), __shfl_down_sync(0xffffffffu, v.y, 1),
+                    __shfl_down_sync(0xffffffffu, v.z, 1), __shfl_down_sync(0xffffffffu, v.w, 1));
+}
+
+// 16-byte destination vectors from a source `delta` (1..15) bytes past a
+// 16-byte boundary: each lane loads the aligned source vector under its
+// destination vector and takes the next one from its neighbour lane, so
+// every source byte is loaded once.  Only aligned vectors that hold at least
+// one byte of the source span are read.
+__device__ __forceinline__ void copy_vec_realign(uint4* dv, const char* s, int64_t nvec, int lane) {
+  const int delta = static_cast<int>(reinterpret_cast<uintptr_t>(s) & 15);
+  const uint4* sa = reinterpret_cast<const uint4*>(s - delta);
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int64_t base = 0; base < nvec; base += 4 * 32) {
+    uint4 a[4], b[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t j = base + 32 * u + lane;
+      a[u] = j <= nvec ? ld_stream(sa + j) : z;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t j = base + 32 * u + lane;
+      b[u] = shfl_down_vec(a[u]);
+      if (lane == 31) b[u] = j + 1 <= nvec ? ld_stream(sa + j + 1) : z;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t j = base + 32 * u + lane;
+      if (j < nvec) st_stream(dv + j, realign(a[u], b[u], delta));
+    }
+  }
+}
+
+// Copy n elements with unit strides.  The head up to the first 16-byte
+// aligned destination byte and the tail go element by element.
+__device__ void copy_span(char* d, const char* s, int64_t n, int esize, int lane) {
+  const uintptr_t da = reinterpret_cast<uintptr_t>(d);
   const int64_t nbytes = n * esize;
-  const uintptr_t da = reinterpret_cast<uintptr_t>(d), sa = reinterpret_cast<uintptr_t>(s);
-  int U = esize;
-  if (((da ^ sa) & 15) == 0) U = 16;
-  else if (((da ^ sa) & 7) == 0) U = 8;
-  else if (((da ^ sa) & 3) == 0) U = 4;
-  if (U < esize) U = esize;
-  int64_t head = (int64_t)((U - (da % U)) % U);
+  int64_t head = static_cast<int64_t>((16 - (da & 15)) & 15);
   if (head > nbytes) head = nbytes;
-  const int64_t units = (nbytes - head) / U;
-  const int64_t tail = nbytes - head - units * U;
+  const int64_t nvec = (nbytes - head) / 16;
+  const int64_t tail = nbytes - head - nvec * 16;
   copy_elems(d, s, head / esize, esize, lane);
   char* db = d + head;
   const char* sb = s + head;
-  switch (U) {
-    case 16: copy_body<16>(db, sb, units, lane); break;
-    case 8: copy_body<8>(db, sb, units, lane); break;
-    case 4: copy_body<4>(db, sb, units, lane); break;
-    default: copy_body<2>(db, sb, units, lane); break;
-  }
-  copy_elems(db + units * U, sb + units * U, tail / esize, esize, lane);
+  if ((reinterpret_cast<uintptr_t>(sb) & 15) == 0)
+    copy_vec_aligned(reinterpret_cast<uint4*>(db), reinterpret_cast<const uint4*>(sb), nvec, lane);
+  else
+    copy_vec_realign(reinterpret_cast<uint4*>(db), sb, nvec, lane);
+  copy_elems(db + nvec * 16, sb + nvec * 16, tail / esize, esize, lane);
 }
 
-__device__ void copy_row_strided(char* d, const char* s, int64_t n, int64_t dstr, int64_t sstr, int esize, int lane) {
+__device__ void copy_span_strided(char* d, const char* s, int64_t n, int64_t dstr, int64_t sstr, int esize, int lane) {
   if (esize == 2) {
     for (int64_t i = lane; i < n; i += 32)
       reinterpret_cast<uint16_t*>(d)[i * dstr] = reinterpret_cast<const uint16_t*>(s)[i * sstr];
@@ -149,11 +184,11 @@ __device__ void copy_row_strided(char* d, const char* s, int64_t n, int64_t dstr
   }
 }
 
-__device__ void zero_row(char* d, int64_t n, int64_t dstr, int esize, int lane) {
+__device__ void zero_span(char* d, int64_t n, int64_t dstr, int esize, int lane) {
   const uintptr_t da = reinterpret_cast<uintptr_t>(d);
   if (dstr == 1) {
     const int64_t nbytes = n * esize;
-    int64_t head = (int64_t)((16 - (da & 15)) & 15);
+    int64_t head = static_cast<int64_t>((16 - (da & 15)) & 15);
     if (head > nbytes) head = nbytes;
     const int64_t units = (nbytes - head) / 16;
     const int64_t tail = nbytes - head - units * 16;
@@ -185,135 +220,144 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float to_f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 __device__ __forceinline__ uint16_t from_f(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
 
-// Sum of nsrc partial rows in rank order, fp32 accumulation.  The first value
-// is taken as is; the rest are added with round-to-nearest fp32 adds.
-__device__ void sum_row(char* d, const char* const* s, int nsrc, int64_t n, int64_t dstr, const int64_t* sstr,
-                        int dtype, int lane) {
-  bool vec = dstr == 1;
-  const uintptr_t da = reinterpret_cast<uintptr_t>(d);
-  for (int k = 0; k < nsrc; ++k) {
-    vec = vec && sstr[k] == 1 && ((reinterpret_cast<uintptr_t>(s[k]) ^ da) & 15) == 0;
-  }
-  const int esize = dtype == DT_BF16 ? 2 : 4;
-  int64_t head = 0, units = 0;
-  if (vec) {
-    head = (int64_t)(((16 - (da & 15)) & 15) / esize);
-    if (head > n) head = n;
-    units = (n - head) * esize / 16;
-  }
-  const int64_t vec_end = head + units * (16 / esize);
-  auto scalar = [&](int64_t lo, int64_t hi) {
-    for (int64_t i = lo + lane; i < hi; i += 32) {
-      if (dtype == DT_BF16) {
-        float acc = to_f(reinterpret_cast<const uint16_t*>(s[0])[i * sstr[0]]);
-        for (int k = 1; k < nsrc; ++k)
-          acc = __fadd_rn(acc, to_f(reinterpret_cast<const uint16_t*>(s[k])[i * sstr[k]]));
-        reinterpret_cast<uint16_t*>(d)[i * dstr] = from_f(acc);
-      } else {
-        float acc = reinterpret_cast<const float*>(s[0])[i * sstr[0]];
-        for (int k = 1; k < nsrc; ++k) acc = __fadd_rn(acc, reinterpret_cast<const float*>(s[k])[i * sstr[k]]);
-        reinterpret_cast<float*>(d)[i * dstr] = acc;
-      }
-    }
-  };
-  if (!vec) {
-    scalar(0, n);
-    return;
-  }
-  scalar(0, head);
-  scalar(vec_end, n);
-  const int64_t hb = head * esize;
-  uint4* dv = reinterpret_cast<uint4*>(d + hb);
-  for (int64_t u = lane; u < units; u += 64) {
-    const bool two = u + 32 < units;
-    float a0[8], a1[8];
-    for (int k = 0; k < nsrc; ++k) {
-      const uint4* sv = reinterpret_cast<const uint4*>(s[k] + hb);
-      uint4 v0 = ld_stream(sv + u);
-      uint4 v1 = two ? ld_stream(sv + u + 32) : make_uint4(0, 0, 0, 0);
-      if (dtype == DT_BF16) {
-        const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
-        const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (k == 0) {
-            a0[2 * j] = bf16_lo(w0[j]);
-            a0[2 * j + 1] = bf16_hi(w0[j]);
-            a1[2 * j] = bf16_lo(w1[j]);
-            a1[2 * j + 1] = bf16_hi(w1[j]);
-          } else {
-            a0[2 * j] = __fadd_rn(a0[2 * j], bf16_lo(w0[j]));
-            a0[2 * j + 1] = __fadd_rn(a0[2 * j + 1], bf16_hi(w0[j]));
-            a1[2 * j] = __fadd_rn(a1[2 * j], bf16_lo(w1[j]));
-            a1[2 * j + 1] = __fadd_rn(a1[2 * j + 1], bf16_hi(w1[j]));
-          }
-        }
-      } else {
-        const float f0[4] = {__uint_as_float(v0.x), __uint_as_float(v0.y), __uint_as_float(v0.z), __uint_as_float(v0.w)};
-        const float f1[4] = {__uint_as_float(v1.x), __uint_as_float(v1.y), __uint_as_float(v1.z), __uint_as_float(v1.w)};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          a0[j] = k == 0 ? f0[j] : __fadd_rn(a0[j], f0[j]);
-          a1[j] = k == 0 ? f1[j] : __fadd_rn(a1[j], f1[j]);
-        }
-      }
-    }
-    uint4 o0, o1;
+// Element-wise Partial sum, rank order, fp32: the first value as is, the
+// others added with round-to-nearest fp32 adds; bf16 rounded once at the end.
+__device__ __forceinline__ void sum_elems(char* d, const char* const* s, int nsrc, int64_t lo, int64_t hi, int64_t dstr,
+                                          const int64_t* sstr, int dtype, int lane) {
+  for (int64_t i = lo + lane; i < hi; i += 32) {
     if (dtype == DT_BF16) {
-      o0 = make_uint4(pack_bf16x2(a0[0], a0[1]), pack_bf16x2(a0[2], a0[3]), pack_bf16x2(a0[4], a0[5]),
-                      pack_bf16x2(a0[6], a0[7]));
-      o1 = make_uint4(pack_bf16x2(a1[0], a1[1]), pack_bf16x2(a1[2], a1[3]), pack_bf16x2(a1[4], a1[5]),
-                      pack_bf16x2(a1[6], a1[7]));
+      float acc = to_f(reinterpret_cast<const uint16_t*>(s[0])[i * sstr[0]]);
+      for (int k = 1; k < nsrc; ++k) acc = __fadd_rn(acc, to_f(reinterpret_cast<const uint16_t*>(s[k])[i * sstr[k]]));
+      reinterpret_cast<uint16_t*>(d)[i * dstr] = from_f(acc);
     } else {
-      o0 = make_uint4(__float_as_uint(a0[0]), __float_as_uint(a0[1]), __float_as_uint(a0[2]), __float_as_uint(a0[3]));
-      o1 = make_uint4(__float_as_uint(a1[0]), __float_as_uint(a1[1]), __float_as_uint(a1[2]), __float_as_uint(a1[3]));
+      float acc = reinterpret_cast<const float*>(s[0])[i * sstr[0]];
+      for (int k = 1; k < nsrc; ++k) acc = __fadd_rn(acc, reinterpret_cast<const float*>(s[k])[i * sstr[k]]);
+      reinterpret_cast<float*>(d)[i * dstr] = acc;
     }
-    st_stream(dv + u, o0);
-    if (two) st_stream(dv + u + 32, o1);
   }
 }
 
-// SUM = false: every task copies (nsrc <= 1) or zero-fills; SUM = true: every
-// task adds nsrc >= 2 partial sources.  One instantiation per kind keeps the
-// copy path's register use low.
-template <bool SUM>
-__global__ void __launch_bounds__(RD_THREADS) rd_kernel(const __grid_constant__ RdParams p) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int esize = p.esize;
-  for (int64_t c = blockIdx.x; c < p.nchunks; c += gridDim.x) {
-    int t = 0;
-    while (t + 1 < p.ntasks && p.task[t + 1].chunk_begin <= c) ++t;
-    const RdTask& T = p.task[t];
-    const int64_t rows = T.ext[0] * T.ext[1] * T.ext[2];
-    const int64_t r0 = (c - T.chunk_begin) * T.rows_per_chunk;
-    const int64_t r1 = min(rows, r0 + (int64_t)T.rows_per_chunk);
-    const RdSlot& D = p.dst[T.dst_slot];
-    for (int64_t r = r0 + warp; r < r1; r += RD_WARPS) {
-      const int64_t i2 = r % T.ext[2];
-      const int64_t q = r / T.ext[2];
-      const int64_t i1 = q % T.ext[1];
-      const int64_t i0 = q / T.ext[1];
-      char* d = D.ptr + (T.dst_off + i0 * D.stride[0] + i1 * D.stride[1] + i2 * D.stride[2]) * esize;
-      const int64_t n = T.ext[3];
-      if (!SUM && T.nsrc == 0) {
-        zero_row(d, n, D.stride[3], esize, lane);
-      } else if (!SUM) {
-        const RdRef& R = p.ref[T.ref_begin];
-        const RdSlot& S = p.src[R.slot];
-        const char* s = S.ptr + (R.off + i0 * S.stride[0] + i1 * S.stride[1] + i2 * S.stride[2]) * esize;
-        if (D.stride[3] == 1 && S.stride[3] == 1) copy_row(d, s, n, esize, lane);
-        else copy_row_strided(d, s, n, D.stride[3], S.stride[3], esize, lane);
-      } else {
-        const char* sp[RD_MAX_SRC];
-        int64_t ss[RD_MAX_SRC];
-        for (int k = 0; k < T.nsrc; ++k) {
-          const RdRef& R = p.ref[T.ref_begin + k];
-          const RdSlot& S = p.src[R.slot];
-          sp[k] = S.ptr + (R.off + i0 * S.stride[0] + i1 * S.stride[1] + i2 * S.stride[2]) * esize;
-          ss[k] = S.stride[3];
-        }
-        sum_row(d, sp, T.nsrc, n, D.stride[3], ss, p.dtype, lane);
+// Vector body of the Partial sum with the source count fixed at compile time:
+// every lane issues NSRC x VPL 16-byte loads (at most 16) before the first add.
+template <int NSRC, int DTYPE>
+__device__ __forceinline__ void sum_vec(uint4* dv, const char* const* s, int64_t byte_off, int64_t nvec, int lane) {
+  constexpr int EPV = DTYPE == DT_BF16 ? 8 : 4;                        // elements per vector
+  constexpr int VPL = NSRC >= 8 ? 2 : 4;                               // vectors per lane per pass
+  const uint4* sv[NSRC];
+#pragma unroll
+  for (int k = 0; k < NSRC; ++k) sv[k] = reinterpret_cast<const uint4*>(s[k] + byte_off);
+  for (int64_t base = 0; base < nvec; base += VPL * 32) {
+    uint4 v[NSRC][VPL];
+#pragma unroll
+    for (int k = 0; k < NSRC; ++k)
+#pragma unroll
+      for (int u = 0; u < VPL; ++u) {
+        const int64_t j = base + 32 * u + lane;
+        v[k][u] = j < nvec ? ld_stream(sv[k] + j) : make_uint4(0, 0, 0, 0);
       }
+#pragma unroll
+    for (int u = 0; u < VPL; ++u) {
+      const int64_t j = base + 32 * u + lane;
+      if (j >= nvec) continue;
+      float acc[EPV];
+#pragma unroll
+      for (int k = 0; k < NSRC; ++k) {
+        const uint32_t w[4] = {v[k][u].x, v[k][u].y, v[k][u].z, v[k][u].w};
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          const float f = DTYPE == DT_BF16 ? ((e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1])) : __uint_as_float(w[e]);
+          acc[e] = k == 0 ? f : __fadd_rn(acc[e], f);
+        }
+      }
+      uint4 o;
+      if (DTYPE == DT_BF16)
+        o = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                       pack_bf16x2(acc[6], acc[7]));
+      else
+        o = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
+                       __float_as_uint(acc[3]));
+      st_stream(dv + j, o);
+    }
+  }
+}
+
+template <int DTYPE>
+__device__ __forceinline__ bool sum_vec_dispatch(uint4* dv, const char* const* s, int nsrc, int64_t off, int64_t nvec,
+                                                 int lane) {
+  switch (nsrc) {
+    case 2: sum_vec<2, DTYPE>(dv, s, off, nvec, lane); return true;
+    case 3: sum_vec<3, DTYPE>(dv, s, off, nvec, lane); return true;
+    case 4: sum_vec<4, DTYPE>(dv, s, off, nvec, lane); return true;
+    case 8: sum_vec<8, DTYPE>(dv, s, off, nvec, lane); return true;
+    default: return false;
+  }
+}
+
+__device__ void sum_span(char* d, const char* const* s, int nsrc, int64_t n, int64_t dstr, const int64_t* sstr,
+                         int dtype, int lane) {
+  const uintptr_t da = reinterpret_cast<uintptr_t>(d);
+  bool vec = dstr == 1;
+  for (int k = 0; k < nsrc; ++k)
+    vec = vec && sstr[k] == 1 && ((reinterpret_cast<uintptr_t>(s[k]) ^ da) & 15) == 0;
+  if (!vec) {
+    sum_elems(d, s, nsrc, 0, n, dstr, sstr, dtype, lane);
+    return;
+  }
+  const int esize = dtype == DT_BF16 ? 2 : 4;
+  int64_t head = static_cast<int64_t>(((16 - (da & 15)) & 15) / esize);
+  if (head > n) head = n;
+  const int64_t nvec = (n - head) * esize / 16;
+  const int64_t vec_end = head + nvec * (16 / esize);
+  sum_elems(d, s, nsrc, 0, head, 1, sstr, dtype, lane);
+  sum_elems(d, s, nsrc, vec_end, n, 1, sstr, dtype, lane);
+  uint4* dv = reinterpret_cast<uint4*>(d + head * esize);
+  const bool done = dtype == DT_BF16 ? sum_vec_dispatch<DT_BF16>(dv, s, nsrc, head * esize, nvec, lane)
+                                     : sum_vec_dispatch<DT_FP32>(dv, s, nsrc, head * esize, nvec, lane);
+  if (!done) sum_elems(d, s, nsrc, head, vec_end, 1, sstr, dtype, lane);
+}
+
+// SUM = false: every task copies (nsrc == 1) or zero-fills (nsrc == 0);
+// SUM = true: every task adds nsrc >= 2 partial sources.  One instantiation
+// per kind keeps the copy path's register use low.  Warps take work items
+// (row, segment) in a grid-stride loop.
+template <bool SUM>
+__global__ void __launch_bounds__(RD_THREADS, SUM ? 2 : 3) rd_kernel(const __grid_constant__ RdParams p) {
+  const int lane = threadIdx.x & 31;
+  const int esize = p.esize;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * RD_WARPS;
+  int t = 0;
+  for (int64_t it = static_cast<int64_t>(blockIdx.x) * RD_WARPS + (threadIdx.x >> 5); it < p.nitems; it += nw) {
+    while (t + 1 < p.ntasks && p.task[t + 1].item_begin <= it) ++t;
+    const RdTask& T = p.task[t];
+    const int64_t local = it - T.item_begin;
+    const int64_t r = local / T.segs_per_row;
+    const int64_t e0 = (local - r * T.segs_per_row) * T.seg_elems;
+    const int64_t n = min(T.ext[3] - e0, T.seg_elems);
+    const int64_t i2 = r % T.ext[2];
+    const int64_t q = r / T.ext[2];
+    const int64_t i1 = q % T.ext[1];
+    const int64_t i0 = q / T.ext[1];
+    const RdSlot& D = p.dst[T.dst_slot];
+    char* d = D.ptr + (T.dst_off + i0 * D.stride[0] + i1 * D.stride[1] + i2 * D.stride[2] + e0 * D.stride[3]) * esize;
+    if (!SUM && T.nsrc == 0) {
+      zero_span(d, n, D.stride[3], esize, lane);
+    } else if (!SUM) {
+      const RdRef& R = p.ref[T.ref_begin];
+      const RdSlot& S = p.src[R.slot];
+      const char* s =
+          S.ptr + (R.off + i0 * S.stride[0] + i1 * S.stride[1] + i2 * S.stride[2] + e0 * S.stride[3]) * esize;
+      if (D.stride[3] == 1 && S.stride[3] == 1) copy_span(d, s, n, esize, lane);
+      else copy_span_strided(d, s, n, D.stride[3], S.stride[3], esize, lane);
+    } else {
+      const char* sp[RD_MAX_SRC];
+      int64_t ss[RD_MAX_SRC];
+      for (int k = 0; k < T.nsrc; ++k) {
+        const RdRef& R = p.ref[T.ref_begin + k];
+        const RdSlot& S = p.src[R.slot];
+        sp[k] = S.ptr + (R.off + i0 * S.stride[0] + i1 * S.stride[1] + i2 * S.stride[2] + e0 * S.stride[3]) * esize;
+        ss[k] = S.stride[3];
+      }
+      sum_span(d, sp, T.nsrc, n, D.stride[3], ss, p.dtype, lane);
     }
   }
 }
@@ -476,48 +520,53 @@ extern "C" dt_status dt_redistribute(const dt_dtensor* src, const dt_dtensor* ds
   for (int s = 0; s < ls.nslots; ++s) fill_slot(&p.src[s], S.slots[s], nd);
   p.dtype = ls.dtype;
   p.esize = ls.esize;
-  const int grid_cap = device_sm_count() * 8;
+  const int sms = device_sm_count();
 
   auto launch_all = [&](const std::vector<HostTask>& tasks, bool sum) -> dt_status {
-  size_t i = 0;
-  while (i < tasks.size()) {
-    int nt = 0, nref = 0;
-    int64_t chunks = 0;
-    for (; i < tasks.size() && nt < RD_MAX_TASKS; ++i) {
-      const HostTask& ht = tasks[i];
-      if (nref + (int)ht.src_slots.size() > RD_MAX_REFS) break;
-      RdTask& t = p.task[nt];
-      for (int d = 0; d < 4; ++d) t.ext[d] = d < pad ? 1 : ht.box.size[d - pad];
-      t.dst_slot = ht.dst_slot;
-      t.dst_off = local_offset(D.slots[ht.dst_slot], ht.box, nd);
-      t.nsrc = (int)ht.src_slots.size();
-      t.ref_begin = nref;
-      for (int k = 0; k < t.nsrc; ++k) {
-        p.ref[nref].slot = ht.src_slots[k];
-        p.ref[nref].off = local_offset(S.slots[ht.src_slots[k]], ht.box, nd);
-        ++nref;
+    size_t i = 0;
+    while (i < tasks.size()) {
+      int nt = 0, nref = 0;
+      int64_t items = 0;
+      for (; i < tasks.size() && nt < RD_MAX_TASKS; ++i) {
+        const HostTask& ht = tasks[i];
+        if (nref + (int)ht.src_slots.size() > RD_MAX_REFS) break;
+        RdTask& t = p.task[nt];
+        for (int d = 0; d < 4; ++d) t.ext[d] = d < pad ? 1 : ht.box.size[d - pad];
+        t.dst_slot = ht.dst_slot;
+        t.dst_off = local_offset(D.slots[ht.dst_slot], ht.box, nd);
+        t.nsrc = (int)ht.src_slots.size();
+        t.ref_begin = nref;
+        for (int k = 0; k < t.nsrc; ++k) {
+          p.ref[nref].slot = ht.src_slots[k];
+          p.ref[nref].off = local_offset(S.slots[ht.src_slots[k]], ht.box, nd);
+          ++nref;
+        }
+        // segments are whole 16-byte multiples so every segment of a row
+        // keeps the row's alignment
+        const int64_t seg_bytes = sum ? SUM_SEG_BYTES : COPY_SEG_BYTES;
+        t.seg_elems = seg_bytes / ls.esize;
+        const int64_t spr = std::max<int64_t>(1, (t.ext[3] + t.seg_elems - 1) / t.seg_elems);
+        if (spr > (1ll << 30)) return fail(DT_ERR_CAPACITY, "row of %lld elements", (long long)t.ext[3]);
+        t.segs_per_row = (int32_t)spr;
+        const int64_t rows = t.ext[0] * t.ext[1] * t.ext[2];
+        t.item_begin = items;
+        items += rows * spr;
+        ++nt;
       }
-      const int64_t row_bytes = std::max<int64_t>(1, t.ext[3] * ls.esize);
-      const int64_t rows = t.ext[0] * t.ext[1] * t.ext[2];
-      int64_t rpc = std::max<int64_t>(1, (32 * 1024) / row_bytes);
-      rpc = std::min<int64_t>(rpc, 1 << 20);
-      t.rows_per_chunk = (int32_t)rpc;
-      t.chunk_begin = chunks;
-      chunks += (rows + rpc - 1) / rpc;
-      ++nt;
+      p.ntasks = nt;
+      p.nitems = items;
+      const int64_t blocks = (items + RD_WARPS - 1) / RD_WARPS;
+      // one wave of resident CTAs (3 per SM for copies, 2 for sums), grid-stride over items
+      const int grid = (int)std::min<int64_t>(blocks, (int64_t)sms * (sum ? 2 : 3));
+      if (sum)
+        rd_kernel<true><<<grid, RD_THREADS, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+      else
+        rd_kernel<false><<<grid, RD_THREADS, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return fail(DT_ERR_CUDA, "redistribute launch: %s", cudaGetErrorString(e));
+      count_launch();
     }
-    p.ntasks = nt;
-    p.nchunks = chunks;
-    const int grid = (int)std::min<int64_t>(chunks, grid_cap);
-    if (sum)
-      rd_kernel<true><<<grid, RD_THREADS, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
-    else
-      rd_kernel<false><<<grid, RD_THREADS, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(DT_ERR_CUDA, "redistribute launch: %s", cudaGetErrorString(e));
-    count_launch();
-  }
-  return DT_OK;
+    return DT_OK;
   };
   if ((st = launch_all(copies, false)) != DT_OK) return st;
   if ((st = launch_all(sums, true)) != DT_OK) return st;

@@ -13,7 +13,7 @@ from oracle.placement import chunk_bounds
 from tensor_sharded_linear_gb300 import workloads
 
 from helpers import to_dev, to_host
-from test_gpu_linear import check_fp32, col_dtensor, mesh1, row_dtensor, w64, x_rep
+from test_gpu_linear import check_bf16_pair, check_fp32, col_dtensor, mesh1, row_dtensor, w64, x_rep
 
 pytestmark = pytest.mark.gpu
 
@@ -66,7 +66,6 @@ def test_attention_full_size(lib):
     got = np.concatenate([to_host(t, "fp32") for t in o.slots], axis=0)
     assert got.shape == (cfg["tokens"], H) and [t.shape[0] for t in o.slots] == [s for _, s in blocks]
     check_fp32(got[rows], eo[0], "o sampled rows")
-    for got_t, ref in ((q, eq), (k, ek), (v, ev)):
-        g = bf16.widen64(np.concatenate([to_host(t, "bf16") for t in got_t.slots], axis=-1)[rows])
-        r = bf16.widen64(np.concatenate(ref, axis=-1))
-        assert (np.abs(g - r) <= 2.0 ** -7 * np.abs(r) + 1e-6).all()
+    for name, got_t, ref in (("q", q, eq), ("k", k, ek), ("v", v, ev)):
+        g = np.concatenate([to_host(t, "bf16") for t in got_t.slots], axis=-1)[rows]
+        check_bf16_pair(g, np.concatenate(ref, axis=-1), f"{name} sampled rows")
