@@ -197,27 +197,6 @@ bool out_vec_ok(const HostGroup& g) {
   return true;
 }
 
-// Tile width choice: fewer, wider tiles unless the last wave of 256-wide
-// tiles leaves enough SMs idle that 128-wide tiles finish sooner.
-int choose_bn(const std::vector<HostGroup>& groups, size_t g0, size_t g1, int sms) {
-  double best_cost = 1e300;
-  int best = 256;
-  for (int bn : {256, 128}) {
-    int64_t tiles = 0;
-    for (size_t i = g0; i < g1; ++i) {
-      if (groups[i].dual) return 128;
-      tiles += ((groups[i].m + BM - 1) / BM) * ((groups[i].n + bn - 1) / bn);
-    }
-    const int64_t waves = (tiles + sms - 1) / sms;
-    const double cost = (double)waves * bn * (bn == 128 ? 1.12 : 1.0);
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = bn;
-    }
-  }
-  return best;
-}
-
 dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStream_t stream) {
   static thread_local Params p;
   const int sms = device_sm_count();
@@ -236,9 +215,21 @@ dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStrea
       ++g_end;
     }
     if (g_end == gi) return fail(DT_ERR_CAPACITY, "one GEMM group needs more than %d segments", MAX_SEGS);
-    const int bn = choose_bn(groups, gi, g_end, sms);
+    // 256-column tiles: one N=256 MMA per 16-deep K step reads each A row
+    // once for 256 outputs (128-wide tiles re-read A and halve the MMA work
+    // per pipeline stage)
+    const int bn = BN_MAX;
     int map_i = 0, seg_i = 0, tiles = 0;
     p.ngroups = 0;
+    int common_m = -1;
+    int64_t max_k = 0;
+    for (size_t g = gi; g < g_end; ++g) {
+      const int mt = (int)((groups[g].m + BM - 1) / BM);
+      common_m = (common_m == -1 || common_m == mt) ? mt : -2;
+      int64_t k = 0;
+      for (const HostSeg& s : groups[g].segs) k += s.a.cols;
+      max_k = std::max(max_k, k);
+    }
     for (size_t g = gi; g < g_end; ++g) {
       const HostGroup& H = groups[g];
       Group& G = p.groups[p.ngroups++];
@@ -282,6 +273,18 @@ dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStrea
     }
     p.total_tiles = tiles;
     p.status = status;
+    p.n_tile_begin[0] = 0;
+    for (int g = 0; g < p.ngroups; ++g) p.n_tile_begin[g + 1] = p.n_tile_begin[g] + p.groups[g].n_tiles;
+    p.m_tiles = common_m > 0 ? common_m : 0;
+    // band height: the band's A rows (band_m x 128 x K bf16) take about a
+    // quarter of L2, and a band holds at least one wave of tiles
+    {
+      const int64_t a_tile_bytes = (int64_t)BM * std::max<int64_t>(max_k, 1) * 2;
+      int band = (int)std::max<int64_t>(1, (32ll << 20) / a_tile_bytes);
+      const int total_n = std::max(1, p.n_tile_begin[p.ngroups]);
+      band = std::max(band, (sms + total_n - 1) / total_n);
+      p.band_m = std::max(1, std::min(band, p.m_tiles > 0 ? p.m_tiles : 1));
+    }
     if (tiles > 0) {
       const int grid = std::min(tiles, sms);
       cudaError_t e = launch_tcgen05(p, grid, stream);

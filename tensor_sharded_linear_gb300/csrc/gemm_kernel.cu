@@ -10,7 +10,24 @@ struct TileCoord {
   int g, m0, n0;
 };
 
+// Tile order.  When every group has the same M tiles (all groups of a
+// column-parallel launch share x; a row-parallel launch is one group), the
+// groups' N tiles form one sweep: a band of band_m M tiles visits every
+// (group, N tile) with M fastest, so concurrent CTAs share A rows and each
+// B panel is fetched once per band.  Otherwise each group is rastered on
+// its own in bands of GROUP_M M tiles.
 __device__ __forceinline__ TileCoord decode_tile(const Params& p, int t) {
+  if (p.m_tiles > 0) {
+    const int total_n = p.n_tile_begin[p.ngroups];
+    const int span = p.band_m * total_n;
+    const int first_m = (t / span) * p.band_m;
+    const int gm = min(p.band_m, p.m_tiles - first_m);
+    const int r = t % span;
+    const int jn = r / gm;  // N tile across all groups
+    int g = 0;
+    while (g + 1 < p.ngroups && p.n_tile_begin[g + 1] <= jn) ++g;
+    return TileCoord{g, (first_m + r % gm) * BM, (jn - p.n_tile_begin[g]) * p.groups[g].bn};
+  }
   int g = 0;
   while (g + 1 < p.ngroups && p.groups[g + 1].tile_begin <= t) ++g;
   const Group& G = p.groups[g];

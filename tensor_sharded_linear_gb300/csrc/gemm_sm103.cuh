@@ -44,7 +44,7 @@ constexpr int B_TILE_BYTES = BN_MAX * BK * 2; // 32 KiB
 constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 512;                // two 256-column accumulators
-constexpr int GROUP_M = 8;                    // tile raster: 8 M tiles per band
+constexpr int GROUP_M = 8;                    // per-group raster: 8 M tiles per band
 constexpr int MAX_MAPS = 48;
 constexpr int MAX_SEGS = 96;
 constexpr int MAX_GROUPS = 32;
@@ -71,7 +71,10 @@ struct Params {  // CUtensorMap carries its own 128-byte alignment
   CUtensorMap maps[MAX_MAPS];
   Seg segs[MAX_SEGS];
   Group groups[MAX_GROUPS];
+  int32_t n_tile_begin[MAX_GROUPS + 1];  // prefix sums of the groups' N tiles
   int32_t ngroups, total_tiles;
+  int32_t m_tiles;  // > 0: every group has this many M tiles, rastered together
+  int32_t band_m;   // M tiles per raster band
   int32_t* status;
 };
 
