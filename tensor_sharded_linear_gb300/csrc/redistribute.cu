@@ -78,14 +78,6 @@ struct RdParams {
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(uint4* p, uint4 v) { __stcs(p, v); }
 
-__device__ __forceinline__ void copy_elems(char* d, const char* s, int64_t n, int esize, int lane) {
-  if (esize == 2) {
-    for (int64_t i = lane; i < n; i += 32) reinterpret_cast<uint16_t*>(d)[i] = reinterpret_cast<const uint16_t*>(s)[i];
-  } else {
-    for (int64_t i = lane; i < n; i += 32) reinterpret_cast<uint32_t*>(d)[i] = reinterpret_cast<const uint32_t*>(s)[i];
-  }
-}
-
 // 16-byte vectors, source and destination equally aligned: every lane keeps
 // up to 8 loads in flight before storing.
 __device__ __forceinline__ void copy_vec_aligned(uint4* dv, const uint4* sv, int64_t nvec, int lane) {
@@ -155,8 +147,10 @@ __device__ __forceinline__ void copy_vec_realign(uint4* dv, const char* s, int64
   }
 }
 
-// Copy n elements with unit strides.  The head up to the first 16-byte
-// aligned destination byte and the tail go element by element.
+// Copy n elements with unit strides.  The elements before the first 16-byte
+// aligned destination byte (lanes 0..7) and after the last whole vector
+// (lanes 16..23) are loaded in the same pass as the vector body, so a
+// segment costs one memory round trip whatever its alignment.
 __device__ void copy_span(char* d, const char* s, int64_t n, int esize, int lane) {
   const uintptr_t da = reinterpret_cast<uintptr_t>(d);
   const int64_t nbytes = n * esize;
@@ -164,14 +158,22 @@ __device__ void copy_span(char* d, const char* s, int64_t n, int esize, int lane
   if (head > nbytes) head = nbytes;
   const int64_t nvec = (nbytes - head) / 16;
   const int64_t tail = nbytes - head - nvec * 16;
-  copy_elems(d, s, head / esize, esize, lane);
+  const int head_n = static_cast<int>(head / esize), tail_n = static_cast<int>(tail / esize);
+  int64_t edge = -1;  // element index this lane moves outside the vector body
+  if (lane < head_n) edge = lane;
+  else if (lane >= 16 && lane - 16 < tail_n) edge = (head + nvec * 16) / esize + (lane - 16);
+  uint32_t ev = 0;
+  if (edge >= 0) ev = esize == 2 ? reinterpret_cast<const uint16_t*>(s)[edge] : reinterpret_cast<const uint32_t*>(s)[edge];
   char* db = d + head;
   const char* sb = s + head;
   if ((reinterpret_cast<uintptr_t>(sb) & 15) == 0)
     copy_vec_aligned(reinterpret_cast<uint4*>(db), reinterpret_cast<const uint4*>(sb), nvec, lane);
   else
     copy_vec_realign(reinterpret_cast<uint4*>(db), sb, nvec, lane);
-  copy_elems(db + nvec * 16, sb + nvec * 16, tail / esize, esize, lane);
+  if (edge >= 0) {
+    if (esize == 2) reinterpret_cast<uint16_t*>(d)[edge] = static_cast<uint16_t>(ev);
+    else reinterpret_cast<uint32_t*>(d)[edge] = ev;
+  }
 }
 
 __device__ void copy_span_strided(char* d, const char* s, int64_t n, int64_t dstr, int64_t sstr, int esize, int lane) {
@@ -308,12 +310,27 @@ __device__ void sum_span(char* d, const char* const* s, int nsrc, int64_t n, int
   if (head > n) head = n;
   const int64_t nvec = (n - head) * esize / 16;
   const int64_t vec_end = head + nvec * (16 / esize);
-  sum_elems(d, s, nsrc, 0, head, 1, sstr, dtype, lane);
-  sum_elems(d, s, nsrc, vec_end, n, 1, sstr, dtype, lane);
+  // edge elements (lanes 0..7: head, lanes 16..23: tail): loads issued
+  // before the vector body's, summed and stored after it
+  int64_t edge = -1;
+  if (lane < head) edge = lane;
+  else if (lane >= 16 && vec_end + (lane - 16) < n) edge = vec_end + (lane - 16);
+  float ev[RD_MAX_SRC];
+  if (edge >= 0) {
+    for (int k = 0; k < nsrc; ++k)
+      ev[k] = dtype == DT_BF16 ? to_f(reinterpret_cast<const uint16_t*>(s[k])[edge])
+                               : reinterpret_cast<const float*>(s[k])[edge];
+  }
   uint4* dv = reinterpret_cast<uint4*>(d + head * esize);
   const bool done = dtype == DT_BF16 ? sum_vec_dispatch<DT_BF16>(dv, s, nsrc, head * esize, nvec, lane)
                                      : sum_vec_dispatch<DT_FP32>(dv, s, nsrc, head * esize, nvec, lane);
   if (!done) sum_elems(d, s, nsrc, head, vec_end, 1, sstr, dtype, lane);
+  if (edge >= 0) {
+    float acc = ev[0];
+    for (int k = 1; k < nsrc; ++k) acc = __fadd_rn(acc, ev[k]);
+    if (dtype == DT_BF16) reinterpret_cast<uint16_t*>(d)[edge] = from_f(acc);
+    else reinterpret_cast<float*>(d)[edge] = acc;
+  }
 }
 
 // SUM = false: every task copies (nsrc == 1) or zero-fills (nsrc == 0);
