@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
@@ -197,9 +198,24 @@ bool out_vec_ok(const HostGroup& g) {
   return true;
 }
 
+// The CTA-pair kernel (256 x 256 tiles on tcgen05 .cta_group::2) is the
+// default; DT_GEMM_PAIR=0 in the environment selects the single-CTA kernel
+// (128 x 256 tiles), e.g. to compare the two.
+bool use_pair_kernel() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("DT_GEMM_PAIR");
+    v = (e && e[0] == '0') ? 0 : 1;
+  }
+  return v == 1;
+}
+
 dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStream_t stream) {
   static thread_local Params p;
   const int sms = device_sm_count();
+  const bool pair = use_pair_kernel();
+  const int tile_m = pair ? PAIR_TILE_M : BM;
+  const int ctas = pair ? sms / 2 : sms;  // CTAs (single) or clusters (pair) in one wave
   size_t gi = 0;
   while (gi < groups.size()) {
     // pack as many groups as fit one parameter block
@@ -224,7 +240,7 @@ dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStrea
     int common_m = -1;
     int64_t max_k = 0;
     for (size_t g = gi; g < g_end; ++g) {
-      const int mt = (int)((groups[g].m + BM - 1) / BM);
+      const int mt = (int)((groups[g].m + tile_m - 1) / tile_m);
       common_m = (common_m == -1 || common_m == mt) ? mt : -2;
       int64_t k = 0;
       for (const HostSeg& s : groups[g].segs) k += s.a.cols;
@@ -236,7 +252,7 @@ dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStrea
       G.m = (int32_t)H.m;
       G.n = (int32_t)H.n;
       G.bn = H.dual ? 128 : bn;
-      G.m_tiles = (int32_t)((H.m + BM - 1) / BM);
+      G.m_tiles = (int32_t)((H.m + tile_m - 1) / tile_m);
       G.n_tiles = (int32_t)((H.n + G.bn - 1) / G.bn);
       G.tile_begin = tiles;
       tiles += G.m_tiles * G.n_tiles;
@@ -279,15 +295,15 @@ dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStrea
     // band height: the band's A rows (band_m x 128 x K bf16) take about a
     // quarter of L2, and a band holds at least one wave of tiles
     {
-      const int64_t a_tile_bytes = (int64_t)BM * std::max<int64_t>(max_k, 1) * 2;
+      const int64_t a_tile_bytes = (int64_t)tile_m * std::max<int64_t>(max_k, 1) * 2;
       int band = (int)std::max<int64_t>(1, (32ll << 20) / a_tile_bytes);
       const int total_n = std::max(1, p.n_tile_begin[p.ngroups]);
-      band = std::max(band, (sms + total_n - 1) / total_n);
+      band = std::max(band, (ctas + total_n - 1) / total_n);
       p.band_m = std::max(1, std::min(band, p.m_tiles > 0 ? p.m_tiles : 1));
     }
     if (tiles > 0) {
-      const int grid = std::min(tiles, sms);
-      cudaError_t e = launch_tcgen05(p, grid, stream);
+      const int grid = std::min(tiles, ctas);
+      cudaError_t e = pair ? launch_tcgen05_pair(p, grid, stream) : launch_tcgen05(p, grid, stream);
       if (e != cudaSuccess) return fail(DT_ERR_CUDA, "tcgen05 GEMM launch: %s", cudaGetErrorString(e));
       count_launch();
     }

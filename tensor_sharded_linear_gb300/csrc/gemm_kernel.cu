@@ -6,89 +6,6 @@
 namespace dt {
 namespace gemm {
 
-struct TileCoord {
-  int g, m0, n0;
-};
-
-// Tile order.  When every group has the same M tiles (all groups of a
-// column-parallel launch share x; a row-parallel launch is one group), the
-// groups' N tiles form one sweep: a band of band_m M tiles visits every
-// (group, N tile) with M fastest, so concurrent CTAs share A rows and each
-// B panel is fetched once per band.  Otherwise each group is rastered on
-// its own in bands of GROUP_M M tiles.
-__device__ __forceinline__ TileCoord decode_tile(const Params& p, int t) {
-  if (p.m_tiles > 0) {
-    const int total_n = p.n_tile_begin[p.ngroups];
-    const int span = p.band_m * total_n;
-    const int first_m = (t / span) * p.band_m;
-    const int gm = min(p.band_m, p.m_tiles - first_m);
-    const int r = t % span;
-    const int jn = r / gm;  // N tile across all groups
-    int g = 0;
-    while (g + 1 < p.ngroups && p.n_tile_begin[g + 1] <= jn) ++g;
-    return TileCoord{g, (first_m + r % gm) * BM, (jn - p.n_tile_begin[g]) * p.groups[g].bn};
-  }
-  int g = 0;
-  while (g + 1 < p.ngroups && p.groups[g + 1].tile_begin <= t) ++g;
-  const Group& G = p.groups[g];
-  const int local = t - G.tile_begin;
-  const int span = GROUP_M * G.n_tiles;
-  const int first_m = (local / span) * GROUP_M;
-  const int gm = min(GROUP_M, G.m_tiles - first_m);
-  const int r = local % span;
-  return TileCoord{g, (first_m + r % gm) * BM, (r / gm) * G.bn};
-}
-
-// MMA width of a tile: the gated MLP always uses both 128-column halves;
-// otherwise the tile's remaining columns rounded up to the MMA's N step of 16.
-__device__ __forceinline__ int tile_mma_n(const Group& G, int n0) {
-  if (G.dual) return 256;
-  int rem = G.n - n0;
-  rem = (rem + 15) & ~15;
-  return rem < G.bn ? rem : G.bn;
-}
-
-__device__ __forceinline__ float bias_at(const Group& G, int col) {
-  if (G.bias_dtype == DT_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(G.bias)[col]);
-  return reinterpret_cast<const float*>(G.bias)[col];
-}
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// Store 32 fp32 values of one output row at columns [col0, col0 + 32).
-__device__ __forceinline__ void store_row32(const Group& G, char* row_ptr, int col0, const float (&v)[32]) {
-  const int valid = min(32, G.n - col0);
-  if (valid <= 0) return;
-  if (G.out_dtype == DT_BF16) {
-    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(row_ptr) + col0;
-    if (valid == 32 && G.out_vec) {
-      uint4* o4 = reinterpret_cast<uint4*>(o);
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        o4[q] = make_uint4(pack2(v[8 * q + 0], v[8 * q + 1]), pack2(v[8 * q + 2], v[8 * q + 3]),
-                           pack2(v[8 * q + 4], v[8 * q + 5]), pack2(v[8 * q + 6], v[8 * q + 7]));
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < valid) o[i] = __float2bfloat16_rn(v[i]);
-    }
-  } else {
-    float* o = reinterpret_cast<float*>(row_ptr) + col0;
-    if (valid == 32 && G.out_vec) {
-      float4* o4 = reinterpret_cast<float4*>(o);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) o4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < valid) o[i] = v[i];
-    }
-  }
-}
-
 __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -140,7 +57,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
       int stage = 0;
       uint32_t phase = 0;
       for (int t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
-        const TileCoord tc = decode_tile(p, t);
+        const TileCoord tc = decode_tile<BM>(p, t);
         const Group& G = p.groups[tc.g];
         const int nmma = tile_mma_n(G, tc.n0);
         const int nchunks = (nmma + 63) / 64;
@@ -184,7 +101,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
       uint32_t tphase = 0;
       const uint32_t a_base = smem_u32(smem);
       for (int t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
-        const TileCoord tc = decode_tile(p, t);
+        const TileCoord tc = decode_tile<BM>(p, t);
         const Group& G = p.groups[tc.g];
         const uint32_t idesc = instr_desc(BM, tile_mma_n(G, tc.n0));
         if (!mbar_wait(&tempty[buf], tphase ^ 1u, abort_flag)) {
@@ -239,7 +156,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
     int buf = 0;
     uint32_t tphase = 0;
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-      const TileCoord tc = decode_tile(p, t);
+      const TileCoord tc = decode_tile<BM>(p, t);
       const Group& G = p.groups[tc.g];
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&tfull[buf], tphase, abort_flag) ? 1 : 0;
@@ -308,6 +225,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
   }
 
   // ------------------------------------------------------------ teardown
+  __syncwarp();  // lanes 1..31 of warps 0 and 1 wait here for their lane 0
   if (aborted && lane == 0) {
     atomicOr(p.status, DT_DEV_ERR_TIMEOUT);
   }

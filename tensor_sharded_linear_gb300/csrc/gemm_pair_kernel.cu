@@ -1,0 +1,289 @@
+// The tensor-parallel GEMM on CTA pairs: a cluster of two CTAs computes one
+// 256 x 256 tile with tcgen05.mma.cta_group::2 (M = 256: each CTA holds its
+// 128 rows of A and 128 of the 256 columns of B, and its 128 rows of the
+// accumulator in its own TMEM).  Per SM this stages 32 KiB per 64-deep K
+// step instead of 48 KiB for a 128 x 256 single-CTA tile, which halves the
+// B traffic into each SM and leaves room for 6 pipeline stages.
+//
+// Roles per CTA (192 threads): warp 0 TMA producer, warp 1 MMA issuer (rank
+// 0 only; it owns the pair's MMAs), warps 2..5 epilogue.  Barriers:
+//   full[s]    in rank 0: 2 arrivals (rank 0 with the byte count of both
+//              CTAs' loads, rank 1 plain) + the loads' bytes;
+//   empty[s]   in each CTA: 1 arrival, rank 0's MMA commit multicast to both;
+//   tfull[b]   in each CTA: 1 arrival, multicast commit after a tile's MMAs;
+//   tempty[b]  in rank 0: 8 arrivals, the 4 epilogue warps of each CTA.
+// Every wait is bounded as in the single-CTA kernel.
+#include "gemm_plan.h"
+#include "gemm_sm103.cuh"
+
+namespace dt {
+namespace gemm {
+
+__global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + PAIR_STAGES * PAIR_STAGE_BYTES);
+  uint64_t* empty = full + PAIR_STAGES;
+  uint64_t* tfull = empty + PAIR_STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int cid = static_cast<int>(cluster_id_x());
+  const int ncl = static_cast<int>(nclusters_x());
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PAIR_STAGES; ++s) {
+      mbar_init(&full[s], 2);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 8);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised, TMEM of both allocated
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  bool aborted = false;
+  int8_t issued_parity[PAIR_STAGES];
+#pragma unroll
+  for (int s = 0; s < PAIR_STAGES; ++s) issued_parity[s] = -1;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      for (int i = 0; i < p.ngroups; ++i) {
+        const Group& G = p.groups[i];
+        for (int s = G.seg_begin; s < G.seg_begin + G.seg_count && s < G.seg_begin + 2; ++s) {
+          prefetch_map(&p.maps[p.segs[s].a_map]);
+          prefetch_map(&p.maps[p.segs[s].b_map]);
+        }
+      }
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = cid; t < p.total_tiles && !aborted; t += ncl) {
+        const TileCoord tc = decode_tile<PAIR_TILE_M>(p, t);
+        const Group& G = p.groups[tc.g];
+        const int a_row = tc.m0 + static_cast<int>(rank) * BM;
+        // this CTA's B columns: plain tiles split N in halves; the gated MLP
+        // puts gate (rank 0) and up (rank 1) side by side
+        const int b_col = G.dual ? tc.n0 : tc.n0 + static_cast<int>(rank) * 128;
+        for (int si = G.seg_begin; si < G.seg_begin + G.seg_count && !aborted; ++si) {
+          const Seg& S = p.segs[si];
+          const CUtensorMap* bmap = &p.maps[(G.dual && rank == 1) ? S.b_map2 : S.b_map];
+          for (int kt = 0; kt < S.k_tiles; ++kt) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+              aborted = true;
+              *abort_flag = 1;
+              break;
+            }
+            const uint32_t full0 = mapa_shared(smem_u32(&full[stage]), 0);
+            if (rank == 0) mbar_expect_tx(&full[stage], 2 * PAIR_STAGE_BYTES);
+            else mbar_arrive_cluster(full0);
+            uint8_t* a = smem + stage * PAIR_STAGE_BYTES;
+            uint8_t* b = a + PAIR_A_BYTES;
+            tma_load_2d_pair(a, &p.maps[S.a_map], kt * BK, a_row, full0);
+            tma_load_2d_pair(b, bmap, b_col, kt * BK, full0);
+            tma_load_2d_pair(b + B_CHUNK_BYTES, bmap, b_col + 64, kt * BK, full0);
+            issued_parity[stage] = static_cast<int8_t>(phase);
+            if (++stage == PAIR_STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (rank 0)
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int buf = 0;
+      uint32_t tphase = 0;
+      const uint32_t a_base = smem_u32(smem);
+      const uint32_t idesc = instr_desc(PAIR_TILE_M, 256);
+      for (int t = cid; t < p.total_tiles && !aborted; t += ncl) {
+        const TileCoord tc = decode_tile<PAIR_TILE_M>(p, t);
+        const Group& G = p.groups[tc.g];
+        if (!mbar_wait(&tempty[buf], tphase ^ 1u, abort_flag)) {
+          aborted = true;
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN_MAX);
+        uint32_t acc = 0;
+        for (int si = G.seg_begin; si < G.seg_begin + G.seg_count && !aborted; ++si) {
+          const int kts = p.segs[si].k_tiles;
+          for (int kt = 0; kt < kts; ++kt) {
+            if (!mbar_wait(&full[stage], phase, abort_flag)) {
+              aborted = true;
+              *abort_flag = 1;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = a_base + stage * PAIR_STAGE_BYTES;
+            const uint32_t b_addr = a_addr + PAIR_A_BYTES;
+#pragma unroll
+            for (int j = 0; j < BK / 16; ++j) {
+              // same operand layouts as the single-CTA kernel; each CTA's
+              // B half is two 64-column chunks 8 KiB apart
+              const uint64_t adesc = smem_desc(a_addr + j * 32, 16, 1024);
+              const uint64_t bdesc = smem_desc(b_addr + j * 2048, B_CHUNK_BYTES, 1024);
+              mma_bf16_pair(d_tmem, adesc, bdesc, idesc, acc);
+              acc = 1;
+            }
+            mma_commit_pair_mc(&empty[stage], 0x3);
+            if (++stage == PAIR_STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        if (aborted) break;
+        mma_commit_pair_mc(&tfull[buf], 0x3);
+        if (++buf == 2) {
+          buf = 0;
+          tphase ^= 1u;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    const uint32_t tempty0[2] = {mapa_shared(smem_u32(&tempty[0]), 0), mapa_shared(smem_u32(&tempty[1]), 0)};
+    int buf = 0;
+    uint32_t tphase = 0;
+    for (int t = cid; t < p.total_tiles; t += ncl) {
+      const TileCoord tc = decode_tile<PAIR_TILE_M>(p, t);
+      const Group& G = p.groups[tc.g];
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&tfull[buf], tphase, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);  // tcgen05.ld below is warp-collective
+      if (!ok) {
+        aborted = true;
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int64_t r = tc.m0 + static_cast<int>(rank) * BM + row_in_tile;
+      char* row_ptr = nullptr;
+      if (r < G.m) {
+        int j = 0;
+        while (j + 1 < G.nout && G.out_row_begin[j + 1] <= r) ++j;
+        const int esize = G.out_dtype == DT_BF16 ? 2 : 4;
+        row_ptr = G.out_ptr[j] + (r - G.out_row_begin[j]) * G.out_ld[j] * esize;
+      }
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN_MAX);
+      if (!G.dual) {
+        const int ncols = min(256, G.n - tc.n0);
+        for (int c = 0; c < ncols; c += 32) {
+          uint32_t raw[32];
+          tmem_ld32(tbase + c, raw);
+          tmem_ld_wait();
+          if (row_ptr) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(raw[i]);
+            if (G.bias_dtype >= 0) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int col = tc.n0 + c + i;
+                if (col < G.n) v[i] += bias_at(G, col);
+              }
+            }
+            store_row32(G, row_ptr, tc.n0 + c, v);
+          }
+        }
+      } else {
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(tbase + c, g);
+          tmem_ld32(tbase + 128 + c, u);
+          tmem_ld_wait();
+          if (row_ptr) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float gv = __uint_as_float(g[i]);
+              const float uv = __uint_as_float(u[i]);
+              v[i] = gv / (1.0f + __expf(-gv)) * uv;  // SiLU(g) * u in fp32
+            }
+            store_row32(G, row_ptr, tc.n0 + c, v);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty0[buf]);
+      if (++buf == 2) {
+        buf = 0;
+        tphase ^= 1u;
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncwarp();  // lanes 1..31 of warps 0 and 1 wait here for their lane 0
+  if (aborted && lane == 0) atomicOr(p.status, DT_DEV_ERR_TIMEOUT);
+  if (warp == 0 && lane == 0 && aborted) {
+    // copies this CTA issued count on rank 0's barrier; give them a bounded
+    // time to land before the pair leaves
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 20000000ull) {
+    }
+  }
+  if (warp == 1 && lane == 0 && rank == 0) {
+    // every MMA of the pair has completed before either CTA frees TMEM
+    mma_commit_pair(drain);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < 100000000ull) {
+    }
+  }
+  tc_fence_before();
+  cluster_sync();  // no CTA leaves while its peer may still touch its smem or TMEM
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+}
+
+cudaError_t launch_tcgen05_pair(const Params& p, int clusters, cudaStream_t stream) {
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!configured[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(tcgen05_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tcgen05_gemm_pair_kernel, p);
+}
+
+}  // namespace gemm
+}  // namespace dt

@@ -31,6 +31,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/dt.h"
+
 namespace dt {
 namespace gemm {
 
@@ -216,6 +218,185 @@ __host__ __device__ constexpr uint32_t instr_desc(int m, int n) {
          | (1u << 16)                              // B MN-major
          | (static_cast<uint32_t>(n >> 3) << 17)   // N / 8
          | (static_cast<uint32_t>(m >> 4) << 24);  // M / 16
+}
+
+// ---------------------------------------------------------------- CTA-pair helpers
+// A cluster of two CTAs shares one MMA (tcgen05 .cta_group::2): rank 0 issues
+// it, each CTA holds half the operands and its half of the accumulator.
+
+constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_A_BYTES = BM * BK * 2;           // this CTA's 128 rows of A: 16 KiB
+constexpr int PAIR_B_BYTES = 128 * BK * 2;          // this CTA's 128 columns of B: 16 KiB
+constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
+constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + 1024 + 256;
+constexpr int PAIR_TILE_M = 2 * BM;                 // rows of one pair tile
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t nclusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+
+// Address, in the cluster's shared window, of the same object in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t cta_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(cta_addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// TMA load into this CTA's smem whose completion is counted on an mbarrier
+// that may live in the peer CTA (`bar` is a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                                 uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+// Issued by one warp in EACH CTA of the pair.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem of both CTAs] (+)= A[smem of both] * B[smem of both]; issued by rank 0.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the mbarrier at this smem offset in every CTA of `mask`
+// when all tcgen05 operations issued so far by this thread complete.
+__device__ __forceinline__ void mma_commit_pair_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// ---------------------------------------------------------------- tile helpers
+
+struct TileCoord {
+  int g, m0, n0;
+};
+
+// Tile order.  When every group has the same M tiles (all groups of a
+// column-parallel launch share x; a row-parallel launch is one group), the
+// groups' N tiles form one sweep: a band of band_m M tiles visits every
+// (group, N tile) with M fastest, so concurrent CTAs share A rows and each
+// B panel is fetched once per band.  Otherwise each group is rastered on
+// its own in bands of GROUP_M M tiles.
+template <int TILE_M>
+__device__ __forceinline__ TileCoord decode_tile(const Params& p, int t) {
+  if (p.m_tiles > 0) {
+    const int total_n = p.n_tile_begin[p.ngroups];
+    const int span = p.band_m * total_n;
+    const int first_m = (t / span) * p.band_m;
+    const int gm = min(p.band_m, p.m_tiles - first_m);
+    const int r = t % span;
+    const int jn = r / gm;  // N tile across all groups
+    int g = 0;
+    while (g + 1 < p.ngroups && p.n_tile_begin[g + 1] <= jn) ++g;
+    return TileCoord{g, (first_m + r % gm) * TILE_M, (jn - p.n_tile_begin[g]) * p.groups[g].bn};
+  }
+  int g = 0;
+  while (g + 1 < p.ngroups && p.groups[g + 1].tile_begin <= t) ++g;
+  const Group& G = p.groups[g];
+  const int local = t - G.tile_begin;
+  const int span = GROUP_M * G.n_tiles;
+  const int first_m = (local / span) * GROUP_M;
+  const int gm = min(GROUP_M, G.m_tiles - first_m);
+  const int r = local % span;
+  return TileCoord{g, (first_m + r % gm) * TILE_M, (r / gm) * G.bn};
+}
+
+// MMA width of a tile: the gated MLP always uses both 128-column halves;
+// otherwise the tile's remaining columns rounded up to the MMA's N step of 16.
+__device__ __forceinline__ int tile_mma_n(const Group& G, int n0) {
+  if (G.dual) return 256;
+  int rem = G.n - n0;
+  rem = (rem + 15) & ~15;
+  return rem < G.bn ? rem : G.bn;
+}
+
+__device__ __forceinline__ float bias_at(const Group& G, int col) {
+  if (G.bias_dtype == DT_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(G.bias)[col]);
+  return reinterpret_cast<const float*>(G.bias)[col];
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Store 32 fp32 values of one output row at columns [col0, col0 + 32).
+__device__ __forceinline__ void store_row32(const Group& G, char* row_ptr, int col0, const float (&v)[32]) {
+  const int valid = min(32, G.n - col0);
+  if (valid <= 0) return;
+  if (G.out_dtype == DT_BF16) {
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(row_ptr) + col0;
+    if (valid == 32 && G.out_vec) {
+      uint4* o4 = reinterpret_cast<uint4*>(o);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        o4[q] = make_uint4(pack2(v[8 * q + 0], v[8 * q + 1]), pack2(v[8 * q + 2], v[8 * q + 3]),
+                           pack2(v[8 * q + 4], v[8 * q + 5]), pack2(v[8 * q + 6], v[8 * q + 7]));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < valid) o[i] = __float2bfloat16_rn(v[i]);
+    }
+  } else {
+    float* o = reinterpret_cast<float*>(row_ptr) + col0;
+    if (valid == 32 && G.out_vec) {
+      float4* o4 = reinterpret_cast<float4*>(o);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) o4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < valid) o[i] = v[i];
+    }
+  }
 }
 
 }  // namespace gemm
