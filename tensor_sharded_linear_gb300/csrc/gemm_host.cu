@@ -213,9 +213,10 @@ bool use_pair_kernel() {
 dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStream_t stream) {
   static thread_local Params p;
   const int sms = device_sm_count();
-  const bool pair = use_pair_kernel();
+  const int max_clusters = use_pair_kernel() ? pair_max_clusters() : 0;
+  const bool pair = max_clusters > 0;
   const int tile_m = pair ? PAIR_TILE_M : BM;
-  const int ctas = pair ? sms / 2 : sms;  // CTAs (single) or clusters (pair) in one wave
+  const int ctas = pair ? max_clusters : sms;  // CTAs (single) or clusters (pair) in one wave
   size_t gi = 0;
   while (gi < groups.size()) {
     // pack as many groups as fit one parameter block

@@ -259,17 +259,55 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
   if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
-cudaError_t launch_tcgen05_pair(const Params& p, int clusters, cudaStream_t stream) {
-  static bool configured[64] = {};
+namespace {
+
+void pair_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int clusters, cudaStream_t stream) {
+  *cfg = cudaLaunchConfig_t{};
+  cfg->gridDim = dim3(2 * clusters, 1, 1);
+  cfg->blockDim = dim3(THREADS, 1, 1);
+  cfg->dynamicSmemBytes = PAIR_SMEM_BYTES;
+  cfg->stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
+}
+
+int g_max_clusters[64] = {};
+
+}  // namespace
+
+// Clusters that can be resident at once.  The kernel is persistent with a
+// static tile assignment, so launching more than this would run the extra
+// clusters as a second wave; SMs whose TPC partner is fused off cannot host
+// a pair, so this can be below SMs / 2.
+int pair_max_clusters() {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
-  if (!configured[dev]) {
-    cudaError_t e =
-        cudaFuncSetAttribute(tcgen05_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
+  if (!g_max_clusters[dev]) {
+    if (cudaFuncSetAttribute(tcgen05_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PAIR_SMEM_BYTES) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    pair_config(&cfg, attr, 1, nullptr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tcgen05_gemm_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return 0;
+    }
+    g_max_clusters[dev] = n;
   }
+  return g_max_clusters[dev];
+}
+
+cudaError_t launch_tcgen05_pair(const Params& p, int clusters, cudaStream_t stream) {
+  if (pair_max_clusters() <= 0) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);

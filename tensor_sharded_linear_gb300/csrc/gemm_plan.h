@@ -45,6 +45,7 @@ dt_status run_groups(std::vector<HostGroup>& groups, int32_t* d_status, cudaStre
 struct Params;
 cudaError_t launch_tcgen05(const Params& p, int grid, cudaStream_t stream);
 cudaError_t launch_tcgen05_pair(const Params& p, int clusters, cudaStream_t stream);
+int pair_max_clusters();  // co-resident clusters of the pair kernel (0: unavailable)
 
 }  // namespace gemm
 }  // namespace dt
