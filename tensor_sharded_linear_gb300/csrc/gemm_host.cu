@@ -290,6 +290,11 @@ dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStrea
     }
     p.total_tiles = tiles;
     p.status = status;
+#ifdef DT_GEMM_TRACE
+    p.trace = trace_ptr();
+#else
+    p.trace = nullptr;
+#endif
     p.n_tile_begin[0] = 0;
     for (int g = 0; g < p.ngroups; ++g) p.n_tile_begin[g + 1] = p.n_tile_begin[g] + p.groups[g].n_tiles;
     p.m_tiles = common_m > 0 ? common_m : 0;
@@ -373,6 +378,18 @@ dt_status run_simt(std::vector<HostGroup>& groups, cudaStream_t stream) {
   return DT_OK;
 }
 
+#ifdef DT_GEMM_TRACE
+__device__ unsigned long long g_trace[1024 * TRACE_SLOTS];
+unsigned long long* trace_ptr() {
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_trace) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return static_cast<unsigned long long*>(ptr);
+}
+#endif
+
 }  // namespace
 
 dt_status run_groups(std::vector<HostGroup>& groups, int32_t* d_status, cudaStream_t stream) {
@@ -407,6 +424,20 @@ dt_status run_groups(std::vector<HostGroup>& groups, int32_t* d_status, cudaStre
 
 }  // namespace gemm
 }  // namespace dt
+
+#ifdef DT_GEMM_TRACE
+// Traced builds only: copy (and optionally clear) the per-CTA wait records.
+extern "C" __attribute__((visibility("default"))) int dt_gemm_trace_read(unsigned long long* out, int n, int clear) {
+  using dt::gemm::g_trace;
+  if (n > 1024 * dt::gemm::TRACE_SLOTS) n = 1024 * dt::gemm::TRACE_SLOTS;
+  if (cudaMemcpyFromSymbol(out, g_trace, n * sizeof(unsigned long long)) != cudaSuccess) return -1;
+  if (clear) {
+    static unsigned long long zeros[1024 * dt::gemm::TRACE_SLOTS] = {};
+    if (cudaMemcpyToSymbol(g_trace, zeros, sizeof(zeros)) != cudaSuccess) return -1;
+  }
+  return n;
+}
+#endif
 
 extern "C" dt_status dt_clear_cache(void) {
   std::lock_guard<std::mutex> lk(dt::gemm::g_map_mu);

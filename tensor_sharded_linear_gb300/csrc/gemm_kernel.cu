@@ -40,6 +40,9 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
   const uint32_t tmem_base = *tmem_slot;
 
   bool aborted = false;
+#ifdef DT_GEMM_TRACE
+  const long long _trace_start = clock64();
+#endif
   int8_t issued_parity[STAGES];
 #pragma unroll
   for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
@@ -65,7 +68,13 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
         for (int si = G.seg_begin; si < G.seg_begin + G.seg_count && !aborted; ++si) {
           const Seg& S = p.segs[si];
           for (int kt = 0; kt < S.k_tiles; ++kt) {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+            bool _ok;
+            {
+              DT_TRACE_T0();
+              _ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
+              DT_TRACE_ADD(TR_PROD_EMPTY);
+            }
+            if (!_ok) {
               aborted = true;
               *abort_flag = 1;
               break;
@@ -104,7 +113,14 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
         const TileCoord tc = decode_tile<BM>(p, t);
         const Group& G = p.groups[tc.g];
         const uint32_t idesc = instr_desc(BM, tile_mma_n(G, tc.n0));
-        if (!mbar_wait(&tempty[buf], tphase ^ 1u, abort_flag)) {
+        bool _ok;
+        {
+          DT_TRACE_T0();
+          _ok = mbar_wait(&tempty[buf], tphase ^ 1u, abort_flag);
+          DT_TRACE_ADD(TR_MMA_TEMPTY);
+        }
+        DT_TRACE_COUNT(TR_TILES);
+        if (!_ok) {
           aborted = true;
           *abort_flag = 1;
           break;
@@ -115,7 +131,14 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
         for (int si = G.seg_begin; si < G.seg_begin + G.seg_count && !aborted; ++si) {
           const int kts = p.segs[si].k_tiles;
           for (int kt = 0; kt < kts; ++kt) {
-            if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            bool _okf;
+            {
+              DT_TRACE_T0();
+              _okf = mbar_wait(&full[stage], phase, abort_flag);
+              DT_TRACE_ADD(TR_MMA_FULL);
+            }
+            DT_TRACE_COUNT(TR_STAGES);
+            if (!_okf) {
               aborted = true;
               *abort_flag = 1;
               break;
@@ -159,7 +182,11 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
       const TileCoord tc = decode_tile<BM>(p, t);
       const Group& G = p.groups[tc.g];
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(&tfull[buf], tphase, abort_flag) ? 1 : 0;
+      if (lane == 0) {
+        DT_TRACE_T0();
+        ok = mbar_wait(&tfull[buf], tphase, abort_flag) ? 1 : 0;
+        if (warp == 2) DT_TRACE_ADD(TR_EPI_TFULL);
+      }
       ok = __shfl_sync(0xffffffffu, ok, 0);  // tcgen05.ld below is warp-collective
       if (!ok) {
         aborted = true;
@@ -226,6 +253,9 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
 
   // ------------------------------------------------------------ teardown
   __syncwarp();  // lanes 1..31 of warps 0 and 1 wait here for their lane 0
+#ifdef DT_GEMM_TRACE
+  if (threadIdx.x == 0 && p.trace) atomicAdd(&p.trace[blockIdx.x * TRACE_SLOTS + TR_TOTAL], (unsigned long long)(clock64() - _trace_start));
+#endif
   if (aborted && lane == 0) {
     atomicOr(p.status, DT_DEV_ERR_TIMEOUT);
   }

@@ -56,6 +56,9 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
   const uint32_t tmem_base = *tmem_slot;
 
   bool aborted = false;
+#ifdef DT_GEMM_TRACE
+  const long long _trace_start = clock64();
+#endif
   int8_t issued_parity[PAIR_STAGES];
 #pragma unroll
   for (int s = 0; s < PAIR_STAGES; ++s) issued_parity[s] = -1;
@@ -83,7 +86,13 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
           const Seg& S = p.segs[si];
           const CUtensorMap* bmap = &p.maps[(G.dual && rank == 1) ? S.b_map2 : S.b_map];
           for (int kt = 0; kt < S.k_tiles; ++kt) {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+            bool _ok;
+            {
+              DT_TRACE_T0();
+              _ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
+              DT_TRACE_ADD(TR_PROD_EMPTY);
+            }
+            if (!_ok) {
               aborted = true;
               *abort_flag = 1;
               break;
@@ -117,7 +126,14 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
       for (int t = cid; t < p.total_tiles && !aborted; t += ncl) {
         const TileCoord tc = decode_tile<PAIR_TILE_M>(p, t);
         const Group& G = p.groups[tc.g];
-        if (!mbar_wait(&tempty[buf], tphase ^ 1u, abort_flag)) {
+        bool _ok;
+        {
+          DT_TRACE_T0();
+          _ok = mbar_wait(&tempty[buf], tphase ^ 1u, abort_flag);
+          DT_TRACE_ADD(TR_MMA_TEMPTY);
+        }
+        DT_TRACE_COUNT(TR_TILES);
+        if (!_ok) {
           aborted = true;
           *abort_flag = 1;
           break;
@@ -128,7 +144,14 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
         for (int si = G.seg_begin; si < G.seg_begin + G.seg_count && !aborted; ++si) {
           const int kts = p.segs[si].k_tiles;
           for (int kt = 0; kt < kts; ++kt) {
-            if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            bool _okf;
+            {
+              DT_TRACE_T0();
+              _okf = mbar_wait(&full[stage], phase, abort_flag);
+              DT_TRACE_ADD(TR_MMA_FULL);
+            }
+            DT_TRACE_COUNT(TR_STAGES);
+            if (!_okf) {
               aborted = true;
               *abort_flag = 1;
               break;
@@ -171,7 +194,11 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
       const TileCoord tc = decode_tile<PAIR_TILE_M>(p, t);
       const Group& G = p.groups[tc.g];
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(&tfull[buf], tphase, abort_flag) ? 1 : 0;
+      if (lane == 0) {
+        DT_TRACE_T0();
+        ok = mbar_wait(&tfull[buf], tphase, abort_flag) ? 1 : 0;
+        if (warp == 2) DT_TRACE_ADD(TR_EPI_TFULL);
+      }
       ok = __shfl_sync(0xffffffffu, ok, 0);  // tcgen05.ld below is warp-collective
       if (!ok) {
         aborted = true;
@@ -238,6 +265,9 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
 
   // ------------------------------------------------------------ teardown
   __syncwarp();  // lanes 1..31 of warps 0 and 1 wait here for their lane 0
+#ifdef DT_GEMM_TRACE
+  if (threadIdx.x == 0 && p.trace) atomicAdd(&p.trace[blockIdx.x * TRACE_SLOTS + TR_TOTAL], (unsigned long long)(clock64() - _trace_start));
+#endif
   if (aborted && lane == 0) atomicOr(p.status, DT_DEV_ERR_TIMEOUT);
   if (warp == 0 && lane == 0 && aborted) {
     // copies this CTA issued count on rank 0's barrier; give them a bounded

@@ -69,6 +69,20 @@ struct Group {
   int64_t out_ld[MAX_OUT];  // elements
 };
 
+// Wait-time tracing (build with -DDT_GEMM_TRACE): every CTA adds the clock
+// cycles each role spends in each kind of barrier wait to its record in
+// Params::trace (TRACE_SLOTS uint64 per CTA, indexed by blockIdx.x).
+enum TraceSlot {
+  TR_TOTAL = 0,        // cycles from the first role loop to teardown (warp 0)
+  TR_PROD_EMPTY = 1,   // producer waiting for a free stage
+  TR_MMA_FULL = 2,     // MMA issuer waiting for a filled stage
+  TR_MMA_TEMPTY = 3,   // MMA issuer waiting for a drained accumulator
+  TR_EPI_TFULL = 4,    // epilogue (warp 2) waiting for a finished accumulator
+  TR_TILES = 5,        // tiles this CTA processed
+  TR_STAGES = 6,       // stages the MMA issuer consumed
+  TRACE_SLOTS = 8
+};
+
 struct Params {  // CUtensorMap carries its own 128-byte alignment
   CUtensorMap maps[MAX_MAPS];
   Seg segs[MAX_SEGS];
@@ -78,7 +92,26 @@ struct Params {  // CUtensorMap carries its own 128-byte alignment
   int32_t m_tiles;  // > 0: every group has this many M tiles, rastered together
   int32_t band_m;   // M tiles per raster band
   int32_t* status;
+  unsigned long long* trace;  // TRACE_SLOTS per CTA when built with DT_GEMM_TRACE, else unused
 };
+
+#ifdef DT_GEMM_TRACE
+#define DT_TRACE_T0() const long long _tr0 = clock64()
+#define DT_TRACE_ADD(slot) \
+  if (p.trace) atomicAdd(&p.trace[blockIdx.x * TRACE_SLOTS + (slot)], (unsigned long long)(clock64() - _tr0))
+#define DT_TRACE_COUNT(slot) \
+  if (p.trace) atomicAdd(&p.trace[blockIdx.x * TRACE_SLOTS + (slot)], 1ull)
+#else
+#define DT_TRACE_T0() \
+  do {            \
+  } while (0)
+#define DT_TRACE_ADD(slot) \
+  do {                     \
+  } while (0)
+#define DT_TRACE_COUNT(slot) \
+  do {                       \
+  } while (0)
+#endif
 
 // ---------------------------------------------------------------- PTX helpers
 
