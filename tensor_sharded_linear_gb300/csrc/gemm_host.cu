@@ -17,6 +17,18 @@ namespace dt {
 namespace gemm {
 namespace {
 
+#ifdef DT_GEMM_TRACE
+__device__ unsigned long long g_trace[1024 * TRACE_SLOTS];
+unsigned long long* trace_ptr() {
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_trace) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return static_cast<unsigned long long*>(ptr);
+}
+#endif
+
 // ------------------------------------------------------------ TMA descriptors
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -377,18 +389,6 @@ dt_status run_simt(std::vector<HostGroup>& groups, cudaStream_t stream) {
   }
   return DT_OK;
 }
-
-#ifdef DT_GEMM_TRACE
-__device__ unsigned long long g_trace[1024 * TRACE_SLOTS];
-unsigned long long* trace_ptr() {
-  void* ptr = nullptr;
-  if (cudaGetSymbolAddress(&ptr, g_trace) != cudaSuccess) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  return static_cast<unsigned long long*>(ptr);
-}
-#endif
 
 }  // namespace
 
