@@ -166,7 +166,7 @@ class ClockSampler:
 class Block:
     """Every tensor of one step, resident on one GPU, with prebuilt ABI descriptors."""
 
-    def __init__(self, device, only=("embedding", "redistribute", "mlp", "attention")):
+    def __init__(self, device, only=("embedding", "redistribute", "mlp", "attention"), weights_kmajor=False):
         import ctypes as C
 
         import tensor_sharded_linear_gb300 as tsl
@@ -182,6 +182,11 @@ class Block:
             if a.dtype == np.uint16:
                 return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(bf).to(device)
             return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+        def wdev(a):  # a [K, N] weight, stored [K, N] or (weights_kmajor) [N, K]
+            return dev(np.ascontiguousarray(a.T)).t() if weights_kmajor else dev(a)
+
+        self.wdev = wdev
 
         self.calls = []  # (name, kind, work, fn)
         self.h2d = []  # device tensors holding this step's activations
@@ -248,9 +253,10 @@ class Block:
         F = cfg["ffn"]
         fc = [(i * (F // P), F // P) for i in range(P)]
         xd = DTensor([dev(x)], tp8, [R], x.shape, bf)
-        wgd = DTensor([dev(wg[:, o:o + s]) for o, s in fc], tp8, [S1], wg.shape, bf)
-        wud = DTensor([dev(wu[:, o:o + s]) for o, s in fc], tp8, [S1], wu.shape, bf)
-        wdd = DTensor([dev(wd[o:o + s]) for o, s in fc], tp8, [S0], wd.shape, bf)
+        wdev = self.wdev
+        wgd = DTensor([wdev(wg[:, o:o + s]) for o, s in fc], tp8, [S1], wg.shape, bf)
+        wud = DTensor([wdev(wu[:, o:o + s]) for o, s in fc], tp8, [S1], wu.shape, bf)
+        wdd = DTensor([wdev(wd[o:o + s]) for o, s in fc], tp8, [S0], wd.shape, bf)
         yd = DTensor.empty(tp8, [R], (cfg["tokens"], cfg["hidden"]), bf, device=device)
         nbytes = tsl.tp_mlp_workspace_bytes(xd, wgd)
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
@@ -267,8 +273,9 @@ class Block:
         H = cfg["hidden"]
         hc = [(i * (H // P), H // P) for i in range(P)]
         xa = DTensor([dev(x)], tp4, [R], x.shape, bf)
-        wcols = [DTensor([dev(w[:, o:o + s]) for o, s in hc], tp4, [S1], w.shape, bf) for w in (wq, wk, wv)]
-        wod = DTensor([dev(wo[o:o + s]) for o, s in hc], tp4, [S0], wo.shape, bf)
+        wdev = self.wdev
+        wcols = [DTensor([wdev(w[:, o:o + s]) for o, s in hc], tp4, [S1], w.shape, bf) for w in (wq, wk, wv)]
+        wod = DTensor([wdev(wo[o:o + s]) for o, s in hc], tp4, [S0], wo.shape, bf)
         qkv = [DTensor.empty(tp4, [S1], (cfg["tokens"], H), bf, device=device) for _ in range(3)]
         od = DTensor.empty(tp4, [S0], (cfg["tokens"], H), bf, device=device)
         self.h2d += xa.slots

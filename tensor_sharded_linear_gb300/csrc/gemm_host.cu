@@ -101,7 +101,19 @@ dt_status encode_map(const Mat& m, int box_rows, CUtensorMap* out) {
   return DT_OK;
 }
 
-bool tma_ok(const Mat& m) {
+// The matrix as it lies in memory: rows x cols row-major with pitch ld
+// (a K-major weight [K, N] is stored as N rows of K).
+Mat stored(const Mat& m) {
+  if (!m.kmajor) return m;
+  Mat s = m;
+  s.rows = m.cols;
+  s.cols = m.rows;
+  s.kmajor = false;
+  return s;
+}
+
+bool tma_ok(const Mat& m0) {
+  const Mat m = stored(m0);
   return m.dtype == DT_BF16 && m.rows > 0 && m.cols > 0 && (reinterpret_cast<uintptr_t>(m.ptr) % 16) == 0 &&
          (m.ld * 2) % 16 == 0 && m.ld >= m.cols && m.rows < (1ll << 31) && m.cols < (1ll << 31);
 }
@@ -115,6 +127,7 @@ struct SSeg {
   const char* b;
   int64_t lda, ldb;
   int32_t k, dtype;
+  int32_t b_kmajor, pad;
 };
 
 struct SGroup {
@@ -160,7 +173,9 @@ __global__ void __launch_bounds__(S_THREADS) simt_gemm_kernel(const __grid_const
           As[kk][rr] = (row < G.m && k < S.k) ? load_elem(S.a, row * S.lda + k, S.dtype) : 0.f;
           const int cc = e % S_TILE, kb = e / S_TILE;
           const int64_t col = n0 + cc, kr = k0 + kb;
-          Bs[kb][cc] = (col < G.n && kr < S.k) ? load_elem(S.b, kr * S.ldb + col, S.dtype) : 0.f;
+          Bs[kb][cc] = (col < G.n && kr < S.k)
+                           ? load_elem(S.b, S.b_kmajor ? col * S.ldb + kr : kr * S.ldb + col, S.dtype)
+                           : 0.f;
         }
         __syncthreads();
 #pragma unroll
@@ -283,6 +298,10 @@ dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStrea
       G.bias = H.bias;
       G.bias_dtype = H.bias ? H.bias_dtype : -1;
       G.out_vec = out_vec_ok(H) ? 1 : 0;
+      G.b_kmajor = H.segs.empty() ? 0 : (H.segs[0].b.kmajor ? 1 : 0);
+      // K-major B boxes: 128 N rows per CTA of a pair or per gated-MLP half,
+      // 256 for a plain single-CTA tile; MN-major B boxes: 64 K rows
+      const int b_box_rows = G.b_kmajor ? ((pair || H.dual) ? 128 : 256) : BK;
       for (const HostSeg& s : H.segs) {
         Seg& S = p.segs[seg_i++];
         S.k_tiles = (int32_t)((s.a.cols + BK - 1) / BK);
@@ -290,12 +309,12 @@ dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStrea
         dt_status st = encode_map(s.a, BM, &p.maps[map_i++]);
         if (st != DT_OK) return st;
         S.b_map = map_i;
-        st = encode_map(s.b, BK, &p.maps[map_i++]);
+        st = encode_map(stored(s.b), b_box_rows, &p.maps[map_i++]);
         if (st != DT_OK) return st;
         S.b_map2 = S.b_map;
         if (H.dual) {
           S.b_map2 = map_i;
-          st = encode_map(s.b2, BK, &p.maps[map_i++]);
+          st = encode_map(stored(s.b2), b_box_rows, &p.maps[map_i++]);
           if (st != DT_OK) return st;
         }
       }
@@ -375,6 +394,7 @@ dt_status run_simt(std::vector<HostGroup>& groups, cudaStream_t stream) {
         S.ldb = s.b.ld;
         S.k = (int32_t)s.a.cols;
         S.dtype = s.a.dtype;
+        S.b_kmajor = s.b.kmajor ? 1 : 0;
       }
     }
     p.total_tiles = tiles;
@@ -412,6 +432,8 @@ dt_status run_groups(std::vector<HostGroup>& groups, int32_t* d_status, cudaStre
     if (g.segs.empty()) tc = false;
     for (const auto& s : g.segs) {
       if (!tma_ok(s.a) || !tma_ok(s.b) || (g.dual && !tma_ok(s.b2))) tc = false;
+      // one B major-ness per group (the kernel decides it per tile)
+      if (s.b.kmajor != g.segs[0].b.kmajor || (g.dual && s.b2.kmajor != s.b.kmajor)) tc = false;
     }
   }
   if (tc) {

@@ -64,7 +64,9 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
         const Group& G = p.groups[tc.g];
         const int nmma = tile_mma_n(G, tc.n0);
         const int nchunks = (nmma + 63) / 64;
-        const uint32_t bytes = A_TILE_BYTES + nchunks * B_CHUNK_BYTES;
+        // K-major B arrives as one 256-row box (two 128-row boxes for the
+        // gated MLP); MN-major B as 64-column chunks
+        const uint32_t bytes = A_TILE_BYTES + (G.b_kmajor ? B_TILE_BYTES : nchunks * B_CHUNK_BYTES);
         for (int si = G.seg_begin; si < G.seg_begin + G.seg_count && !aborted; ++si) {
           const Seg& S = p.segs[si];
           for (int kt = 0; kt < S.k_tiles; ++kt) {
@@ -83,7 +85,14 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
             uint8_t* a = smem + stage * STAGE_BYTES;
             uint8_t* b = a + A_TILE_BYTES;
             tma_load_2d(a, &p.maps[S.a_map], kt * BK, tc.m0, &full[stage]);
-            if (!G.dual) {
+            if (G.b_kmajor) {
+              if (!G.dual) {
+                tma_load_2d(b, &p.maps[S.b_map], kt * BK, tc.n0, &full[stage]);
+              } else {
+                tma_load_2d(b, &p.maps[S.b_map], kt * BK, tc.n0, &full[stage]);
+                tma_load_2d(b + B_TILE_BYTES / 2, &p.maps[S.b_map2], kt * BK, tc.n0, &full[stage]);
+              }
+            } else if (!G.dual) {
               for (int c = 0; c < nchunks; ++c)
                 tma_load_2d(b + c * B_CHUNK_BYTES, &p.maps[S.b_map], tc.n0 + 64 * c, kt * BK, &full[stage]);
             } else {
@@ -112,7 +121,8 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
       for (int t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
         const TileCoord tc = decode_tile<BM>(p, t);
         const Group& G = p.groups[tc.g];
-        const uint32_t idesc = instr_desc(BM, tile_mma_n(G, tc.n0));
+        const uint32_t idesc = instr_desc(BM, tile_mma_n(G, tc.n0), G.b_kmajor != 0);
+        const bool bk = G.b_kmajor != 0;
         bool _ok;
         {
           DT_TRACE_T0();
@@ -152,8 +162,11 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
               //    elements moves 32 B inside the swizzled row.
               // B: MN-major, 64-column chunks 8 KiB apart (LBO), 8-row K groups
               //    1024 B apart (SBO); a K step of 16 rows moves 2 KiB.
+              // K-major B is laid out like A: 128-byte rows of K, a K step of
+              // 16 moves 32 B.
               const uint64_t adesc = smem_desc(a_addr + j * 32, 16, 1024);
-              const uint64_t bdesc = smem_desc(b_addr + j * 2048, B_CHUNK_BYTES, 1024);
+              const uint64_t bdesc =
+                  bk ? smem_desc(b_addr + j * 32, 16, 1024) : smem_desc(b_addr + j * 2048, B_CHUNK_BYTES, 1024);
               mma_bf16(d_tmem, adesc, bdesc, idesc, acc);
               acc = 1;
             }

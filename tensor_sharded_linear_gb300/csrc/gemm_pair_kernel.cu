@@ -103,8 +103,12 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
             uint8_t* a = smem + stage * PAIR_STAGE_BYTES;
             uint8_t* b = a + PAIR_A_BYTES;
             tma_load_2d_pair(a, &p.maps[S.a_map], kt * BK, a_row, full0);
-            tma_load_2d_pair(b, bmap, b_col, kt * BK, full0);
-            tma_load_2d_pair(b + B_CHUNK_BYTES, bmap, b_col + 64, kt * BK, full0);
+            if (G.b_kmajor) {
+              tma_load_2d_pair(b, bmap, kt * BK, b_col, full0);  // 128 N rows of 64 K
+            } else {
+              tma_load_2d_pair(b, bmap, b_col, kt * BK, full0);
+              tma_load_2d_pair(b + B_CHUNK_BYTES, bmap, b_col + 64, kt * BK, full0);
+            }
             issued_parity[stage] = static_cast<int8_t>(phase);
             if (++stage == PAIR_STAGES) {
               stage = 0;
@@ -122,10 +126,11 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
       int buf = 0;
       uint32_t tphase = 0;
       const uint32_t a_base = smem_u32(smem);
-      const uint32_t idesc = instr_desc(PAIR_TILE_M, 256);
       for (int t = cid; t < p.total_tiles && !aborted; t += ncl) {
         const TileCoord tc = decode_tile<PAIR_TILE_M>(p, t);
         const Group& G = p.groups[tc.g];
+        const bool bk = G.b_kmajor != 0;
+        const uint32_t idesc = instr_desc(PAIR_TILE_M, 256, bk);
         bool _ok;
         {
           DT_TRACE_T0();
@@ -164,7 +169,8 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
               // same operand layouts as the single-CTA kernel; each CTA's
               // B half is two 64-column chunks 8 KiB apart
               const uint64_t adesc = smem_desc(a_addr + j * 32, 16, 1024);
-              const uint64_t bdesc = smem_desc(b_addr + j * 2048, B_CHUNK_BYTES, 1024);
+              const uint64_t bdesc =
+                  bk ? smem_desc(b_addr + j * 32, 16, 1024) : smem_desc(b_addr + j * 2048, B_CHUNK_BYTES, 1024);
               mma_bf16_pair(d_tmem, adesc, bdesc, idesc, acc);
               acc = 1;
             }

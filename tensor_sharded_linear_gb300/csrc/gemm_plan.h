@@ -13,11 +13,15 @@
 namespace dt {
 namespace gemm {
 
-// Row-major matrix view: element (r, c) at ptr + (r * ld + c) * esize.
+// Matrix view of rows x cols.  Row-major: element (r, c) at
+// ptr + (r * ld + c) * esize.  kmajor (weights only, rows = K): element
+// (k, n) at ptr + (n * ld + k) * esize -- the [out, in] storage of a weight,
+// passed as a transposed view.
 struct Mat {
   char* ptr = nullptr;
   int64_t rows = 0, cols = 0, ld = 0;
   int dtype = DT_BF16;
+  bool kmajor = false;
 };
 
 struct HostSeg {

@@ -62,7 +62,8 @@ struct Group {
   int32_t m, n, m_tiles, n_tiles;
   int32_t tile_begin, seg_begin, seg_count, bn;  // bn: output columns per tile
   int32_t dual, out_dtype, nout, bias_dtype;     // bias_dtype < 0: no bias
-  int32_t out_vec, pad0, pad1, pad2;             // out_vec: 16-byte stores allowed
+  int32_t out_vec, b_kmajor, pad1, pad2;         // out_vec: 16-byte stores allowed;
+                                                 // b_kmajor: B stored [N, K] (K contiguous)
   const void* bias;
   int64_t out_row_begin[MAX_OUT + 1];  // output row blocks: rows [begin[j], begin[j+1]) -> out j
   char* out_ptr[MAX_OUT];
@@ -242,13 +243,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 }
 
 // Instruction descriptor, kind::f16: fp32 D, bf16 A and B, A K-major,
-// B MN-major, shape M x N.
-__host__ __device__ constexpr uint32_t instr_desc(int m, int n) {
+// B MN-major ([in, out] weights) or K-major ([out, in] weights), M x N.
+__host__ __device__ constexpr uint32_t instr_desc(int m, int n, bool b_kmajor = false) {
   return (1u << 4)                                 // D format: f32
          | (1u << 7)                               // A format: bf16
          | (1u << 10)                              // B format: bf16
          | (0u << 15)                              // A K-major
-         | (1u << 16)                              // B MN-major
+         | ((b_kmajor ? 0u : 1u) << 16)            // B major-ness
          | (static_cast<uint32_t>(n >> 3) << 17)   // N / 8
          | (static_cast<uint32_t>(m >> 4) << 24);  // M / 16
 }

@@ -24,6 +24,11 @@ using gemm::HostGroup;
 using gemm::HostSeg;
 using gemm::Mat;
 
+// A [K, N] weight slot: row-major ([in, out] storage), or a transposed view
+// of [N, K] storage (unit stride along K: the [out, in] convention of
+// nn.Linear), which the GEMM reads as a K-major B operand.
+dt_status weight_matrix(const SlotView& v, int dtype, Mat* out, const char* what);
+
 // Matrix view of a slot: leading dims flattened to rows, last dim = cols.
 dt_status slot_matrix(const SlotView& v, int ndim, int dtype, Mat* out, const char* what) {
   Mat m;
@@ -45,6 +50,23 @@ dt_status slot_matrix(const SlotView& v, int ndim, int dtype, Mat* out, const ch
   if (m.rows > 1 && m.ld < m.cols) return fail(DT_ERR_UNSUPPORTED, "%s: rows overlap", what);
   *out = m;
   return DT_OK;
+}
+
+dt_status weight_matrix(const SlotView& v, int dtype, Mat* out, const char* what) {
+  const int64_t K = v.shape[0], N = v.shape[1];
+  if (N > 1 && K > 1 && v.stride[1] != 1 && v.stride[0] == 1) {
+    if (v.stride[1] < K) return fail(DT_ERR_UNSUPPORTED, "%s: columns overlap", what);
+    Mat m;
+    m.ptr = v.ptr;
+    m.dtype = dtype;
+    m.rows = K;
+    m.cols = N;
+    m.ld = v.stride[1];
+    m.kmajor = true;
+    *out = m;
+    return DT_OK;
+  }
+  return slot_matrix(v, 2, dtype, out, what);
 }
 
 bool same_mesh(const Layout& a, const Layout& b) {
@@ -144,7 +166,7 @@ dt_status add_column_groups(const DTensor& X, const ColumnSpec& c, std::vector<H
     Mat a, b, y;
     dt_status st = slot_matrix(xv, nd, lx.dtype, &a, "x");
     if (st != DT_OK) return st;
-    st = slot_matrix(wv, 2, c.w->layout.dtype, &b, "w");
+    st = weight_matrix(wv, c.w->layout.dtype, &b, "w");
     if (st != DT_OK) return st;
     st = slot_matrix(yv, nd, c.y->layout.dtype, &y, "y");
     if (st != DT_OK) return st;
@@ -236,7 +258,7 @@ dt_status row_groups(const Layout& lx, const std::vector<Mat>* x_mats, const DTe
       }
       x_row0 = lx.slot_box(xs).off[0];
       const SlotView& wv = W.slots[lw.slot_of_coords(cj)];
-      if ((st = slot_matrix(wv, 2, lw.dtype, &b, "w")) != DT_OK) return st;
+      if ((st = weight_matrix(wv, lw.dtype, &b, "w")) != DT_OK) return st;
       if (a.cols != b.rows) return fail(DT_ERR_SHAPE, "x shard width %lld != w shard rows %lld", (long long)a.cols, (long long)b.rows);
       if (j == 0) xm0 = a;
       if (a.rows != xm0.rows) return fail(DT_ERR_SHAPE, "x shards have different row counts");
@@ -550,8 +572,8 @@ dt_status dt_tp_mlp(const dt_dtensor* x, const dt_dtensor* w_gate, const dt_dten
     if (!done.insert(hs).second) continue;
     Mat a, bg, bu;
     if ((st = slot_matrix(X.slots[lx.slot_of_coords(c)], nd, DT_BF16, &a, "x")) != DT_OK) return st;
-    if ((st = slot_matrix(Wg.slots[Wg.layout.slot_of_coords(c)], 2, DT_BF16, &bg, "w_gate")) != DT_OK) return st;
-    if ((st = slot_matrix(Wu.slots[Wu.layout.slot_of_coords(c)], 2, DT_BF16, &bu, "w_up")) != DT_OK) return st;
+    if ((st = weight_matrix(Wg.slots[Wg.layout.slot_of_coords(c)], DT_BF16, &bg, "w_gate")) != DT_OK) return st;
+    if ((st = weight_matrix(Wu.slots[Wu.layout.slot_of_coords(c)], DT_BF16, &bu, "w_up")) != DT_OK) return st;
     const Mat& h = hmats[hs];
     if (bg.cols != h.cols || bu.cols != h.cols || a.cols != bg.rows || a.rows != h.rows)
       return fail(DT_ERR_SHAPE, "gate/up local shapes disagree");

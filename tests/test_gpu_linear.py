@@ -55,11 +55,18 @@ def mesh1(p):
     return tsl.DeviceMesh((p,), ("tp",))
 
 
-def col_dtensor(w_bits, p, dtype="bf16", views=False):
+def kmajor(a, dtype="bf16"):
+    """[K, N] as a transposed view of [N, K] storage (the [out, in] layout)."""
+    return to_dev(np.ascontiguousarray(a.T), dtype).t()
+
+
+def col_dtensor(w_bits, p, dtype="bf16", views=False, k_major=False):
     """[K, N] weight, Shard(1) over p: separate slots, or column views of one parent."""
     K, N = w_bits.shape
     td = torch.bfloat16 if dtype == "bf16" else torch.float32
-    if views:
+    if k_major:
+        slots = [kmajor(w_bits[:, o:o + s], dtype) for o, s in chunk_bounds(N, p)]
+    elif views:
         parent = to_dev(w_bits, dtype)
         slots = [parent[:, o:o + s] for o, s in chunk_bounds(N, p)]
     else:
@@ -67,10 +74,13 @@ def col_dtensor(w_bits, p, dtype="bf16", views=False):
     return tsl.DTensor(slots, mesh1(p), [tsl.Shard(1)], (K, N), td)
 
 
-def row_dtensor(w_bits, p, dtype="bf16"):
+def row_dtensor(w_bits, p, dtype="bf16", k_major=False):
     K, N = w_bits.shape
     td = torch.bfloat16 if dtype == "bf16" else torch.float32
-    slots = [to_dev(np.ascontiguousarray(w_bits[o:o + s]), dtype) for o, s in chunk_bounds(K, p)]
+    if k_major:
+        slots = [kmajor(w_bits[o:o + s], dtype) for o, s in chunk_bounds(K, p)]
+    else:
+        slots = [to_dev(np.ascontiguousarray(w_bits[o:o + s]), dtype) for o, s in chunk_bounds(K, p)]
     return tsl.DTensor(slots, mesh1(p), [tsl.Shard(0)], (K, N), td)
 
 
@@ -226,3 +236,53 @@ def test_attention_projections_small(lib):
         for name, got, ref in (("q", q, eq), ("k", k, ek), ("v", v, ev)):
             check_bf16_pair(to_host(got.slots[i], "bf16"), ref[i], f"{name} shard {i}")
         check_fp32(to_host(o.slots[i], "fp32"), eo[i], f"o block {i}")
+
+
+# ---------------------------------------------------------------- [out, in] weights (K-major B)
+
+@pytest.mark.parametrize("M,K,N,p", [(300, 200, 1056, 4), (517, 328, 8 * 136, 8)])
+def test_column_parallel_kmajor_weights(lib, M, K, N, p):
+    x = workloads.randn_bf16((M, K), 61)
+    w = workloads.randn_bf16((K, N), 62, (1.0 / K) ** 0.5)
+    y = tsl.column_parallel_linear(x_rep(x, p), col_dtensor(w, p, k_major=True), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    expect = olin.column_parallel(w64(x), [w64(w[:, o:o + s]) for o, s in chunk_bounds(N, p)])
+    for i in range(p):
+        check_fp32(to_host(y.slots[i], "fp32"), expect[i], f"shard {i}")
+
+
+@pytest.mark.parametrize("mode", [tsl.ALL_REDUCE, tsl.REDUCE_SCATTER])
+def test_row_parallel_kmajor_weights(lib, mode):
+    M, K, N, p = 300, 288, 320, 4
+    x = workloads.randn_bf16((M, K), 71)
+    w = workloads.randn_bf16((K, N), 72, (1.0 / K) ** 0.5)
+    y = tsl.row_parallel_linear(x_shard(x, p), row_dtensor(w, p, k_major=True), mode=mode, out_dtype=torch.float32)
+    omode = olin.ALL_REDUCE if mode == tsl.ALL_REDUCE else olin.REDUCE_SCATTER
+    expect = olin.row_parallel([w64(x[:, o:o + s]) for o, s in chunk_bounds(K, p)],
+                               [w64(w[o:o + s]) for o, s in chunk_bounds(K, p)], None, omode, parts=p)
+    for i, e in enumerate(expect):
+        check_fp32(to_host(y.slots[i], "fp32"), e, f"{mode} out {i}")
+
+
+def test_tp_mlp_kmajor_weights(lib):
+    M, K, F, N, p = 256, 256, 8 * 136, 384, 8
+    x, wg, wu, _ = workloads.mlp_inputs(M, K, F, seed_base=680)
+    wd = workloads.randn_bf16((F, N), 684, (1.0 / F) ** 0.5)
+    xd = x_rep(x, p)
+    y = tsl.tp_mlp(xd, col_dtensor(wg, p, k_major=True), col_dtensor(wu, p, k_major=True),
+                   row_dtensor(wd, p, k_major=True), out_dtype=torch.float32)
+    cols = chunk_bounds(F, p)
+    (expect,), _ = olin.tp_mlp(w64(x), [w64(wg[:, o:o + s]) for o, s in cols], [w64(wu[:, o:o + s]) for o, s in cols],
+                               [w64(wd[o:o + s]) for o, s in cols])
+    check_fp32(to_host(y.slots[0], "fp32"), expect, "mlp")
+
+
+def test_unaligned_kmajor_weights_use_cuda_cores(lib):
+    M, K, N, p = 33, 50, 30, 4
+    x = workloads.randn_bf16((M, K), 81)
+    w = workloads.randn_bf16((K, N), 82, (1.0 / K) ** 0.5)
+    y = tsl.column_parallel_linear(x_rep(x, p), col_dtensor(w, p, k_major=True), out_dtype=torch.float32)
+    expect = olin.column_parallel(w64(x), [w64(w[:, o:o + s]) for o, s in chunk_bounds(N, p)])
+    for i in range(p):
+        check_fp32(to_host(y.slots[i], "fp32"), expect[i], f"shard {i}")
