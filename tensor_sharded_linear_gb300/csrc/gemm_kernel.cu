@@ -16,6 +16,11 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+#ifdef DT_GEMM_TRACE
+  volatile long long* t_issue = reinterpret_cast<volatile long long*>(drain + 2);   // per stage
+  volatile long long* t_commit = t_issue + STAGES;
+  for (int i = threadIdx.x; i < 2 * STAGES; i += blockDim.x) t_issue[i] = 0;
+#endif
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -75,6 +80,12 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
               DT_TRACE_T0();
               _ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
               DT_TRACE_ADD(TR_PROD_EMPTY);
+#ifdef DT_GEMM_TRACE
+              if (p.trace && t_commit[stage] != 0)
+                atomicAdd(&p.trace[blockIdx.x * TRACE_SLOTS + TR_COMMIT_LAT],
+                          (unsigned long long)(clock64() - t_commit[stage]));
+              t_issue[stage] = clock64();
+#endif
             }
             if (!_ok) {
               aborted = true;
@@ -146,6 +157,10 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
               DT_TRACE_T0();
               _okf = mbar_wait(&full[stage], phase, abort_flag);
               DT_TRACE_ADD(TR_MMA_FULL);
+#ifdef DT_GEMM_TRACE
+              if (p.trace) atomicAdd(&p.trace[blockIdx.x * TRACE_SLOTS + TR_TMA_LAT],
+                                     (unsigned long long)(clock64() - t_issue[stage]));
+#endif
             }
             DT_TRACE_COUNT(TR_STAGES);
             if (!_okf) {
@@ -170,6 +185,9 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
               mma_bf16(d_tmem, adesc, bdesc, idesc, acc);
               acc = 1;
             }
+#ifdef DT_GEMM_TRACE
+            t_commit[stage] = clock64();
+#endif
             mma_commit(&empty[stage]);
             if (++stage == STAGES) {
               stage = 0;

@@ -29,6 +29,11 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+#ifdef DT_GEMM_TRACE
+  volatile long long* t_issue = reinterpret_cast<volatile long long*>(drain + 2);   // per stage
+  volatile long long* t_commit = t_issue + PAIR_STAGES;
+  for (int i = threadIdx.x; i < 2 * PAIR_STAGES; i += blockDim.x) t_issue[i] = 0;
+#endif
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -91,6 +96,12 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
               DT_TRACE_T0();
               _ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
               DT_TRACE_ADD(TR_PROD_EMPTY);
+#ifdef DT_GEMM_TRACE
+              if (p.trace && t_commit[stage] != 0)
+                atomicAdd(&p.trace[blockIdx.x * TRACE_SLOTS + TR_COMMIT_LAT],
+                          (unsigned long long)(clock64() - t_commit[stage]));
+              t_issue[stage] = clock64();
+#endif
             }
             if (!_ok) {
               aborted = true;
@@ -154,6 +165,10 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
               DT_TRACE_T0();
               _okf = mbar_wait(&full[stage], phase, abort_flag);
               DT_TRACE_ADD(TR_MMA_FULL);
+#ifdef DT_GEMM_TRACE
+              if (p.trace) atomicAdd(&p.trace[blockIdx.x * TRACE_SLOTS + TR_TMA_LAT],
+                                     (unsigned long long)(clock64() - t_issue[stage]));
+#endif
             }
             DT_TRACE_COUNT(TR_STAGES);
             if (!_okf) {
@@ -174,6 +189,9 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
               mma_bf16_pair(d_tmem, adesc, bdesc, idesc, acc);
               acc = 1;
             }
+#ifdef DT_GEMM_TRACE
+            t_commit[stage] = clock64();
+#endif
             mma_commit_pair_mc(&empty[stage], 0x3);
             if (++stage == PAIR_STAGES) {
               stage = 0;

@@ -81,7 +81,9 @@ enum TraceSlot {
   TR_EPI_TFULL = 4,    // epilogue (warp 2) waiting for a finished accumulator
   TR_TILES = 5,        // tiles this CTA processed
   TR_STAGES = 6,       // stages the MMA issuer consumed
-  TRACE_SLOTS = 8
+  TR_TMA_LAT = 7,      // sum over stages: stage's first TMA issued -> MMA issuer sees it full
+  TR_COMMIT_LAT = 8,   // sum over stages: MMA commit issued -> producer sees the stage empty
+  TRACE_SLOTS = 16
 };
 
 struct Params {  // CUtensorMap carries its own 128-byte alignment
