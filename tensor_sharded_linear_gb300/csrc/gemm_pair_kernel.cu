@@ -7,8 +7,11 @@
 //
 // Roles per CTA (192 threads): warp 0 TMA producer, warp 1 MMA issuer (rank
 // 0 only; it owns the pair's MMAs), warps 2..5 epilogue.  Barriers:
-//   full[s]    in rank 0: 2 arrivals (rank 0 with the byte count of both
-//              CTAs' loads, rank 1 plain) + the loads' bytes;
+//   full[s]    in rank 0: 1 arrival (rank 0, with the byte count of both
+//              CTAs' loads) + the loads' bytes.  Rank 1 only issues its loads:
+//              its bytes are its share.  (A cluster-scope release arrive from
+//              rank 1 before each stage would wait for that thread's copies
+//              still in flight and serialise rank 1's pipeline.)
 //   empty[s]   in each CTA: 1 arrival, rank 0's MMA commit multicast to both;
 //   tfull[b]   in each CTA: 1 arrival, multicast commit after a tile's MMAs;
 //   tempty[b]  in rank 0: 8 arrivals, the 4 epilogue warps of each CTA.
@@ -43,7 +46,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < PAIR_STAGES; ++s) {
-      mbar_init(&full[s], 2);
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -110,7 +113,6 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
             }
             const uint32_t full0 = mapa_shared(smem_u32(&full[stage]), 0);
             if (rank == 0) mbar_expect_tx(&full[stage], 2 * PAIR_STAGE_BYTES);
-            else mbar_arrive_cluster(full0);
             uint8_t* a = smem + stage * PAIR_STAGE_BYTES;
             uint8_t* b = a + PAIR_A_BYTES;
             tma_load_2d_pair(a, &p.maps[S.a_map], kt * BK, a_row, full0);
