@@ -238,6 +238,29 @@ DT_API dt_status dt_tp_mlp(const dt_dtensor* x, const dt_dtensor* w_gate, const 
                     const dt_dtensor* w_down, const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim,
                     void* workspace, size_t workspace_bytes, int32_t* d_status, dt_stream_t stream);
 
+/*
+ * The TP MLP for callers that cannot allocate device memory at call time
+ * (for example a serving loop that must not allocate once running, or host
+ * code that does not own the device allocator).  Same operands, results and
+ * errors as dt_tp_mlp, but H lives in a buffer built into the library: a
+ * device array of DT_TP_MLP_STATIC_WORKSPACE_BYTES that every GPU which
+ * loads the library holds until the process exits.  This entry point has no
+ * counterpart in the pages; it exists for such callers only.
+ *  - It allocates nothing (no cudaMalloc, no allocator of any library).
+ *  - Problems whose H (dt_tp_mlp_workspace_size) exceeds the array are
+ *    rejected with DT_ERR_CAPACITY.
+ *  - The first call on a device looks up the array's device address on that
+ *    device (cudaGetSymbolAddress); make that first call before any stream
+ *    capture.
+ *  - All calls share the one array: calls whose kernels overlap on the GPU
+ *    (different streams, or different host threads) race on H.  H is fully
+ *    rewritten by every call, so nothing needs clearing in between.
+ */
+#define DT_TP_MLP_STATIC_WORKSPACE_BYTES (32 * 1024 * 1024)
+DT_API dt_status dt_tp_mlp_static_workspace(const dt_dtensor* x, const dt_dtensor* w_gate, const dt_dtensor* w_up,
+                                            const dt_dtensor* w_down, const dt_dtensor* y, int32_t mode,
+                                            int32_t tp_mesh_dim, int32_t* d_status, dt_stream_t stream);
+
 /* ---- utilities ---- */
 
 /* Static description of a status code. */

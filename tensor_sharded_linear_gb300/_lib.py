@@ -23,6 +23,7 @@ REPLICATE, SHARD, PARTIAL = 0, 1, 2
 SUM = 0
 # dt_tp_mode
 TP_PARTIAL, TP_ALL_REDUCE, TP_REDUCE_SCATTER = 0, 1, 2
+TP_MLP_STATIC_WORKSPACE_BYTES = 32 * 1024 * 1024
 
 
 class Placement(C.Structure):
@@ -55,6 +56,7 @@ EXPORTS = [
     "dt_tp_embedding", "dt_column_parallel_linear", "dt_column_parallel_linear_multi",
     "dt_row_parallel_linear", "dt_tp_mlp_workspace_size", "dt_tp_mlp", "dt_status_string",
     "dt_last_error", "dt_read_device_status", "dt_clear_cache", "dt_version", "dt_launch_count",
+    "dt_tp_mlp_static_workspace",
 ]
 
 _lib = None
@@ -98,6 +100,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
             "dt_clear_cache": (st, []),
             "dt_version": (C.c_int32, []),
             "dt_launch_count": (C.c_uint64, []),
+            "dt_tp_mlp_static_workspace": (st, [D, D, D, D, D, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
