@@ -50,7 +50,7 @@ G_ODD = 8191 * 8190 * 2
 EMB_BYTES = 4 * 4096 * 4096 * 2 * 2 + 4 * 4096 * 4
 MLP_FLOPS = 3 * 2 * 4096 * 4096 * 11008
 ATTN_FLOPS = 4 * 2 * 8192 * 4096 * 4096
-GEMM_SOURCES = ["gemm_sm103.cuh", "gemm_kernel.cu"]
+GEMM_SOURCES = ["gemm_sm103.cuh", "gemm_kernel.cu", "gemm_pair_kernel.cu"]
 ALL_COMPONENTS = "embedding,redistribute,mlp,attention"
 
 
