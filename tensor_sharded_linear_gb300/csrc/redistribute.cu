@@ -27,13 +27,31 @@
 namespace dt {
 namespace {
 
+// Tuning (overridable at build time for sweeps): bytes of a row per work
+// item, resident CTAs per SM, 16-byte vectors in flight per lane.
+#ifndef RD_COPY_SEG
+#define RD_COPY_SEG 4096
+#endif
+#ifndef RD_COPY_CTAS
+#define RD_COPY_CTAS 3
+#endif
+#ifndef RD_COPY_UNROLL
+#define RD_COPY_UNROLL 8
+#endif
+#ifndef RD_REALIGN_UNROLL
+#define RD_REALIGN_UNROLL 4
+#endif
+#ifndef RD_SUM_CTAS
+#define RD_SUM_CTAS 2
+#endif
+
 constexpr int RD_MAX_TASKS = 64;
 constexpr int RD_MAX_REFS = 256;
 constexpr int RD_MAX_SRC = 16;
 constexpr int RD_THREADS = 256;
 constexpr int RD_WARPS = RD_THREADS / 32;
-constexpr int COPY_SEG_BYTES = 4096;  // one warp moves up to 4 KiB of a row per work item
-constexpr int SUM_SEG_BYTES = 2048;   // of the destination, for Partial sums
+constexpr int COPY_SEG_BYTES = RD_COPY_SEG;  // one warp moves up to this much of a row per work item
+constexpr int SUM_SEG_BYTES = 2048;          // of the destination, for Partial sums
 
 struct RdSlot {
   char* ptr;
@@ -81,13 +99,14 @@ __device__ __forceinline__ void st_stream(uint4* p, uint4 v) { __stcs(p, v); }
 // 16-byte vectors, source and destination equally aligned: every lane keeps
 // up to 8 loads in flight before storing.
 __device__ __forceinline__ void copy_vec_aligned(uint4* dv, const uint4* sv, int64_t nvec, int lane) {
+  constexpr int UN = RD_COPY_UNROLL;
   int64_t i = lane;
-  for (; i + 7 * 32 < nvec; i += 8 * 32) {
-    uint4 v[8];
+  for (; i + (UN - 1) * 32 < nvec; i += UN * 32) {
+    uint4 v[UN];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = ld_stream(sv + i + 32 * u);
+    for (int u = 0; u < UN; ++u) v[u] = ld_stream(sv + i + 32 * u);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) st_stream(dv + i + 32 * u, v[u]);
+    for (int u = 0; u < UN; ++u) st_stream(dv + i + 32 * u, v[u]);
   }
   for (; i < nvec; i += 32) st_stream(dv + i, ld_stream(sv + i));
 }
@@ -126,21 +145,21 @@ __device__ __forceinline__ void copy_vec_realign(uint4* dv, const char* s, int64
   const int delta = static_cast<int>(reinterpret_cast<uintptr_t>(s) & 15);
   const uint4* sa = reinterpret_cast<const uint4*>(s - delta);
   const uint4 z = make_uint4(0, 0, 0, 0);
-  for (int64_t base = 0; base < nvec; base += 4 * 32) {
-    uint4 a[4], b[4];
+  for (int64_t base = 0; base < nvec; base += RD_REALIGN_UNROLL * 32) {
+    uint4 a[RD_REALIGN_UNROLL], b[RD_REALIGN_UNROLL];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < RD_REALIGN_UNROLL; ++u) {
       const int64_t j = base + 32 * u + lane;
       a[u] = j <= nvec ? ld_stream(sa + j) : z;
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < RD_REALIGN_UNROLL; ++u) {
       const int64_t j = base + 32 * u + lane;
       b[u] = shfl_down_vec(a[u]);
       if (lane == 31) b[u] = j + 1 <= nvec ? ld_stream(sa + j + 1) : z;
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < RD_REALIGN_UNROLL; ++u) {
       const int64_t j = base + 32 * u + lane;
       if (j < nvec) st_stream(dv + j, realign(a[u], b[u], delta));
     }
@@ -338,7 +357,7 @@ __device__ void sum_span(char* d, const char* const* s, int nsrc, int64_t n, int
 // per kind keeps the copy path's register use low.  Warps take work items
 // (row, segment) in a grid-stride loop.
 template <bool SUM>
-__global__ void __launch_bounds__(RD_THREADS, SUM ? 2 : 3) rd_kernel(const __grid_constant__ RdParams p) {
+__global__ void __launch_bounds__(RD_THREADS, SUM ? RD_SUM_CTAS : RD_COPY_CTAS) rd_kernel(const __grid_constant__ RdParams p) {
   const int lane = threadIdx.x & 31;
   const int esize = p.esize;
   const int64_t nw = static_cast<int64_t>(gridDim.x) * RD_WARPS;
@@ -573,8 +592,8 @@ extern "C" dt_status dt_redistribute(const dt_dtensor* src, const dt_dtensor* ds
       p.ntasks = nt;
       p.nitems = items;
       const int64_t blocks = (items + RD_WARPS - 1) / RD_WARPS;
-      // one wave of resident CTAs (3 per SM for copies, 2 for sums), grid-stride over items
-      const int grid = (int)std::min<int64_t>(blocks, (int64_t)sms * (sum ? 2 : 3));
+      // one wave of resident CTAs, grid-stride over items
+      const int grid = (int)std::min<int64_t>(blocks, (int64_t)sms * (sum ? RD_SUM_CTAS : RD_COPY_CTAS));
       if (sum)
         rd_kernel<true><<<grid, RD_THREADS, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
       else
