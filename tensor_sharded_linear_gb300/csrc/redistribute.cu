@@ -33,10 +33,10 @@ namespace {
 #define RD_COPY_SEG 4096
 #endif
 #ifndef RD_COPY_CTAS
-#define RD_COPY_CTAS 3
+#define RD_COPY_CTAS 4
 #endif
 #ifndef RD_COPY_UNROLL
-#define RD_COPY_UNROLL 8
+#define RD_COPY_UNROLL 4
 #endif
 #ifndef RD_REALIGN_UNROLL
 #define RD_REALIGN_UNROLL 4
