@@ -56,6 +56,21 @@ def column_parallel(x, w_shards, bias_shards=None):
     return ys
 
 
+def column_parallel_seq(x_token_shards, w_shards, bias_shards=None):
+    """Sequence-parallel column entry (nanotron tutorial 5.1, REDUCE_SCATTER
+    mode of TensorParallelColumnLinear): the input arrives sharded over tokens
+    (dim 0); it is all-gathered, then every column shard is applied to all
+    tokens.  Returns the Shard(-1) outputs with all tokens."""
+    x = np.concatenate(list(x_token_shards), axis=0)
+    return column_parallel(x, w_shards, bias_shards)
+
+
+def column_parallel_replicate(x, w_shards, bias_shards=None):
+    """ColumnParallelLinearWithReplicateOutput (DTorch guide, section 3): the
+    Shard(-1) outputs gathered into one Replicate tensor along features."""
+    return np.concatenate(column_parallel(x, w_shards, bias_shards), axis=-1)
+
+
 def row_sum(x_shards, w_shards):
     """sum_i X_i W_i in fp64, terms added in rank order."""
     y = None

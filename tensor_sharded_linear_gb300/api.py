@@ -299,20 +299,27 @@ def _tp_index(mesh: DeviceMesh, tp_dim) -> int:
     return -1 if m is None else m
 
 
-def _col_out(x: DTensor, w: DTensor, tp: int, out_dtype) -> DTensor:
+def _col_out(x: DTensor, w: DTensor, tp: int, out_dtype, output: str = "shard") -> DTensor:
+    """Output of a column layer: Shard(-1) on tp, or Replicate with
+    output="replicate" (all tokens either way, also for a token-sharded x)."""
     nd = len(x.gshape)
     pls = list(x.placements)
     if tp >= 0:
-        pls[tp] = Shard(nd - 1)
+        pls[tp] = Replicate() if output == "replicate" else Shard(nd - 1)
     return DTensor.empty(x.mesh, pls, x.gshape[:-1] + (w.gshape[1],), out_dtype or x.dtype,
                          device=x.slots[0].device)
 
 
 def column_parallel_linear(x: DTensor, w: DTensor, bias: Optional[DTensor] = None, tp_dim="tp",
-                           out_dtype=None, out: Optional[DTensor] = None) -> DTensor:
-    """Y_i = X W_i (+ b_i): output Shard(-1) on tp."""
+                           out_dtype=None, out: Optional[DTensor] = None, output: str = "shard") -> DTensor:
+    """Y_i = X W_i (+ b_i).
+
+    x Replicate on tp, or Shard(0) on tp (sequence-parallel entry: the token
+    shards are read in place, no gathered copy is made).  The output is
+    Shard(-1) on tp, or Replicate with output="replicate" (each shard writes
+    its column block of the one Replicate tensor)."""
     tp = _tp_index(x.mesh, tp_dim)
-    y = out if out is not None else _col_out(x, w, tp, out_dtype)
+    y = out if out is not None else _col_out(x, w, tp, out_dtype, output)
     b = bias._desc() if bias is not None else None
     L.check(L.load().dt_column_parallel_linear(C.byref(x._desc()), C.byref(w._desc()),
                                                C.byref(b) if b is not None else None, C.byref(y._desc()), tp,
@@ -321,10 +328,10 @@ def column_parallel_linear(x: DTensor, w: DTensor, bias: Optional[DTensor] = Non
 
 
 def column_parallel_linear_multi(x: DTensor, ws: Sequence[DTensor], biases=None, tp_dim="tp", out_dtype=None,
-                                 outs=None):
+                                 outs=None, output: str = "shard"):
     """Several column-parallel linears sharing x, in one launch (fused q/k/v)."""
     tp = _tp_index(x.mesh, tp_dim)
-    ys = list(outs) if outs is not None else [_col_out(x, w, tp, out_dtype) for w in ws]
+    ys = list(outs) if outs is not None else [_col_out(x, w, tp, out_dtype, output) for w in ws]
     n = len(ws)
     # the descriptors own the slot/stride arrays the copies below point at
     wdescs = [w._desc() for w in ws]
@@ -465,12 +472,26 @@ class ColumnParallelLinear(Linear):
 
 
 class ColumnParallelLinearWithReplicateOutput(ColumnParallelLinear):
-    output_placement = Replicate()
+    """Column linear whose output is Replicate on tp: fused, every shard's GEMM
+    writes its column block of the Replicate output (no separate all-gather)."""
+
+    def forward(self, x: DTensor) -> DTensor:
+        if self.tp_dim is None:
+            return super().forward(x)
+        return column_parallel_linear(x, self.weight, self.bias, tp_dim=self.tp_dim, output="replicate")
 
 
-class ColumnParallelLinearWithReplicateInputOutput(ColumnParallelLinear):
-    input_placement = Replicate()
-    output_placement = Replicate()
+class ColumnParallelLinearWithReplicateInputOutput(ColumnParallelLinearWithReplicateOutput):
+    """Input converted to Replicate on tp, output Replicate.  A token-sharded
+    (Shard(0)) input is consumed in place by the GEMM instead of being
+    gathered first; any other placement is redistributed to Replicate."""
+
+    def redistribute_input(self, x: DTensor) -> DTensor:
+        if self.tp_dim is not None and x.placements[self.tp_dim] == Shard(0):
+            return x
+        if self.tp_dim is not None:
+            x = x.redistribute_by_dict({self.tp_dim: Replicate()})
+        return super().redistribute_input(x)
 
 
 class RowParallelLinear(Linear):

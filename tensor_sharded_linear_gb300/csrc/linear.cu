@@ -135,9 +135,18 @@ dt_status check_column(const DTensor& X, const ColumnSpec& c, int tp, bool allow
   }
   for (int m = 0; m < lx.mesh_ndim; ++m) {
     if (m == tp) {
-      if (!lx.is_replicate(m)) return fail(DT_ERR_PLACEMENT, "column-parallel input must be Replicate on tp, got %s", pname(lx, m));
+      // input: Replicate (DTorch's rule), or sharded on a leading (token) dim:
+      // the sequence-parallel entry, whose all-gather is read in place
+      const bool x_rep = lx.is_replicate(m);
+      const bool x_seq = lx.kind[m] == DT_SHARD && lx.dim[m] < nd - 1;
+      if (!x_rep && !x_seq)
+        return fail(DT_ERR_PLACEMENT, "column-parallel input must be Replicate (or token-sharded) on tp, got %s%s",
+                    pname(lx, m), lx.kind[m] == DT_SHARD && lx.dim[m] == nd - 1 ? "(-1)" : "");
       if (!lw.is_shard(m, 1)) return fail(DT_ERR_PLACEMENT, "column-parallel weight [in, out] must be Shard(1) on tp");
-      if (!ly.is_shard(m, nd - 1)) return fail(DT_ERR_PLACEMENT, "column-parallel output must be Shard(-1) on tp");
+      // output: Shard(-1) (ColumnParallelLinear) or Replicate (the
+      // ...WithReplicateOutput layers: each shard writes its column block)
+      if (!ly.is_shard(m, nd - 1) && !ly.is_replicate(m))
+        return fail(DT_ERR_PLACEMENT, "column-parallel output must be Shard(-1) or Replicate on tp");
       if (c.bias && !c.bias->layout.is_shard(m, 0)) return fail(DT_ERR_PLACEMENT, "column-parallel bias must be Shard(0) on tp");
     } else {
       if (!lw.is_replicate(m)) return fail(DT_ERR_PLACEMENT, "weight must be Replicate off tp");
@@ -150,45 +159,77 @@ dt_status check_column(const DTensor& X, const ColumnSpec& c, int tp, bool allow
   return DT_OK;
 }
 
-dt_status add_column_groups(const DTensor& X, const ColumnSpec& c, std::vector<HostGroup>* groups,
-                            std::set<std::pair<const void*, int>>* done) {
+dt_status add_column_groups(const DTensor& X, const ColumnSpec& c, int tp, std::vector<HostGroup>* groups,
+                            std::set<std::tuple<const void*, int, int, int>>* done) {
   const Layout& lx = X.layout;
+  const Layout& ly = c.y->layout;
   const int nd = lx.ndim;
-  int coords[DT_MAX_MESH_DIMS];
+  const bool x_seq = tp >= 0 && lx.kind[tp] == DT_SHARD;        // token-sharded input
+  const bool y_rep = tp >= 0 && ly.is_replicate(tp);             // Replicate output
+  const int P = tp >= 0 ? lx.mesh[tp] : 1;
+  int coords[DT_MAX_MESH_DIMS], cj[DT_MAX_MESH_DIMS];
   for (int r = 0; r < lx.mesh_size; ++r) {
     lx.rank_coords(r, coords);
-    const int ys = c.y->layout.slot_of_coords(coords);
-    if (!done->insert({c.y, ys}).second) continue;
-    const SlotView& xv = X.slots[lx.slot_of_coords(coords)];
-    const SlotView& wv = c.w->slots[c.w->layout.slot_of_coords(coords)];
+    const int ys = ly.slot_of_coords(coords);
+    const int ws = c.w->layout.slot_of_coords(coords);
+    const SlotView& wv = c.w->slots[ws];
     const SlotView& yv = c.y->slots[ys];
-    HostGroup g;
-    Mat a, b, y;
-    dt_status st = slot_matrix(xv, nd, lx.dtype, &a, "x");
+    Mat b, y;
+    dt_status st = weight_matrix(wv, c.w->layout.dtype, &b, "w");
     if (st != DT_OK) return st;
-    st = weight_matrix(wv, c.w->layout.dtype, &b, "w");
+    st = slot_matrix(yv, nd, ly.dtype, &y, "y");
     if (st != DT_OK) return st;
-    st = slot_matrix(yv, nd, c.y->layout.dtype, &y, "y");
-    if (st != DT_OK) return st;
-    if (y.rows != a.rows || y.cols != b.cols || a.cols != b.rows)
-      return fail(DT_ERR_SHAPE, "local shapes disagree: x [%lld, %lld] w [%lld, %lld] y [%lld, %lld]",
-                  (long long)a.rows, (long long)a.cols, (long long)b.rows, (long long)b.cols, (long long)y.rows,
-                  (long long)y.cols);
-    g.m = y.rows;
-    g.n = y.cols;
-    g.segs.push_back(HostSeg{a, b, Mat()});
-    g.out_dtype = c.y->layout.dtype;
-    g.row_begin = {0};
-    g.out_ptr = {y.ptr};
-    g.out_ld = {y.ld};
-    if (c.bias) {
-      const SlotView& bv = c.bias->slots[c.bias->layout.slot_of_coords(coords)];
-      if (bv.shape[0] != y.cols) return fail(DT_ERR_SHAPE, "bias shard width differs from the output shard");
-      if (bv.shape[0] > 1 && bv.stride[0] != 1) return fail(DT_ERR_UNSUPPORTED, "bias must be contiguous");
-      g.bias = bv.ptr;
-      g.bias_dtype = c.bias->layout.dtype;
+    // the weight shard's columns inside y: all of y (Shard(-1) output) or
+    // its column block of the Replicate output
+    const int64_t col0 = y_rep ? wv.goff[1] : 0;
+    if (y_rep) {
+      if (col0 + b.cols > y.cols) return fail(DT_ERR_SHAPE, "weight shard columns exceed the output");
+    } else if (y.cols != b.cols) {
+      return fail(DT_ERR_SHAPE, "output shard width %lld != weight shard width %lld", (long long)y.cols, (long long)b.cols);
     }
-    groups->push_back(std::move(g));
+    // the x slots feeding this output: one (Replicate on tp) or the P token
+    // shards, each writing its own block of rows
+    const int nx = x_seq ? P : 1;
+    for (int j = 0; j < nx; ++j) {
+      std::copy(coords, coords + DT_MAX_MESH_DIMS, cj);
+      if (x_seq) cj[tp] = j;
+      const int xs = lx.slot_of_coords(cj);
+      if (!done->insert(std::make_tuple((const void*)c.y, ys, ws, xs)).second) continue;
+      const SlotView& xv = X.slots[xs];
+      Mat a;
+      if ((st = slot_matrix(xv, nd, lx.dtype, &a, "x")) != DT_OK) return st;
+      if (a.cols != b.rows) return fail(DT_ERR_SHAPE, "x width %lld != w rows %lld", (long long)a.cols, (long long)b.rows);
+      if (a.rows == 0) continue;
+      int64_t row0 = 0;
+      if (x_seq) {
+        // x slot j holds dim-0 entries [goff, goff + n) of the y slot's, i.e.
+        // a contiguous block of the flattened rows
+        if (lx.dim[tp] != 0) return fail(DT_ERR_UNSUPPORTED, "a token-sharded input must be sharded on dim 0");
+        int64_t inner = 1;
+        for (int e = 1; e < nd - 1; ++e) inner *= xv.shape[e];
+        row0 = (xv.goff[0] - yv.goff[0]) * inner;
+        if (row0 < 0 || row0 + a.rows > y.rows) return fail(DT_ERR_SHAPE, "token shard rows outside the output");
+      } else if (y.rows != a.rows) {
+        return fail(DT_ERR_SHAPE, "x rows %lld != y rows %lld", (long long)a.rows, (long long)y.rows);
+      }
+      HostGroup g;
+      g.m = a.rows;
+      g.n = b.cols;
+      g.segs.push_back(HostSeg{a, b, Mat()});
+      g.out_dtype = ly.dtype;
+      const int esize = dtype_size(ly.dtype);
+      g.row_begin = {0};
+      g.out_ptr = {y.ptr + (row0 * y.ld + col0) * esize};
+      g.out_ld = {y.ld};
+      if (c.bias) {
+        const SlotView& bv = c.bias->slots[c.bias->layout.slot_of_coords(coords)];
+        if (bv.shape[0] != b.cols) return fail(DT_ERR_SHAPE, "bias shard width differs from the weight shard");
+        if (bv.shape[0] > 1 && bv.stride[0] != 1) return fail(DT_ERR_UNSUPPORTED, "bias must be contiguous");
+        g.bias = bv.ptr;
+        g.bias_dtype = c.bias->layout.dtype;
+      }
+      groups->push_back(std::move(g));
+    }
   }
   return DT_OK;
 }
@@ -215,10 +256,10 @@ dt_status column_multi(const dt_dtensor* x, int32_t n, const dt_dtensor* w, cons
     if ((st = check_column(X, c, tp, true)) != DT_OK) return st;
   }
   std::vector<HostGroup> groups;
-  std::set<std::pair<const void*, int>> done;
+  std::set<std::tuple<const void*, int, int, int>> done;
   for (int j = 0; j < n; ++j) {
     ColumnSpec c{&W[j], has_bias[j] ? &B[j] : nullptr, &Y[j]};
-    if ((st = add_column_groups(X, c, &groups, &done)) != DT_OK) return st;
+    if ((st = add_column_groups(X, c, tp, &groups, &done)) != DT_OK) return st;
   }
   if (groups.empty()) return DT_OK;
   const void* any = groups[0].out_ptr[0];

@@ -166,3 +166,18 @@ def test_planted_linear_mistakes_are_caught(monkeypatch, bad):
         monkeypatch.setattr(ol, "row_sum", lambda xs, ws: -sum(np.matmul(a, b) for a, b in zip(xs, ws)))
     with pytest.raises(AssertionError):
         check_worked_example()
+
+
+def test_sequence_parallel_entry_and_replicate_output():
+    """The gathered-token column entry equals the column linear on the full
+    input, and the Replicate output equals the dense product (brute force)."""
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((11, 6))
+    w = rng.standard_normal((6, 10))
+    p = 4
+    xs = [x[o:o + s] for o, s in chunk_bounds(11, p)]
+    seq = ol.column_parallel_seq(xs, col_shards(w, p))
+    dense = brute_matmul(x, w)
+    np.testing.assert_allclose(np.concatenate(seq, -1), dense, atol=1e-12, rtol=0)
+    assert all(y.shape[0] == 11 for y in seq)
+    np.testing.assert_allclose(ol.column_parallel_replicate(x, col_shards(w, p)), dense, atol=1e-12, rtol=0)
