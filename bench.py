@@ -347,6 +347,78 @@ class Block:
         return s
 
 
+class Extras:
+    """Rows built beyond the hot path, timed separately (not part of `value`):
+    the sequence-parallel q/k/v entry (x token-sharded, read in place), the
+    fused Replicate-output column linear, q/k/v with [out, in] weights (K-major
+    B), and the Ulysses Shard(2) -> Shard(1) move of [2, 32, 8192, 128]."""
+
+    def __init__(self, device):
+        import tensor_sharded_linear_gb300 as tsl
+        from tensor_sharded_linear_gb300 import workloads as W
+        from tensor_sharded_linear_gb300.api import DTensor
+        self.tsl = tsl
+        bf = torch.bfloat16
+        self.items = []
+
+        def dev(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(bf).to(device)
+
+        cfg = W.ATTENTION
+        P, H, T = cfg["parts"], cfg["hidden"], cfg["tokens"]
+        mesh = tsl.DeviceMesh((P,), ("tp",), device=device)
+        x, wq, wk, wv, _ = W.attention_inputs()
+        hc = [(i * (H // P), H // P) for i in range(P)]
+        tc = [(i * (T // P), T // P) for i in range(P)]
+        x_tok = DTensor([dev(x[o:o + s]) for o, s in tc], mesh, [tsl.Shard(0)], x.shape, bf)
+        x_rep = DTensor([dev(x)], mesh, [tsl.Replicate()], x.shape, bf)
+        ws = [DTensor([dev(w[:, o:o + s]) for o, s in hc], mesh, [tsl.Shard(1)], w.shape, bf) for w in (wq, wk, wv)]
+        ws_k = [DTensor([dev(np.ascontiguousarray(w[:, o:o + s].T)).t() for o, s in hc], mesh, [tsl.Shard(1)],
+                        w.shape, bf) for w in (wq, wk, wv)]
+        outs = [DTensor.empty(mesh, [tsl.Shard(1)], (T, H), bf, device=device) for _ in range(3)]
+        rep_out = DTensor.empty(mesh, [tsl.Replicate()], (T, H), bf, device=device)
+        qkv_flops = 3 * 2 * T * H * H
+        self._keep = (x_tok, x_rep, ws, ws_k, outs, rep_out)
+        self.items.append(("sequence-parallel q/k/v entry", "flops", qkv_flops,
+                           lambda: tsl.column_parallel_linear_multi(x_tok, ws, outs=outs)))
+        self.items.append(("column linear, Replicate output", "flops", 2 * T * H * H,
+                           lambda: tsl.column_parallel_linear(x_rep, ws[0], out=rep_out, output="replicate")))
+        self.items.append(("q/k/v with [out, in] weights", "flops", qkv_flops,
+                           lambda: tsl.column_parallel_linear_multi(x_rep, ws_k, outs=outs)))
+        shape = (2, 32, 8192, 128)
+        g = dev(W.randn_bf16(shape, 990))
+        cp = tsl.DeviceMesh((4,), ("cp",), device=device)
+        useq = DTensor.distribute_tensor(g, cp, [tsl.Shard(2)])
+        uhead = DTensor.empty(cp, [tsl.Shard(1)], shape, bf, device=device)
+        self._keep2 = (useq, uhead)
+        self.items.append(("Ulysses S(2)->S(1) [2,32,8192,128]", "bytes", 2 * 2 * int(np.prod(shape)),
+                           lambda: tsl.redistribute(useq, uhead)))
+
+    def measure(self, steps, peaks):
+        for _, _, _, fn in self.items:  # warm up every item (descriptor caches, first launches)
+            for _ in range(3):
+                fn()
+        torch.cuda.synchronize()
+        out = {}
+        for name, kind, work, fn in self.items:
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+            for a, b in evs:
+                a.record()
+                fn()
+                b.record()
+            torch.cuda.synchronize()
+            ms = statistics.fmean(a.elapsed_time(b) for a, b in evs)
+            if kind == "flops":
+                ach = work / (ms / 1e3) / 1e12
+                out[name] = {"us": round(ms * 1e3, 2), "achieved": round(ach, 1), "unit": "TFLOP/s",
+                             "frac": round(ach / peaks["bf16_tflops"], 4)}
+            else:
+                ach = work / (ms / 1e3) / 1e9
+                out[name] = {"us": round(ms * 1e3, 2), "achieved": round(ach, 1), "unit": "GB/s",
+                             "frac": round(ach / peaks["hbm_gbs"], 4)}
+        return out
+
+
 def gemm_source_hash():
     h = hashlib.sha256()
     for name in GEMM_SOURCES:
@@ -435,6 +507,11 @@ def run_ours(args):
     red_gbs = red_bytes / (red_ms / 1e3) / 1e9 if red_ms else 0.0
 
     e2e = None if args.no_e2e else run_e2e(blk, args, peaks, world, device)
+    extras = None
+    if not args.no_extras and args.only == ALL_COMPONENTS:
+        ex = Extras(device)
+        extras = ex.measure(max(3, min(args.steps, 10)), peaks)
+        del ex
 
     line = {
         "metric": METRIC, "value": round(100.0 * roof_sum / step_max, 3), "unit": UNIT, "n_gpus": world,
@@ -450,6 +527,7 @@ def run_ours(args):
         "redistribute_gbs": round(red_gbs, 1),
         "redistribute_frac": round(red_gbs / peaks["hbm_gbs"], 4),
         "components": comps,
+        "extras": extras,
         "clocks": clk,
         "e2e": e2e,
         "gpu_launches": int(launches),
@@ -626,6 +704,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the rows timed outside the step")
     ap.add_argument("--only", default=ALL_COMPONENTS,
                     help="comma-separated subset of embedding,redistribute,mlp,attention (profiling)")
     args = ap.parse_args()
