@@ -246,16 +246,38 @@ dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStrea
   const int ctas = pair ? max_clusters : sms;  // CTAs (single) or clusters (pair) in one wave
   size_t gi = 0;
   while (gi < groups.size()) {
-    // pack as many groups as fit one parameter block
+    // pack as many groups as fit one parameter block; descriptors of the
+    // same matrix and box (e.g. x shared by every column shard) are shared
+    auto b_rows = [&](const HostGroup& G) { return G.segs.empty() || !G.segs[0].b.kmajor ? BK : ((pair || G.dual) ? 128 : 256); };
+    std::vector<MapKey> keys;
+    auto key_of = [](const Mat& m, int box) {
+      return MapKey{reinterpret_cast<uintptr_t>(m.ptr), m.rows, m.cols, m.ld, box};
+    };
+    auto count_new = [&](const HostGroup& G, std::vector<MapKey>* ks) {
+      int added = 0;
+      auto add = [&](const MapKey& k) {
+        for (const auto& e : *ks)
+          if (e == k) return;
+        ks->push_back(k);
+        ++added;
+      };
+      for (const HostSeg& s : G.segs) {
+        add(key_of(s.a, BM));
+        add(key_of(stored(s.b), b_rows(G)));
+        if (G.dual) add(key_of(stored(s.b2), b_rows(G)));
+      }
+      return added;
+    };
     size_t g_end = gi;
-    int nmaps = 0, nsegs = 0;
+    int nsegs = 0;
     while (g_end < groups.size()) {
       const HostGroup& G = groups[g_end];
       const int need_segs = (int)G.segs.size();
-      const int need_maps = need_segs * (G.dual ? 3 : 2);
-      if ((int)(g_end - gi) + 1 > MAX_GROUPS || nsegs + need_segs > MAX_SEGS || nmaps + need_maps > MAX_MAPS) break;
+      std::vector<MapKey> trial = keys;
+      count_new(G, &trial);
+      if ((int)(g_end - gi) + 1 > MAX_GROUPS || nsegs + need_segs > MAX_SEGS || (int)trial.size() > MAX_MAPS) break;
+      keys.swap(trial);
       nsegs += need_segs;
-      nmaps += need_maps;
       ++g_end;
     }
     if (g_end == gi) return fail(DT_ERR_CAPACITY, "one GEMM group needs more than %d segments", MAX_SEGS);
@@ -264,6 +286,22 @@ dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStrea
     // per pipeline stage)
     const int bn = BN_MAX;
     int map_i = 0, seg_i = 0, tiles = 0;
+    std::vector<MapKey> encoded;
+    // index of the descriptor for (matrix, box rows) in this launch, encoding it once
+    auto map_index = [&](const Mat& m, int box, int32_t* idx) -> dt_status {
+      const MapKey k{reinterpret_cast<uintptr_t>(m.ptr), m.rows, m.cols, m.ld, box};
+      for (size_t i = 0; i < encoded.size(); ++i)
+        if (encoded[i] == k) {
+          *idx = (int32_t)i;
+          return DT_OK;
+        }
+      if (map_i >= MAX_MAPS) return fail(DT_ERR_CAPACITY, "more than %d TMA descriptors in one launch", MAX_MAPS);
+      dt_status st = encode_map(m, box, &p.maps[map_i]);
+      if (st != DT_OK) return st;
+      encoded.push_back(k);
+      *idx = map_i++;
+      return DT_OK;
+    };
     p.ngroups = 0;
     int common_m = -1;
     int64_t max_k = 0;
@@ -305,18 +343,11 @@ dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStrea
       for (const HostSeg& s : H.segs) {
         Seg& S = p.segs[seg_i++];
         S.k_tiles = (int32_t)((s.a.cols + BK - 1) / BK);
-        S.a_map = map_i;
-        dt_status st = encode_map(s.a, BM, &p.maps[map_i++]);
-        if (st != DT_OK) return st;
-        S.b_map = map_i;
-        st = encode_map(stored(s.b), b_box_rows, &p.maps[map_i++]);
-        if (st != DT_OK) return st;
+        dt_status st;
+        if ((st = map_index(s.a, BM, &S.a_map)) != DT_OK) return st;
+        if ((st = map_index(stored(s.b), b_box_rows, &S.b_map)) != DT_OK) return st;
         S.b_map2 = S.b_map;
-        if (H.dual) {
-          S.b_map2 = map_i;
-          st = encode_map(stored(s.b2), b_box_rows, &p.maps[map_i++]);
-          if (st != DT_OK) return st;
-        }
+        if (H.dual && (st = map_index(stored(s.b2), b_box_rows, &S.b_map2)) != DT_OK) return st;
       }
     }
     p.total_tiles = tiles;

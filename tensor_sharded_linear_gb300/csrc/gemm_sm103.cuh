@@ -49,7 +49,7 @@ constexpr int TMEM_COLS = 512;                // two 256-column accumulators
 constexpr int GROUP_M = 8;                    // per-group raster: 8 M tiles per band
 constexpr int MAX_MAPS = 48;
 constexpr int MAX_SEGS = 96;
-constexpr int MAX_GROUPS = 32;
+constexpr int MAX_GROUPS = 64;
 constexpr int MAX_OUT = 8;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait

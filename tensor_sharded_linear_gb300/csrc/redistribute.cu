@@ -71,6 +71,8 @@ struct RdTask {
   int32_t nsrc;
   int32_t ref_begin;
   int32_t segs_per_row;
+  int8_t dmap[4];  // slot stride used for each padded position (dims merged on the host)
+  int32_t pad;
 };
 
 struct RdRef {
@@ -374,26 +376,28 @@ __global__ void __launch_bounds__(RD_THREADS, SUM ? RD_SUM_CTAS : RD_COPY_CTAS) 
     const int64_t i1 = q % T.ext[1];
     const int64_t i0 = q / T.ext[1];
     const RdSlot& D = p.dst[T.dst_slot];
-    char* d = D.ptr + (T.dst_off + i0 * D.stride[0] + i1 * D.stride[1] + i2 * D.stride[2] + e0 * D.stride[3]) * esize;
+    const int m0 = T.dmap[0], m1 = T.dmap[1], m2 = T.dmap[2], m3 = T.dmap[3];
+    char* d =
+        D.ptr + (T.dst_off + i0 * D.stride[m0] + i1 * D.stride[m1] + i2 * D.stride[m2] + e0 * D.stride[m3]) * esize;
     if (!SUM && T.nsrc == 0) {
-      zero_span(d, n, D.stride[3], esize, lane);
+      zero_span(d, n, D.stride[m3], esize, lane);
     } else if (!SUM) {
       const RdRef& R = p.ref[T.ref_begin];
       const RdSlot& S = p.src[R.slot];
       const char* s =
-          S.ptr + (R.off + i0 * S.stride[0] + i1 * S.stride[1] + i2 * S.stride[2] + e0 * S.stride[3]) * esize;
-      if (D.stride[3] == 1 && S.stride[3] == 1) copy_span(d, s, n, esize, lane);
-      else copy_span_strided(d, s, n, D.stride[3], S.stride[3], esize, lane);
+          S.ptr + (R.off + i0 * S.stride[m0] + i1 * S.stride[m1] + i2 * S.stride[m2] + e0 * S.stride[m3]) * esize;
+      if (D.stride[m3] == 1 && S.stride[m3] == 1) copy_span(d, s, n, esize, lane);
+      else copy_span_strided(d, s, n, D.stride[m3], S.stride[m3], esize, lane);
     } else {
       const char* sp[RD_MAX_SRC];
       int64_t ss[RD_MAX_SRC];
       for (int k = 0; k < T.nsrc; ++k) {
         const RdRef& R = p.ref[T.ref_begin + k];
         const RdSlot& S = p.src[R.slot];
-        sp[k] = S.ptr + (R.off + i0 * S.stride[0] + i1 * S.stride[1] + i2 * S.stride[2] + e0 * S.stride[3]) * esize;
-        ss[k] = S.stride[3];
+        sp[k] = S.ptr + (R.off + i0 * S.stride[m0] + i1 * S.stride[m1] + i2 * S.stride[m2] + e0 * S.stride[m3]) * esize;
+        ss[k] = S.stride[m3];
       }
-      sum_span(d, sp, T.nsrc, n, D.stride[3], ss, p.dtype, lane);
+      sum_span(d, sp, T.nsrc, n, D.stride[m3], ss, p.dtype, lane);
     }
   }
 }
@@ -503,6 +507,45 @@ dt_status plan(const DTensor& S, const DTensor& D, std::vector<HostTask>* tasks)
   return DT_OK;
 }
 
+// Collapse the task's box dims that are contiguous in the destination and in
+// every source (padded position p-1 folds into p when its stride equals
+// ext[p] * stride[p] everywhere), so short rows become long runs; extent-1
+// dims fold away.  Fills t->ext (front-padded) and t->dmap.
+void merge_dims(const HostTask& ht, const DTensor& D, const DTensor& S, int pad, RdTask* t) {
+  int64_t ext[4];
+  for (int d = 0; d < 4; ++d) ext[d] = d < pad ? 1 : ht.box.size[d - pad];
+  auto stride = [&](const SlotView& v, int p) -> int64_t { return p < pad ? 0 : v.stride[p - pad]; };
+  // merged dims from the innermost outwards: (extent, padded position whose stride is used)
+  int64_t me[4];
+  int mp[4];
+  int n = 0;
+  me[0] = ext[3];
+  mp[0] = 3;
+  n = 1;
+  for (int p = 2; p >= 0; --p) {
+    if (ext[p] == 1) continue;
+    const int in = mp[n - 1];
+    const int64_t run = me[n - 1];
+    bool ok = stride(D.slots[ht.dst_slot], p) == run * stride(D.slots[ht.dst_slot], in);
+    for (int k = 0; ok && k < (int)ht.src_slots.size(); ++k)
+      ok = stride(S.slots[ht.src_slots[k]], p) == run * stride(S.slots[ht.src_slots[k]], in);
+    if (ok && me[n - 1] > 0) {
+      me[n - 1] *= ext[p];
+    } else {
+      me[n] = ext[p];
+      mp[n] = p;
+      ++n;
+    }
+  }
+  // back to front-padded order, innermost at position 3; dmap holds padded
+  // positions, which is how RdSlot::stride is indexed
+  for (int q = 0; q < 4; ++q) {
+    const int k = 3 - q;  // merged dim for padded position q
+    t->ext[q] = k < n ? me[k] : 1;
+    t->dmap[q] = (int8_t)(k < n ? mp[k] : 0);
+  }
+}
+
 void fill_slot(RdSlot* out, const SlotView& v, int ndim) {
   out->ptr = v.ptr;
   // pad dims at the front so the innermost tensor dim is padded dim 3
@@ -567,7 +610,7 @@ extern "C" dt_status dt_redistribute(const dt_dtensor* src, const dt_dtensor* ds
         const HostTask& ht = tasks[i];
         if (nref + (int)ht.src_slots.size() > RD_MAX_REFS) break;
         RdTask& t = p.task[nt];
-        for (int d = 0; d < 4; ++d) t.ext[d] = d < pad ? 1 : ht.box.size[d - pad];
+        merge_dims(ht, D, S, pad, &t);
         t.dst_slot = ht.dst_slot;
         t.dst_off = local_offset(D.slots[ht.dst_slot], ht.box, nd);
         t.nsrc = (int)ht.src_slots.size();
