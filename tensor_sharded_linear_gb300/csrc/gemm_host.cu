@@ -228,6 +228,29 @@ bool out_vec_ok(const HostGroup& g) {
 // The CTA-pair kernel (256 x 256 tiles on tcgen05 .cta_group::2) is the
 // default; DT_GEMM_PAIR=0 in the environment selects the single-CTA kernel
 // (128 x 256 tiles), e.g. to compare the two.
+// Test hooks, read once from the environment: DT_GEMM_WAIT_LIMIT_MS bounds
+// every mbarrier wait (default 2000 ms); DT_GEMM_STARVE=1 makes the TMA
+// producers issue no loads, so the MMA waits run out and the kernels report
+// DT_DEV_ERR_TIMEOUT -- it exercises the bounded-wait exit without a fault.
+unsigned long long gemm_wait_limit_ns() {
+  static unsigned long long v = 0;
+  if (!v) {
+    const char* e = getenv("DT_GEMM_WAIT_LIMIT_MS");
+    const long ms = e ? atol(e) : 0;
+    v = (ms > 0 && ms <= 10000) ? (unsigned long long)ms * 1000000ull : WAIT_LIMIT_NS;
+  }
+  return v;
+}
+
+int gemm_starve() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("DT_GEMM_STARVE");
+    v = (e && e[0] == '1') ? 1 : 0;
+  }
+  return v;
+}
+
 bool use_pair_kernel() {
   static int v = -1;
   if (v < 0) {
@@ -352,6 +375,8 @@ dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStrea
     }
     p.total_tiles = tiles;
     p.status = status;
+    p.wait_limit_ns = gemm_wait_limit_ns();
+    p.starve = gemm_starve();
 #ifdef DT_GEMM_TRACE
     p.trace = trace_ptr();
 #else

@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
       }
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
+      for (int t = blockIdx.x; t < p.total_tiles && !aborted && !p.starve; t += gridDim.x) {
         const TileCoord tc = decode_tile<BM>(p, t);
         const Group& G = p.groups[tc.g];
         const int nmma = tile_mma_n(G, tc.n0);
@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
             bool _ok;
             {
               DT_TRACE_T0();
-              _ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
+              _ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.wait_limit_ns);
               DT_TRACE_ADD(TR_PROD_EMPTY);
 #ifdef DT_GEMM_TRACE
               if (p.trace && t_commit[stage] != 0)
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
         bool _ok;
         {
           DT_TRACE_T0();
-          _ok = mbar_wait(&tempty[buf], tphase ^ 1u, abort_flag);
+          _ok = mbar_wait(&tempty[buf], tphase ^ 1u, abort_flag, p.wait_limit_ns);
           DT_TRACE_ADD(TR_MMA_TEMPTY);
         }
         DT_TRACE_COUNT(TR_TILES);
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
             bool _okf;
             {
               DT_TRACE_T0();
-              _okf = mbar_wait(&full[stage], phase, abort_flag);
+              _okf = mbar_wait(&full[stage], phase, abort_flag, p.wait_limit_ns);
               DT_TRACE_ADD(TR_MMA_FULL);
 #ifdef DT_GEMM_TRACE
               if (p.trace) atomicAdd(&p.trace[blockIdx.x * TRACE_SLOTS + TR_TMA_LAT],
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_kernel(const __grid_c
       int ok = 1;
       if (lane == 0) {
         DT_TRACE_T0();
-        ok = mbar_wait(&tfull[buf], tphase, abort_flag) ? 1 : 0;
+        ok = mbar_wait(&tfull[buf], tphase, abort_flag, p.wait_limit_ns) ? 1 : 0;
         if (warp == 2) DT_TRACE_ADD(TR_EPI_TFULL);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);  // tcgen05.ld below is warp-collective

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
       }
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = cid; t < p.total_tiles && !aborted; t += ncl) {
+      for (int t = cid; t < p.total_tiles && !aborted && !p.starve; t += ncl) {
         const TileCoord tc = decode_tile<PAIR_TILE_M>(p, t);
         const Group& G = p.groups[tc.g];
         const int a_row = tc.m0 + static_cast<int>(rank) * BM;
@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
             bool _ok;
             {
               DT_TRACE_T0();
-              _ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
+              _ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.wait_limit_ns);
               DT_TRACE_ADD(TR_PROD_EMPTY);
 #ifdef DT_GEMM_TRACE
               if (p.trace && t_commit[stage] != 0)
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
         bool _ok;
         {
           DT_TRACE_T0();
-          _ok = mbar_wait(&tempty[buf], tphase ^ 1u, abort_flag);
+          _ok = mbar_wait(&tempty[buf], tphase ^ 1u, abort_flag, p.wait_limit_ns);
           DT_TRACE_ADD(TR_MMA_TEMPTY);
         }
         DT_TRACE_COUNT(TR_TILES);
@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
             bool _okf;
             {
               DT_TRACE_T0();
-              _okf = mbar_wait(&full[stage], phase, abort_flag);
+              _okf = mbar_wait(&full[stage], phase, abort_flag, p.wait_limit_ns);
               DT_TRACE_ADD(TR_MMA_FULL);
 #ifdef DT_GEMM_TRACE
               if (p.trace) atomicAdd(&p.trace[blockIdx.x * TRACE_SLOTS + TR_TMA_LAT],
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
       int ok = 1;
       if (lane == 0) {
         DT_TRACE_T0();
-        ok = mbar_wait(&tfull[buf], tphase, abort_flag) ? 1 : 0;
+        ok = mbar_wait(&tfull[buf], tphase, abort_flag, p.wait_limit_ns) ? 1 : 0;
         if (warp == 2) DT_TRACE_ADD(TR_EPI_TFULL);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);  // tcgen05.ld below is warp-collective

@@ -94,6 +94,8 @@ struct Params {  // CUtensorMap carries its own 128-byte alignment
   int32_t ngroups, total_tiles;
   int32_t m_tiles;  // > 0: every group has this many M tiles, rastered together
   int32_t band_m;   // M tiles per raster band
+  int32_t starve;   // test hook: producers issue no loads, so every MMA wait runs out
+  unsigned long long wait_limit_ns;  // bound of every mbarrier wait
   int32_t* status;
   unsigned long long* trace;  // TRACE_SLOTS per CTA when built with DT_GEMM_TRACE, else unused
 };
@@ -160,7 +162,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait for the phase of parity `parity` to complete.  Gives up (and
 // returns false) when another role has raised the CTA's abort flag or after
 // WAIT_LIMIT_NS; the caller then records DT_DEV_ERR_TIMEOUT and unwinds.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long limit_ns = WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   uint32_t spins = 0;
@@ -168,7 +171,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try_wait(bar, parity)) return true;
     if ((++spins & 255u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > WAIT_LIMIT_NS) return false;
+      if (globaltimer() - t0 > limit_ns) return false;
     }
   }
 }
