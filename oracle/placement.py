@@ -48,6 +48,8 @@ class Replicate:
 
 @dataclass(frozen=True)
 class Partial:
+    """A pending reduction across this mesh dim: op is "sum" (the default),
+    "avg" or "max" (Hyper-Parallel DTensor API: Partial(reduce_op))."""
     op: str = "sum"
 
 

@@ -23,6 +23,12 @@ Readings where the pages are silent (listed in the design notes):
 * Replicate -> Partial: coordinate 0 of that mesh dim keeps the value, the
   other coordinates hold zeros, so the partial values still sum to the
   tensor.  Shard -> Partial is not defined here (``NotImplementedError``).
+* Partial(avg): the rank-order fp32 sum, then one correctly rounded fp32
+  division by the number of partial values, then (bf16) one rounding.
+  Partial(max): rank order, a = v if v > a else a, first value as is.
+  Replicate -> Partial(avg / max): every coordinate keeps the value (it is
+  its own average and maximum).  A layout reduces all its Partial dims with
+  one op.
 * Materialised replicas are read at Replicate coordinate 0.
 """
 from __future__ import annotations
@@ -70,10 +76,18 @@ def distribute(global_arr: np.ndarray, layout: Layout, dtype: str) -> list[np.nd
     for slot in range(layout.nslots):
         coords = layout.slot_coords(slot)
         block = np.array(g[_sl(layout.box_of_coords(coords))], dtype=_STORE[dtype], copy=True)
-        if any(coords[m] != 0 for m in layout.partial_dims()):
+        zero_dims = [m for m in layout.partial_dims() if layout.placements[m].op == "sum"]
+        if any(coords[m] != 0 for m in zero_dims):
             block[...] = 0
         out.append(block)
     return out
+
+
+def partial_op(layout: Layout) -> str:
+    ops = {layout.placements[m].op for m in layout.partial_dims()}
+    if len(ops) > 1:
+        raise NotImplementedError("one reduce op per layout")
+    return ops.pop() if ops else "sum"
 
 
 def to_global(locals_: list[np.ndarray], layout: Layout, dtype: str, keep=None) -> np.ndarray:
@@ -84,7 +98,11 @@ def to_global(locals_: list[np.ndarray], layout: Layout, dtype: str, keep=None) 
     """
     keep = dict(keep or {})
     nm = len(layout.mesh_shape)
+    op = partial_op(layout)
     sum_dims = [m for m in layout.partial_dims() if m not in keep]
+    count = 1
+    for m in sum_dims:
+        count *= layout.mesh_shape[m]
     shard_dims = [m for m, p in enumerate(layout.placements) if isinstance(p, Shard)]
     acc = np.zeros(layout.gshape, dtype=_ACC[dtype])
     seen = np.zeros(layout.gshape, dtype=bool)
@@ -108,10 +126,17 @@ def to_global(locals_: list[np.ndarray], layout: Layout, dtype: str, keep=None) 
             val = _widen(local, dtype)
             sl = _sl(box)
             first = ~seen[sl]
-            # first contribution is assigned, later ones are added
-            acc[sl] = np.where(first, val, acc[sl] + val)
+            # first contribution is assigned, later ones are combined
+            if op == "max":
+                acc[sl] = np.where(first, val, np.where(val > acc[sl], val, acc[sl]))
+            else:
+                acc[sl] = np.where(first, val, acc[sl] + val)
             seen[sl] = True
     assert seen.all() or acc.size == 0, "coverage: some global index has no owner"
+    if op == "avg" and sum_dims:
+        if dtype == "int32":
+            raise NotImplementedError("Partial(avg) of int32")
+        acc = (acc.astype(np.float32) / np.float32(count)).astype(np.float32)
     return _narrow(acc, dtype)
 
 
@@ -122,11 +147,15 @@ def redistribute(src_locals, src: Layout, dst: Layout, dtype: str) -> list[np.nd
     nm = len(src.mesh_shape)
     kept = [m for m in range(nm)
             if isinstance(src.placements[m], Partial) and isinstance(dst.placements[m], Partial)]
+    for m in kept:
+        if src.placements[m].op != dst.placements[m].op:
+            raise NotImplementedError("a kept Partial dim cannot change its reduce op")
     zero_rule = []
     for m in range(nm):
         if isinstance(dst.placements[m], Partial) and m not in kept:
             if isinstance(src.placements[m], Replicate):
-                zero_rule.append(m)
+                if dst.placements[m].op == "sum":
+                    zero_rule.append(m)
             else:
                 raise NotImplementedError("Shard -> Partial is not defined")
     cache = {}

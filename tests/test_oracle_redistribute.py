@@ -219,3 +219,55 @@ def test_planted_sum_order_mistake_is_caught(monkeypatch):
     monkeypatch.setattr(rd, "to_global", reversed_order)
     with pytest.raises(AssertionError):
         test_partial_sum_order_is_rank_order()
+
+
+def test_partial_avg_and_max_brute_force():
+    """Partial(avg): rank-order fp32 sum, one fp32 division, one bf16 rounding;
+    Partial(max): rank-order maximum -- checked against scalar loops."""
+    nrng = np.random.default_rng(21)
+    mesh = (2, 3)
+    gshape = (4, 7)
+    for op in ("avg", "max"):
+        src = pl.Layout(mesh, [pl.Partial(op), pl.Shard(1)], gshape)
+        dst = pl.Layout(mesh, [pl.Replicate(), pl.Replicate()], gshape)
+        locals_ = [bf16.round_rne(nrng.standard_normal(src.local_shape(s)) * 7.0) for s in range(src.nslots)]
+        out = rd.redistribute(locals_, src, dst, "bf16")[0]
+        for i in range(gshape[0]):
+            for j in range(gshape[1]):
+                vals = []
+                for c0 in range(2):  # rank order over the Partial dim
+                    c = (c0, None)
+                    for c1 in range(3):
+                        box = src.box_of_coords((c0, c1))
+                        (o0, s0), (o1, s1) = box
+                        if o1 <= j < o1 + s1:
+                            v = bf16.widen(np.array([locals_[src.slot_of_coords((c0, c1))][i - o0, j - o1]]))[0]
+                            vals.append(np.float32(v))
+                if op == "avg":
+                    acc = vals[0]
+                    for v in vals[1:]:
+                        acc = np.float32(acc + v)
+                    ref = np.float32(acc / np.float32(len(vals)))
+                else:
+                    ref = vals[0]
+                    for v in vals[1:]:
+                        ref = v if v > ref else ref
+                assert out[i, j] == bf16.round_rne(np.array([ref], dtype=np.float32))[0], (op, i, j)
+
+
+def test_partial_avg_max_round_trips_and_closed_forms():
+    g = np.arange(24, dtype=np.float32).reshape(4, 6)
+    for op in ("avg", "max"):
+        rep = pl.Layout((4,), [pl.Replicate()], (4, 6))
+        par = pl.Layout((4,), [pl.Partial(op)], (4, 6))
+        lp = rd.redistribute([g], rep, par, "fp32")
+        assert all(np.array_equal(x, g) for x in lp)          # every coordinate keeps the value
+        np.testing.assert_array_equal(rd.redistribute(lp, par, rep, "fp32")[0], g)
+    # avg of 4 partials 1, 2, 3, 6 is 3; max is 6; sum is 12
+    vals = [np.full((1,), v, np.float32) for v in (1.0, 2.0, 3.0, 6.0)]
+    for op, want in (("sum", 12.0), ("avg", 3.0), ("max", 6.0)):
+        src = pl.Layout((4,), [pl.Partial(op)], (1,))
+        assert rd.redistribute(vals, src, pl.Layout((4,), [pl.Replicate()], (1,)), "fp32")[0][0] == want
+    with pytest.raises(NotImplementedError):
+        rd.redistribute(vals, pl.Layout((4,), [pl.Partial("avg")], (1,)), pl.Layout((4,), [pl.Partial("max")], (1,)),
+                        "fp32")
