@@ -81,7 +81,11 @@ typedef enum dt_dtype { DT_BF16 = 0, DT_FP32 = 1, DT_INT32 = 2 } dt_dtype;
 
 /* Placement kinds (Hyper-Parallel DTensor API, placement-type table). */
 typedef enum dt_pkind { DT_REPLICATE = 0, DT_SHARD = 1, DT_PARTIAL = 2 } dt_pkind;
-typedef enum dt_reduce_op { DT_SUM = 0 } dt_reduce_op;
+/* Partial reductions.  SUM adds the partial values in rank order in fp32;
+ * AVG divides that sum once (fp32, correctly rounded) by the number of
+ * partial values; MAX keeps the largest in rank order.  bf16 results are
+ * rounded once at the end.  All Partial dims of one layout use one op. */
+typedef enum dt_reduce_op { DT_SUM = 0, DT_AVG = 1, DT_MAX = 2 } dt_reduce_op;
 
 /* Row-parallel output modes (nanotron 5.1; DTorch RowParallelLinear keeps Partial). */
 typedef enum dt_tp_mode {

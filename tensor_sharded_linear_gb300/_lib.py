@@ -20,7 +20,7 @@ DEV_ERR_TIMEOUT = 0x2
 BF16, FP32, INT32 = 0, 1, 2
 # dt_pkind
 REPLICATE, SHARD, PARTIAL = 0, 1, 2
-SUM = 0
+SUM, AVG, MAX = 0, 1, 2
 # dt_tp_mode
 TP_PARTIAL, TP_ALL_REDUCE, TP_REDUCE_SCATTER = 0, 1, 2
 TP_MLP_STATIC_WORKSPACE_BYTES = 32 * 1024 * 1024

@@ -103,9 +103,10 @@ def _layout(mesh: DeviceMesh, placements, gshape, dtype, materialize) -> L.Layou
         elif isinstance(p, Replicate):
             lay.placements[m].kind = L.REPLICATE
         elif isinstance(p, Partial):
-            if p.reduce_op != "sum":
-                raise ValueError("only Partial(sum) is provided")
-            lay.placements[m].kind, lay.placements[m].op = L.PARTIAL, L.SUM
+            ops = {"sum": L.SUM, "avg": L.AVG, "max": L.MAX}
+            if p.reduce_op not in ops:
+                raise ValueError(f"Partial reduce op {p.reduce_op!r}: one of sum, avg, max")
+            lay.placements[m].kind, lay.placements[m].op = L.PARTIAL, ops[p.reduce_op]
         else:
             raise TypeError(p)
     lay.ndim = len(gshape)

@@ -52,6 +52,12 @@ struct Layout {
   int mesh_size = 1;
   int kind[DT_MAX_MESH_DIMS] = {0, 0, 0, 0};
   int dim[DT_MAX_MESH_DIMS] = {0, 0, 0, 0};  // normalised shard dim
+  int op[DT_MAX_MESH_DIMS] = {0, 0, 0, 0};   // dt_reduce_op of a Partial dim
+  int partial_op() const {                     // the layout's one reduce op (SUM if none)
+    for (int m = 0; m < mesh_ndim; ++m)
+      if (kind[m] == DT_PARTIAL) return op[m];
+    return DT_SUM;
+  }
   int ndim = 0;
   int64_t gshape[DT_MAX_TENSOR_DIMS] = {1, 1, 1, 1};
   int dtype = 0;

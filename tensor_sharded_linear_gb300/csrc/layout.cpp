@@ -106,8 +106,13 @@ dt_status parse_layout(const dt_layout* in, Layout* out) {
       if (d < 0 || d >= L.ndim) return fail(DT_ERR_INVALID_ARG, "Shard(%d) on a rank-%d tensor", p.dim, L.ndim);
       L.dim[m] = d;
     } else if (p.kind == DT_PARTIAL) {
-      if (p.op != DT_SUM) return fail(DT_ERR_UNSUPPORTED, "Partial reduce op %d", p.op);
+      if (p.op != DT_SUM && p.op != DT_AVG && p.op != DT_MAX)
+        return fail(DT_ERR_INVALID_ARG, "Partial reduce op %d", p.op);
+      for (int q = 0; q < m; ++q)
+        if (L.kind[q] == DT_PARTIAL && L.op[q] != p.op)
+          return fail(DT_ERR_UNSUPPORTED, "Partial dims of one layout must share one reduce op");
       L.dim[m] = 0;
+      L.op[m] = p.op;
     } else if (p.kind == DT_REPLICATE) {
       L.dim[m] = 0;
     } else {

@@ -415,6 +415,7 @@ dt_status check_row(const Layout& lx, const Layout& lw, const Layout* lb, const 
       if (mode == DT_TP_REDUCE_SCATTER && !ly.is_shard(m, 0)) return fail(DT_ERR_PLACEMENT, "REDUCE_SCATTER output must be Shard(0) on tp");
       if (mode == DT_TP_REDUCE_SCATTER && nd < 2) return fail(DT_ERR_SHAPE, "REDUCE_SCATTER needs a leading dim");
       if (mode == DT_TP_PARTIAL && !ly.is_partial(m)) return fail(DT_ERR_PLACEMENT, "PARTIAL output must be Partial on tp");
+      if (mode == DT_TP_PARTIAL && ly.op[m] != DT_SUM) return fail(DT_ERR_UNSUPPORTED, "a linear's partial products are summed: Partial(sum) only");
     } else {
       if (!lw.is_replicate(m)) return fail(DT_ERR_PLACEMENT, "weight must be Replicate off tp");
       if (lb && !lb->is_replicate(m)) return fail(DT_ERR_PLACEMENT, "bias must be Replicate off tp");

@@ -90,7 +90,7 @@ struct RdParams {
   int32_t ntasks;
   int32_t dtype;
   int32_t esize;
-  int32_t pad;
+  int32_t op;  // dt_reduce_op of the Partial sources
 };
 
 // ---------------------------------------------------------------- device
@@ -243,19 +243,29 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float to_f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 __device__ __forceinline__ uint16_t from_f(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
 
-// Element-wise Partial sum, rank order, fp32: the first value as is, the
-// others added with round-to-nearest fp32 adds; bf16 rounded once at the end.
+// Reduction step and final step of the Partial ops, in fp32: SUM and AVG
+// add with round-to-nearest adds (AVG then divides once by the count), MAX
+// keeps the larger value (rank order decides between equal ones).
+__device__ __forceinline__ float red_step(float acc, float v, int op) {
+  return op == DT_MAX ? (v > acc ? v : acc) : __fadd_rn(acc, v);
+}
+__device__ __forceinline__ float red_final(float acc, int nsrc, int op) {
+  return op == DT_AVG ? __fdiv_rn(acc, static_cast<float>(nsrc)) : acc;
+}
+
+// Element-wise Partial reduction, rank order, fp32: the first value as is,
+// the others combined by red_step; bf16 rounded once at the end.
 __device__ __forceinline__ void sum_elems(char* d, const char* const* s, int nsrc, int64_t lo, int64_t hi, int64_t dstr,
-                                          const int64_t* sstr, int dtype, int lane) {
+                                          const int64_t* sstr, int dtype, int op, int lane) {
   for (int64_t i = lo + lane; i < hi; i += 32) {
     if (dtype == DT_BF16) {
       float acc = to_f(reinterpret_cast<const uint16_t*>(s[0])[i * sstr[0]]);
-      for (int k = 1; k < nsrc; ++k) acc = __fadd_rn(acc, to_f(reinterpret_cast<const uint16_t*>(s[k])[i * sstr[k]]));
-      reinterpret_cast<uint16_t*>(d)[i * dstr] = from_f(acc);
+      for (int k = 1; k < nsrc; ++k) acc = red_step(acc, to_f(reinterpret_cast<const uint16_t*>(s[k])[i * sstr[k]]), op);
+      reinterpret_cast<uint16_t*>(d)[i * dstr] = from_f(red_final(acc, nsrc, op));
     } else {
       float acc = reinterpret_cast<const float*>(s[0])[i * sstr[0]];
-      for (int k = 1; k < nsrc; ++k) acc = __fadd_rn(acc, reinterpret_cast<const float*>(s[k])[i * sstr[k]]);
-      reinterpret_cast<float*>(d)[i * dstr] = acc;
+      for (int k = 1; k < nsrc; ++k) acc = red_step(acc, reinterpret_cast<const float*>(s[k])[i * sstr[k]], op);
+      reinterpret_cast<float*>(d)[i * dstr] = red_final(acc, nsrc, op);
     }
   }
 }
@@ -263,7 +273,8 @@ __device__ __forceinline__ void sum_elems(char* d, const char* const* s, int nsr
 // Vector body of the Partial sum with the source count fixed at compile time:
 // every lane issues NSRC x VPL 16-byte loads (at most 16) before the first add.
 template <int NSRC, int DTYPE>
-__device__ __forceinline__ void sum_vec(uint4* dv, const char* const* s, int64_t byte_off, int64_t nvec, int lane) {
+__device__ __forceinline__ void sum_vec(uint4* dv, const char* const* s, int64_t byte_off, int64_t nvec, int op,
+                                        int lane) {
   constexpr int EPV = DTYPE == DT_BF16 ? 8 : 4;                        // elements per vector
   constexpr int VPL = NSRC >= 8 ? 2 : 4;                               // vectors per lane per pass
   const uint4* sv[NSRC];
@@ -289,9 +300,11 @@ __device__ __forceinline__ void sum_vec(uint4* dv, const char* const* s, int64_t
 #pragma unroll
         for (int e = 0; e < EPV; ++e) {
           const float f = DTYPE == DT_BF16 ? ((e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1])) : __uint_as_float(w[e]);
-          acc[e] = k == 0 ? f : __fadd_rn(acc[e], f);
+          acc[e] = k == 0 ? f : red_step(acc[e], f, op);
         }
       }
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) acc[e] = red_final(acc[e], NSRC, op);
       uint4 o;
       if (DTYPE == DT_BF16)
         o = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
@@ -306,24 +319,24 @@ __device__ __forceinline__ void sum_vec(uint4* dv, const char* const* s, int64_t
 
 template <int DTYPE>
 __device__ __forceinline__ bool sum_vec_dispatch(uint4* dv, const char* const* s, int nsrc, int64_t off, int64_t nvec,
-                                                 int lane) {
+                                                 int op, int lane) {
   switch (nsrc) {
-    case 2: sum_vec<2, DTYPE>(dv, s, off, nvec, lane); return true;
-    case 3: sum_vec<3, DTYPE>(dv, s, off, nvec, lane); return true;
-    case 4: sum_vec<4, DTYPE>(dv, s, off, nvec, lane); return true;
-    case 8: sum_vec<8, DTYPE>(dv, s, off, nvec, lane); return true;
+    case 2: sum_vec<2, DTYPE>(dv, s, off, nvec, op, lane); return true;
+    case 3: sum_vec<3, DTYPE>(dv, s, off, nvec, op, lane); return true;
+    case 4: sum_vec<4, DTYPE>(dv, s, off, nvec, op, lane); return true;
+    case 8: sum_vec<8, DTYPE>(dv, s, off, nvec, op, lane); return true;
     default: return false;
   }
 }
 
 __device__ void sum_span(char* d, const char* const* s, int nsrc, int64_t n, int64_t dstr, const int64_t* sstr,
-                         int dtype, int lane) {
+                         int dtype, int op, int lane) {
   const uintptr_t da = reinterpret_cast<uintptr_t>(d);
   bool vec = dstr == 1;
   for (int k = 0; k < nsrc; ++k)
     vec = vec && sstr[k] == 1 && ((reinterpret_cast<uintptr_t>(s[k]) ^ da) & 15) == 0;
   if (!vec) {
-    sum_elems(d, s, nsrc, 0, n, dstr, sstr, dtype, lane);
+    sum_elems(d, s, nsrc, 0, n, dstr, sstr, dtype, op, lane);
     return;
   }
   const int esize = dtype == DT_BF16 ? 2 : 4;
@@ -343,12 +356,13 @@ __device__ void sum_span(char* d, const char* const* s, int nsrc, int64_t n, int
                                : reinterpret_cast<const float*>(s[k])[edge];
   }
   uint4* dv = reinterpret_cast<uint4*>(d + head * esize);
-  const bool done = dtype == DT_BF16 ? sum_vec_dispatch<DT_BF16>(dv, s, nsrc, head * esize, nvec, lane)
-                                     : sum_vec_dispatch<DT_FP32>(dv, s, nsrc, head * esize, nvec, lane);
-  if (!done) sum_elems(d, s, nsrc, head, vec_end, 1, sstr, dtype, lane);
+  const bool done = dtype == DT_BF16 ? sum_vec_dispatch<DT_BF16>(dv, s, nsrc, head * esize, nvec, op, lane)
+                                     : sum_vec_dispatch<DT_FP32>(dv, s, nsrc, head * esize, nvec, op, lane);
+  if (!done) sum_elems(d, s, nsrc, head, vec_end, 1, sstr, dtype, op, lane);
   if (edge >= 0) {
     float acc = ev[0];
-    for (int k = 1; k < nsrc; ++k) acc = __fadd_rn(acc, ev[k]);
+    for (int k = 1; k < nsrc; ++k) acc = red_step(acc, ev[k], op);
+    acc = red_final(acc, nsrc, op);
     if (dtype == DT_BF16) reinterpret_cast<uint16_t*>(d)[edge] = from_f(acc);
     else reinterpret_cast<float*>(d)[edge] = acc;
   }
@@ -397,7 +411,7 @@ __global__ void __launch_bounds__(RD_THREADS, SUM ? RD_SUM_CTAS : RD_COPY_CTAS) 
         sp[k] = S.ptr + (R.off + i0 * S.stride[m0] + i1 * S.stride[m1] + i2 * S.stride[m2] + e0 * S.stride[m3]) * esize;
         ss[k] = S.stride[m3];
       }
-      sum_span(d, sp, T.nsrc, n, D.stride[m3], ss, p.dtype, lane);
+      sum_span(d, sp, T.nsrc, n, D.stride[m3], ss, p.dtype, p.op, lane);
     }
   }
 }
@@ -440,9 +454,16 @@ dt_status plan(const DTensor& S, const DTensor& D, std::vector<HostTask>* tasks)
   bool kept[DT_MAX_MESH_DIMS] = {}, summed[DT_MAX_MESH_DIMS] = {}, zeroed[DT_MAX_MESH_DIMS] = {};
   for (int m = 0; m < nm; ++m) {
     if (ld.is_partial(m)) {
-      if (ls.is_partial(m)) kept[m] = true;
-      else if (ls.is_replicate(m)) zeroed[m] = true;
-      else return fail(DT_ERR_UNSUPPORTED, "Shard -> Partial on mesh dim %d is not defined", m);
+      if (ls.is_partial(m)) {
+        if (ls.op[m] != ld.op[m]) return fail(DT_ERR_UNSUPPORTED, "a kept Partial dim cannot change its reduce op");
+        kept[m] = true;
+      } else if (ls.is_replicate(m)) {
+        // SUM: coordinate 0 keeps the value, the others are zero; AVG / MAX:
+        // every coordinate keeps it (a plain copy from the replica)
+        zeroed[m] = ld.op[m] == DT_SUM;
+      } else {
+        return fail(DT_ERR_UNSUPPORTED, "Shard -> Partial on mesh dim %d is not defined", m);
+      }
     } else if (ls.is_partial(m)) {
       summed[m] = true;
     }
@@ -599,6 +620,7 @@ extern "C" dt_status dt_redistribute(const dt_dtensor* src, const dt_dtensor* ds
   for (int s = 0; s < ls.nslots; ++s) fill_slot(&p.src[s], S.slots[s], nd);
   p.dtype = ls.dtype;
   p.esize = ls.esize;
+  p.op = ls.partial_op();
   const int sms = device_sm_count();
 
   auto launch_all = [&](const std::vector<HostTask>& tasks, bool sum) -> dt_status {

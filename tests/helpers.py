@@ -35,7 +35,7 @@ def oracle_placements(pls):
         elif isinstance(p, tsl.Replicate):
             out.append(opl.Replicate())
         else:
-            out.append(opl.Partial())
+            out.append(opl.Partial(p.reduce_op))
     return out
 
 
@@ -47,7 +47,7 @@ def lib_placements(pls):
         elif isinstance(p, opl.Replicate):
             out.append(tsl.Replicate())
         else:
-            out.append(tsl.Partial())
+            out.append(tsl.Partial(p.op))
     return out
 
 

@@ -161,3 +161,46 @@ def test_sweep_transitions(lib, gshape):
         else:
             src_locals = ord_.distribute(g, src, "bf16")
         run_pair(src_locals, src, dst, "bf16")
+
+
+@pytest.mark.parametrize("op", ["avg", "max"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_partial_avg_max_random(lib, op, dtype):
+    """Partial(avg) / Partial(max) sources and destinations on random small
+    layouts, bit-exact against the oracle."""
+    rng = random.Random(hash((op, dtype)) % 1000)
+    nrng = np.random.default_rng(17)
+    done = 0
+    for _ in range(60):
+        nm = rng.randint(1, 3)
+        mesh = tuple(rng.randint(1, 4) for _ in range(nm))
+        nd = rng.randint(1, 3)
+        gshape = tuple(rng.choice([1, 3, 7, 16, 33, 70]) for _ in range(nd))
+
+        def pls():
+            out = []
+            for _ in range(nm):
+                r = rng.random()
+                out.append(S(rng.randrange(nd)) if r < 0.4 else (R if r < 0.65 else opl.Partial(op)))
+            return out
+        src = opl.Layout(mesh, pls(), gshape)
+        dst = opl.Layout(mesh, pls(), gshape)
+        src_locals = [random_values(src.local_shape(s), dtype, nrng) for s in range(src.nslots)]
+        try:
+            ord_.redistribute(src_locals, src, dst, dtype)
+        except NotImplementedError:
+            continue
+        run_pair(src_locals, src, dst, dtype)
+        done += 1
+    assert done >= 10
+
+
+@pytest.mark.parametrize("op", ["avg", "max"])
+def test_partial_avg_max_full_size(lib, op):
+    gshape = workloads.REDISTRIBUTE["shape"]
+    mesh = workloads.REDISTRIBUTE["mesh"]
+    for dp in ([S(0), R], [S(0), S(0)]):
+        src = opl.Layout(mesh, [S(0), opl.Partial(op)], gshape)
+        dst = opl.Layout(mesh, dp, gshape)
+        src_locals = [workloads.redistribute_partials(src.local_shape(s), 1, seed=410 + s)[0] for s in range(src.nslots)]
+        run_pair(src_locals, src, dst, "bf16")
