@@ -168,7 +168,7 @@ def test_sweep_transitions(lib, gshape):
 def test_partial_avg_max_random(lib, op, dtype):
     """Partial(avg) / Partial(max) sources and destinations on random small
     layouts, bit-exact against the oracle."""
-    rng = random.Random(hash((op, dtype)) % 1000)
+    rng = random.Random({"avg": 11, "max": 23}[op] + {"bf16": 0, "fp32": 100}[dtype])
     nrng = np.random.default_rng(17)
     done = 0
     for _ in range(60):
