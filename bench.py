@@ -6,7 +6,9 @@ One STEP is one pass of the whole path over one batch of synthetic input:
      ids [4, 4096] -> Replicate [4, 4096, 4096]
   2. the redistribute sweep on a (dp=2, tp=4) mesh, dp kept Shard(0), for a
      bf16 [8192, 8192] tensor and an uneven [8191, 8190] one:
-     S0->S1, S1->S0, S0->R, S1->R, R->S0, R->S1, P->R, P->S0 on tp
+     S0->S1, S1->S0, S0->R, S1->R, R->S0, R->S1, P->R, P->S0 on tp, all 16
+     moves in one dt_redistribute_batch call (one copy launch, one reduction
+     launch); each move alone is also timed, outside the step
   3. the TP MLP: X [4096, 4096], gate/up [4096, 11008] Shard(1) over 8,
      SiLU*mul, down [11008, 4096] Shard(0), ALL_REDUCE
   4. the TP attention projections: X [8192, 4096], q/k/v [4096, 4096]
@@ -166,7 +168,8 @@ class ClockSampler:
 class Block:
     """Every tensor of one step, resident on one GPU, with prebuilt ABI descriptors."""
 
-    def __init__(self, device, only=("embedding", "redistribute", "mlp", "attention"), weights_kmajor=False):
+    def __init__(self, device, only=("embedding", "redistribute", "mlp", "attention"), weights_kmajor=False,
+                 batch_sweep=True):
         import ctypes as C
 
         import tensor_sharded_linear_gb300 as tsl
@@ -189,6 +192,8 @@ class Block:
         self.wdev = wdev
 
         self.calls = []  # (name, kind, work, fn)
+        self.sweep = []  # (name, bytes, src, dst) of every redistribute transition
+        self.batch_sweep = batch_sweep
         self.h2d = []  # device tensors holding this step's activations
         self.d2h = []  # device tensors holding this step's results
         stream = torch.cuda.current_stream(device).cuda_stream
@@ -242,7 +247,16 @@ class Block:
             tag = "x".join(str(s) for s in gshape)
             for name, a, b in transitions():
                 work = 5 * G if a == "S0P" else 2 * G
-                self._add(f"redistribute {name} {tag}", "bytes", work, "dt_redistribute", src[a], out[b])
+                self.sweep.append((f"redistribute {name} {tag}", work, src[a], out[b]))
+        if self.batch_sweep:
+            # every transition in one dt_redistribute_batch call: one copy
+            # launch and one reduction launch
+            self._add(f"redistribute sweep ({len(self.sweep)} transitions, one batch)", "bytes",
+                      sum(w for _, w, _, _ in self.sweep), "dt_redistribute_batch",
+                      [(a, b) for _, _, a, b in self.sweep])
+        else:
+            for name, work, a, b in self.sweep:
+                self._add(name, "bytes", work, "dt_redistribute", a, b)
 
     def _build_mlp(self, W, dev, DTensor, bf, device, S0, S1, R):
         tsl, L = self.tsl, self.L
@@ -302,6 +316,15 @@ class Block:
             src, dst = args
             a = (desc(src), desc(dst))
             fn = lambda: lib.dt_redistribute(*a, None, stream)  # noqa: E731
+        elif fn_name == "dt_redistribute_batch":
+            (pairs,) = args
+            sdescs = [a._desc() for a, _ in pairs]
+            ddescs = [b._desc() for _, b in pairs]
+            sa = (L.DTensorDesc * len(pairs))(*sdescs)
+            da = (L.DTensorDesc * len(pairs))(*ddescs)
+            keep.extend(sdescs + ddescs + [sa, da])
+            npairs = len(pairs)
+            fn = lambda: lib.dt_redistribute_batch(npairs, sa, da, None, stream)  # noqa: E731
         elif fn_name == "dt_tp_mlp":
             x, wg, wu, wd, y = args
             a = (desc(x), desc(wg), desc(wu), desc(wd), desc(y), L.TP_ALL_REDUCE, 0, self.ws.data_ptr(),
@@ -339,6 +362,32 @@ class Block:
             call()
             if events is not None:
                 events[i][1].record()
+
+    def measure_transitions(self, steps, peaks):
+        """Each sweep transition alone, one dt_redistribute call per
+        transition (outside the timed step): where the batch's time goes."""
+        lib, stream, C = self.lib, self.stream, self.C
+        rows = []
+        for name, work, a, b in self.sweep:
+            da, db = a._desc(), b._desc()
+            rows.append((name, work, da, db))
+        out = {}
+        for name, work, da, db in rows:
+            for _ in range(3):
+                lib.dt_redistribute(C.byref(da), C.byref(db), None, stream)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+            for e0, e1 in evs:
+                e0.record()
+                st = lib.dt_redistribute(C.byref(da), C.byref(db), None, stream)
+                e1.record()
+                if st != self.L.OK:
+                    raise RuntimeError(f"{name}: {lib.dt_last_error().decode()}")
+            torch.cuda.synchronize()
+            ms = statistics.fmean(e0.elapsed_time(e1) for e0, e1 in evs)
+            ach = work / (ms / 1e3) / 1e9
+            out[name] = {"us": round(ms * 1e3, 2), "achieved": round(ach, 1), "unit": "GB/s",
+                         "frac": round(ach / peaks["hbm_gbs"], 4)}
+        return out
 
     def roofline_seconds(self, peaks):
         s = 0.0
@@ -509,8 +558,11 @@ def run_ours(args):
     e2e = None if args.no_e2e else run_e2e(blk, args, peaks, world, device)
     extras = None
     if not args.no_extras and args.only == ALL_COMPONENTS:
+        nx = max(3, min(args.steps, 10))
+        transitions_alone = blk.measure_transitions(nx, peaks)
         ex = Extras(device)
-        extras = ex.measure(max(3, min(args.steps, 10)), peaks)
+        extras = ex.measure(nx, peaks)
+        extras["redistribute transitions, one call each"] = transitions_alone
         del ex
 
     line = {

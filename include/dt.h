@@ -167,6 +167,22 @@ DT_API dt_status dt_redistribute(const dt_dtensor* src, const dt_dtensor* dst, i
                           dt_stream_t stream);
 
 /*
+ * n independent redistributes, src[i] -> dst[i], each with the rules and
+ * results of dt_redistribute.  The pages move one tensor per call; this
+ * batched form (no counterpart there) packs the copies of all n pairs into
+ * one kernel launch and their Partial reductions into one more, as far as a
+ * launch's parameter block holds (128 source and 128 destination slots, 192
+ * boxes, 256 partial references), and starts further launches beyond that.
+ * Pairs may differ in mesh, shape, dtype and reduce op; a launch holds one
+ * dtype (and, for reductions, one op), so each further dtype or op adds a
+ * launch.  No dst[i] may overlap any src[j] or another dst[j] of the same
+ * call: the pairs run concurrently.  Every pair is checked before anything launches; an error
+ * names the pair and nothing runs.  n == 0 is a no-op.
+ */
+DT_API dt_status dt_redistribute_batch(int32_t n, const dt_dtensor* src, const dt_dtensor* dst,
+                                int32_t* d_status, dt_stream_t stream);
+
+/*
  * EmbeddingWithReplicateOutput (DTorch guide, section 2): table Shard(1) on
  * tp (slot i holds [vocab, d_i] bf16 or fp32, d_i from the torch.chunk split
  * of the embedding dim), ids int32 Replicate on tp, out Replicate on tp with

@@ -10,5 +10,6 @@ from .api import (  # noqa: F401
     ColumnParallelLinearWithReplicateOutput, DeviceMesh, DTensor, EmbeddingWithReplicateOutput, Linear, Partial,
     Replicate, ReplicateParallelLinear, RowParallelLinear, RowParallelLinearWithReplicateOutput, Shard,
     column_parallel_linear, column_parallel_linear_multi, init_device_mesh, read_device_status, redistribute,
+    redistribute_batch,
     row_parallel_linear, tp_attention_projections, tp_embedding, tp_mlp, tp_mlp_workspace_bytes)
 from ._lib import DtError  # noqa: F401

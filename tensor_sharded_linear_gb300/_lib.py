@@ -53,6 +53,7 @@ class DTensorDesc(C.Structure):
 
 EXPORTS = [
     "dt_layout_nslots", "dt_layout_slot_of_rank", "dt_layout_slot_box", "dt_redistribute",
+    "dt_redistribute_batch",
     "dt_tp_embedding", "dt_column_parallel_linear", "dt_column_parallel_linear_multi",
     "dt_row_parallel_linear", "dt_tp_mlp_workspace_size", "dt_tp_mlp", "dt_status_string",
     "dt_last_error", "dt_read_device_status", "dt_clear_cache", "dt_version", "dt_launch_count",
@@ -88,6 +89,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
             "dt_layout_slot_of_rank": (st, [P(Layout), C.c_int32, P(C.c_int32)]),
             "dt_layout_slot_box": (st, [P(Layout), C.c_int32, P(C.c_int64), P(C.c_int64)]),
             "dt_redistribute": (st, [D, D, C.c_void_p, C.c_void_p]),
+            "dt_redistribute_batch": (st, [C.c_int32, D, D, C.c_void_p, C.c_void_p]),
             "dt_tp_embedding": (st, [D, D, D, C.c_int32, C.c_void_p, C.c_void_p]),
             "dt_column_parallel_linear": (st, [D, D, D, D, C.c_int32, C.c_void_p, C.c_void_p]),
             "dt_column_parallel_linear_multi": (st, [D, C.c_int32, D, D, D, C.c_int32, C.c_void_p, C.c_void_p]),

@@ -287,6 +287,21 @@ def redistribute(src: DTensor, dst: DTensor) -> None:
             "redistribute")
 
 
+def redistribute_batch(pairs: Sequence[tuple]) -> None:
+    """dt_redistribute_batch: every (src, dst) pair in as few launches as fit
+    (one for the copies, one for the Partial reductions)."""
+    n = len(pairs)
+    if n == 0:
+        return
+    # the descriptors own the slot/stride arrays the copies below point at
+    sdescs = [s._desc() for s, _ in pairs]
+    ddescs = [d._desc() for _, d in pairs]
+    sd = (L.DTensorDesc * n)(*sdescs)
+    dd = (L.DTensorDesc * n)(*ddescs)
+    L.check(L.load().dt_redistribute_batch(n, sd, dd, None, _stream_handle()), "redistribute_batch")
+    del sdescs, ddescs
+
+
 def read_device_status(clear: bool = True) -> int:
     """Synchronise and read the library's device status word (DT_DEV_* bits)."""
     torch.cuda.synchronize()

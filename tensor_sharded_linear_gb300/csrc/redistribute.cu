@@ -45,9 +45,10 @@ namespace {
 #define RD_SUM_CTAS 2
 #endif
 
-constexpr int RD_MAX_TASKS = 64;
+constexpr int RD_MAX_TASKS = 192;
 constexpr int RD_MAX_REFS = 256;
-constexpr int RD_MAX_SRC = 16;
+constexpr int RD_MAX_LAUNCH_SLOTS = 128;  // per side, over every tensor of a batch
+constexpr int RD_MAX_SRC = 16;  // sources a lane keeps addresses of; more take sum_many
 constexpr int RD_THREADS = 256;
 constexpr int RD_WARPS = RD_THREADS / 32;
 constexpr int COPY_SEG_BYTES = RD_COPY_SEG;  // one warp moves up to this much of a row per work item
@@ -66,13 +67,13 @@ struct RdTask {
   int64_t ext[4];
   int64_t dst_off;
   int64_t item_begin;
-  int64_t seg_elems;
-  int32_t dst_slot;
-  int32_t nsrc;
-  int32_t ref_begin;
+  int32_t seg_elems;
   int32_t segs_per_row;
+  int16_t dst_slot;
+  int16_t nsrc;
+  int16_t ref_begin;
   int8_t dmap[4];  // slot stride used for each padded position (dims merged on the host)
-  int32_t pad;
+  int16_t pad;
 };
 
 struct RdRef {
@@ -81,17 +82,26 @@ struct RdRef {
   int32_t pad;
 };
 
-struct RdParams {
-  RdSlot dst[DT_MAX_SLOTS];
-  RdSlot src[DT_MAX_SLOTS];
-  RdTask task[RD_MAX_TASKS];
-  RdRef ref[RD_MAX_REFS];
+// Everything a launch needs travels in its parameter block (limit 32 KB).
+// The block's size costs launch time (about 1 us per 10 KB measured on
+// GB300), so a launch whose tables fit the compact capacities uses the
+// compact block and only large batches take the full one.
+template <int NSLOT, int NTASK, int NREF>
+struct RdParamsT {
+  static constexpr int kSlots = NSLOT, kTasks = NTASK, kRefs = NREF;
+  RdSlot dst[NSLOT];
+  RdSlot src[NSLOT];
+  RdTask task[NTASK];
+  RdRef ref[NREF];
   int64_t nitems;
   int32_t ntasks;
-  int32_t dtype;
+  int32_t dtype;  // one dtype, element size and reduce op per launch
   int32_t esize;
-  int32_t op;  // dt_reduce_op of the Partial sources
+  int32_t op;
 };
+using RdParams = RdParamsT<RD_MAX_LAUNCH_SLOTS, RD_MAX_TASKS, RD_MAX_REFS>;
+using RdParamsSmall = RdParamsT<32, 48, 64>;
+static_assert(sizeof(RdParams) <= 32000, "redistribute parameter block over the launch limit");
 
 // ---------------------------------------------------------------- device
 
@@ -368,23 +378,48 @@ __device__ void sum_span(char* d, const char* const* s, int nsrc, int64_t n, int
   }
 }
 
+// More than RD_MAX_SRC partial sources (several Partial mesh dims): one
+// element per lane per pass, each source's address formed from the parameter
+// block as it is read, in rank order like sum_elems.
+template <class P>
+__device__ void sum_many(char* d, int64_t dstr, const P& p, const RdTask& T, int64_t i0, int64_t i1, int64_t i2,
+                         int64_t e0, int64_t n, int lane) {
+  const int m0 = T.dmap[0], m1 = T.dmap[1], m2 = T.dmap[2], m3 = T.dmap[3];
+  const int esize = p.esize;
+  for (int64_t i = lane; i < n; i += 32) {
+    float acc = 0.f;
+    for (int k = 0; k < T.nsrc; ++k) {
+      const RdRef& R = p.ref[T.ref_begin + k];
+      const RdSlot& S = p.src[R.slot];
+      const char* sp =
+          S.ptr + (R.off + i0 * S.stride[m0] + i1 * S.stride[m1] + i2 * S.stride[m2] + (e0 + i) * S.stride[m3]) * esize;
+      const float v = p.dtype == DT_BF16 ? to_f(*reinterpret_cast<const uint16_t*>(sp))
+                                         : *reinterpret_cast<const float*>(sp);
+      acc = k == 0 ? v : red_step(acc, v, p.op);
+    }
+    acc = red_final(acc, T.nsrc, p.op);
+    if (p.dtype == DT_BF16) reinterpret_cast<uint16_t*>(d)[i * dstr] = from_f(acc);
+    else reinterpret_cast<float*>(d)[i * dstr] = acc;
+  }
+}
+
 // SUM = false: every task copies (nsrc == 1) or zero-fills (nsrc == 0);
 // SUM = true: every task adds nsrc >= 2 partial sources.  One instantiation
 // per kind keeps the copy path's register use low.  Warps take work items
 // (row, segment) in a grid-stride loop.
-template <bool SUM>
-__global__ void __launch_bounds__(RD_THREADS, SUM ? RD_SUM_CTAS : RD_COPY_CTAS) rd_kernel(const __grid_constant__ RdParams p) {
+template <bool SUM, class P>
+__global__ void __launch_bounds__(RD_THREADS, SUM ? RD_SUM_CTAS : RD_COPY_CTAS) rd_kernel(const __grid_constant__ P p) {
   const int lane = threadIdx.x & 31;
-  const int esize = p.esize;
   const int64_t nw = static_cast<int64_t>(gridDim.x) * RD_WARPS;
   int t = 0;
   for (int64_t it = static_cast<int64_t>(blockIdx.x) * RD_WARPS + (threadIdx.x >> 5); it < p.nitems; it += nw) {
     while (t + 1 < p.ntasks && p.task[t + 1].item_begin <= it) ++t;
     const RdTask& T = p.task[t];
+    const int esize = p.esize;
     const int64_t local = it - T.item_begin;
     const int64_t r = local / T.segs_per_row;
     const int64_t e0 = (local - r * T.segs_per_row) * T.seg_elems;
-    const int64_t n = min(T.ext[3] - e0, T.seg_elems);
+    const int64_t n = min(T.ext[3] - e0, static_cast<int64_t>(T.seg_elems));
     const int64_t i2 = r % T.ext[2];
     const int64_t q = r / T.ext[2];
     const int64_t i1 = q % T.ext[1];
@@ -402,6 +437,8 @@ __global__ void __launch_bounds__(RD_THREADS, SUM ? RD_SUM_CTAS : RD_COPY_CTAS) 
           S.ptr + (R.off + i0 * S.stride[m0] + i1 * S.stride[m1] + i2 * S.stride[m2] + e0 * S.stride[m3]) * esize;
       if (D.stride[m3] == 1 && S.stride[m3] == 1) copy_span(d, s, n, esize, lane);
       else copy_span_strided(d, s, n, D.stride[m3], S.stride[m3], esize, lane);
+    } else if (T.nsrc > RD_MAX_SRC) {
+      sum_many(d, D.stride[m3], p, T, i0, i1, i2, e0, n, lane);
     } else {
       const char* sp[RD_MAX_SRC];
       int64_t ss[RD_MAX_SRC];
@@ -475,7 +512,7 @@ dt_status plan(const DTensor& S, const DTensor& D, std::vector<HostTask>* tasks)
   int nsum = 1;
   for (int m = 0; m < nm; ++m)
     if (summed[m]) nsum *= ls.mesh[m];
-  if (nsum > RD_MAX_SRC) return fail(DT_ERR_CAPACITY, "%d partial sources per element (max %d)", nsum, RD_MAX_SRC);
+  if (nsum > RD_MAX_REFS) return fail(DT_ERR_CAPACITY, "%d partial sources per element (max %d)", nsum, RD_MAX_REFS);
 
   int shard_dims[DT_MAX_MESH_DIMS], nshard = 0;
   for (int m = 0; m < nm; ++m)
@@ -574,22 +611,18 @@ void fill_slot(RdSlot* out, const SlotView& v, int ndim) {
   for (int d = 0; d < 4; ++d) out->stride[d] = d < pad ? 0 : v.stride[d - pad];
 }
 
-}  // namespace
-}  // namespace dt
-
-using namespace dt;
-
-extern "C" dt_status dt_redistribute(const dt_dtensor* src, const dt_dtensor* dst, int32_t* d_status,
-                                     dt_stream_t stream) {
-  clear_error();
-  (void)d_status;  // data movement reports no device-side errors
+struct PairPlan {
   DTensor S, D;
-  dt_status st = parse_dtensor(src, &S, "src");
+  std::vector<HostTask> copies, sums;
+};
+
+dt_status plan_pair(const dt_dtensor* src, const dt_dtensor* dst, PairPlan* pp) {
+  dt_status st = parse_dtensor(src, &pp->S, "src");
   if (st != DT_OK) return st;
-  st = parse_dtensor(dst, &D, "dst");
+  st = parse_dtensor(dst, &pp->D, "dst");
   if (st != DT_OK) return st;
-  const Layout& ls = S.layout;
-  const Layout& ld = D.layout;
+  const Layout& ls = pp->S.layout;
+  const Layout& ld = pp->D.layout;
   if (ls.mesh_ndim != ld.mesh_ndim) return fail(DT_ERR_SHAPE, "src and dst meshes differ");
   for (int m = 0; m < ls.mesh_ndim; ++m)
     if (ls.mesh[m] != ld.mesh[m]) return fail(DT_ERR_SHAPE, "src and dst meshes differ");
@@ -597,79 +630,153 @@ extern "C" dt_status dt_redistribute(const dt_dtensor* src, const dt_dtensor* ds
   for (int d = 0; d < ls.ndim; ++d)
     if (ls.gshape[d] != ld.gshape[d]) return fail(DT_ERR_SHAPE, "global shapes differ on dim %d", d);
   if (ls.dtype != ld.dtype) return fail(DT_ERR_INVALID_ARG, "src and dst dtypes differ");
-
   std::vector<HostTask> tasks;
-  st = plan(S, D, &tasks);
-  if (st != DT_OK) return st;
-  if (tasks.empty()) return DT_OK;
-  // a plan either sums (every non-zero-fill task has the same >= 2 sources)
-  // or copies; zero-fill tasks of a summing plan go to a copy launch
-  std::vector<HostTask> sums, copies;
-  for (auto& t : tasks) (t.src_slots.size() >= 2 ? sums : copies).push_back(std::move(t));
+  if ((st = plan(pp->S, pp->D, &tasks)) != DT_OK) return st;
+  // reductions (>= 2 sources) and copies / zero fills run in separate kernels
+  for (auto& t : tasks) (t.src_slots.size() >= 2 ? pp->sums : pp->copies).push_back(std::move(t));
+  return DT_OK;
+}
 
-  const void* any = nullptr;
-  for (auto& v : D.slots)
-    if (v.numel) { any = v.ptr; break; }
-  st = bind_device_of(any);
-  if (st != DT_OK) return st;
+// Launch every task of `plans` of one kind, packing tasks of all pairs into as
+// few launches as the parameter block holds.
+template <class P>
+void launch_rd(const P& p, bool sum, int grid, cudaStream_t stream) {
+  if (sum)
+    rd_kernel<true, P><<<grid, RD_THREADS, 0, stream>>>(p);
+  else
+    rd_kernel<false, P><<<grid, RD_THREADS, 0, stream>>>(p);
+}
 
-  const int nd = ls.ndim;
-  const int pad = 4 - nd;
-  static thread_local RdParams p;  // ~13 KB: keep it off the stack
-  for (int s = 0; s < ld.nslots; ++s) fill_slot(&p.dst[s], D.slots[s], nd);
-  for (int s = 0; s < ls.nslots; ++s) fill_slot(&p.src[s], S.slots[s], nd);
-  p.dtype = ls.dtype;
-  p.esize = ls.esize;
-  p.op = ls.partial_op();
+dt_status launch_kind(std::vector<PairPlan>& plans, bool sum, cudaStream_t stream) {
+  static thread_local RdParams p;  // ~28 KB: off the stack
+  static thread_local RdParamsSmall ps;
   const int sms = device_sm_count();
-
-  auto launch_all = [&](const std::vector<HostTask>& tasks, bool sum) -> dt_status {
-    size_t i = 0;
-    while (i < tasks.size()) {
-      int nt = 0, nref = 0;
-      int64_t items = 0;
-      for (; i < tasks.size() && nt < RD_MAX_TASKS; ++i) {
-        const HostTask& ht = tasks[i];
-        if (nref + (int)ht.src_slots.size() > RD_MAX_REFS) break;
-        RdTask& t = p.task[nt];
-        merge_dims(ht, D, S, pad, &t);
-        t.dst_slot = ht.dst_slot;
-        t.dst_off = local_offset(D.slots[ht.dst_slot], ht.box, nd);
-        t.nsrc = (int)ht.src_slots.size();
-        t.ref_begin = nref;
-        for (int k = 0; k < t.nsrc; ++k) {
-          p.ref[nref].slot = ht.src_slots[k];
-          p.ref[nref].off = local_offset(S.slots[ht.src_slots[k]], ht.box, nd);
-          ++nref;
-        }
-        // segments are whole 16-byte multiples so every segment of a row
-        // keeps the row's alignment
-        const int64_t seg_bytes = sum ? SUM_SEG_BYTES : COPY_SEG_BYTES;
-        t.seg_elems = seg_bytes / ls.esize;
-        const int64_t spr = std::max<int64_t>(1, (t.ext[3] + t.seg_elems - 1) / t.seg_elems);
-        if (spr > (1ll << 30)) return fail(DT_ERR_CAPACITY, "row of %lld elements", (long long)t.ext[3]);
-        t.segs_per_row = (int32_t)spr;
-        const int64_t rows = t.ext[0] * t.ext[1] * t.ext[2];
-        t.item_begin = items;
-        items += rows * spr;
-        ++nt;
+  int nd_slots = 0, ns_slots = 0, nt = 0, nref = 0;
+  int64_t items = 0;
+  auto flush = [&]() -> dt_status {
+    if (nt == 0) return DT_OK;
+    p.ntasks = nt;
+    p.nitems = items;
+    const int64_t blocks = (items + RD_WARPS - 1) / RD_WARPS;
+    // one wave of resident CTAs, grid-stride over items
+    const int grid = (int)std::min<int64_t>(blocks, (int64_t)sms * (sum ? RD_SUM_CTAS : RD_COPY_CTAS));
+    if (grid > 0) {
+      if (nd_slots <= ps.kSlots && ns_slots <= ps.kSlots && nt <= ps.kTasks && nref <= ps.kRefs) {
+        std::copy(p.dst, p.dst + nd_slots, ps.dst);
+        std::copy(p.src, p.src + ns_slots, ps.src);
+        std::copy(p.task, p.task + nt, ps.task);
+        std::copy(p.ref, p.ref + nref, ps.ref);
+        ps.nitems = p.nitems;
+        ps.ntasks = p.ntasks;
+        ps.dtype = p.dtype;
+        ps.esize = p.esize;
+        ps.op = p.op;
+        launch_rd(ps, sum, grid, stream);
+      } else {
+        launch_rd(p, sum, grid, stream);
       }
-      p.ntasks = nt;
-      p.nitems = items;
-      const int64_t blocks = (items + RD_WARPS - 1) / RD_WARPS;
-      // one wave of resident CTAs, grid-stride over items
-      const int grid = (int)std::min<int64_t>(blocks, (int64_t)sms * (sum ? RD_SUM_CTAS : RD_COPY_CTAS));
-      if (sum)
-        rd_kernel<true><<<grid, RD_THREADS, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
-      else
-        rd_kernel<false><<<grid, RD_THREADS, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return fail(DT_ERR_CUDA, "redistribute launch: %s", cudaGetErrorString(e));
       count_launch();
     }
+    nd_slots = ns_slots = nt = nref = 0;
+    items = 0;
     return DT_OK;
   };
-  if ((st = launch_all(copies, false)) != DT_OK) return st;
-  if ((st = launch_all(sums, true)) != DT_OK) return st;
-  return DT_OK;
+  dt_status st;
+  // pairs of one dtype and reduce op share launches: visit them grouped
+  std::vector<int> order(plans.size());
+  for (size_t i = 0; i < plans.size(); ++i) order[i] = (int)i;
+  auto key = [&](int i) { return plans[i].S.layout.dtype * 8 + (sum ? plans[i].S.layout.partial_op() : 0); };
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return key(a) < key(b); });
+  for (int pi : order) {
+    PairPlan& pp = plans[pi];
+    const std::vector<HostTask>& tasks = sum ? pp.sums : pp.copies;
+    if (tasks.empty()) continue;
+    const Layout& ls = pp.S.layout;
+    const int nd = ls.ndim;
+    const int pad = 4 - nd;
+    const int op = sum ? ls.partial_op() : DT_SUM;
+    if (nt > 0 && (p.dtype != ls.dtype || p.op != op))
+      if ((st = flush()) != DT_OK) return st;
+    p.dtype = ls.dtype;
+    p.esize = ls.esize;
+    p.op = op;
+    int dbase = -1, sbase = -1;
+    for (const HostTask& ht : tasks) {
+      const bool need_slots = dbase < 0;
+      const bool fits = nt < RD_MAX_TASKS && nref + (int)ht.src_slots.size() <= RD_MAX_REFS &&
+                        (!need_slots || (nd_slots + pp.D.layout.nslots <= RD_MAX_LAUNCH_SLOTS &&
+                                         ns_slots + ls.nslots <= RD_MAX_LAUNCH_SLOTS));
+      if (!fits) {
+        if ((st = flush()) != DT_OK) return st;
+        dbase = sbase = -1;
+      }
+      if (dbase < 0) {
+        dbase = nd_slots;
+        sbase = ns_slots;
+        for (int s = 0; s < pp.D.layout.nslots; ++s) fill_slot(&p.dst[nd_slots++], pp.D.slots[s], nd);
+        for (int s = 0; s < ls.nslots; ++s) fill_slot(&p.src[ns_slots++], pp.S.slots[s], nd);
+      }
+      RdTask& t = p.task[nt];
+      merge_dims(ht, pp.D, pp.S, pad, &t);
+      t.dst_slot = (int16_t)(dbase + ht.dst_slot);
+      t.dst_off = local_offset(pp.D.slots[ht.dst_slot], ht.box, nd);
+      t.nsrc = (int16_t)ht.src_slots.size();
+      t.ref_begin = (int16_t)nref;
+      for (int k = 0; k < t.nsrc; ++k) {
+        p.ref[nref].slot = sbase + ht.src_slots[k];
+        p.ref[nref].off = local_offset(pp.S.slots[ht.src_slots[k]], ht.box, nd);
+        ++nref;
+      }
+      // segments are whole 16-byte multiples so every segment of a row
+      // keeps the row's alignment
+      const int64_t seg_bytes = sum ? SUM_SEG_BYTES : COPY_SEG_BYTES;
+      t.seg_elems = (int32_t)(seg_bytes / ls.esize);
+      const int64_t spr = std::max<int64_t>(1, (t.ext[3] + t.seg_elems - 1) / t.seg_elems);
+      if (spr > (1ll << 30)) return fail(DT_ERR_CAPACITY, "row of %lld elements", (long long)t.ext[3]);
+      t.segs_per_row = (int32_t)spr;
+      t.item_begin = items;
+      items += t.ext[0] * t.ext[1] * t.ext[2] * spr;
+      ++nt;
+    }
+  }
+  return flush();
+}
+
+dt_status redistribute_many(int32_t n, const dt_dtensor* src, const dt_dtensor* dst, dt_stream_t stream) {
+  clear_error();
+  if (n < 0 || (n > 0 && (!src || !dst))) return fail(DT_ERR_INVALID_ARG, "need n >= 0 and src/dst arrays");
+  std::vector<PairPlan> plans(n);
+  const void* any = nullptr;
+  dt_status st;
+  for (int i = 0; i < n; ++i) {
+    if ((st = plan_pair(&src[i], &dst[i], &plans[i])) != DT_OK) {
+      if (n == 1) return st;
+      std::string inner = dt_last_error();
+      return fail(st, "pair %d: %s", i, inner.c_str());
+    }
+    for (auto& v : plans[i].D.slots)
+      if (!any && v.numel) any = v.ptr;
+  }
+  if (!any) return DT_OK;
+  if ((st = bind_device_of(any)) != DT_OK) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launch_kind(plans, false, s)) != DT_OK) return st;
+  return launch_kind(plans, true, s);
+}
+
+}  // namespace
+}  // namespace dt
+
+extern "C" dt_status dt_redistribute(const dt_dtensor* src, const dt_dtensor* dst, int32_t* d_status,
+                                     dt_stream_t stream) {
+  (void)d_status;  // data movement reports no device-side errors
+  return dt::redistribute_many(1, src, dst, stream);
+}
+
+extern "C" dt_status dt_redistribute_batch(int32_t n, const dt_dtensor* src, const dt_dtensor* dst,
+                                           int32_t* d_status, dt_stream_t stream) {
+  (void)d_status;
+  return dt::redistribute_many(n, src, dst, stream);
 }

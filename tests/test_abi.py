@@ -116,6 +116,16 @@ def test_host_rejections_before_launch(lib):
     bad = fake_desc(opl.Layout(mesh, [S0], (8, 8)))
     bad.nslots = 3
     assert lib.dt_redistribute(C.byref(bad), C.byref(src), None, None) == L.ERR_INVALID_ARG
+    # a batch is checked pair by pair before anything launches; the error names the pair
+    ok_s = fake_desc(opl.Layout(mesh, [S0], (8, 8)))
+    ok_d = fake_desc(opl.Layout(mesh, [S1], (8, 8)))
+    srcs = (L.DTensorDesc * 2)(ok_s, src)
+    dsts = (L.DTensorDesc * 2)(ok_d, fake_desc(opl.Layout(mesh, [P], (8, 8))))
+    assert lib.dt_redistribute_batch(2, srcs, dsts, None, None) == L.ERR_UNSUPPORTED
+    assert lib.dt_last_error().startswith(b"pair 1:")
+    assert lib.dt_redistribute_batch(0, None, None, None, None) == L.OK
+    assert lib.dt_redistribute_batch(-1, srcs, dsts, None, None) == L.ERR_INVALID_ARG
+    assert lib.dt_redistribute_batch(1, None, dsts, None, None) == L.ERR_INVALID_ARG
     # column-parallel input must be Replicate on tp (DTorch check_placement)
     x = fake_desc(opl.Layout(mesh, [S1], (16, 32)))
     w = fake_desc(opl.Layout(mesh, [S1], (32, 64)))

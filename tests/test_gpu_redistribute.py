@@ -19,7 +19,8 @@ from oracle import placement as opl
 from oracle import redistribute as ord_
 from tensor_sharded_linear_gb300 import workloads
 
-from helpers import dtensor_from_locals, lib_placements, locals_of, to_dev
+from helpers import (dtensor_from_locals, lib_placements, locals_of, random_placements, random_values,
+                     sweep_transitions, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -40,27 +41,6 @@ def run_pair(src_locals, src: opl.Layout, dst: opl.Layout, dtype: str):
     for s, (g, e) in enumerate(zip(got, expect)):
         assert g.shape == e.shape, (s, g.shape, e.shape)
         np.testing.assert_array_equal(g, e, err_msg=f"slot {s}: {src.placements} -> {dst.placements}")
-
-
-def random_values(shape, dtype, rng):
-    if dtype == "bf16":
-        return bf16.round_rne(rng.standard_normal(shape) * 10.0 ** rng.integers(-2, 3))
-    if dtype == "fp32":
-        return (rng.standard_normal(shape) * 10.0 ** rng.integers(-2, 3)).astype(np.float32)
-    return rng.integers(-2 ** 31, 2 ** 31 - 1, size=shape, dtype=np.int64).astype(np.int32)
-
-
-def random_placements(rng, nm, nd, allow_partial=True):
-    out = []
-    for _ in range(nm):
-        r = rng.random()
-        if r < 0.5:
-            out.append(S(rng.randrange(nd)))
-        elif r < 0.8 or not allow_partial:
-            out.append(R)
-        else:
-            out.append(P)
-    return out
 
 
 @pytest.mark.parametrize("seed", range(8))
@@ -133,20 +113,6 @@ def test_empty_shards_and_tiny(lib):
             run_pair(src_locals, src, dst, "bf16")
 
 
-def sweep_transitions():
-    """The benchmark's redistribute sweep on a (dp=2, tp=4) mesh; dp kept Shard(0)."""
-    return [
-        ("S0->S1", [S(0), S(0)], [S(0), S(1)]),
-        ("S1->S0", [S(0), S(1)], [S(0), S(0)]),
-        ("S0->R", [S(0), S(0)], [S(0), R]),
-        ("S1->R", [S(0), S(1)], [S(0), R]),
-        ("R->S0", [S(0), R], [S(0), S(0)]),
-        ("R->S1", [S(0), R], [S(0), S(1)]),
-        ("P->R", [S(0), P], [S(0), R]),
-        ("P->S0", [S(0), P], [S(0), S(0)]),
-    ]
-
-
 @pytest.mark.parametrize("gshape", [(256, 320), (1000, 1030), (8192, 8192), (8191, 8190)])
 def test_sweep_transitions(lib, gshape):
     mesh = workloads.REDISTRIBUTE["mesh"]
@@ -204,3 +170,17 @@ def test_partial_avg_max_full_size(lib, op):
         dst = opl.Layout(mesh, dp, gshape)
         src_locals = [workloads.redistribute_partials(src.local_shape(s), 1, seed=410 + s)[0] for s in range(src.nslots)]
         run_pair(src_locals, src, dst, "bf16")
+
+
+@pytest.mark.parametrize("op", ["sum", "avg", "max"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_many_partial_sources(lib, op, dtype):
+    """Partial on every dim of a (2, 3, 4) and a (4, 4, 4) mesh: 24 and 64
+    sources per element, past the vector path's 16, still in rank order."""
+    nrng = np.random.default_rng(31)
+    for mesh, gshape in [((2, 3, 4), (37, 70)), ((4, 4, 4), (9, 33))]:
+        src = opl.Layout(mesh, [opl.Partial(op)] * 3, gshape)
+        for dp in ([R, R, R], [S(1), R, S(0)]):
+            dst = opl.Layout(mesh, dp, gshape)
+            src_locals = [random_values(src.local_shape(s), dtype, nrng) for s in range(src.nslots)]
+            run_pair(src_locals, src, dst, dtype)
