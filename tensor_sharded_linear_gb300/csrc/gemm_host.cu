@@ -5,8 +5,10 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <unordered_map>
 
@@ -67,6 +69,20 @@ struct MapKeyHash {
 
 std::mutex g_map_mu;
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
+// Split-tail scratch, one per (device, stream): the pieces' fp32 partial
+// accumulators and the tiles' arrival counters.  Made on the first split
+// launch on that stream outside a stream capture (cudaMalloc, then the
+// counters zeroed on that stream) and kept until dt_clear_cache.  Every
+// launch that completes leaves the counters at zero again.
+struct SplitScratch {
+  float* part = nullptr;
+  int32_t* count = nullptr;
+  int pieces = 0, counters = 0;
+};
+std::mutex g_split_mu;
+std::map<std::pair<int, uintptr_t>, SplitScratch> g_split;
+thread_local int g_no_alloc = 0;
 
 // 2-D bf16 map over a row-major [rows, cols] matrix with pitch ld elements:
 // box of 64 columns (128 bytes, the swizzle width) by box_rows rows, 128-byte
@@ -251,6 +267,63 @@ int gemm_starve() {
   return v;
 }
 
+// What a split tail costs beyond its share of the MMAs, in 64-deep K
+// iterations of one 256 x 256 pair tile (~0.3 us each): writing the pieces'
+// partials, finishing the tiles, and the tail's operand traffic squeezed
+// into a fraction of a tile's time.  Measured on GB300 at about 20-25 us
+// per launch (the TP MLP down projection gains 15 us; 64-iteration tiles
+// lose 7-20 us).
+constexpr double SPLIT_OVERHEAD_ITERS = 72.0;
+
+// DT_GEMM_SPLIT=0 in the environment turns the split tail off (every tile
+// whole), e.g. to compare the two schedules.
+bool use_split_tail() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("DT_GEMM_SPLIT");
+    v = (e && e[0] == '0') ? 0 : 1;
+  }
+  return v == 1;
+}
+
+// Scratch for `pieces` partial tiles and `counters` counters on this
+// device and stream; nullptr inside a NoAllocScope or when the allocation
+// fails (the launch then runs every tile whole).
+const SplitScratch* split_scratch(cudaStream_t stream, int pieces, int counters) {
+  if (g_no_alloc) return nullptr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lk(g_split_mu);
+  auto key = std::make_pair(dev, reinterpret_cast<uintptr_t>(stream));
+  auto it = g_split.find(key);
+  if (it != g_split.end() && it->second.pieces >= pieces && it->second.counters >= counters) return &it->second;
+  if (it != g_split.end()) return nullptr;  // sized once, for the largest split a launch can make
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();
+    return nullptr;  // no allocation inside a capture; a later uncaptured launch makes the scratch
+  }
+  // the largest split: fewer tail tiles than clusters, so fewer than twice
+  // the clusters pieces and eight counters per tail tile
+  const int cl = std::max(pair_max_clusters(), 1);
+  SplitScratch sc;
+  sc.pieces = std::max(pieces, 2 * cl);
+  sc.counters = std::max(counters, 8 * cl);
+  if (cudaMalloc(&sc.part, (size_t)sc.pieces * 2 * BM * BN_MAX * sizeof(float)) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  // zeroed on the launch's own stream, so it precedes every launch that uses it
+  if (cudaMalloc(&sc.count, (size_t)sc.counters * sizeof(int32_t)) != cudaSuccess ||
+      cudaMemsetAsync(sc.count, 0, (size_t)sc.counters * sizeof(int32_t), stream) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(sc.part);
+    if (sc.count) cudaFree(sc.count);
+    return nullptr;
+  }
+  return &(g_split[key] = sc);
+}
+
 bool use_pair_kernel() {
   static int v = -1;
   if (v < 0) {
@@ -394,8 +467,49 @@ dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStrea
       band = std::max(band, (ctas + total_n - 1) / total_n);
       p.band_m = std::max(1, std::min(band, p.m_tiles > 0 ? p.m_tiles : 1));
     }
+    // Split tail: when the last wave would leave clusters idle, divide the
+    // remaining tiles' K iterations over every cluster, where every tile has
+    // the same K and a cluster's share plus SPLIT_OVERHEAD_ITERS is shorter
+    // than a whole tile.  The finishing stages partials in shared memory,
+    // which bounds the pieces of a tile.
+    p.sk_tiles = 0;
+    p.sk_kiters = 0;
+    p.sk_part = nullptr;
+    p.sk_count = nullptr;
+    int grid = std::min(tiles, ctas);
+    if (pair && tiles > 0 && use_split_tail()) {
+      int ki = -1;
+      bool uniform = true;
+      for (int g = 0; g < p.ngroups; ++g) {
+        int k = 0;
+        for (int si = p.groups[g].seg_begin; si < p.groups[g].seg_begin + p.groups[g].seg_count; ++si)
+          k += p.segs[si].k_tiles;
+        if (ki < 0) ki = k;
+        uniform = uniform && k == ki;
+      }
+      bool dual = false;
+      for (int g = 0; g < p.ngroups; ++g) dual = dual || p.groups[g].dual;
+      const int rem = tiles % ctas;
+      const int64_t share_min = (int64_t)rem * ki / ctas;  // shortest share, in K iterations
+      // most pieces one tile can have: the shares it meets
+      const int np = share_min > 0 ? (int)((ki + share_min - 1) / share_min) + 1 : 0;
+      const double split_cost = (double)rem * ki / ctas + SPLIT_OVERHEAD_ITERS;
+      // a finishing round stages one 32-column chunk of every piece (gate
+      // and up chunks for the gated MLP) in an epilogue warp's half of its
+      // shared-memory quarter
+      const bool fits = np * (dual ? 2 : 1) <= FIN_MAX_PIECES;
+      if (uniform && rem > 0 && share_min >= 8 && fits && split_cost <= ki) {
+        const SplitScratch* sc = split_scratch(stream, rem + ctas - 1, 8 * rem);
+        if (sc) {
+          p.sk_tiles = rem;
+          p.sk_kiters = ki;
+          p.sk_part = sc->part;
+          p.sk_count = sc->count;
+          grid = ctas;
+        }
+      }
+    }
     if (tiles > 0) {
-      const int grid = std::min(tiles, ctas);
       cudaError_t e = pair ? launch_tcgen05_pair(p, grid, stream) : launch_tcgen05(p, grid, stream);
       if (e != cudaSuccess) return fail(DT_ERR_CUDA, "tcgen05 GEMM launch: %s", cudaGetErrorString(e));
       count_launch();
@@ -517,8 +631,44 @@ extern "C" __attribute__((visibility("default"))) int dt_gemm_trace_read(unsigne
 }
 #endif
 
+namespace dt {
+namespace gemm {
+
+NoAllocScope::NoAllocScope() { ++g_no_alloc; }
+NoAllocScope::~NoAllocScope() { --g_no_alloc; }
+
+// After a launch gave up (DT_DEV_ERR_TIMEOUT) its tiles' arrival counters
+// may be left part-counted; zero every counter so later launches start clean.
+void reset_split_counters() {
+  std::lock_guard<std::mutex> lk(g_split_mu);
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (auto& kv : g_split) {
+    cudaSetDevice(kv.first.first);
+    cudaDeviceSynchronize();  // no launch may still be counting
+    cudaMemset(kv.second.count, 0, (size_t)kv.second.counters * sizeof(int32_t));
+    cudaDeviceSynchronize();  // zero before any later launch on any stream
+  }
+  cudaSetDevice(cur);
+}
+
+}  // namespace gemm
+}  // namespace dt
+
 extern "C" dt_status dt_clear_cache(void) {
-  std::lock_guard<std::mutex> lk(dt::gemm::g_map_mu);
-  dt::gemm::g_maps.clear();
+  {
+    std::lock_guard<std::mutex> lk(dt::gemm::g_map_mu);
+    dt::gemm::g_maps.clear();
+  }
+  std::lock_guard<std::mutex> lk(dt::gemm::g_split_mu);
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (auto& kv : dt::gemm::g_split) {
+    cudaSetDevice(kv.first.first);
+    cudaFree(kv.second.part);  // waits for the device's work first
+    cudaFree(kv.second.count);
+  }
+  dt::gemm::g_split.clear();
+  cudaSetDevice(cur);
   return DT_OK;
 }

@@ -32,6 +32,8 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // two per epilogue warp, for finishing split tiles (256 bytes past `full`)
+  uint64_t* fin_bar = full + 32;
 #ifdef DT_GEMM_TRACE
   volatile long long* t_issue = reinterpret_cast<volatile long long*>(drain + 2);   // per stage
   volatile long long* t_commit = t_issue + PAIR_STAGES;
@@ -54,6 +56,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
       mbar_init(&tempty[b], 8);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&fin_bar[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -83,17 +86,21 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
       }
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = cid; t < p.total_tiles && !aborted && !p.starve; t += ncl) {
-        const TileCoord tc = decode_tile<PAIR_TILE_M>(p, t);
+      WorkIter wi(p, cid, ncl);
+      Work w;
+      while (!aborted && !p.starve && wi.next(&w)) {
+        const TileCoord tc = decode_tile<PAIR_TILE_M>(p, w.t);
         const Group& G = p.groups[tc.g];
         const int a_row = tc.m0 + static_cast<int>(rank) * BM;
         // this CTA's B columns: plain tiles split N in halves; the gated MLP
         // puts gate (rank 0) and up (rank 1) side by side
         const int b_col = G.dual ? tc.n0 : tc.n0 + static_cast<int>(rank) * 128;
+        int kbase = 0;  // K iterations of the tile before segment si
         for (int si = G.seg_begin; si < G.seg_begin + G.seg_count && !aborted; ++si) {
           const Seg& S = p.segs[si];
           const CUtensorMap* bmap = &p.maps[(G.dual && rank == 1) ? S.b_map2 : S.b_map];
-          for (int kt = 0; kt < S.k_tiles; ++kt) {
+          const int kt_end = min(S.k_tiles, w.k1 - kbase);
+          for (int kt = max(0, w.k0 - kbase); kt < kt_end; ++kt) {
             bool _ok;
             {
               DT_TRACE_T0();
@@ -128,6 +135,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
               phase ^= 1u;
             }
           }
+          kbase += S.k_tiles;
         }
       }
     }
@@ -139,8 +147,10 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
       int buf = 0;
       uint32_t tphase = 0;
       const uint32_t a_base = smem_u32(smem);
-      for (int t = cid; t < p.total_tiles && !aborted; t += ncl) {
-        const TileCoord tc = decode_tile<PAIR_TILE_M>(p, t);
+      WorkIter wi(p, cid, ncl);
+      Work w;
+      while (!aborted && wi.next(&w)) {
+        const TileCoord tc = decode_tile<PAIR_TILE_M>(p, w.t);
         const Group& G = p.groups[tc.g];
         const bool bk = G.b_kmajor != 0;
         const uint32_t idesc = instr_desc(PAIR_TILE_M, 256, bk);
@@ -159,9 +169,11 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN_MAX);
         uint32_t acc = 0;
+        int kbase = 0;
         for (int si = G.seg_begin; si < G.seg_begin + G.seg_count && !aborted; ++si) {
           const int kts = p.segs[si].k_tiles;
-          for (int kt = 0; kt < kts; ++kt) {
+          const int kt_end = min(kts, w.k1 - kbase);
+          for (int kt = max(0, w.k0 - kbase); kt < kt_end; ++kt) {
             bool _okf;
             {
               DT_TRACE_T0();
@@ -200,6 +212,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
               phase ^= 1u;
             }
           }
+          kbase += kts;
         }
         if (aborted) break;
         mma_commit_pair_mc(&tfull[buf], 0x3);
@@ -216,8 +229,13 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
     const uint32_t tempty0[2] = {mapa_shared(smem_u32(&tempty[0]), 0), mapa_shared(smem_u32(&tempty[1]), 0)};
     int buf = 0;
     uint32_t tphase = 0;
-    for (int t = cid; t < p.total_tiles; t += ncl) {
-      const TileCoord tc = decode_tile<PAIR_TILE_M>(p, t);
+    // split tiles this warp finishes at the end (a cluster holds at most two pieces)
+    int fin_t[2], fin_s[2], fin_first[2], fin_last[2];
+    int nfin = 0;
+    WorkIter wi(p, cid, ncl);
+    Work w;
+    while (wi.next(&w)) {
+      const TileCoord tc = decode_tile<PAIR_TILE_M>(p, w.t);
       const Group& G = p.groups[tc.g];
       int ok = 1;
       if (lane == 0) {
@@ -241,42 +259,51 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
         row_ptr = G.out_ptr[j] + (r - G.out_row_begin[j]) * G.out_ld[j] * esize;
       }
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN_MAX);
-      if (!G.dual) {
-        const int ncols = min(256, G.n - tc.n0);
+      // accumulator columns that hold outputs (the gated MLP: gate 0..127, up 128..255)
+      const int ncols = G.dual ? 256 : min(256, (G.n - tc.n0 + 31) & ~31);
+      if (w.piece < 0) {
+        if (!G.dual) {
+          for (int c = 0; c < ncols; c += 32) {
+            uint32_t raw[32];
+            tmem_ld32(tbase + c, raw);
+            tmem_ld_wait();
+            if (row_ptr) {
+              float v[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(raw[i]);
+              finish_chunk(G, row_ptr, tc.n0 + c, v);
+            }
+          }
+        } else {
+          for (int c = 0; c < 128; c += 32) {
+            uint32_t g[32], u[32];
+            tmem_ld32(tbase + c, g);
+            tmem_ld32(tbase + 128 + c, u);
+            tmem_ld_wait();
+            if (row_ptr) {
+              float gv[32], uv[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                gv[i] = __uint_as_float(g[i]);
+                uv[i] = __uint_as_float(u[i]);
+              }
+              finish_dual(G, row_ptr, tc.n0 + c, gv, uv);
+            }
+          }
+        }
+      } else {
+        // a piece of a split tile: this warp's 32 accumulator rows go to the
+        // piece's slot in sk_part (L2 only), then TMEM is released
+        float4* mine = sk_slot(p, w.piece, rank, quarter) + lane;
         for (int c = 0; c < ncols; c += 32) {
           uint32_t raw[32];
           tmem_ld32(tbase + c, raw);
           tmem_ld_wait();
-          if (row_ptr) {
-            float v[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(raw[i]);
-            if (G.bias_dtype >= 0) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const int col = tc.n0 + c + i;
-                if (col < G.n) v[i] += bias_at(G, col);
-              }
-            }
-            store_row32(G, row_ptr, tc.n0 + c, v);
-          }
-        }
-      } else {
-        for (int c = 0; c < 128; c += 32) {
-          uint32_t g[32], u[32];
-          tmem_ld32(tbase + c, g);
-          tmem_ld32(tbase + 128 + c, u);
-          tmem_ld_wait();
-          if (row_ptr) {
-            float v[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float gv = __uint_as_float(g[i]);
-              const float uv = __uint_as_float(u[i]);
-              v[i] = gv / (1.0f + __expf(-gv)) * uv;  // SiLU(g) * u in fp32
-            }
-            store_row32(G, row_ptr, tc.n0 + c, v);
-          }
+          for (int q = 0; q < 8; ++q)
+            __stcg(mine + ((c >> 5) * 8 + q) * 32,
+                   make_float4(__uint_as_float(raw[4 * q]), __uint_as_float(raw[4 * q + 1]),
+                               __uint_as_float(raw[4 * q + 2]), __uint_as_float(raw[4 * q + 3])));
         }
       }
       tc_fence_before();
@@ -285,6 +312,118 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
       if (++buf == 2) {
         buf = 0;
         tphase ^= 1u;
+      }
+      if (w.piece >= 0) {
+        // the piece whose arrival completes the tile's count finishes the
+        // tile once this CTA's MMAs are all done (see below)
+        __threadfence();
+        __syncwarp();
+        int c_first = 0, c_last = 0, last = 0;
+        if (lane == 0) {
+          sk_tile_clusters(p, ncl, w.s, &c_first, &c_last);
+          int* cnt = p.sk_count + (w.s * 2 + static_cast<int>(rank)) * 4 + quarter;
+          if (atomicAdd(cnt, 1) == c_last - c_first) {
+            last = 1;
+            atomicExch(cnt, 0);  // ready for the next launch
+            __threadfence();
+          }
+        }
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+          fin_t[nfin] = w.t;
+          fin_s[nfin] = w.s;
+          fin_first[nfin] = __shfl_sync(0xffffffffu, c_first, 0);
+          fin_last[nfin] = __shfl_sync(0xffffffffu, c_last, 0);
+          ++nfin;
+        }
+      }
+    }
+
+    // Finish the split tiles this warp completed.  Every MMA of the pair has
+    // finished (the last tfull wait above), so the operand ring is idle:
+    // this warp streams the pieces' partials for its 32 rows into its
+    // quarter of the ring with bulk copies, two rounds in flight, and adds
+    // them in K order from shared memory.
+    uint8_t* fin_base = smem + quarter * FIN_WARP_BYTES;
+    uint32_t fin_phase = 0;  // bit b: parity of the next completion of fin_bar[quarter * 2 + b]
+    for (int f = 0; f < nfin && !aborted; ++f) {
+      const TileCoord tc = decode_tile<PAIR_TILE_M>(p, fin_t[f]);
+      const Group& G = p.groups[tc.g];
+      const int64_t r = tc.m0 + static_cast<int>(rank) * BM + row_in_tile;
+      char* row_ptr = nullptr;
+      if (r < G.m) {
+        int j = 0;
+        while (j + 1 < G.nout && G.out_row_begin[j + 1] <= r) ++j;
+        const int esize = G.out_dtype == DT_BF16 ? 2 : 4;
+        row_ptr = G.out_ptr[j] + (r - G.out_row_begin[j]) * G.out_ld[j] * esize;
+      }
+      const int np = fin_last[f] - fin_first[f] + 1;
+      const int per_round = G.dual ? 2 : 1;  // 32-column chunks per round (gate and up)
+      if (np * per_round > FIN_MAX_PIECES) {  // the host never splits this finely
+        if (lane == 0) atomicOr(p.status, DT_DEV_ERR_INDEX);
+        continue;
+      }
+      const int nrounds = G.dual ? 4 : min(8, (G.n - tc.n0 + 31) >> 5);
+      const int first_piece = fin_s[f] + fin_first[f];
+      auto issue = [&](int rd, int b) {
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          mbar_expect_tx(&fin_bar[quarter * 2 + b], static_cast<uint32_t>(np * per_round * FIN_CHUNK_BYTES));
+          uint8_t* dst = fin_base + b * FIN_BUF_BYTES;
+          for (int q = 0; q < np; ++q)
+            for (int j = 0; j < per_round; ++j) {
+              const int chunk = rd + 4 * j;  // gated MLP: up chunk 4 columns-of-32 after gate
+              bulk_load(dst + (q * per_round + j) * FIN_CHUNK_BYTES,
+                        sk_slot(p, first_piece + q, rank, quarter) + chunk * 8 * 32, FIN_CHUNK_BYTES,
+                        &fin_bar[quarter * 2 + b]);
+            }
+        }
+      };
+      issue(0, 0);
+      for (int rd = 0; rd < nrounds; ++rd) {
+        const int b = rd & 1;
+        if (rd + 1 < nrounds) issue(rd + 1, b ^ 1);  // buffer b^1 was last read in round rd - 1
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(&fin_bar[quarter * 2 + b], (fin_phase >> b) & 1u, abort_flag, p.wait_limit_ns) ? 1 : 0;
+        fin_phase ^= 1u << b;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          aborted = true;
+          *abort_flag = 1;
+          if (lane == 0) {  // let this warp's copies still in flight land before the CTA leaves
+            const uint64_t t0 = globaltimer();
+            while (globaltimer() - t0 < 20000000ull) {
+            }
+          }
+          break;
+        }
+        const float4* buf = reinterpret_cast<const float4*>(fin_base + b * FIN_BUF_BYTES);
+        float v[2][32];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          if (j >= per_round) break;
+          for (int q = 0; q < np; ++q) {
+            const float4* src = buf + (q * per_round + j) * (FIN_CHUNK_BYTES / 16) + lane;
+#pragma unroll
+            for (int qv = 0; qv < 8; ++qv) {
+              const float4 x = src[qv * 32];
+              if (q == 0) {
+                v[j][4 * qv] = x.x;
+                v[j][4 * qv + 1] = x.y;
+                v[j][4 * qv + 2] = x.z;
+                v[j][4 * qv + 3] = x.w;
+              } else {
+                v[j][4 * qv] += x.x;
+                v[j][4 * qv + 1] += x.y;
+                v[j][4 * qv + 2] += x.z;
+                v[j][4 * qv + 3] += x.w;
+              }
+            }
+          }
+        }
+        if (row_ptr) {
+          if (G.dual) finish_dual(G, row_ptr, tc.n0 + rd * 32, v[0], v[1]);
+          else finish_chunk(G, row_ptr, tc.n0 + rd * 32, v[0]);
+        }
+        __syncwarp();  // every lane is done with buffer b before it is refilled
       }
     }
   }

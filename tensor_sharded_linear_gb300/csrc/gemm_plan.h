@@ -51,5 +51,17 @@ cudaError_t launch_tcgen05(const Params& p, int grid, cudaStream_t stream);
 cudaError_t launch_tcgen05_pair(const Params& p, int clusters, cudaStream_t stream);
 int pair_max_clusters();  // co-resident clusters of the pair kernel (0: unavailable)
 
+// While one of these exists on a thread, GEMM launches from that thread
+// neither allocate nor use the split tail's scratch: every tile runs whole.
+struct NoAllocScope {
+  NoAllocScope();
+  ~NoAllocScope();
+  NoAllocScope(const NoAllocScope&) = delete;
+  NoAllocScope& operator=(const NoAllocScope&) = delete;
+};
+
+// Zero the split tail's arrival counters (after a launch reported a timeout).
+void reset_split_counters();
+
 }  // namespace gemm
 }  // namespace dt

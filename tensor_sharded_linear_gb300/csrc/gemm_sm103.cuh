@@ -98,6 +98,17 @@ struct Params {  // CUtensorMap carries its own 128-byte alignment
   unsigned long long wait_limit_ns;  // bound of every mbarrier wait
   int32_t* status;
   unsigned long long* trace;  // TRACE_SLOTS per CTA when built with DT_GEMM_TRACE, else unused
+  // Split tail (pair kernel only).  The last sk_tiles tiles are not given to
+  // clusters whole: their sk_tiles * sk_kiters K iterations are divided
+  // evenly over all clusters, and each (cluster, tile) piece accumulates
+  // its K range on its own.  Every piece writes its fp32 accumulator to
+  // sk_part; the piece whose arrival completes a tile's count (sk_count,
+  // one counter per tile, CTA and 32-row quarter, left at zero) adds all
+  // pieces in K order and runs the tile's epilogue.
+  int32_t sk_tiles;   // 0: every tile whole
+  int32_t sk_kiters;  // K iterations of every tile (uniform when sk_tiles > 0)
+  float* sk_part;     // [piece][2 CTAs][128 rows][256 columns]
+  int32_t* sk_count;  // [sk_tiles][2 CTAs][4 quarters]
 };
 
 #ifdef DT_GEMM_TRACE
@@ -267,7 +278,16 @@ constexpr int PAIR_STAGES = 6;
 constexpr int PAIR_A_BYTES = BM * BK * 2;           // this CTA's 128 rows of A: 16 KiB
 constexpr int PAIR_B_BYTES = 128 * BK * 2;          // this CTA's 128 columns of B: 16 KiB
 constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
-constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + 1024 + 256;
+constexpr int PAIR_BAR_BYTES = 512;  // barriers, flags and (traced builds) timestamps
+constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + 1024 + PAIR_BAR_BYTES;
+// Split-tail finishing reuses the operand ring once a CTA's MMAs are all
+// done: each epilogue warp stages pieces' partials in its own quarter of
+// it, double-buffered.  A round moves one 32-column chunk (two, gate and up,
+// for the gated MLP) of every piece: 4 KiB per chunk per piece.
+constexpr int FIN_WARP_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES / 4;  // 48 KiB
+constexpr int FIN_BUF_BYTES = FIN_WARP_BYTES / 2;
+constexpr int FIN_CHUNK_BYTES = 32 * 32 * 4;                        // 32 rows x 32 fp32 columns
+constexpr int FIN_MAX_PIECES = FIN_BUF_BYTES / FIN_CHUNK_BYTES;     // 6 (3 for the gated MLP)
 constexpr int PAIR_TILE_M = 2 * BM;                 // rows of one pair tile
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -312,6 +332,23 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
           smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
+}
+
+// Untiled bulk copy global -> this CTA's shared memory, completion counted
+// on `bar` (addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  uint64_t g;
+  asm volatile("cvta.to.global.u64 %0, %1;" : "=l"(g) : "l"(gsrc));
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(smem_dst)),
+               "l"(g), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy ones (a bulk copy overwriting what was just read).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Issued by one warp in EACH CTA of the pair.
@@ -388,6 +425,80 @@ __device__ __forceinline__ TileCoord decode_tile(const Params& p, int t) {
   return TileCoord{g, (first_m + r % gm) * TILE_M, (r / gm) * G.bn};
 }
 
+// ---------------------------------------------------------------- work list
+// What one cluster does, in order: whole tiles cid, cid + ncl, ... below
+// the split tail, then its share [b(cid), b(cid + 1)) of the tail's K
+// iterations, b(c) = c * I / ncl, I = sk_tiles * sk_kiters.  The host only
+// splits when a share is shorter than a tile, so a share covers the end of
+// one tail tile and the start of the next at most: one piece each.  The
+// piece of tail tile s done by cluster c has id s + c, unique because both
+// grow along the K axis.
+struct Work {
+  int t;       // tile
+  int k0, k1;  // K iterations [k0, k1) of the tile
+  int piece;   // < 0: the whole tile, finished directly
+  int s;       // tail tile index (pieces only)
+};
+
+__device__ __forceinline__ int64_t sk_bound(int c, int64_t total, int ncl) { return (int64_t)c * total / ncl; }
+
+struct WorkIter {
+  int cid, ncl, t_dp, dp_end, kiters;
+  int64_t it, it_end;
+  __device__ WorkIter(const Params& p, int cid_, int ncl_) : cid(cid_), ncl(ncl_) {
+    dp_end = p.total_tiles - p.sk_tiles;
+    t_dp = cid;
+    kiters = p.sk_kiters;
+    const int64_t total = (int64_t)p.sk_tiles * p.sk_kiters;
+    it = p.sk_tiles > 0 ? sk_bound(cid, total, ncl) : 0;
+    it_end = p.sk_tiles > 0 ? sk_bound(cid + 1, total, ncl) : 0;
+  }
+  __device__ bool next(Work* w) {
+    if (t_dp < dp_end) {
+      w->t = t_dp;
+      w->k0 = 0;
+      w->k1 = 1 << 30;
+      w->piece = -1;
+      w->s = -1;
+      t_dp += ncl;
+      return true;
+    }
+    if (it >= it_end) return false;
+    const int s = (int)(it / kiters);
+    const int k0 = (int)(it - (int64_t)s * kiters);
+    const int64_t k1_wide = k0 + (it_end - it);
+    const int k1 = k1_wide < kiters ? (int)k1_wide : kiters;
+    w->t = dp_end + s;
+    w->k0 = k0;
+    w->k1 = k1;
+    w->piece = s + cid;
+    w->s = s;
+    it += k1 - k0;
+    return true;
+  }
+};
+
+// A piece's fp32 accumulator in sk_part, per (CTA, 32-row quarter): 8
+// column chunks x 8 float4 x 32 lanes, so every warp access to it moves
+// 512 contiguous bytes (lane = accumulator row within the quarter).
+__device__ __forceinline__ float4* sk_slot(const Params& p, int piece, uint32_t rank, int quarter) {
+  return reinterpret_cast<float4*>(p.sk_part) + ((static_cast<size_t>(piece) * 2 + rank) * 4 + quarter) * (8 * 8 * 32);
+}
+
+// Clusters whose shares meet tail tile s: [c_first, c_last].
+__device__ __forceinline__ void sk_tile_clusters(const Params& p, int ncl, int s, int* c_first, int* c_last) {
+  const int64_t total = (int64_t)p.sk_tiles * p.sk_kiters;
+  const int64_t lo = (int64_t)s * p.sk_kiters, hi = lo + p.sk_kiters;  // [lo, hi)
+  const int64_t c_est = lo * ncl / total;
+  int c = c_est < ncl - 1 ? (int)c_est : ncl - 1;
+  while (c + 1 < ncl && sk_bound(c + 1, total, ncl) <= lo) ++c;
+  while (c > 0 && sk_bound(c, total, ncl) > lo) --c;
+  *c_first = c;
+  int e = c;
+  while (e + 1 < ncl && sk_bound(e + 1, total, ncl) < hi) ++e;
+  *c_last = e;
+}
+
 // MMA width of a tile: the gated MLP always uses both 128-column halves;
 // otherwise the tile's remaining columns rounded up to the MMA's N step of 16.
 __device__ __forceinline__ int tile_mma_n(const Group& G, int n0) {
@@ -436,6 +547,27 @@ __device__ __forceinline__ void store_row32(const Group& G, char* row_ptr, int c
         if (i < valid) o[i] = v[i];
     }
   }
+}
+
+// Epilogue of 32 accumulator columns of one row: bias, cast, store.
+__device__ __forceinline__ void finish_chunk(const Group& G, char* row_ptr, int col0, float (&v)[32]) {
+  if (G.bias_dtype >= 0) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int col = col0 + i;
+      if (col < G.n) v[i] += bias_at(G, col);
+    }
+  }
+  store_row32(G, row_ptr, col0, v);
+}
+
+// Gated-MLP epilogue of 32 columns of one row: SiLU(g) * u in fp32, cast, store.
+__device__ __forceinline__ void finish_dual(const Group& G, char* row_ptr, int col0, const float (&g)[32],
+                                            const float (&u)[32]) {
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
+  store_row32(G, row_ptr, col0, v);
 }
 
 }  // namespace gemm

@@ -16,6 +16,7 @@
 #include <mutex>
 
 #include "dt_internal.h"
+#include "gemm_plan.h"
 
 namespace dt {
 namespace {
@@ -78,7 +79,9 @@ extern "C" dt_status dt_tp_mlp_static_workspace(const dt_dtensor* x, const dt_dt
   void* ws = nullptr;
   if ((st = static_workspace_address(&ws)) != DT_OK) return st;
   // H is written in full by the gate/up GEMM before the down GEMM reads it,
-  // so nothing in the array needs clearing between calls.
+  // so nothing in the array needs clearing between calls.  The GEMMs run
+  // every tile whole: the split tail's scratch would be an allocation.
+  gemm::NoAllocScope no_alloc;
   return dt_tp_mlp(x, w_gate, w_up, w_down, y, mode, tp_mesh_dim, ws, (size_t)DT_TP_MLP_STATIC_WORKSPACE_BYTES,
                    d_status, stream);
 }

@@ -1,0 +1,224 @@
+"""GPU parity of the GEMM's split tail against the fp64 oracle.
+
+When the last wave of 256 x 256 tiles would leave CTA pairs idle and the
+tiles are long in K, the tail tiles' K iterations are divided over every pair; each piece writes an
+fp32 partial accumulator and the piece that completes a tile's count adds
+them in K order and runs the epilogue.  The shapes below have fewer tiles
+than the 76 pairs a GB300 holds and enough K for the split to pay:
+column (bias, ragged M/N/K, fp32 and bf16 outputs), row-parallel in every
+output mode, the gated MLP (gate/up end to end, down on the oracle's H)
+and fused q/k/v.  Also: the
+split result is bit-identical from launch to launch (the partials are
+added in a fixed order and the arrival counters return to zero), two
+streams split concurrently with separate scratch, and the unsplit schedule
+(DT_GEMM_SPLIT=0, in a child process) agrees with the oracle on the same
+shapes.  Tolerances as in the other linear tests (the MLP output: the
+relative Frobenius bound, for the reason its test gives).
+"""
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+import tensor_sharded_linear_gb300 as tsl
+from oracle import linear as olin
+from oracle.placement import chunk_bounds
+from tensor_sharded_linear_gb300 import workloads
+
+from helpers import to_dev, to_host
+from test_gpu_linear import (REL_FRO_TOL, check_bf16, check_bf16_pair, check_fp32, col_dtensor, mesh1, row_dtensor,
+                             w64, x_rep, x_shard)
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def ceil_div(a, b):
+    return -(-a // b)
+
+
+def split_expected(tiles, kiters, dual=False, pairs=76):
+    """The library's rule: a pair's share of the tail's K iterations plus
+    the split's fixed cost (72 iterations) is shorter than a tile, and a
+    finishing round's partials fit the epilogue warp's buffer."""
+    rem = tiles % pairs
+    share_min = rem * kiters // pairs
+    if rem == 0 or share_min < 8:
+        return False
+    np_ = ceil_div(kiters, share_min) + 1
+    return np_ * (2 if dual else 1) <= 6 and rem * kiters / pairs + 72 <= kiters
+
+
+def column_case(seed=11):
+    M, K, N, p = 300, 12000, 4 * 520, 4
+    assert split_expected(ceil_div(M, 256) * p * ceil_div(N // p, 256), ceil_div(K, 64))
+    x = workloads.randn_bf16((M, K), seed)
+    w = workloads.randn_bf16((K, N), seed + 1, (1.0 / K) ** 0.5)
+    b = workloads.randn_bf16((N,), seed + 2, 0.5)
+    bd = tsl.DTensor([to_dev(np.ascontiguousarray(b[o:o + s]), "bf16") for o, s in chunk_bounds(N, p)], mesh1(p),
+                     [tsl.Shard(0)], (N,), torch.bfloat16)
+    expect = olin.column_parallel(w64(x), [w64(w[:, o:o + s]) for o, s in chunk_bounds(N, p)],
+                                  [w64(b[o:o + s]) for o, s in chunk_bounds(N, p)])
+    return x_rep(x, p), col_dtensor(w, p), bd, expect
+
+
+def test_column_split(lib):
+    xd, wd, bd, expect = column_case()
+    y32 = tsl.column_parallel_linear(xd, wd, bd, out_dtype=torch.float32)
+    y16 = tsl.column_parallel_linear(xd, wd, bd)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    for i, e in enumerate(expect):
+        f = to_host(y32.slots[i], "fp32")
+        check_fp32(f, e, f"shard {i}")
+        check_bf16(to_host(y16.slots[i], "bf16"), f, e, f"shard {i}")
+
+
+@pytest.mark.parametrize("mode", [tsl.ALL_REDUCE, tsl.REDUCE_SCATTER, tsl.PARTIAL])
+def test_row_split(lib, mode):
+    """ALL_REDUCE and REDUCE_SCATTER split (one group, 4 K segments); the
+    PARTIAL launch (one group per shard) is too short to split and runs
+    whole, checked all the same."""
+    M, K, N, p = 700, 4 * 2000, 1300, 4
+    tiles = ceil_div(M, 256) * ceil_div(N, 256) * (p if mode == tsl.PARTIAL else 1)
+    kiters = ceil_div(K // p, 64) * (1 if mode == tsl.PARTIAL else p)
+    assert split_expected(tiles, kiters) == (mode != tsl.PARTIAL)
+    x = workloads.randn_bf16((M, K), 41)
+    w = workloads.randn_bf16((K, N), 42, (1.0 / K) ** 0.5)
+    b = workloads.randn_bf16((N,), 43, 0.5)
+    bd = tsl.DTensor([to_dev(b, "bf16")], mesh1(p), [tsl.Replicate()], (N,), torch.bfloat16)
+    xd, wd = x_shard(x, p), row_dtensor(w, p)
+    y32 = tsl.row_parallel_linear(xd, wd, bd, mode=mode, out_dtype=torch.float32)
+    y16 = tsl.row_parallel_linear(xd, wd, bd, mode=mode)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    omode = {tsl.ALL_REDUCE: olin.ALL_REDUCE, tsl.REDUCE_SCATTER: olin.REDUCE_SCATTER, tsl.PARTIAL: olin.PARTIAL}[mode]
+    expect = olin.row_parallel([w64(x[:, o:o + s]) for o, s in chunk_bounds(K, p)],
+                               [w64(w[o:o + s]) for o, s in chunk_bounds(K, p)], w64(b), omode, parts=p)
+    for i, e in enumerate(expect):
+        f = to_host(y32.slots[i], "fp32")
+        check_fp32(f, e, f"{mode} out {i}")
+        check_bf16(to_host(y16.slots[i], "bf16"), f, e, f"{mode} out {i}")
+
+
+def test_mlp_split(lib):
+    """The fused MLP with its gated gate/up GEMM split (40 dual tiles, 157 K
+    iterations).  The split GEMM's output, H, is checked per element; the
+    MLP output with the relative Frobenius bound.  (Its max-abs error also
+    carries H's bf16 rounding: where the kernel's fp32 SiLU(g)*u and the
+    oracle's fp64 one round to neighbouring bf16 values, each such element
+    moves outputs by one bf16 ulp of H times a weight, which at this K can
+    pass 2e-3 on a few outputs with either schedule.  The down GEMM's split
+    is test_mlp_down_split, on the oracle's H.)"""
+    M, K, F, N, p = 256, 10000, 8 * 640, 384, 8
+    assert split_expected(ceil_div(M, 256) * p * ceil_div(F // p, 128), ceil_div(K, 64), dual=True)
+    x, wg, wu, wd = workloads.mlp_inputs(M, K, F, seed_base=700)
+    wd = workloads.randn_bf16((F, N), 704, (1.0 / F) ** 0.5)
+    xd = x_rep(x, p)
+    ws = torch.empty(tsl.tp_mlp_workspace_bytes(xd, col_dtensor(wg, p)), dtype=torch.uint8, device="cuda")
+    y = tsl.tp_mlp(xd, col_dtensor(wg, p), col_dtensor(wu, p), row_dtensor(wd, p), mode=tsl.ALL_REDUCE,
+                   out_dtype=torch.float32, workspace=ws)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    cols = chunk_bounds(F, p)
+    expect, hs = olin.tp_mlp(w64(x), [w64(wg[:, o:o + s]) for o, s in cols], [w64(wu[:, o:o + s]) for o, s in cols],
+                             [w64(wd[o:o + s]) for o, s in cols], olin.ALL_REDUCE)
+    check_bf16_pair(to_host(tsl.api.mlp_hidden_view(xd, col_dtensor(wg, p), ws), "bf16"),
+                    np.concatenate(hs, axis=-1), "H")
+    got = to_host(y.slots[0], "fp32").astype(np.float64)
+    assert np.isfinite(got).all()
+    fro = np.linalg.norm(got - expect[0]) / np.linalg.norm(expect[0])
+    assert fro <= REL_FRO_TOL, fro
+
+
+def test_mlp_down_split(lib):
+    """The MLP's down projection split (20 tiles, 8 segments of 16 K
+    iterations), fed the oracle's own bf16 H: ALL_REDUCE of H_i Wd_i."""
+    M, K, F, N, p = 512, 256, 8 * 1024, 2560, 8
+    assert split_expected(ceil_div(M, 256) * ceil_div(N, 256), p * ceil_div(F // p, 64))
+    x, wg, wu, _ = workloads.mlp_inputs(M, K, F, seed_base=720)
+    wd = workloads.randn_bf16((F, N), 724, (1.0 / F) ** 0.5)
+    cols = chunk_bounds(F, p)
+    hs = olin.mlp_hidden(w64(x), [w64(wg[:, o:o + s]) for o, s in cols], [w64(wu[:, o:o + s]) for o, s in cols])
+    h = np.concatenate(hs, axis=-1)
+    y = tsl.row_parallel_linear(x_shard(h, p), row_dtensor(wd, p), mode=tsl.ALL_REDUCE, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    expect = olin.row_parallel([w64(hi) for hi in hs], [w64(wd[o:o + s]) for o, s in cols], None, olin.ALL_REDUCE)
+    check_fp32(to_host(y.slots[0], "fp32"), expect[0], "down projection")
+
+
+def test_qkv_split(lib):
+    """Fused q/k/v: 3 weights x 4 shards, 24 tiles of 128 K iterations."""
+    T, K, N, p = 512, 8192, 1024, 4
+    assert split_expected(ceil_div(T, 256) * 3 * p * ceil_div(N // p, 256), ceil_div(K, 64))
+    x = workloads.randn_bf16((T, K), 751)
+    ws = [workloads.randn_bf16((K, N), 752 + j, (1.0 / K) ** 0.5) for j in range(3)]
+    ys = tsl.column_parallel_linear_multi(x_rep(x, p), [col_dtensor(w, p) for w in ws], out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    for j, w in enumerate(ws):
+        expect = olin.column_parallel(w64(x), [w64(w[:, o:o + s]) for o, s in chunk_bounds(N, p)])
+        for i in range(p):
+            check_fp32(to_host(ys[j].slots[i], "fp32"), expect[i], f"weight {j} shard {i}")
+
+
+def test_split_is_deterministic(lib):
+    """Ten launches of one split GEMM give the same bits: fixed summation
+    order, and every launch leaves the arrival counters at zero."""
+    xd, wd, bd, expect = column_case(seed=21)
+    out = tsl.column_parallel_linear(xd, wd, bd, out_dtype=torch.float32)
+    first = [t.clone() for t in out.slots]
+    for _ in range(10):
+        tsl.column_parallel_linear(xd, wd, bd, out_dtype=torch.float32, out=out)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    for a, b in zip(first, out.slots):
+        assert torch.equal(a, b)
+    for i, e in enumerate(expect):
+        check_fp32(to_host(out.slots[i], "fp32"), e, f"shard {i}")
+
+
+def test_split_on_two_streams(lib):
+    """Two streams run split GEMMs at the same time, each with its own scratch."""
+    cases = [column_case(seed=31), column_case(seed=41)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    torch.cuda.synchronize()
+    for (xd, wd, bd, _), s in zip(cases, streams):
+        with torch.cuda.stream(s):
+            outs.append(tsl.column_parallel_linear(xd, wd, bd, out_dtype=torch.float32))
+    for _ in range(3):  # interleave more launches on both
+        for (xd, wd, bd, _), s, o in zip(cases, streams, outs):
+            with torch.cuda.stream(s):
+                tsl.column_parallel_linear(xd, wd, bd, out_dtype=torch.float32, out=o)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    for (_, _, _, expect), o in zip(cases, outs):
+        for i, e in enumerate(expect):
+            check_fp32(to_host(o.slots[i], "fp32"), e, f"shard {i}")
+
+
+CHILD = r"""
+import sys
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+import test_gpu_split_tail as T
+T.test_column_split(None)
+T.test_row_split(None, T.tsl.ALL_REDUCE)
+T.test_mlp_split(None)
+T.test_mlp_down_split(None)
+print("OK")
+"""
+
+
+def test_unsplit_schedule_agrees(lib):
+    """The same shapes with every tile whole (DT_GEMM_SPLIT=0)."""
+    env = dict(os.environ, DT_GEMM_SPLIT="0")
+    code = CHILD.format(root=ROOT, tests=os.path.join(ROOT, "tests"))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "OK" in r.stdout
