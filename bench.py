@@ -407,9 +407,11 @@ class Extras:
     """Rows built beyond the hot path, timed separately (not part of `value`):
     the sequence-parallel q/k/v entry (x token-sharded, read in place), the
     fused Replicate-output column linear, q/k/v with [out, in] weights (K-major
-    B), and the Ulysses Shard(2) -> Shard(1) move of [2, 32, 8192, 128]."""
+    B), the Ulysses Shard(2) -> Shard(1) move of [2, 32, 8192, 128], and the
+    secondary rows of the step's own operations: S0/S1 -> Replicate with a
+    materialised copy per rank, and the TP MLP and q/k/v with fp32 outputs."""
 
-    def __init__(self, device):
+    def __init__(self, device, blk=None):
         import tensor_sharded_linear_gb300 as tsl
         from tensor_sharded_linear_gb300 import workloads as W
         from tensor_sharded_linear_gb300.api import DTensor
@@ -449,6 +451,41 @@ class Extras:
         self._keep2 = (useq, uhead)
         self.items.append(("Ulysses S(2)->S(1) [2,32,8192,128]", "bytes", 2 * 2 * int(np.prod(shape)),
                            lambda: tsl.redistribute(useq, uhead)))
+        # secondary rows: Replicate outputs materialised per rank (read G,
+        # write 4G) and fp32-output variants of the GEMMs
+        rmesh = tsl.DeviceMesh(W.REDISTRIBUTE["mesh"], ("dp", "tp"), device=device)
+        rshape = W.REDISTRIBUTE["shape"]
+        rg = dev(W.redistribute_global(rshape))
+        S0, S1, R = tsl.Shard(0), tsl.Shard(1), tsl.Replicate()
+        rsrc = {k: DTensor.distribute_tensor(rg, rmesh, pl) for k, pl in (("S0", [S0, S0]), ("S1", [S0, S1]))}
+        rdst = DTensor.empty(rmesh, [S0, R], rshape, bf, materialize_replicas=True, device=device)
+        del rg
+        self._keep3 = (rsrc, rdst)
+        G = 2 * int(np.prod(rshape))
+        for k in ("S0", "S1"):
+            self.items.append((f"redistribute {k}->R materialised [8192,8192]", "bytes", 5 * G,
+                               lambda k=k: tsl.redistribute(rsrc[k], rdst)))
+        mlp = [c for c in blk.calls if c[0] == "tp_mlp"] if blk is not None else []
+        if mlp:
+            # the step's own MLP tensors, an fp32 output, descriptors built once
+            import ctypes as C
+            from tensor_sharded_linear_gb300 import _lib as L
+            xm, wgm, wum, wdm, ym16 = mlp[0][3]._keep[:5]
+            ym = DTensor.empty(xm.mesh, [R], ym16.gshape, torch.float32, device=device)
+            descs = [d._desc() for d in (xm, wgm, wum, wdm, ym)]
+            lib, stream = L.load(), torch.cuda.current_stream(device).cuda_stream
+            self._keep4 = (ym, descs)
+
+            def mlp32():
+                st = lib.dt_tp_mlp(*[C.byref(d) for d in descs], L.TP_ALL_REDUCE, 0, blk.ws.data_ptr(),
+                                   blk.ws.numel(), None, stream)
+                if st != L.OK:
+                    raise RuntimeError(lib.dt_last_error().decode())
+            self.items.append(("TP MLP, fp32 output", "flops", MLP_FLOPS, mlp32))
+        outs32 = [DTensor.empty(mesh, [tsl.Shard(1)], (T, H), torch.float32, device=device) for _ in range(3)]
+        self._keep5 = outs32
+        self.items.append(("q/k/v, fp32 outputs", "flops", qkv_flops,
+                           lambda: tsl.column_parallel_linear_multi(x_rep, ws, outs=outs32)))
 
     def measure(self, steps, peaks):
         for _, _, _, fn in self.items:  # warm up every item (descriptor caches, first launches)
@@ -567,7 +604,7 @@ def run_ours(args):
     if not args.no_extras and args.only == ALL_COMPONENTS:
         nx = max(3, min(args.steps, 10))
         transitions_alone = blk.measure_transitions(nx, peaks)
-        ex = Extras(device)
+        ex = Extras(device, blk)
         extras = ex.measure(nx, peaks)
         extras["redistribute transitions, one call each"] = transitions_alone
         del ex

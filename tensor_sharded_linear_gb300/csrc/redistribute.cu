@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <mutex>
 #include <vector>
 
 #include "dt_internal.h"
@@ -744,6 +745,50 @@ dt_status launch_kind(std::vector<PairPlan>& plans, bool sum, cudaStream_t strea
   return flush();
 }
 
+// The copies and the Partial reductions of one call are independent (no
+// output overlaps an input), so the reductions run on an auxiliary stream
+// forked from the caller's and joined back before the call returns: one
+// launch's ramp and tail overlap the other's.  One auxiliary stream and
+// event pair per device, made on first use and kept; the mutex keeps
+// concurrent callers' fork/join pairs apart.
+struct AuxStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool failed = false;
+};
+std::mutex g_aux_mu;
+AuxStream g_aux[64];
+
+dt_status launch_forked(std::vector<PairPlan>& plans, cudaStream_t s) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::unique_lock<std::mutex> lk(g_aux_mu);
+  AuxStream* a = (dev >= 0 && dev < 64) ? &g_aux[dev] : nullptr;
+  if (a && !a->s && !a->failed) {
+    if (cudaStreamCreateWithFlags(&a->s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&a->fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&a->join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      a->failed = true;
+    }
+  }
+  dt_status st;
+  if (!a || a->failed || cudaEventRecord(a->fork, s) != cudaSuccess ||
+      cudaStreamWaitEvent(a->s, a->fork, 0) != cudaSuccess) {
+    cudaGetLastError();
+    lk.unlock();
+    if ((st = launch_kind(plans, false, s)) != DT_OK) return st;  // one stream, one after the other
+    return launch_kind(plans, true, s);
+  }
+  st = launch_kind(plans, true, a->s);
+  if (st == DT_OK) st = launch_kind(plans, false, s);
+  // join even after a failed launch, so the caller's stream never runs ahead of the auxiliary one
+  cudaError_t e = cudaEventRecord(a->join, a->s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, a->join, 0);
+  if (e != cudaSuccess && st == DT_OK) st = fail(DT_ERR_CUDA, "redistribute join: %s", cudaGetErrorString(e));
+  return st;
+}
+
 dt_status redistribute_many(int32_t n, const dt_dtensor* src, const dt_dtensor* dst, dt_stream_t stream) {
   clear_error();
   if (n < 0 || (n > 0 && (!src || !dst))) return fail(DT_ERR_INVALID_ARG, "need n >= 0 and src/dst arrays");
@@ -762,6 +807,12 @@ dt_status redistribute_many(int32_t n, const dt_dtensor* src, const dt_dtensor* 
   if (!any) return DT_OK;
   if ((st = bind_device_of(any)) != DT_OK) return st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  bool copies = false, sums = false;
+  for (const PairPlan& pp : plans) {
+    copies = copies || !pp.copies.empty();
+    sums = sums || !pp.sums.empty();
+  }
+  if (copies && sums) return launch_forked(plans, s);
   if ((st = launch_kind(plans, false, s)) != DT_OK) return st;
   return launch_kind(plans, true, s);
 }
