@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
 #include <vector>
 
@@ -50,6 +51,7 @@ constexpr int RD_MAX_TASKS = 192;
 constexpr int RD_MAX_REFS = 256;
 constexpr int RD_MAX_LAUNCH_SLOTS = 128;  // per side, over every tensor of a batch
 constexpr int RD_MAX_SRC = 16;  // sources a lane keeps addresses of; more take sum_many
+constexpr int RD_MAX_EXTRA_DST = 15;  // further destinations of one copy task
 constexpr int RD_THREADS = 256;
 constexpr int RD_WARPS = RD_THREADS / 32;
 constexpr int COPY_SEG_BYTES = RD_COPY_SEG;  // one warp moves up to this much of a row per work item
@@ -72,9 +74,10 @@ struct RdTask {
   int32_t segs_per_row;
   int16_t dst_slot;
   int16_t nsrc;
-  int16_t ref_begin;
-  int8_t dmap[4];  // slot stride used for each padded position (dims merged on the host)
-  int16_t pad;
+  int16_t ref_begin;  // sources, then (copies) the extra destinations as byte distances
+  int8_t dmap[4];     // slot stride used for each padded position (dims merged on the host)
+  int8_t nextra;      // copies: further destination slots receiving the same box
+  int8_t pad;
 };
 
 struct RdRef {
@@ -404,11 +407,12 @@ __device__ void sum_many(char* d, int64_t dstr, const P& p, const RdTask& T, int
   }
 }
 
-// SUM = false: every task copies (nsrc == 1) or zero-fills (nsrc == 0);
+// SUM = false: every task copies (nsrc == 1) or zero-fills (nsrc == 0),
+// REPL = true: to its destination and its replicas (nextra of them);
 // SUM = true: every task adds nsrc >= 2 partial sources.  One instantiation
-// per kind keeps the copy path's register use low.  Warps take work items
-// (row, segment) in a grid-stride loop.
-template <bool SUM, class P>
+// per kind keeps the plain copy path's register use low.  Warps take work
+// items (row, segment) in a grid-stride loop.
+template <bool SUM, bool REPL, class P>
 __global__ void __launch_bounds__(RD_THREADS, SUM ? RD_SUM_CTAS : RD_COPY_CTAS) rd_kernel(const __grid_constant__ P p) {
   const int lane = threadIdx.x & 31;
   const int64_t nw = static_cast<int64_t>(gridDim.x) * RD_WARPS;
@@ -436,8 +440,22 @@ __global__ void __launch_bounds__(RD_THREADS, SUM ? RD_SUM_CTAS : RD_COPY_CTAS) 
       const RdSlot& S = p.src[R.slot];
       const char* s =
           S.ptr + (R.off + i0 * S.stride[m0] + i1 * S.stride[m1] + i2 * S.stride[m2] + e0 * S.stride[m3]) * esize;
-      if (D.stride[m3] == 1 && S.stride[m3] == 1) copy_span(d, s, n, esize, lane);
-      else copy_span_strided(d, s, n, D.stride[m3], S.stride[m3], esize, lane);
+      const bool unit = D.stride[m3] == 1 && S.stride[m3] == 1;
+      if (!REPL) {
+        if (unit) copy_span(d, s, n, esize, lane);
+        else copy_span_strided(d, s, n, D.stride[m3], S.stride[m3], esize, lane);
+      } else {
+        // the replicas of a materialised Replicate layout: each has the first
+        // destination's strides and sits a fixed number of bytes from it (the
+        // host stores that distance); the source span is re-read from L1/L2
+        for (int j = 0; j <= T.nextra; ++j) {
+          char* dj = j == 0 ? d
+                            : reinterpret_cast<char*>(reinterpret_cast<uintptr_t>(d) +
+                                                      static_cast<uintptr_t>(p.ref[T.ref_begin + j].off));
+          if (unit) copy_span(dj, s, n, esize, lane);
+          else copy_span_strided(dj, s, n, D.stride[m3], S.stride[m3], esize, lane);
+        }
+      }
     } else if (T.nsrc > RD_MAX_SRC) {
       sum_many(d, D.stride[m3], p, T, i0, i1, i2, e0, n, lane);
     } else {
@@ -460,6 +478,7 @@ struct HostTask {
   Box box;  // global box moved
   int dst_slot;
   std::vector<int> src_slots;  // rank order; empty = zero fill
+  std::vector<int> extra_dst;  // copies: further destination slots, same box and strides
 };
 
 int64_t local_offset(const SlotView& v, const Box& b, int ndim) {
@@ -612,9 +631,55 @@ void fill_slot(RdSlot* out, const SlotView& v, int ndim) {
   for (int d = 0; d < 4; ++d) out->stride[d] = d < pad ? 0 : v.stride[d - pad];
 }
 
+// Copies of one source box into several destination slots with the same
+// strides (the replicas of a materialised Replicate layout) become one task
+// with up to RD_MAX_EXTRA_DST further destinations: the kernel reads the
+// source once from DRAM and writes every replica.
+void group_replica_copies(const DTensor& D, std::vector<HostTask>* tasks) {
+  const int nd = D.layout.ndim;
+  auto same_strides = [&](int a, int b) {
+    for (int d = 0; d < nd; ++d)
+      if (D.slots[a].stride[d] != D.slots[b].stride[d]) return false;
+    return true;
+  };
+  auto same_box = [&](const Box& a, const Box& b) {
+    for (int d = 0; d < nd; ++d)
+      if (a.off[d] != b.off[d] || a.size[d] != b.size[d]) return false;
+    return true;
+  };
+  // open groups by (source slot, box): indices into `out`
+  std::map<std::vector<int64_t>, std::vector<int>> groups;
+  std::vector<HostTask> out;
+  out.reserve(tasks->size());
+  for (HostTask& t : *tasks) {
+    if (t.src_slots.size() == 1) {
+      std::vector<int64_t> key{t.src_slots[0]};
+      for (int d = 0; d < nd; ++d) {
+        key.push_back(t.box.off[d]);
+        key.push_back(t.box.size[d]);
+      }
+      std::vector<int>& open = groups[key];
+      bool merged = false;
+      for (int li : open) {
+        HostTask& g = out[li];
+        if ((int)g.extra_dst.size() < RD_MAX_EXTRA_DST && same_box(g.box, t.box) &&
+            same_strides(g.dst_slot, t.dst_slot)) {
+          g.extra_dst.push_back(t.dst_slot);
+          merged = true;
+          break;
+        }
+      }
+      if (merged) continue;
+      open.push_back((int)out.size());
+    }
+    out.push_back(std::move(t));
+  }
+  tasks->swap(out);
+}
+
 struct PairPlan {
   DTensor S, D;
-  std::vector<HostTask> copies, sums;
+  std::vector<HostTask> copies, sums, repl;  // repl: copies with replica destinations
 };
 
 dt_status plan_pair(const dt_dtensor* src, const dt_dtensor* dst, PairPlan* pp) {
@@ -633,22 +698,30 @@ dt_status plan_pair(const dt_dtensor* src, const dt_dtensor* dst, PairPlan* pp) 
   if (ls.dtype != ld.dtype) return fail(DT_ERR_INVALID_ARG, "src and dst dtypes differ");
   std::vector<HostTask> tasks;
   if ((st = plan(pp->S, pp->D, &tasks)) != DT_OK) return st;
-  // reductions (>= 2 sources) and copies / zero fills run in separate kernels
-  for (auto& t : tasks) (t.src_slots.size() >= 2 ? pp->sums : pp->copies).push_back(std::move(t));
+  group_replica_copies(pp->D, &tasks);
+  // reductions (>= 2 sources), copies / zero fills and copies to replicas
+  // run in separate kernels
+  for (auto& t : tasks)
+    (t.src_slots.size() >= 2 ? pp->sums : !t.extra_dst.empty() ? pp->repl : pp->copies).push_back(std::move(t));
   return DT_OK;
 }
 
 // Launch every task of `plans` of one kind, packing tasks of all pairs into as
 // few launches as the parameter block holds.
+enum RdKind { RD_COPY = 0, RD_SUM = 1, RD_COPY_REPL = 2 };
+
 template <class P>
-void launch_rd(const P& p, bool sum, int grid, cudaStream_t stream) {
-  if (sum)
-    rd_kernel<true, P><<<grid, RD_THREADS, 0, stream>>>(p);
+void launch_rd(const P& p, int kind, int grid, cudaStream_t stream) {
+  if (kind == RD_SUM)
+    rd_kernel<true, false, P><<<grid, RD_THREADS, 0, stream>>>(p);
+  else if (kind == RD_COPY_REPL)
+    rd_kernel<false, true, P><<<grid, RD_THREADS, 0, stream>>>(p);
   else
-    rd_kernel<false, P><<<grid, RD_THREADS, 0, stream>>>(p);
+    rd_kernel<false, false, P><<<grid, RD_THREADS, 0, stream>>>(p);
 }
 
-dt_status launch_kind(std::vector<PairPlan>& plans, bool sum, cudaStream_t stream) {
+dt_status launch_kind(std::vector<PairPlan>& plans, int kind, cudaStream_t stream) {
+  const bool sum = kind == RD_SUM;
   static thread_local RdParams p;  // ~28 KB: off the stack
   static thread_local RdParamsSmall ps;
   const int sms = device_sm_count();
@@ -672,9 +745,9 @@ dt_status launch_kind(std::vector<PairPlan>& plans, bool sum, cudaStream_t strea
         ps.dtype = p.dtype;
         ps.esize = p.esize;
         ps.op = p.op;
-        launch_rd(ps, sum, grid, stream);
+        launch_rd(ps, kind, grid, stream);
       } else {
-        launch_rd(p, sum, grid, stream);
+        launch_rd(p, kind, grid, stream);
       }
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return fail(DT_ERR_CUDA, "redistribute launch: %s", cudaGetErrorString(e));
@@ -692,7 +765,7 @@ dt_status launch_kind(std::vector<PairPlan>& plans, bool sum, cudaStream_t strea
   std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return key(a) < key(b); });
   for (int pi : order) {
     PairPlan& pp = plans[pi];
-    const std::vector<HostTask>& tasks = sum ? pp.sums : pp.copies;
+    const std::vector<HostTask>& tasks = kind == RD_SUM ? pp.sums : kind == RD_COPY ? pp.copies : pp.repl;
     if (tasks.empty()) continue;
     const Layout& ls = pp.S.layout;
     const int nd = ls.ndim;
@@ -706,7 +779,8 @@ dt_status launch_kind(std::vector<PairPlan>& plans, bool sum, cudaStream_t strea
     int dbase = -1, sbase = -1;
     for (const HostTask& ht : tasks) {
       const bool need_slots = dbase < 0;
-      const bool fits = nt < RD_MAX_TASKS && nref + (int)ht.src_slots.size() <= RD_MAX_REFS &&
+      const int task_refs = (int)(ht.src_slots.size() + ht.extra_dst.size());
+      const bool fits = nt < RD_MAX_TASKS && nref + task_refs <= RD_MAX_REFS &&
                         (!need_slots || (nd_slots + pp.D.layout.nslots <= RD_MAX_LAUNCH_SLOTS &&
                                          ns_slots + ls.nslots <= RD_MAX_LAUNCH_SLOTS));
       if (!fits) {
@@ -728,6 +802,15 @@ dt_status launch_kind(std::vector<PairPlan>& plans, bool sum, cudaStream_t strea
       for (int k = 0; k < t.nsrc; ++k) {
         p.ref[nref].slot = sbase + ht.src_slots[k];
         p.ref[nref].off = local_offset(pp.S.slots[ht.src_slots[k]], ht.box, nd);
+        ++nref;
+      }
+      t.nextra = (int8_t)ht.extra_dst.size();
+      const uintptr_t first = reinterpret_cast<uintptr_t>(pp.D.slots[ht.dst_slot].ptr) + (uintptr_t)(t.dst_off * ls.esize);
+      for (int x : ht.extra_dst) {  // replica x: byte distance from the first destination
+        const uintptr_t at =
+            reinterpret_cast<uintptr_t>(pp.D.slots[x].ptr) + (uintptr_t)(local_offset(pp.D.slots[x], ht.box, nd) * ls.esize);
+        p.ref[nref].slot = dbase + x;
+        p.ref[nref].off = static_cast<int64_t>(at - first);
         ++nref;
       }
       // segments are whole 16-byte multiples so every segment of a row
@@ -777,11 +860,13 @@ dt_status launch_forked(std::vector<PairPlan>& plans, cudaStream_t s) {
       cudaStreamWaitEvent(a->s, a->fork, 0) != cudaSuccess) {
     cudaGetLastError();
     lk.unlock();
-    if ((st = launch_kind(plans, false, s)) != DT_OK) return st;  // one stream, one after the other
-    return launch_kind(plans, true, s);
+    for (int k : {RD_COPY, RD_COPY_REPL, RD_SUM})  // one stream, one after the other
+      if ((st = launch_kind(plans, k, s)) != DT_OK) return st;
+    return DT_OK;
   }
-  st = launch_kind(plans, true, a->s);
-  if (st == DT_OK) st = launch_kind(plans, false, s);
+  st = launch_kind(plans, RD_SUM, a->s);
+  if (st == DT_OK) st = launch_kind(plans, RD_COPY, s);
+  if (st == DT_OK) st = launch_kind(plans, RD_COPY_REPL, s);
   // join even after a failed launch, so the caller's stream never runs ahead of the auxiliary one
   cudaError_t e = cudaEventRecord(a->join, a->s);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(s, a->join, 0);
@@ -809,12 +894,13 @@ dt_status redistribute_many(int32_t n, const dt_dtensor* src, const dt_dtensor* 
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   bool copies = false, sums = false;
   for (const PairPlan& pp : plans) {
-    copies = copies || !pp.copies.empty();
+    copies = copies || !pp.copies.empty() || !pp.repl.empty();
     sums = sums || !pp.sums.empty();
   }
   if (copies && sums) return launch_forked(plans, s);
-  if ((st = launch_kind(plans, false, s)) != DT_OK) return st;
-  return launch_kind(plans, true, s);
+  for (int k : {RD_COPY, RD_COPY_REPL, RD_SUM})
+    if ((st = launch_kind(plans, k, s)) != DT_OK) return st;
+  return DT_OK;
 }
 
 }  // namespace

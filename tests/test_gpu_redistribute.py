@@ -184,3 +184,33 @@ def test_many_partial_sources(lib, op, dtype):
             dst = opl.Layout(mesh, dp, gshape)
             src_locals = [random_values(src.local_shape(s), dtype, nrng) for s in range(src.nslots)]
             run_pair(src_locals, src, dst, dtype)
+
+
+@pytest.mark.parametrize("gshape", [(8192, 8192), (8191, 8190), (70, 33)])
+def test_materialised_replicas(lib, gshape):
+    """Shard -> Replicate and Replicate -> Replicate with a copy per rank
+    (each source box is read once and written to every replica), and back."""
+    mesh = workloads.REDISTRIBUTE["mesh"]
+    g = workloads.redistribute_global(gshape)
+    for sp, dp, smat, dmat in (([S(0), S(0)], [S(0), R], False, True), ([S(0), S(1)], [S(0), R], False, True),
+                               ([S(0), R], [R, R], True, True), ([S(0), R], [S(0), S(1)], True, False)):
+        src = opl.Layout(mesh, sp, gshape, smat)
+        dst = opl.Layout(mesh, dp, gshape, dmat)
+        run_pair(ord_.distribute(g, src, "bf16"), src, dst, "bf16")
+
+
+def test_materialised_replicas_strided_views(lib):
+    """Replica slots with different strides are written by separate tasks."""
+    gshape = (40, 52)
+    g = bf16.round_rne(np.random.default_rng(8).standard_normal(gshape))
+    mesh = tsl.DeviceMesh((4,))
+    src = tsl.DTensor([to_dev(np.ascontiguousarray(g[o:o + s]), "bf16") for o, s in opl.chunk_bounds(40, 4)], mesh,
+                      [tsl.Shard(0)], gshape, torch.bfloat16)
+    parent = torch.zeros((40, 2 * 52), dtype=torch.bfloat16, device="cuda")
+    slots = [torch.empty(gshape, dtype=torch.bfloat16, device="cuda"), parent[:, :52],
+             torch.empty(gshape, dtype=torch.bfloat16, device="cuda"), parent[:, 52:]]
+    dst = tsl.DTensor(slots, mesh, [tsl.Replicate()], gshape, torch.bfloat16, materialize_replicas=True)
+    tsl.redistribute(src, dst)
+    torch.cuda.synchronize()
+    for t in dst.slots:
+        np.testing.assert_array_equal(t.cpu().view(torch.int16).numpy().view(np.uint16), g)
