@@ -43,43 +43,56 @@ struct EmbParams {
   int32_t* status;
 };
 
+// One warp per (token, shard) row copy, in a grid-stride loop.  The ids of
+// a warp's next 32 items are loaded together, one per lane, and handed out
+// by shuffle, so a row's loads never wait behind its id's load.
+__device__ __forceinline__ void emb_item(const EmbParams& p, int64_t w, int32_t id, int lane) {
+  const int64_t t = w / p.nshard;
+  const int i = (int)(w - t * p.nshard);
+  const EmbShard& S = p.shard[i];
+  const bool ok = id >= 0 && id < p.vocab;
+  if (!ok && lane == 0 && i == 0) atomicOr(p.status, DT_DEV_ERR_INDEX);
+  const char* src = S.ptr + (int64_t)(ok ? id : 0) * S.row_stride * p.esize;
+  const int64_t nbytes = S.width * p.esize;
+  for (int o = 0; o < p.nout; ++o) {
+    char* dst = p.out[o].ptr + (t * p.out[o].row_stride + S.col_off) * p.esize;
+    if (p.vec16) {
+      const uint4* sv = reinterpret_cast<const uint4*>(src);
+      uint4* dv = reinterpret_cast<uint4*>(dst);
+      const int64_t n = nbytes / 16;
+      int64_t u = lane;
+      for (; u + 32 < n; u += 64) {
+        uint4 a = ok ? __ldg(sv + u) : make_uint4(0, 0, 0, 0);
+        uint4 b = ok ? __ldg(sv + u + 32) : make_uint4(0, 0, 0, 0);
+        __stcs(dv + u, a);
+        __stcs(dv + u + 32, b);
+      }
+      for (; u < n; u += 32) __stcs(dv + u, ok ? __ldg(sv + u) : make_uint4(0, 0, 0, 0));
+    } else if (p.esize == 2) {
+      const uint16_t* sv = reinterpret_cast<const uint16_t*>(src);
+      uint16_t* dv = reinterpret_cast<uint16_t*>(dst);
+      for (int64_t e = lane; e < S.width; e += 32) dv[e] = ok ? sv[e] : (uint16_t)0;
+    } else {
+      const uint32_t* sv = reinterpret_cast<const uint32_t*>(src);
+      uint32_t* dv = reinterpret_cast<uint32_t*>(dst);
+      for (int64_t e = lane; e < S.width; e += 32) dv[e] = ok ? sv[e] : 0u;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(EMB_THREADS) embedding_kernel(const __grid_constant__ EmbParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t warp_global = (int64_t)blockIdx.x * (EMB_THREADS / 32) + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * (EMB_THREADS / 32);
   const int64_t pairs = p.ntok * p.nshard;
-  for (int64_t w = warp_global; w < pairs; w += nwarps) {
-    const int64_t t = w / p.nshard;
-    const int i = (int)(w - t * p.nshard);
-    const EmbShard& S = p.shard[i];
-    const int32_t id = __ldg(p.ids + t);
-    const bool ok = id >= 0 && id < p.vocab;
-    if (!ok && lane == 0 && i == 0) atomicOr(p.status, DT_DEV_ERR_INDEX);
-    const char* src = S.ptr + (int64_t)(ok ? id : 0) * S.row_stride * p.esize;
-    const int64_t nbytes = S.width * p.esize;
-    for (int o = 0; o < p.nout; ++o) {
-      char* dst = p.out[o].ptr + (t * p.out[o].row_stride + S.col_off) * p.esize;
-      if (p.vec16) {
-        const uint4* sv = reinterpret_cast<const uint4*>(src);
-        uint4* dv = reinterpret_cast<uint4*>(dst);
-        const int64_t n = nbytes / 16;
-        int64_t u = lane;
-        for (; u + 32 < n; u += 64) {
-          uint4 a = ok ? __ldg(sv + u) : make_uint4(0, 0, 0, 0);
-          uint4 b = ok ? __ldg(sv + u + 32) : make_uint4(0, 0, 0, 0);
-          __stcs(dv + u, a);
-          __stcs(dv + u + 32, b);
-        }
-        for (; u < n; u += 32) __stcs(dv + u, ok ? __ldg(sv + u) : make_uint4(0, 0, 0, 0));
-      } else if (p.esize == 2) {
-        const uint16_t* sv = reinterpret_cast<const uint16_t*>(src);
-        uint16_t* dv = reinterpret_cast<uint16_t*>(dst);
-        for (int64_t e = lane; e < S.width; e += 32) dv[e] = ok ? sv[e] : (uint16_t)0;
-      } else {
-        const uint32_t* sv = reinterpret_cast<const uint32_t*>(src);
-        uint32_t* dv = reinterpret_cast<uint32_t*>(dst);
-        for (int64_t e = lane; e < S.width; e += 32) dv[e] = ok ? sv[e] : 0u;
-      }
+  for (int64_t w0 = warp_global; w0 < pairs; w0 += 32 * nwarps) {
+    // lane k holds the id of item w0 + k * nwarps
+    const int64_t mine = w0 + lane * nwarps;
+    const int32_t my_id = mine < pairs ? __ldg(p.ids + mine / p.nshard) : 0;
+    for (int k = 0; k < 32; ++k) {
+      const int64_t w = w0 + k * nwarps;
+      if (w >= pairs) break;  // warp-uniform
+      emb_item(p, w, __shfl_sync(0xffffffffu, my_id, k), lane);
     }
   }
 }
