@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
         const TileCoord tc = decode_tile<PAIR_TILE_M>(p, w.t);
         const Group& G = p.groups[tc.g];
         const bool bk = G.b_kmajor != 0;
-        const uint32_t idesc = instr_desc(PAIR_TILE_M, 256, bk);
+        const uint32_t idesc = instr_desc(PAIR_TILE_M, G.dual ? 2 * pair_dual_half(G, tc.n0) : 256, bk);
         bool _ok;
         {
           DT_TRACE_T0();
@@ -259,8 +259,9 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
         row_ptr = G.out_ptr[j] + (r - G.out_row_begin[j]) * G.out_ld[j] * esize;
       }
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN_MAX);
-      // accumulator columns that hold outputs (the gated MLP: gate 0..127, up 128..255)
-      const int ncols = G.dual ? 256 : min(256, (G.n - tc.n0 + 31) & ~31);
+      // accumulator columns that hold outputs (the gated MLP: gate [0, hh), up [hh, 2 hh))
+      const int hh = G.dual ? pair_dual_half(G, tc.n0) : 0;
+      const int ncols = G.dual ? 2 * hh : min(256, (G.n - tc.n0 + 31) & ~31);
       if (w.piece < 0) {
         if (!G.dual) {
           for (int c = 0; c < ncols; c += 32) {
@@ -275,10 +276,10 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
             }
           }
         } else {
-          for (int c = 0; c < 128; c += 32) {
+          for (int c = 0; c < hh; c += 32) {
             uint32_t g[32], u[32];
             tmem_ld32(tbase + c, g);
-            tmem_ld32(tbase + 128 + c, u);
+            tmem_ld32(tbase + hh + c, u);
             tmem_ld_wait();
             if (row_ptr) {
               float gv[32], uv[32];
@@ -362,7 +363,8 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
         if (lane == 0) atomicOr(p.status, DT_DEV_ERR_INDEX);
         continue;
       }
-      const int nrounds = G.dual ? 4 : min(8, (G.n - tc.n0 + 31) >> 5);
+      const int hh = G.dual ? pair_dual_half(G, tc.n0) : 0;
+      const int nrounds = G.dual ? hh >> 5 : min(8, (G.n - tc.n0 + 31) >> 5);
       const int first_piece = fin_s[f] + fin_first[f];
       auto issue = [&](int rd, int b) {
         if (lane == 0) {
@@ -371,7 +373,7 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
           uint8_t* dst = fin_base + b * FIN_BUF_BYTES;
           for (int q = 0; q < np; ++q)
             for (int j = 0; j < per_round; ++j) {
-              const int chunk = rd + 4 * j;  // gated MLP: up chunk 4 columns-of-32 after gate
+              const int chunk = rd + j * (hh >> 5);  // gated MLP: up starts hh columns after gate
               bulk_load(dst + (q * per_round + j) * FIN_CHUNK_BYTES,
                         sk_slot(p, first_piece + q, rank, quarter) + chunk * 8 * 32, FIN_CHUNK_BYTES,
                         &fin_bar[quarter * 2 + b]);

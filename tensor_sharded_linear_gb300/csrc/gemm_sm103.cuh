@@ -499,6 +499,14 @@ __device__ __forceinline__ void sk_tile_clusters(const Params& p, int ncl, int s
   *c_last = e;
 }
 
+// Gated-MLP pair tile: columns of gate (and of up) it holds, a multiple of
+// 32 up to 128.  The MMA is 2 * that wide; gate fills accumulator columns
+// [0, h) and up [h, 2h), so a shard's short last tile does no wasted work.
+__device__ __forceinline__ int pair_dual_half(const Group& G, int n0) {
+  const int r = (G.n - n0 + 31) & ~31;
+  return r < 128 ? r : 128;
+}
+
 // MMA width of a tile: the gated MLP always uses both 128-column halves;
 // otherwise the tile's remaining columns rounded up to the MMA's N step of 16.
 __device__ __forceinline__ int tile_mma_n(const Group& G, int n0) {

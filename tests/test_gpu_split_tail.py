@@ -107,14 +107,14 @@ def test_row_split(lib, mode):
 
 def test_mlp_split(lib):
     """The fused MLP with its gated gate/up GEMM split (40 dual tiles, 157 K
-    iterations).  The split GEMM's output, H, is checked per element; the
+    iterations, each shard's last tile 96 columns of gate and up).  The split GEMM's output, H, is checked per element; the
     MLP output with the relative Frobenius bound.  (Its max-abs error also
     carries H's bf16 rounding: where the kernel's fp32 SiLU(g)*u and the
     oracle's fp64 one round to neighbouring bf16 values, each such element
     moves outputs by one bf16 ulp of H times a weight, which at this K can
     pass 2e-3 on a few outputs with either schedule.  The down GEMM's split
     is test_mlp_down_split, on the oracle's H.)"""
-    M, K, F, N, p = 256, 10000, 8 * 640, 384, 8
+    M, K, F, N, p = 256, 10000, 8 * 600, 384, 8  # 600 = 4 x 128 + 88: a short last tile per shard
     assert split_expected(ceil_div(M, 256) * p * ceil_div(F // p, 128), ceil_div(K, 64), dual=True)
     x, wg, wu, wd = workloads.mlp_inputs(M, K, F, seed_base=700)
     wd = workloads.randn_bf16((F, N), 704, (1.0 / F) ** 0.5)
