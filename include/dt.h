@@ -23,8 +23,18 @@
  *    everything else (descriptors, slot arrays, stride arrays, output
  *    scalars) is host memory that is read during the call only.
  *  - The caller owns all device memory (inputs, outputs, workspaces).  The
- *    library allocates no device memory per call; it keeps host-side caches
- *    only (TMA descriptors, planned launches) which dt_clear_cache() drops.
+ *    library allocates no device memory per call.  It keeps host-side caches
+ *    (TMA descriptors) and, made once and kept: per device, one auxiliary
+ *    stream with two events (a redistribute call with both copies and
+ *    Partial reductions runs the reductions there, forked from and joined
+ *    back to the caller's stream); per (device, stream), the split-tail
+ *    scratch of the tensor-core GEMM (about 39 MB of partial accumulators
+ *    and counters, made by the first linear whose last wave is split, with
+ *    cudaMalloc outside a stream capture; inside a capture, or when it
+ *    cannot be made, every tile runs whole).  dt_clear_cache() drops the
+ *    descriptors and frees the scratch.
+ *  - Environment switches, read once per process: DT_GEMM_PAIR=0 selects the
+ *    single-CTA GEMM kernel, DT_GEMM_SPLIT=0 turns the split tail off.
  *  - Compute calls are asynchronous on the given stream (a cudaStream_t;
  *    NULL = the legacy default stream).  Their return value covers the checks
  *    done on the host before any launch; on any error nothing is launched.
@@ -290,10 +300,16 @@ DT_API const char* dt_status_string(dt_status status);
 DT_API const char* dt_last_error(void);
 
 /* Copy the library's own device status word (used when d_status == NULL)
- * to *bits and, if clear != 0, reset it.  Synchronous on the current device. */
+ * to *bits and, if clear != 0, reset it.  Synchronous on the current device.
+ * When the word holds DT_DEV_ERR_TIMEOUT it also zeroes the split-tail
+ * counters (a GEMM that gave up may have left them part-counted); that
+ * waits for the devices to go idle. */
 DT_API dt_status dt_read_device_status(int32_t* bits, int32_t clear);
 
-/* Drop host-side caches (TMA descriptors, planned launches). */
+/* Drop host-side caches (TMA descriptors) and free the GEMM split-tail
+ * scratch (which waits for each device's work to finish).  Not to be called
+ * while another thread launches, or while a captured graph that uses the
+ * scratch may still run. */
 DT_API dt_status dt_clear_cache(void);
 
 /* Number of kernels this library has launched in this process so far
