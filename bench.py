@@ -194,6 +194,7 @@ class Block:
         self.calls = []  # (name, kind, work, fn)
         self.call_io = []  # per call: (device inputs the host supplies, device outputs the host reads)
         self.sweep = []  # (name, bytes, src, dst) of every redistribute transition
+        self.rd_fine = []  # the sweep as one batch call per shape: (name, kind, work, call, io)
         self.batch_sweep = batch_sweep
         stream = torch.cuda.current_stream(device).cuda_stream
         self.stream = stream
@@ -239,14 +240,19 @@ class Block:
                 partial_slots.append(dev(W.redistribute_partials(tuple(t.shape), 1, seed=310 + s)[0]))
             src["S0P"] = DTensor(partial_slots, mesh, pls["S0P"], gshape, bf)
             out = {k: DTensor.empty(mesh, pls[k], gshape, bf, device=device) for k in ("S0S0", "S0S1", "S0R")}
-            for k in src:
-                rd_in += src[k].slots
-            for k in out:
-                rd_out += out[k].slots
+            shape_in = [t for k in src for t in src[k].slots]
+            shape_out = [t for k in out for t in out[k].slots]
+            rd_in += shape_in
+            rd_out += shape_out
             tag = "x".join(str(s) for s in gshape)
+            pairs, work_sum = [], 0
             for name, a, b in transitions():
                 work = 5 * G if a == "S0P" else 2 * G
                 self.sweep.append((f"redistribute {name} {tag}", work, src[a], out[b]))
+                pairs.append((src[a], out[b]))
+                work_sum += work
+            self._add(f"redistribute sweep {tag}", "bytes", work_sum, "dt_redistribute_batch", pairs,
+                      io=(shape_in, shape_out), target=self.rd_fine)
         if self.batch_sweep:
             # every transition in one dt_redistribute_batch call: one copy
             # launch and one reduction launch
@@ -297,7 +303,7 @@ class Block:
         self._add("attention o", "flops", 2 * cfg["tokens"] * H * H, "dt_row_parallel_linear", qkv[0], wod, od,
                   L.TP_REDUCE_SCATTER, io=([], list(od.slots)))
 
-    def _add(self, name, kind, work, fn_name, *args, io=((), ())):
+    def _add(self, name, kind, work, fn_name, *args, io=((), ()), target=None):
         C, L, lib, stream = self.C, self.L, self.lib, self.stream
         keep = list(args)  # the DTensors own the device memory the descriptors point at
 
@@ -351,8 +357,24 @@ class Block:
                 raise RuntimeError(f"{name}: {lib.dt_status_string(st).decode()}: {lib.dt_last_error().decode()}")
 
         call._keep = keep
+        if target is not None:
+            target.append((name, kind, work, call, (list(io[0]), list(io[1]))))
+            return
         self.calls.append((name, kind, work, call))
         self.call_io.append((list(io[0]), list(io[1])))
+
+    def pipeline_calls(self):
+        """The step's calls with their inputs and outputs, the redistribute
+        sweep split into one batch call per shape: the same work, in pieces
+        small enough that copying one piece's next inputs overlaps the other
+        piece's kernels."""
+        out = []
+        for (name, kind, work, call), io in zip(self.calls, self.call_io):
+            if name.startswith("redistribute sweep") and self.rd_fine:
+                out += self.rd_fine
+            else:
+                out.append((name, kind, work, call, io))
+        return out
 
     @property
     def h2d(self):
@@ -645,23 +667,24 @@ def run_e2e(blk, args, peaks, world, device):
     """Same metric through the public API with host buffers: every step
     copies its activations in from pinned host memory and reads its results
     back.  The copies are pipelined with the compute on three streams, per
-    call: a call's inputs for the next step go in once the call has finished
+    call (the redistribute sweep as one batch per shape): a call's inputs for the next step go in once the call has finished
     this step, the call runs once its inputs are in and its previous results
     have been read back, and its results go out as soon as it finishes, so
     the link carries both directions while the kernels run.  The timed
     region ends when the last step's results are on the host."""
     comp = torch.cuda.current_stream(device)
     hs, ds = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    calls = blk.pipeline_calls()
     io = []
-    for ins, outs in blk.call_io:
+    for _, _, _, _, (ins, outs) in calls:
         hin = [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)) for t in ins]
         hout = [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)) for t in outs]
         for dev_t, host in hin:
             host.copy_(dev_t)
         io.append((hin, hout))
-    bi = sum(t.numel() * t.element_size() for ins, _ in blk.call_io for t in ins)
-    bo = sum(t.numel() * t.element_size() for _, outs in blk.call_io for t in outs)
-    n = len(blk.calls)
+    bi = sum(t.numel() * t.element_size() for _, _, _, _, (ins, _) in calls for t in ins)
+    bo = sum(t.numel() * t.element_size() for _, _, _, _, (_, outs) in calls for t in outs)
+    n = len(calls)
     ev_in = [torch.cuda.Event() for _ in range(n)]     # call's inputs are on the device
     ev_done = [torch.cuda.Event() for _ in range(n)]   # call finished (its inputs may be overwritten)
     ev_out = [torch.cuda.Event() for _ in range(n)]    # call's results are on the host
@@ -670,7 +693,7 @@ def run_e2e(blk, args, peaks, world, device):
     steps = max(2, args.steps)  # the pipeline fills on the first step and drains after the last
 
     def one():
-        for i, (_, _, _, call) in enumerate(blk.calls):
+        for i, (_, _, _, call, _) in enumerate(calls):
             hin, hout = io[i]
             hs.wait_event(ev_done[i])
             with torch.cuda.stream(hs):
