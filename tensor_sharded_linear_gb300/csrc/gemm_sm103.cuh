@@ -110,6 +110,7 @@ struct Params {  // CUtensorMap carries its own 128-byte alignment
   float* sk_part;     // [piece][2 CTAs][128 rows][256 columns]
   int32_t* sk_count;  // [sk_tiles][2 CTAs][4 quarters]
 };
+static_assert(sizeof(Params) <= 32000, "GEMM parameter block over the launch limit");
 
 #ifdef DT_GEMM_TRACE
 #define DT_TRACE_T0() const long long _tr0 = clock64()
