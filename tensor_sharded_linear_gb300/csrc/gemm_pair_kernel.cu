@@ -329,7 +329,9 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
             __threadfence();
           }
         }
-        if (__shfl_sync(0xffffffffu, last, 0)) {
+        if (__shfl_sync(0xffffffffu, last, 0) && nfin == 2) {  // the host never gives a pair three pieces
+          if (lane == 0) atomicOr(p.status, DT_DEV_ERR_INDEX);
+        } else if (__shfl_sync(0xffffffffu, last, 0)) {
           fin_t[nfin] = w.t;
           fin_s[nfin] = w.s;
           fin_first[nfin] = __shfl_sync(0xffffffffu, c_first, 0);
