@@ -185,8 +185,10 @@ DT_API dt_status dt_redistribute(const dt_dtensor* src, const dt_dtensor* dst, i
  * boxes, 256 partial references), and starts further launches beyond that.
  * Pairs may differ in mesh, shape, dtype and reduce op; a launch holds one
  * dtype (and, for reductions, one op), so each further dtype or op adds a
- * launch.  No dst[i] may overlap any src[j] or another dst[j] of the same
- * call: the pairs run concurrently.  Every pair is checked before anything launches; an error
+ * launch.  All tensors of a call live on one device (that of the first
+ * non-empty destination slot, where the kernels run).  No dst[i] may
+ * overlap any src[j] or another dst[j] of the same call: the pairs run
+ * concurrently.  Every pair is checked before anything launches; an error
  * names the pair and nothing runs.  n == 0 is a no-op.
  */
 DT_API dt_status dt_redistribute_batch(int32_t n, const dt_dtensor* src, const dt_dtensor* dst,
