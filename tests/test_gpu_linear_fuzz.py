@@ -1,0 +1,119 @@
+"""Seeded random cases of the tensor-parallel linears against the fp64 oracle.
+
+Each case draws M, K, N and the part count P, so shards are ragged
+(torch.chunk, empty tails included), tiles are ragged in M, N and K, and
+TMA's out-of-bounds fill is exercised; bias on or off, bf16 and fp32
+outputs, weights stored [in, out] or as [out, in] views, and every
+row-parallel mode.  K a multiple of 8 keeps bf16 row pitches 16-byte
+aligned (the tcgen05 path); other K take the CUDA-core kernel.  Tolerances
+as in the other linear tests.
+"""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import tensor_sharded_linear_gb300 as tsl
+from oracle import linear as olin
+from oracle.placement import chunk_bounds
+from tensor_sharded_linear_gb300 import workloads
+
+from helpers import to_dev, to_host
+from test_gpu_linear import check_bf16, check_fp32, col_dtensor, mesh1, row_dtensor, w64, x_rep, x_shard
+
+pytestmark = pytest.mark.gpu
+
+
+def draw(rng, aligned):
+    M = rng.choice([1, 7, 129, 256, 300, 513, 700])
+    K = rng.choice([8, 64, 136, 512, 1000, 1368]) if aligned else rng.choice([5, 37, 130, 301])
+    N = rng.choice([8, 40, 264, 520, 1032]) if aligned else rng.choice([9, 77, 303])
+    P = rng.choice([1, 2, 3, 4, 8])
+    return M, K, N, P
+
+
+@pytest.mark.parametrize("seed", range(48))
+def test_column_fuzz(lib, seed):
+    rng = random.Random(3000 + seed)
+    aligned = seed % 4 != 3
+    M, K, N, P = draw(rng, aligned)
+    x = workloads.randn_bf16((M, K), 3100 + seed)
+    w = workloads.randn_bf16((K, N), 3200 + seed, (1.0 / K) ** 0.5)
+    use_bias = rng.random() < 0.5
+    kmajor = aligned and rng.random() < 0.3
+    cols = chunk_bounds(N, P)
+    bd = None
+    if use_bias:
+        b = workloads.randn_bf16((N,), 3300 + seed, 0.5)
+        bd = tsl.DTensor([to_dev(np.ascontiguousarray(b[o:o + s]), "bf16") for o, s in cols], mesh1(P),
+                         [tsl.Shard(0)], (N,), torch.bfloat16)
+    xd, wd = x_rep(x, P), col_dtensor(w, P, k_major=kmajor)
+    y32 = tsl.column_parallel_linear(xd, wd, bd, out_dtype=torch.float32)
+    y16 = tsl.column_parallel_linear(xd, wd, bd)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    expect = olin.column_parallel(w64(x), [w64(w[:, o:o + s]) for o, s in cols],
+                                  [w64(b[o:o + s]) for o, s in cols] if use_bias else None)
+    what = f"M={M} K={K} N={N} P={P} bias={use_bias} kmajor={kmajor}"
+    for i, e in enumerate(expect):
+        f = to_host(y32.slots[i], "fp32")
+        check_fp32(f, e, f"{what} shard {i}")
+        check_bf16(to_host(y16.slots[i], "bf16"), f, e, f"{what} shard {i}")
+
+
+@pytest.mark.parametrize("seed", range(48))
+def test_row_fuzz(lib, seed):
+    rng = random.Random(4000 + seed)
+    aligned = seed % 4 != 3
+    M, K, N, P = draw(rng, aligned)
+    mode = [tsl.ALL_REDUCE, tsl.REDUCE_SCATTER, tsl.PARTIAL][seed % 3]
+    x = workloads.randn_bf16((M, K), 4100 + seed)
+    w = workloads.randn_bf16((K, N), 4200 + seed, (1.0 / K) ** 0.5)
+    use_bias = mode != tsl.PARTIAL and rng.random() < 0.5
+    kmajor = aligned and rng.random() < 0.3
+    bd = None
+    if use_bias:
+        b = workloads.randn_bf16((N,), 4300 + seed, 0.5)
+        bd = tsl.DTensor([to_dev(b, "bf16")], mesh1(P), [tsl.Replicate()], (N,), torch.bfloat16)
+    xd, wd = x_shard(x, P), row_dtensor(w, P, k_major=kmajor)
+    y32 = tsl.row_parallel_linear(xd, wd, bd, mode=mode, out_dtype=torch.float32)
+    y16 = tsl.row_parallel_linear(xd, wd, bd, mode=mode)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    omode = {tsl.ALL_REDUCE: olin.ALL_REDUCE, tsl.REDUCE_SCATTER: olin.REDUCE_SCATTER, tsl.PARTIAL: olin.PARTIAL}[mode]
+    rows = chunk_bounds(K, P)
+    expect = olin.row_parallel([w64(x[:, o:o + s]) for o, s in rows], [w64(w[o:o + s]) for o, s in rows],
+                               w64(b) if use_bias else None, omode, parts=P)
+    what = f"M={M} K={K} N={N} P={P} mode={mode} bias={use_bias} kmajor={kmajor}"
+    assert len(expect) == len(y32.slots)
+    for i, e in enumerate(expect):
+        f = to_host(y32.slots[i], "fp32")
+        check_fp32(f, e, f"{what} out {i}")
+        check_bf16(to_host(y16.slots[i], "bf16"), f, e, f"{what} out {i}")
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_mlp_fuzz(lib, seed):
+    rng = random.Random(5000 + seed)
+    M = rng.choice([1, 100, 256, 333])
+    K = rng.choice([64, 136, 256])
+    P = rng.choice([1, 2, 4, 8])
+    F = P * rng.choice([8, 64, 96, 136])
+    N = rng.choice([8, 200, 384])
+    mode = tsl.ALL_REDUCE if seed % 2 == 0 else tsl.REDUCE_SCATTER
+    x, wg, wu, _ = workloads.mlp_inputs(M, K, F, seed_base=5100 + 10 * seed)
+    wd = workloads.randn_bf16((F, N), 5200 + seed, (1.0 / F) ** 0.5)
+    xd = x_rep(x, P)
+    y = tsl.tp_mlp(xd, col_dtensor(wg, P), col_dtensor(wu, P), row_dtensor(wd, P), mode=mode,
+                   out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    cols = chunk_bounds(F, P)
+    expect, _ = olin.tp_mlp(w64(x), [w64(wg[:, o:o + s]) for o, s in cols], [w64(wu[:, o:o + s]) for o, s in cols],
+                            [w64(wd[o:o + s]) for o, s in cols],
+                            olin.ALL_REDUCE if mode == tsl.ALL_REDUCE else olin.REDUCE_SCATTER)
+    what = f"M={M} K={K} F={F} N={N} P={P} mode={mode}"
+    assert len(expect) == len(y.slots)
+    for i, e in enumerate(expect):
+        check_fp32(to_host(y.slots[i], "fp32"), e, f"{what} out {i}")
