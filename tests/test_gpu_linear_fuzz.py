@@ -117,3 +117,41 @@ def test_mlp_fuzz(lib, seed):
     assert len(expect) == len(y.slots)
     for i, e in enumerate(expect):
         check_fp32(to_host(y.slots[i], "fp32"), e, f"{what} out {i}")
+
+
+def x_tokens(x_bits, p):
+    """[T, K] bf16, Shard(0) over p (token shards)."""
+    slots = [to_dev(np.ascontiguousarray(x_bits[o:o + s]), "bf16") for o, s in chunk_bounds(x_bits.shape[0], p)]
+    return tsl.DTensor(slots, mesh1(p), [tsl.Shard(0)], x_bits.shape, torch.bfloat16)
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_column_variants_fuzz(lib, seed):
+    """Sequence-parallel entry (token-sharded x), Replicate output, and
+    several weights sharing x in one launch, on random shapes."""
+    rng = random.Random(6000 + seed)
+    aligned = seed % 4 != 3
+    M, K, N, P = draw(rng, aligned)
+    seq = rng.random() < 0.5
+    x = workloads.randn_bf16((M, K), 6100 + seed)
+    xd = x_tokens(x, P) if seq else x_rep(x, P)
+    cols = chunk_bounds(N, P)
+    xs = [w64(x[o:o + s]) for o, s in chunk_bounds(M, P)]
+    what = f"M={M} K={K} N={N} P={P} seq={seq}"
+    if seed % 2 == 0:
+        w = workloads.randn_bf16((K, N), 6200 + seed, (1.0 / K) ** 0.5)
+        y = tsl.column_parallel_linear(xd, col_dtensor(w, P), out_dtype=torch.float32, output="replicate")
+        torch.cuda.synchronize()
+        assert tsl.read_device_status() == 0
+        expect = olin.column_parallel_replicate(w64(x), [w64(w[:, o:o + s]) for o, s in cols])
+        check_fp32(to_host(y.slots[0], "fp32"), expect, f"{what} replicate output")
+    else:
+        ws = [workloads.randn_bf16((K, N), 6300 + 3 * seed + j, (1.0 / K) ** 0.5) for j in range(3)]
+        ys = tsl.column_parallel_linear_multi(xd, [col_dtensor(w, P) for w in ws], out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert tsl.read_device_status() == 0
+        for j, w in enumerate(ws):
+            shards = [w64(w[:, o:o + s]) for o, s in cols]
+            expect = olin.column_parallel_seq(xs, shards) if seq else olin.column_parallel(w64(x), shards)
+            for i, e in enumerate(expect):
+                check_fp32(to_host(ys[j].slots[i], "fp32"), e, f"{what} weight {j} shard {i}")
