@@ -27,6 +27,7 @@ model in oracle/) on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -405,14 +406,17 @@ class Block:
             for _ in range(3):
                 lib.dt_redistribute(C.byref(da), C.byref(db), None, stream)
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+            gc.disable()
             for e0, e1 in evs:
                 e0.record()
                 st = lib.dt_redistribute(C.byref(da), C.byref(db), None, stream)
                 e1.record()
                 if st != self.L.OK:
+                    gc.enable()
                     raise RuntimeError(f"{name}: {lib.dt_last_error().decode()}")
+            gc.enable()
             torch.cuda.synchronize()
-            ms = statistics.fmean(e0.elapsed_time(e1) for e0, e1 in evs)
+            ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
             ach = work / (ms / 1e3) / 1e9
             out[name] = {"us": round(ms * 1e3, 2), "achieved": round(ach, 1), "unit": "GB/s",
                          "frac": round(ach / peaks["hbm_gbs"], 4)}
@@ -517,12 +521,16 @@ class Extras:
         out = {}
         for name, kind, work, fn in self.items:
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+            gc.disable()
             for a, b in evs:
                 a.record()
                 fn()
                 b.record()
+            gc.enable()
             torch.cuda.synchronize()
-            ms = statistics.fmean(a.elapsed_time(b) for a, b in evs)
+            # median: these calls go through the Python API, and a host hiccup
+            # in one iteration leaves the GPU waiting for that launch
+            ms = statistics.median(a.elapsed_time(b) for a, b in evs)
             if kind == "flops":
                 ach = work / (ms / 1e3) / 1e12
                 out[name] = {"us": round(ms * 1e3, 2), "achieved": round(ach, 1), "unit": "TFLOP/s",
@@ -577,6 +585,7 @@ def run_ours(args):
     clocks.start()
     barrier(world)
     torch.cuda.synchronize(device)
+    gc.disable()  # no collector pauses while the timed launches are issued
     launches0 = lib.dt_launch_count()
     wall0 = time.perf_counter()
     t0.record()
@@ -586,6 +595,7 @@ def run_ours(args):
     torch.cuda.synchronize(device)
     wall1 = time.perf_counter()
     launches = lib.dt_launch_count() - launches0
+    gc.enable()
     barrier(world)
     clk = clocks.stop()
     status = blk.tsl.read_device_status()
@@ -717,12 +727,14 @@ def run_e2e(blk, args, peaks, world, device):
         t0.record(comp)
         hs.wait_event(t0)  # no copy starts before the clock does
         ds.wait_event(t0)
+        gc.disable()
         for _ in range(k):
             one()
         for e in ev_out:
             comp.wait_event(e)
         t1.record(comp)
         torch.cuda.synchronize(device)
+        gc.enable()
         return t0.elapsed_time(t1) / 1e3 / k
 
     timed(1)  # warm-up: streams, events, pinned buffers

@@ -70,9 +70,6 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
 #ifdef DT_GEMM_TRACE
   const long long _trace_start = clock64();
 #endif
-  int8_t issued_parity[PAIR_STAGES];
-#pragma unroll
-  for (int s = 0; s < PAIR_STAGES; ++s) issued_parity[s] = -1;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -129,7 +126,6 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
               tma_load_2d_pair(b, bmap, b_col, kt * BK, full0);
               tma_load_2d_pair(b + B_CHUNK_BYTES, bmap, b_col + 64, kt * BK, full0);
             }
-            issued_parity[stage] = static_cast<int8_t>(phase);
             if (++stage == PAIR_STAGES) {
               stage = 0;
               phase ^= 1u;
