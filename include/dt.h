@@ -24,7 +24,9 @@
  *    scalars) is host memory that is read during the call only.
  *  - The caller owns all device memory (inputs, outputs, workspaces).  The
  *    library allocates no device memory per call.  It keeps host-side caches
- *    (TMA descriptors) and, made once and kept: per device, one auxiliary
+ *    (TMA descriptors; redistribute launch plans keyed by the operands'
+ *    layouts, slot pointers and strides, so a repeated call skips planning)
+ *    and, made once and kept: per device, one auxiliary
  *    stream with two events (a redistribute call with both copies and
  *    Partial reductions runs the reductions there, forked from and joined
  *    back to the caller's stream); per (device, stream), the split-tail
@@ -308,7 +310,7 @@ DT_API const char* dt_last_error(void);
  * waits for the devices to go idle. */
 DT_API dt_status dt_read_device_status(int32_t* bits, int32_t clear);
 
-/* Drop host-side caches (TMA descriptors) and free the GEMM split-tail
+/* Drop host-side caches (TMA descriptors, redistribute plans) and free the GEMM split-tail
  * scratch (which waits for each device's work to finish).  Not to be called
  * while another thread launches, or while a captured graph that uses the
  * scratch may still run. */

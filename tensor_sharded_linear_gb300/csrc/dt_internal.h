@@ -107,5 +107,6 @@ dt_status bind_device_of(const void* device_ptr);
 int device_sm_count();
 int32_t* device_status_word(int32_t* user);  // user if non-null, else the library word
 void count_launch();
+void clear_redistribute_plans();  // drop the redistribute plan cache (dt_clear_cache)
 
 }  // namespace dt

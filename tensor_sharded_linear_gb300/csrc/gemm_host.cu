@@ -660,6 +660,7 @@ extern "C" dt_status dt_clear_cache(void) {
     std::lock_guard<std::mutex> lk(dt::gemm::g_map_mu);
     dt::gemm::g_maps.clear();
   }
+  dt::clear_redistribute_plans();
   std::lock_guard<std::mutex> lk(dt::gemm::g_split_mu);
   int cur = 0;
   cudaGetDevice(&cur);

@@ -21,7 +21,10 @@
 
 #include <algorithm>
 #include <map>
+#include <memory>
 #include <mutex>
+#include <string>
+#include <unordered_map>
 #include <vector>
 
 #include "dt_internal.h"
@@ -720,6 +723,21 @@ void launch_rd(const P& p, int kind, int grid, cudaStream_t stream) {
     rd_kernel<false, false, P><<<grid, RD_THREADS, 0, stream>>>(p);
 }
 
+// A call's launches, recorded as issued (kind, grid and the exact parameter
+// block) so a later call with the same operands can replay them without
+// planning again.
+struct RecordedLaunch {
+  int kind = 0;
+  bool small = false;
+  int grid = 0;
+  std::vector<uint8_t> params;
+};
+struct RecordedPlan {
+  bool forked = false;
+  std::vector<RecordedLaunch> launches;
+};
+thread_local RecordedPlan* g_recording = nullptr;
+
 dt_status launch_kind(std::vector<PairPlan>& plans, int kind, cudaStream_t stream) {
   const bool sum = kind == RD_SUM;
   static thread_local RdParams p;  // ~28 KB: off the stack
@@ -746,8 +764,16 @@ dt_status launch_kind(std::vector<PairPlan>& plans, int kind, cudaStream_t strea
         ps.esize = p.esize;
         ps.op = p.op;
         launch_rd(ps, kind, grid, stream);
+        if (g_recording) {
+          const uint8_t* b = reinterpret_cast<const uint8_t*>(&ps);
+          g_recording->launches.push_back({kind, true, grid, std::vector<uint8_t>(b, b + sizeof(ps))});
+        }
       } else {
         launch_rd(p, kind, grid, stream);
+        if (g_recording) {
+          const uint8_t* b = reinterpret_cast<const uint8_t*>(&p);
+          g_recording->launches.push_back({kind, false, grid, std::vector<uint8_t>(b, b + sizeof(p))});
+        }
       }
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return fail(DT_ERR_CUDA, "redistribute launch: %s", cudaGetErrorString(e));
@@ -842,7 +868,8 @@ struct AuxStream {
 std::mutex g_aux_mu;
 AuxStream g_aux[64];
 
-dt_status launch_forked(std::vector<PairPlan>& plans, cudaStream_t s) {
+template <class Launch>  // Launch: dt_status(int kind, cudaStream_t)
+dt_status launch_forked(Launch&& launch, cudaStream_t s) {
   int dev = 0;
   cudaGetDevice(&dev);
   std::unique_lock<std::mutex> lk(g_aux_mu);
@@ -861,12 +888,12 @@ dt_status launch_forked(std::vector<PairPlan>& plans, cudaStream_t s) {
     cudaGetLastError();
     lk.unlock();
     for (int k : {RD_COPY, RD_COPY_REPL, RD_SUM})  // one stream, one after the other
-      if ((st = launch_kind(plans, k, s)) != DT_OK) return st;
+      if ((st = launch(k, s)) != DT_OK) return st;
     return DT_OK;
   }
-  st = launch_kind(plans, RD_SUM, a->s);
-  if (st == DT_OK) st = launch_kind(plans, RD_COPY, s);
-  if (st == DT_OK) st = launch_kind(plans, RD_COPY_REPL, s);
+  st = launch(RD_SUM, a->s);
+  if (st == DT_OK) st = launch(RD_COPY, s);
+  if (st == DT_OK) st = launch(RD_COPY_REPL, s);
   // join even after a failed launch, so the caller's stream never runs ahead of the auxiliary one
   cudaError_t e = cudaEventRecord(a->join, a->s);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(s, a->join, 0);
@@ -874,9 +901,95 @@ dt_status launch_forked(std::vector<PairPlan>& plans, cudaStream_t s) {
   return st;
 }
 
+dt_status redistribute_planned(int32_t n, const dt_dtensor* src, const dt_dtensor* dst, cudaStream_t s,
+                               RecordedPlan* rec);
+
+template <class P>
+dt_status replay_one(const RecordedLaunch& r, cudaStream_t s) {
+  launch_rd(*reinterpret_cast<const P*>(r.params.data()), r.kind, r.grid, s);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(DT_ERR_CUDA, "redistribute launch: %s", cudaGetErrorString(e));
+  count_launch();
+  return DT_OK;
+}
+
+dt_status replay_kind(const RecordedPlan& rp, int kind, cudaStream_t s) {
+  for (const RecordedLaunch& r : rp.launches) {
+    if (r.kind != kind) continue;
+    dt_status st = r.small ? replay_one<RdParamsSmall>(r, s) : replay_one<RdParams>(r, s);
+    if (st != DT_OK) return st;
+  }
+  return DT_OK;
+}
+
+// Plans by operands: the bytes of every pair's layouts, slot pointers and
+// strides decide the launches completely (never the data), so equal keys
+// replay equal launches.  Bounded; dropped whole when full.
+std::mutex g_plan_mu;
+std::unordered_map<std::string, std::shared_ptr<const RecordedPlan>> g_plans;
+constexpr size_t RD_PLAN_CACHE = 128;
+
+// false: a malformed descriptor, left to the checks of the planning path
+bool append_key(std::string* k, const dt_dtensor& d) {
+  if (d.nslots < 0 || d.nslots > DT_MAX_SLOTS || (d.nslots > 0 && !d.slots)) return false;
+  const int nd = d.layout.ndim;
+  if (nd < 0 || nd > DT_MAX_TENSOR_DIMS) return false;
+  k->append(reinterpret_cast<const char*>(&d.layout), sizeof(d.layout));
+  k->append(reinterpret_cast<const char*>(&d.nslots), sizeof(d.nslots));
+  if (d.nslots > 0) k->append(reinterpret_cast<const char*>(d.slots), sizeof(void*) * d.nslots);
+  const char has = d.strides ? 1 : 0;
+  k->push_back(has);
+  if (has) k->append(reinterpret_cast<const char*>(d.strides), sizeof(int64_t) * (size_t)d.nslots * nd);
+  return true;
+}
+
+dt_status replay(const RecordedPlan& rp, cudaStream_t s) {
+  auto launch = [&](int kind, cudaStream_t st) { return replay_kind(rp, kind, st); };
+  if (rp.forked) return launch_forked(launch, s);
+  dt_status st;
+  for (int k : {RD_COPY, RD_COPY_REPL, RD_SUM})
+    if ((st = launch(k, s)) != DT_OK) return st;
+  return DT_OK;
+}
+
 dt_status redistribute_many(int32_t n, const dt_dtensor* src, const dt_dtensor* dst, dt_stream_t stream) {
   clear_error();
   if (n < 0 || (n > 0 && (!src || !dst))) return fail(DT_ERR_INVALID_ARG, "need n >= 0 and src/dst arrays");
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  std::string key;
+  bool keyed = true;
+  for (int i = 0; i < n && keyed; ++i) keyed = append_key(&key, src[i]) && append_key(&key, dst[i]);
+  if (keyed && n > 0) {
+    std::shared_ptr<const RecordedPlan> hit;
+    {
+      std::lock_guard<std::mutex> lk(g_plan_mu);
+      auto it = g_plans.find(key);
+      if (it != g_plans.end()) hit = it->second;
+    }
+    if (hit) {
+      if (hit->launches.empty()) return DT_OK;
+      // the device of the first destination slot with data, as when planned
+      const void* any = nullptr;
+      for (int i = 0; i < n && !any; ++i)
+        for (int sl = 0; sl < dst[i].nslots && !any; ++sl)
+          if (dst[i].slots[sl]) any = dst[i].slots[sl];
+      dt_status st = bind_device_of(any);
+      if (st != DT_OK) return st;
+      return replay(*hit, cs);
+    }
+  }
+  auto rec = std::make_shared<RecordedPlan>();
+  dt_status st = redistribute_planned(n, src, dst, cs, rec.get());
+  if (st == DT_OK && keyed && n > 0) {
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    if (g_plans.size() >= RD_PLAN_CACHE) g_plans.clear();
+    g_plans[key] = rec;
+  }
+  return st;
+}
+
+dt_status redistribute_planned(int32_t n, const dt_dtensor* src, const dt_dtensor* dst, cudaStream_t s,
+                               RecordedPlan* rec) {
   std::vector<PairPlan> plans(n);
   const void* any = nullptr;
   dt_status st;
@@ -891,19 +1004,30 @@ dt_status redistribute_many(int32_t n, const dt_dtensor* src, const dt_dtensor* 
   }
   if (!any) return DT_OK;
   if ((st = bind_device_of(any)) != DT_OK) return st;
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   bool copies = false, sums = false;
   for (const PairPlan& pp : plans) {
     copies = copies || !pp.copies.empty() || !pp.repl.empty();
     sums = sums || !pp.sums.empty();
   }
-  if (copies && sums) return launch_forked(plans, s);
+  struct Recording {  // record the launches this call makes (and stop on return)
+    explicit Recording(RecordedPlan* r) { g_recording = r; }
+    ~Recording() { g_recording = nullptr; }
+  } recording(rec);
+  rec->forked = copies && sums;
+  auto launch = [&](int kind, cudaStream_t stream) { return launch_kind(plans, kind, stream); };
+  if (rec->forked) return launch_forked(launch, s);
   for (int k : {RD_COPY, RD_COPY_REPL, RD_SUM})
-    if ((st = launch_kind(plans, k, s)) != DT_OK) return st;
+    if ((st = launch(k, s)) != DT_OK) return st;
   return DT_OK;
 }
 
 }  // namespace
+
+void clear_redistribute_plans() {
+  std::lock_guard<std::mutex> lk(g_plan_mu);
+  g_plans.clear();
+}
+
 }  // namespace dt
 
 extern "C" dt_status dt_redistribute(const dt_dtensor* src, const dt_dtensor* dst, int32_t* d_status,

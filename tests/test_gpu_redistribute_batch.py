@@ -19,7 +19,7 @@ from tensor_sharded_linear_gb300 import _lib as L
 from tensor_sharded_linear_gb300 import workloads
 
 from helpers import (TORCH_DTYPE, dtensor_from_locals, lib_placements, locals_of, random_placements, random_values,
-                     sweep_transitions)
+                     sweep_transitions, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -150,3 +150,35 @@ def test_empty_batch_and_empty_pairs(lib):
         dst = opl.Layout((2,), [opl.Replicate()], gshape)
         cases.append((str(gshape), [random_values(src.local_shape(s), "bf16", nrng) for s in range(2)], src, dst))
     run_batch(cases, ["bf16"] * 3)
+
+
+def test_repeated_calls_replay_the_plan(lib):
+    """A repeated call with the same operands replays its recorded launches:
+    new source data each time, every result bit-exact, batch and single call,
+    before and after dt_clear_cache."""
+    mesh = (2, 4)
+    gshape = (130, 70)
+    cases = [("S0->S1", [opl.Shard(0), opl.Shard(0)], [opl.Shard(0), opl.Shard(1)]),
+             ("P->S0", [opl.Shard(0), opl.Partial()], [opl.Shard(0), opl.Shard(0)])]
+    layouts = [(opl.Layout(mesh, sp, gshape), opl.Layout(mesh, dp, gshape)) for _, sp, dp in cases]
+    nrng = np.random.default_rng(61)
+    first = [make_pair([random_values(src.local_shape(s), "bf16", nrng) for s in range(src.nslots)], src, dst, "bf16")
+             for src, dst in layouts]
+    lib_ = L.load()
+    for rnd in range(4):
+        if rnd == 2:
+            assert lib_.dt_clear_cache() == L.OK
+        locals_ = []
+        for (dsrc, _), (src, _) in zip(first, layouts):  # fresh data in the same buffers
+            loc = [random_values(src.local_shape(s), "bf16", nrng) for s in range(src.nslots)]
+            for t, a in zip(dsrc.slots, loc):
+                t.copy_(to_dev(a, "bf16"))
+            locals_.append(loc)
+        if rnd % 2 == 0:
+            tsl.redistribute_batch(first)
+        else:
+            for dsrc, ddst in first:
+                tsl.redistribute(dsrc, ddst)
+        torch.cuda.synchronize()
+        for (_, ddst), (src, dst), loc in zip(first, layouts, locals_):
+            check(ddst, "bf16", ord_.redistribute(loc, src, dst, "bf16"), f"round {rnd}")
