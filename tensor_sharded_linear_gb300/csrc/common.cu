@@ -59,6 +59,24 @@ int32_t* device_status_word(int32_t* user) {
   return static_cast<int32_t*>(p);
 }
 
+bool append_plan_key(std::string* k, const dt_dtensor* d) {
+  if (!d) {
+    k->push_back('\0');
+    return true;
+  }
+  k->push_back('\1');
+  if (d->nslots < 0 || d->nslots > DT_MAX_SLOTS || (d->nslots > 0 && !d->slots)) return false;
+  const int nd = d->layout.ndim;
+  if (nd < 0 || nd > DT_MAX_TENSOR_DIMS) return false;
+  k->append(reinterpret_cast<const char*>(&d->layout), sizeof(d->layout));
+  k->append(reinterpret_cast<const char*>(&d->nslots), sizeof(d->nslots));
+  if (d->nslots > 0) k->append(reinterpret_cast<const char*>(d->slots), sizeof(void*) * d->nslots);
+  const char has = d->strides ? 1 : 0;
+  k->push_back(has);
+  if (has) k->append(reinterpret_cast<const char*>(d->strides), sizeof(int64_t) * (size_t)d->nslots * nd);
+  return true;
+}
+
 }  // namespace dt
 
 using namespace dt;

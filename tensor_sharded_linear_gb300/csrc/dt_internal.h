@@ -108,5 +108,15 @@ int device_sm_count();
 int32_t* device_status_word(int32_t* user);  // user if non-null, else the library word
 void count_launch();
 void clear_redistribute_plans();  // drop the redistribute plan cache (dt_clear_cache)
+void clear_gemm_plans();          // drop the linears' plan cache (dt_clear_cache)
+
+// Append the bytes that decide a launch plan for descriptor d (its layout,
+// slot pointers and strides; a marker for NULL) to a cache key.  false: a
+// malformed descriptor, left to the planning path's checks.
+bool append_plan_key(std::string* key, const dt_dtensor* d);
+template <class T>
+void append_plan_scalar(std::string* key, const T& v) {
+  key->append(reinterpret_cast<const char*>(&v), sizeof(T));
+}
 
 }  // namespace dt

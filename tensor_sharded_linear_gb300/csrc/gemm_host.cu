@@ -17,6 +17,16 @@
 
 namespace dt {
 namespace gemm {
+
+struct GemmLaunch {
+  int kind = 0;  // 0 pair kernel, 1 single-CTA kernel, 2 CUDA-core kernel
+  int grid = 0;
+  std::shared_ptr<void> params;  // a heap Params (kinds 0, 1; keeps its 128-byte alignment) or SParams
+};
+struct GemmRecord {
+  std::vector<GemmLaunch> launches;
+};
+
 namespace {
 
 #ifdef DT_GEMM_TRACE
@@ -83,6 +93,7 @@ struct SplitScratch {
 std::mutex g_split_mu;
 std::map<std::pair<int, uintptr_t>, SplitScratch> g_split;
 thread_local int g_no_alloc = 0;
+thread_local GemmRecord* g_grec = nullptr;
 
 // 2-D bf16 map over a row-major [rows, cols] matrix with pitch ld elements:
 // box of 64 columns (128 bytes, the swizzle width) by box_rows rows, 128-byte
@@ -447,6 +458,8 @@ dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStrea
       }
     }
     p.total_tiles = tiles;
+    p.nmaps = map_i;
+    p.nsegs = seg_i;
     p.status = status;
     p.wait_limit_ns = gemm_wait_limit_ns();
     p.starve = gemm_starve();
@@ -513,6 +526,7 @@ dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStrea
       cudaError_t e = pair ? launch_tcgen05_pair(p, grid, stream) : launch_tcgen05(p, grid, stream);
       if (e != cudaSuccess) return fail(DT_ERR_CUDA, "tcgen05 GEMM launch: %s", cudaGetErrorString(e));
       count_launch();
+      if (g_grec) g_grec->launches.push_back({pair ? 0 : 1, grid, std::make_shared<Params>(p)});
     }
     gi = g_end;
   }
@@ -574,6 +588,7 @@ dt_status run_simt(std::vector<HostGroup>& groups, cudaStream_t stream) {
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return fail(DT_ERR_CUDA, "CUDA-core GEMM launch: %s", cudaGetErrorString(e));
       count_launch();
+      if (g_grec) g_grec->launches.push_back({2, grid, std::make_shared<SParams>(p)});
     }
     gi = g_end;
   }
@@ -636,6 +651,27 @@ namespace gemm {
 
 NoAllocScope::NoAllocScope() { ++g_no_alloc; }
 NoAllocScope::~NoAllocScope() { --g_no_alloc; }
+bool gemm_no_alloc() { return g_no_alloc > 0; }
+
+GemmRecordScope::GemmRecordScope(GemmRecord* r) { g_grec = r; }
+GemmRecordScope::~GemmRecordScope() { g_grec = nullptr; }
+std::shared_ptr<GemmRecord> new_gemm_record() { return std::make_shared<GemmRecord>(); }
+
+dt_status replay_gemm(const GemmRecord& r, cudaStream_t stream) {
+  for (const GemmLaunch& l : r.launches) {
+    cudaError_t e;
+    if (l.kind == 2) {
+      simt_gemm_kernel<<<l.grid, S_THREADS, 0, stream>>>(*static_cast<const SParams*>(l.params.get()));
+      e = cudaGetLastError();
+    } else {
+      const Params& p = *static_cast<const Params*>(l.params.get());
+      e = l.kind == 0 ? launch_tcgen05_pair(p, l.grid, stream) : launch_tcgen05(p, l.grid, stream);
+    }
+    if (e != cudaSuccess) return fail(DT_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+    count_launch();
+  }
+  return DT_OK;
+}
 
 // After a launch gave up (DT_DEV_ERR_TIMEOUT) its tiles' arrival counters
 // may be left part-counted; zero every counter so later launches start clean.
@@ -661,6 +697,7 @@ extern "C" dt_status dt_clear_cache(void) {
     dt::gemm::g_maps.clear();
   }
   dt::clear_redistribute_plans();
+  dt::clear_gemm_plans();  // their parameters point into the scratch freed below
   std::lock_guard<std::mutex> lk(dt::gemm::g_split_mu);
   int cur = 0;
   cudaGetDevice(&cur);

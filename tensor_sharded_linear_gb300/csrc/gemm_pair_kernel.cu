@@ -16,13 +16,16 @@
 //   tfull[b]   in each CTA: 1 arrival, multicast commit after a tile's MMAs;
 //   tempty[b]  in rank 0: 8 arrivals, the 4 epilogue warps of each CTA.
 // Every wait is bounded as in the single-CTA kernel.
+#include <algorithm>
+
 #include "gemm_plan.h"
 #include "gemm_sm103.cuh"
 
 namespace dt {
 namespace gemm {
 
-__global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __grid_constant__ Params p) {
+template <class P>
+__global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __grid_constant__ P p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + PAIR_STAGES * PAIR_STAGE_BYTES);
@@ -477,13 +480,16 @@ int g_max_clusters[64] = {};
 // Clusters that can be resident at once.  The kernel is persistent with a
 // static tile assignment, so launching more than this would run the extra
 // clusters as a second wave; SMs whose TPC partner is fused off cannot host
-// a pair, so this can be below SMs / 2.
+// a pair, so this can be below SMs / 2.  Both parameter-block sizes get the
+// shared-memory opt-in here (same resources, so the same count).
 int pair_max_clusters() {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
   if (!g_max_clusters[dev]) {
-    if (cudaFuncSetAttribute(tcgen05_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tcgen05_gemm_pair_kernel<Params>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PAIR_SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(tcgen05_gemm_pair_kernel<ParamsSmall>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              PAIR_SMEM_BYTES) != cudaSuccess) {
       cudaGetLastError();
       return 0;
@@ -492,7 +498,7 @@ int pair_max_clusters() {
     cudaLaunchAttribute attr[1];
     pair_config(&cfg, attr, 1, nullptr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tcgen05_gemm_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, tcgen05_gemm_pair_kernel<Params>, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
       return 0;
     }
@@ -503,19 +509,32 @@ int pair_max_clusters() {
 
 cudaError_t launch_tcgen05_pair(const Params& p, int clusters, cudaStream_t stream) {
   if (pair_max_clusters() <= 0) return cudaErrorInvalidConfiguration;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * clusters, 1, 1);
-  cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
-  cfg.stream = stream;
+  cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tcgen05_gemm_pair_kernel, p);
+  pair_config(&cfg, attr, clusters, stream);
+  if (p.nmaps <= ParamsSmall::kMaps && p.nsegs <= ParamsSmall::kSegs && p.ngroups <= ParamsSmall::kGroups) {
+    static thread_local ParamsSmall ps;
+    std::copy(p.maps, p.maps + p.nmaps, ps.maps);
+    std::copy(p.segs, p.segs + p.nsegs, ps.segs);
+    std::copy(p.groups, p.groups + p.ngroups, ps.groups);
+    std::copy(p.n_tile_begin, p.n_tile_begin + p.ngroups + 1, ps.n_tile_begin);
+    ps.nmaps = p.nmaps;
+    ps.nsegs = p.nsegs;
+    ps.ngroups = p.ngroups;
+    ps.total_tiles = p.total_tiles;
+    ps.m_tiles = p.m_tiles;
+    ps.band_m = p.band_m;
+    ps.starve = p.starve;
+    ps.wait_limit_ns = p.wait_limit_ns;
+    ps.status = p.status;
+    ps.trace = p.trace;
+    ps.sk_tiles = p.sk_tiles;
+    ps.sk_kiters = p.sk_kiters;
+    ps.sk_part = p.sk_part;
+    ps.sk_count = p.sk_count;
+    return cudaLaunchKernelEx(&cfg, tcgen05_gemm_pair_kernel<ParamsSmall>, ps);
+  }
+  return cudaLaunchKernelEx(&cfg, tcgen05_gemm_pair_kernel<Params>, p);
 }
 
 }  // namespace gemm

@@ -6,6 +6,7 @@
 
 #include <cuda_runtime.h>
 
+#include <memory>
 #include <vector>
 
 #include "dt_internal.h"
@@ -46,7 +47,13 @@ struct HostGroup {
 // Run every group; returns a host-detected error or DT_OK.
 dt_status run_groups(std::vector<HostGroup>& groups, int32_t* d_status, cudaStream_t stream);
 
-struct Params;
+// Capacities of one launch's parameter block (the device code's ParamsT).
+constexpr int MAX_MAPS = 48;
+constexpr int MAX_SEGS = 96;
+constexpr int MAX_GROUPS = 64;
+template <int NMAPS, int NSEGS, int NGROUPS>
+struct ParamsT;
+using Params = ParamsT<MAX_MAPS, MAX_SEGS, MAX_GROUPS>;
 cudaError_t launch_tcgen05(const Params& p, int grid, cudaStream_t stream);
 cudaError_t launch_tcgen05_pair(const Params& p, int clusters, cudaStream_t stream);
 int pair_max_clusters();  // co-resident clusters of the pair kernel (0: unavailable)
@@ -62,6 +69,17 @@ struct NoAllocScope {
 
 // Zero the split tail's arrival counters (after a launch reported a timeout).
 void reset_split_counters();
+
+// The launches one call made, recorded as issued so a later call with the
+// same operands replays them without planning.
+struct GemmRecord;
+struct GemmRecordScope {  // while alive, run_groups on this thread records into r
+  explicit GemmRecordScope(GemmRecord* r);
+  ~GemmRecordScope();
+};
+std::shared_ptr<GemmRecord> new_gemm_record();
+dt_status replay_gemm(const GemmRecord& r, cudaStream_t stream);
+bool gemm_no_alloc();  // inside a NoAllocScope (plans made there differ)
 
 }  // namespace gemm
 }  // namespace dt

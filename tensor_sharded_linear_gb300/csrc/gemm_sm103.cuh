@@ -32,6 +32,7 @@
 #include <stdint.h>
 
 #include "../../include/dt.h"
+#include "gemm_plan.h"  // Params and its capacities
 
 namespace dt {
 namespace gemm {
@@ -47,9 +48,6 @@ constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 512;                // two 256-column accumulators
 constexpr int GROUP_M = 8;                    // per-group raster: 8 M tiles per band
-constexpr int MAX_MAPS = 48;
-constexpr int MAX_SEGS = 96;
-constexpr int MAX_GROUPS = 64;
 constexpr int MAX_OUT = 8;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
@@ -86,11 +84,17 @@ enum TraceSlot {
   TRACE_SLOTS = 16
 };
 
-struct Params {  // CUtensorMap carries its own 128-byte alignment
-  CUtensorMap maps[MAX_MAPS];
-  Seg segs[MAX_SEGS];
-  Group groups[MAX_GROUPS];
-  int32_t n_tile_begin[MAX_GROUPS + 1];  // prefix sums of the groups' N tiles
+// Every launch's description travels in its parameter block.  Its size
+// costs launch time, so a launch whose tables fit the compact capacities
+// (ParamsSmall, ~8 KB) uses them and only large launches take Params (~25 KB).
+template <int NMAPS, int NSEGS, int NGROUPS>
+struct ParamsT {  // CUtensorMap carries its own 128-byte alignment
+  static constexpr int kMaps = NMAPS, kSegs = NSEGS, kGroups = NGROUPS;
+  CUtensorMap maps[NMAPS];
+  Seg segs[NSEGS];
+  Group groups[NGROUPS];
+  int32_t n_tile_begin[NGROUPS + 1];  // prefix sums of the groups' N tiles
+  int32_t nmaps, nsegs;               // entries of maps and segs in use
   int32_t ngroups, total_tiles;
   int32_t m_tiles;  // > 0: every group has this many M tiles, rastered together
   int32_t band_m;   // M tiles per raster band
@@ -110,6 +114,7 @@ struct Params {  // CUtensorMap carries its own 128-byte alignment
   float* sk_part;     // [piece][2 CTAs][128 rows][256 columns]
   int32_t* sk_count;  // [sk_tiles][2 CTAs][4 quarters]
 };
+using ParamsSmall = ParamsT<24, 32, 16>;
 static_assert(sizeof(Params) <= 32000, "GEMM parameter block over the launch limit");
 
 #ifdef DT_GEMM_TRACE
@@ -402,8 +407,8 @@ struct TileCoord {
 // (group, N tile) with M fastest, so concurrent CTAs share A rows and each
 // B panel is fetched once per band.  Otherwise each group is rastered on
 // its own in bands of GROUP_M M tiles.
-template <int TILE_M>
-__device__ __forceinline__ TileCoord decode_tile(const Params& p, int t) {
+template <int TILE_M, class P>
+__device__ __forceinline__ TileCoord decode_tile(const P& p, int t) {
   if (p.m_tiles > 0) {
     const int total_n = p.n_tile_begin[p.ngroups];
     const int span = p.band_m * total_n;
@@ -446,7 +451,8 @@ __device__ __forceinline__ int64_t sk_bound(int c, int64_t total, int ncl) { ret
 struct WorkIter {
   int cid, ncl, t_dp, dp_end, kiters;
   int64_t it, it_end;
-  __device__ WorkIter(const Params& p, int cid_, int ncl_) : cid(cid_), ncl(ncl_) {
+  template <class P>
+  __device__ WorkIter(const P& p, int cid_, int ncl_) : cid(cid_), ncl(ncl_) {
     dp_end = p.total_tiles - p.sk_tiles;
     t_dp = cid;
     kiters = p.sk_kiters;
@@ -482,12 +488,14 @@ struct WorkIter {
 // A piece's fp32 accumulator in sk_part, per (CTA, 32-row quarter): 8
 // column chunks x 8 float4 x 32 lanes, so every warp access to it moves
 // 512 contiguous bytes (lane = accumulator row within the quarter).
-__device__ __forceinline__ float4* sk_slot(const Params& p, int piece, uint32_t rank, int quarter) {
+template <class P>
+__device__ __forceinline__ float4* sk_slot(const P& p, int piece, uint32_t rank, int quarter) {
   return reinterpret_cast<float4*>(p.sk_part) + ((static_cast<size_t>(piece) * 2 + rank) * 4 + quarter) * (8 * 8 * 32);
 }
 
 // Clusters whose shares meet tail tile s: [c_first, c_last].
-__device__ __forceinline__ void sk_tile_clusters(const Params& p, int ncl, int s, int* c_first, int* c_last) {
+template <class P>
+__device__ __forceinline__ void sk_tile_clusters(const P& p, int ncl, int s, int* c_first, int* c_last) {
   const int64_t total = (int64_t)p.sk_tiles * p.sk_kiters;
   const int64_t lo = (int64_t)s * p.sk_kiters, hi = lo + p.sk_kiters;  // [lo, hi)
   const int64_t c_est = lo * ncl / total;

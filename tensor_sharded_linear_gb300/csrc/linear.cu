@@ -11,8 +11,12 @@
 // nanotron tutorial ch. 5, 5.1: ALL_REDUCE / REDUCE_SCATTER row outputs.
 #include <algorithm>
 #include <cstring>
+#include <memory>
+#include <mutex>
 #include <set>
+#include <string>
 #include <tuple>
+#include <unordered_map>
 #include <vector>
 
 #include "gemm_plan.h"
@@ -429,28 +433,118 @@ dt_status check_row(const Layout& lx, const Layout& lw, const Layout* lb, const 
   return DT_OK;
 }
 
+// Plans of the linears by operands (and stream, status word, workspace and
+// allocation scope, which the launches' parameters also hold).  A hit
+// replays the recorded launches; bounded, dropped whole when full.
+std::mutex g_gemm_plan_mu;
+std::unordered_map<std::string, std::shared_ptr<const gemm::GemmRecord>> g_gemm_plans;
+std::unordered_map<std::string, int> g_gemm_plan_device;
+constexpr size_t GEMM_PLAN_CACHE = 128;
+
+template <class F>
+dt_status with_gemm_plan(const std::string* key, dt_stream_t stream, F&& plan_and_launch) {
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (key) {
+    std::shared_ptr<const gemm::GemmRecord> hit;
+    int dev = -1;
+    {
+      std::lock_guard<std::mutex> lk(g_gemm_plan_mu);
+      auto it = g_gemm_plans.find(*key);
+      if (it != g_gemm_plans.end()) {
+        hit = it->second;
+        dev = g_gemm_plan_device[*key];
+      }
+    }
+    if (hit) {
+      clear_error();
+      int cur = -1;
+      cudaGetDevice(&cur);
+      if (dev >= 0 && cur != dev && cudaSetDevice(dev) != cudaSuccess)
+        return fail(DT_ERR_CUDA, "cudaSetDevice(%d)", dev);
+      return gemm::replay_gemm(*hit, s);
+    }
+  }
+  std::shared_ptr<gemm::GemmRecord> rec = gemm::new_gemm_record();
+  dt_status st;
+  {
+    gemm::GemmRecordScope scope(rec.get());
+    st = plan_and_launch();
+  }
+  if (st == DT_OK && key) {
+    int dev = -1;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(g_gemm_plan_mu);
+    if (g_gemm_plans.size() >= GEMM_PLAN_CACHE) {
+      g_gemm_plans.clear();
+      g_gemm_plan_device.clear();
+    }
+    g_gemm_plans[*key] = rec;
+    g_gemm_plan_device[*key] = dev;
+  }
+  return st;
+}
+
+// The key's common tail: what the recorded parameters hold besides the operands.
+void finish_key(std::string* k, int32_t* d_status, dt_stream_t stream) {
+  append_plan_scalar(k, d_status);
+  append_plan_scalar(k, stream);
+  append_plan_scalar(k, (char)(gemm::gemm_no_alloc() ? 1 : 0));
+}
+
 }  // namespace
+
+void clear_gemm_plans() {
+  std::lock_guard<std::mutex> lk(g_gemm_plan_mu);
+  g_gemm_plans.clear();
+  g_gemm_plan_device.clear();
+}
+
 }  // namespace dt
 
 using namespace dt;
 
 extern "C" {
 
-dt_status dt_column_parallel_linear(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* bias,
-                                    const dt_dtensor* y, int32_t tp_mesh_dim, int32_t* d_status,
-                                    dt_stream_t stream) {
-  return column_multi(x, 1, w, bias, y, tp_mesh_dim, d_status, stream);
-}
-
 dt_status dt_column_parallel_linear_multi(const dt_dtensor* x, int32_t n, const dt_dtensor* w,
                                           const dt_dtensor* bias, const dt_dtensor* y, int32_t tp_mesh_dim,
                                           int32_t* d_status, dt_stream_t stream) {
-  return column_multi(x, n, w, bias, y, tp_mesh_dim, d_status, stream);
+  std::string key(1, 'c');
+  bool keyed = n >= 0 && n <= 64 && (n == 0 || (w && y)) && append_plan_key(&key, x);
+  for (int j = 0; j < n && keyed; ++j)
+    keyed = append_plan_key(&key, &w[j]) && append_plan_key(&key, &y[j]) &&
+            append_plan_key(&key, bias ? &bias[j] : nullptr);
+  append_plan_scalar(&key, tp_mesh_dim);
+  finish_key(&key, d_status, stream);
+  return with_gemm_plan(keyed ? &key : nullptr, stream,
+                        [&] { return column_multi(x, n, w, bias, y, tp_mesh_dim, d_status, stream); });
 }
+
+dt_status dt_column_parallel_linear(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* bias,
+                                    const dt_dtensor* y, int32_t tp_mesh_dim, int32_t* d_status,
+                                    dt_stream_t stream) {
+  return dt_column_parallel_linear_multi(x, 1, w, bias, y, tp_mesh_dim, d_status, stream);
+}
+
+static dt_status row_parallel_planned(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* bias,
+                                      const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim, int32_t* d_status,
+                                      dt_stream_t stream);
 
 dt_status dt_row_parallel_linear(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* bias,
                                  const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim, int32_t* d_status,
                                  dt_stream_t stream) {
+  std::string key(1, 'r');
+  const bool keyed = append_plan_key(&key, x) && append_plan_key(&key, w) && append_plan_key(&key, bias) &&
+                     append_plan_key(&key, y);
+  append_plan_scalar(&key, mode);
+  append_plan_scalar(&key, tp_mesh_dim);
+  finish_key(&key, d_status, stream);
+  return with_gemm_plan(keyed ? &key : nullptr, stream,
+                        [&] { return row_parallel_planned(x, w, bias, y, mode, tp_mesh_dim, d_status, stream); });
+}
+
+static dt_status row_parallel_planned(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* bias,
+                                      const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim, int32_t* d_status,
+                                      dt_stream_t stream) {
   clear_error();
   DTensor X, W, B, Y;
   dt_status st;
@@ -524,9 +618,30 @@ dt_status dt_tp_mlp_workspace_size(const dt_dtensor* x, const dt_dtensor* w_gate
   return DT_OK;
 }
 
+static dt_status tp_mlp_planned(const dt_dtensor* x, const dt_dtensor* w_gate, const dt_dtensor* w_up,
+                                const dt_dtensor* w_down, const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim,
+                                void* workspace, size_t workspace_bytes, int32_t* d_status, dt_stream_t stream);
+
 dt_status dt_tp_mlp(const dt_dtensor* x, const dt_dtensor* w_gate, const dt_dtensor* w_up, const dt_dtensor* w_down,
                     const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim, void* workspace, size_t workspace_bytes,
                     int32_t* d_status, dt_stream_t stream) {
+  std::string key(1, 'm');
+  const bool keyed = append_plan_key(&key, x) && append_plan_key(&key, w_gate) && append_plan_key(&key, w_up) &&
+                     append_plan_key(&key, w_down) && append_plan_key(&key, y);
+  append_plan_scalar(&key, mode);
+  append_plan_scalar(&key, tp_mesh_dim);
+  append_plan_scalar(&key, workspace);
+  append_plan_scalar(&key, workspace_bytes);
+  finish_key(&key, d_status, stream);
+  return with_gemm_plan(keyed ? &key : nullptr, stream, [&] {
+    return tp_mlp_planned(x, w_gate, w_up, w_down, y, mode, tp_mesh_dim, workspace, workspace_bytes, d_status,
+                          stream);
+  });
+}
+
+static dt_status tp_mlp_planned(const dt_dtensor* x, const dt_dtensor* w_gate, const dt_dtensor* w_up,
+                                const dt_dtensor* w_down, const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim,
+                                void* workspace, size_t workspace_bytes, int32_t* d_status, dt_stream_t stream) {
   clear_error();
   DTensor X, Wg, Wu, Wd, Y;
   dt_status st;

@@ -929,20 +929,6 @@ std::mutex g_plan_mu;
 std::unordered_map<std::string, std::shared_ptr<const RecordedPlan>> g_plans;
 constexpr size_t RD_PLAN_CACHE = 128;
 
-// false: a malformed descriptor, left to the checks of the planning path
-bool append_key(std::string* k, const dt_dtensor& d) {
-  if (d.nslots < 0 || d.nslots > DT_MAX_SLOTS || (d.nslots > 0 && !d.slots)) return false;
-  const int nd = d.layout.ndim;
-  if (nd < 0 || nd > DT_MAX_TENSOR_DIMS) return false;
-  k->append(reinterpret_cast<const char*>(&d.layout), sizeof(d.layout));
-  k->append(reinterpret_cast<const char*>(&d.nslots), sizeof(d.nslots));
-  if (d.nslots > 0) k->append(reinterpret_cast<const char*>(d.slots), sizeof(void*) * d.nslots);
-  const char has = d.strides ? 1 : 0;
-  k->push_back(has);
-  if (has) k->append(reinterpret_cast<const char*>(d.strides), sizeof(int64_t) * (size_t)d.nslots * nd);
-  return true;
-}
-
 dt_status replay(const RecordedPlan& rp, cudaStream_t s) {
   auto launch = [&](int kind, cudaStream_t st) { return replay_kind(rp, kind, st); };
   if (rp.forked) return launch_forked(launch, s);
@@ -958,7 +944,7 @@ dt_status redistribute_many(int32_t n, const dt_dtensor* src, const dt_dtensor* 
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   std::string key;
   bool keyed = true;
-  for (int i = 0; i < n && keyed; ++i) keyed = append_key(&key, src[i]) && append_key(&key, dst[i]);
+  for (int i = 0; i < n && keyed; ++i) keyed = append_plan_key(&key, &src[i]) && append_plan_key(&key, &dst[i]);
   if (keyed && n > 0) {
     std::shared_ptr<const RecordedPlan> hit;
     {
