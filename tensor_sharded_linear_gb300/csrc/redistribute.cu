@@ -80,7 +80,7 @@ struct RdTask {
   int16_t ref_begin;  // sources, then (copies) the extra destinations as byte distances
   int8_t dmap[4];     // slot stride used for each padded position (dims merged on the host)
   int8_t nextra;      // copies: further destination slots receiving the same box
-  int8_t pad;
+  int8_t extra16;     // 1: every further destination is a multiple of 16 bytes from the first
 };
 
 struct RdRef {
@@ -211,6 +211,53 @@ __device__ void copy_span(char* d, const char* s, int64_t n, int esize, int lane
   if (edge >= 0) {
     if (esize == 2) reinterpret_cast<uint16_t*>(d)[edge] = static_cast<uint16_t>(ev);
     else reinterpret_cast<uint32_t*>(d)[edge] = ev;
+  }
+}
+
+// copy_span into the first destination d and nx replicas d + x[j].off,
+// each a multiple of 16 bytes from d, with d and s equally aligned: every
+// source vector is loaded once and stored to every replica.
+__device__ __forceinline__ void copy_span_replicas(char* d, const char* s, int64_t n, int esize, int lane,
+                                                   const RdRef* x, int nx) {
+  const uintptr_t da = reinterpret_cast<uintptr_t>(d);
+  const int64_t nbytes = n * esize;
+  int64_t head = static_cast<int64_t>((16 - (da & 15)) & 15);
+  if (head > nbytes) head = nbytes;
+  const int64_t nvec = (nbytes - head) / 16;
+  const int64_t tail = nbytes - head - nvec * 16;
+  const int head_n = static_cast<int>(head / esize), tail_n = static_cast<int>(tail / esize);
+  int64_t edge = -1;
+  if (lane < head_n) edge = lane;
+  else if (lane >= 16 && lane - 16 < tail_n) edge = (head + nvec * 16) / esize + (lane - 16);
+  uint32_t ev = 0;
+  if (edge >= 0) ev = esize == 2 ? reinterpret_cast<const uint16_t*>(s)[edge] : reinterpret_cast<const uint32_t*>(s)[edge];
+  const uint4* sv = reinterpret_cast<const uint4*>(s + head);
+  uint4* dv = reinterpret_cast<uint4*>(d + head);
+  constexpr int UN = RD_COPY_UNROLL;
+  int64_t i = lane;
+  for (; i + (UN - 1) * 32 < nvec; i += UN * 32) {
+    uint4 v[UN];
+#pragma unroll
+    for (int u = 0; u < UN; ++u) v[u] = ld_stream(sv + i + 32 * u);
+    for (int j = 0; j <= nx; ++j) {
+      uint4* dj = j == 0 ? dv : reinterpret_cast<uint4*>(reinterpret_cast<char*>(dv) + x[j - 1].off);
+#pragma unroll
+      for (int u = 0; u < UN; ++u) st_stream(dj + i + 32 * u, v[u]);
+    }
+  }
+  for (; i < nvec; i += 32) {
+    const uint4 v = ld_stream(sv + i);
+    for (int j = 0; j <= nx; ++j) {
+      uint4* dj = j == 0 ? dv : reinterpret_cast<uint4*>(reinterpret_cast<char*>(dv) + x[j - 1].off);
+      st_stream(dj + i, v);
+    }
+  }
+  if (edge >= 0) {
+    for (int j = 0; j <= nx; ++j) {
+      char* dj = j == 0 ? d : d + x[j - 1].off;
+      if (esize == 2) reinterpret_cast<uint16_t*>(dj)[edge] = static_cast<uint16_t>(ev);
+      else reinterpret_cast<uint32_t*>(dj)[edge] = ev;
+    }
   }
 }
 
@@ -450,7 +497,12 @@ __global__ void __launch_bounds__(RD_THREADS, SUM ? RD_SUM_CTAS : RD_COPY_CTAS) 
       } else {
         // the replicas of a materialised Replicate layout: each has the first
         // destination's strides and sits a fixed number of bytes from it (the
-        // host stores that distance); the source span is re-read from L1/L2
+        // host stores that distance).  Equally aligned replicas take each
+        // loaded vector; otherwise the source span is re-read from L1/L2.
+        if (unit && T.extra16 && ((reinterpret_cast<uintptr_t>(d) ^ reinterpret_cast<uintptr_t>(s)) & 15) == 0) {
+          copy_span_replicas(d, s, n, esize, lane, &p.ref[T.ref_begin + 1], T.nextra);
+          continue;
+        }
         for (int j = 0; j <= T.nextra; ++j) {
           char* dj = j == 0 ? d
                             : reinterpret_cast<char*>(reinterpret_cast<uintptr_t>(d) +
@@ -831,12 +883,14 @@ dt_status launch_kind(std::vector<PairPlan>& plans, int kind, cudaStream_t strea
         ++nref;
       }
       t.nextra = (int8_t)ht.extra_dst.size();
+      t.extra16 = 1;
       const uintptr_t first = reinterpret_cast<uintptr_t>(pp.D.slots[ht.dst_slot].ptr) + (uintptr_t)(t.dst_off * ls.esize);
       for (int x : ht.extra_dst) {  // replica x: byte distance from the first destination
         const uintptr_t at =
             reinterpret_cast<uintptr_t>(pp.D.slots[x].ptr) + (uintptr_t)(local_offset(pp.D.slots[x], ht.box, nd) * ls.esize);
         p.ref[nref].slot = dbase + x;
         p.ref[nref].off = static_cast<int64_t>(at - first);
+        if (p.ref[nref].off % 16 != 0) t.extra16 = 0;
         ++nref;
       }
       // segments are whole 16-byte multiples so every segment of a row
