@@ -107,12 +107,58 @@ def aggregate(roofline_s: float, step_s: float, world: int, device="cpu"):
 
 # ---------------------------------------------------------------- clocks
 
+class _Nvml:
+    """Read-only NVML queries through the driver's libnvidia-ml (ctypes):
+    the SM clock, its maximum, board power and the active clock-event
+    reasons of one GPU."""
+
+    CLOCK_SM = 1
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, uuid: str):
+        import ctypes
+        self.C = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle for " + uuid)
+        try:
+            self.reasons_fn = self.lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self.reasons_fn = self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sample(self):
+        C = self.C
+        sm, mw, r = C.c_uint(), C.c_uint(), C.c_ulonglong()
+        if (self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, C.byref(sm)) != 0
+                or self.lib.nvmlDeviceGetPowerUsage(self.h, C.byref(mw)) != 0
+                or self.reasons_fn(self.h, C.byref(r)) != 0):
+            raise RuntimeError("NVML query failed")
+        return float(sm.value), mw.value / 1000.0, int(r.value)
+
+    def max_sm(self):
+        v = self.C.c_uint()
+        return float(v.value) if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, self.C.byref(v)) == 0 else None
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
 class ClockSampler:
-    """nvidia-smi sampling every 200 ms while the timed region runs."""
+    """SM clock, power and throttle reasons while the timed region runs.
+
+    NVML is read from a thread every 2 ms (ctypes releases the interpreter
+    lock during each query), and only samples whose host timestamps fall
+    inside the timed region count; a timed region of a few tens of ms still
+    gets a dozen samples or more.  Where NVML cannot be loaded, nvidia-smi
+    runs every 200 ms around the region instead."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_S = 0.002
 
     def __init__(self, index: int):
         self.index = str(index)
@@ -122,8 +168,32 @@ class ClockSampler:
             pass
         self.proc = None
         self.path = None
+        self.nvml = None
+        self.thread = None
+        self.samples = []
 
     def start(self):
+        try:
+            self.nvml = _Nvml(self.index)
+            self.nvml.sample()
+        except Exception:
+            self.nvml = None
+        if self.nvml is not None:
+            import threading
+            self.stop_flag = threading.Event()
+
+            def loop():
+                while not self.stop_flag.is_set():
+                    t = time.perf_counter()
+                    try:
+                        self.samples.append((t, *self.nvml.sample()))
+                    except Exception:
+                        return
+                    time.sleep(self.PERIOD_S)
+
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+            return
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
         try:
@@ -134,7 +204,19 @@ class ClockSampler:
             self.proc = None
         time.sleep(0.3)
 
-    def stop(self):
+    def stop(self, window=None):
+        """window: (t0, t1) host perf_counter bounds of the timed region."""
+        if self.nvml is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=5)
+            inside = [x for x in self.samples if window is None or window[0] <= x[0] <= window[1]]
+            mx = self.nvml.max_sm()
+            self.nvml.close()
+            reasons = sorted({name for _, _, _, r in inside for bit, name in _Nvml.REASONS.items() if r & bit})
+            return {"sm_mhz": statistics.median(x[1] for x in inside) if inside else None, "sm_max_mhz": mx,
+                    "sm_mhz_min": min(x[1] for x in inside) if inside else None,
+                    "power_w_max": max(x[2] for x in inside) if inside else None, "reasons": reasons,
+                    "samples": len(inside), "source": "NVML every 2 ms, samples inside the timed region"}
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         time.sleep(0.25)
@@ -161,7 +243,8 @@ class ClockSampler:
                         reasons.add(name)
         os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm),
+                "source": "nvidia-smi every 200 ms around the timed region"}
 
 
 # ---------------------------------------------------------------- our arm
@@ -597,7 +680,7 @@ def run_ours(args):
     launches = lib.dt_launch_count() - launches0
     gc.enable()
     barrier(world)
-    clk = clocks.stop()
+    clk = clocks.stop((wall0, wall1))
     status = blk.tsl.read_device_status()
     total_ms = t0.elapsed_time(t1)
     step_s = total_ms / 1e3 / args.steps
