@@ -107,13 +107,16 @@ def aggregate(roofline_s: float, step_s: float, world: int, device="cpu"):
 
 # ---------------------------------------------------------------- clocks
 
+# NVML clock-event reason bits the timing rules name
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+
 class _Nvml:
     """Read-only NVML queries through the driver's libnvidia-ml (ctypes):
     the SM clock, its maximum, board power and the active clock-event
     reasons of one GPU."""
 
     CLOCK_SM = 1
-    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
 
     def __init__(self, uuid: str):
         import ctypes
@@ -212,7 +215,7 @@ class ClockSampler:
             inside = [x for x in self.samples if window is None or window[0] <= x[0] <= window[1]]
             mx = self.nvml.max_sm()
             self.nvml.close()
-            reasons = sorted({name for _, _, _, r in inside for bit, name in _Nvml.REASONS.items() if r & bit})
+            reasons = sorted({name for _, _, _, r in inside for bit, name in NVML_REASONS.items() if r & bit})
             return {"sm_mhz": statistics.median(x[1] for x in inside) if inside else None, "sm_max_mhz": mx,
                     "sm_mhz_min": min(x[1] for x in inside) if inside else None,
                     "power_w_max": max(x[2] for x in inside) if inside else None, "reasons": reasons,
