@@ -710,7 +710,7 @@ def run_ours(args):
     gemm_tflops = gemm_flops / (gemm_ms / 1e3) / 1e12 if gemm_ms else 0.0
     ngemm = sum(1 for c in blk.calls if c[1] == "flops")
     traffic, _ = gemm_traffic()
-    roofline = {"kernel": "tcgen05_gemm_kernel (TP MLP + attention projections, 4 launches per step)",
+    roofline = {"kernel": "tcgen05_gemm_pair_kernel (TP MLP + attention projections, 4 launches per step)",
                 "bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(gemm_tflops / peaks["bf16_tflops"], 4),
                 "peak_kind": f"dense bf16 burst, {peaks['source']}", "traffic": traffic,

@@ -5,14 +5,19 @@
 // step instead of 48 KiB for a 128 x 256 single-CTA tile, which halves the
 // B traffic into each SM and leaves room for 6 pipeline stages.
 //
-// Roles per CTA (192 threads): warp 0 TMA producer, warp 1 MMA issuer (rank
-// 0 only; it owns the pair's MMAs), warps 2..5 epilogue.  Barriers:
-//   full[s]    in rank 0: 1 arrival (rank 0, with the byte count of both
-//              CTAs' loads) + the loads' bytes.  Rank 1 only issues its loads:
-//              its bytes are its share.  (A cluster-scope release arrive from
+// Roles per CTA (224 threads): warp 0 TMA producer of A, warp 6 TMA producer
+// of B, warp 1 MMA issuer (rank 0 only; it owns the pair's MMAs), warps 2..5
+// epilogue.  Two producers because one thread issuing every copy capped the
+// copies alone at ~46 B/clk per SM (the issuing thread blocks ~110 cycles
+// per copy); split, the copies alone run 16-20% faster and the GEMMs ~1%.
+// Barriers:
+//   full[s]    in rank 0: 1 arrival (rank 0's A producer, with the byte
+//              count of both CTAs' loads) + the loads' bytes.  Every other
+//              producer only issues its loads: its bytes are its share.  (A cluster-scope release arrive from
 //              rank 1 before each stage would wait for that thread's copies
 //              still in flight and serialise rank 1's pipeline.)
-//   empty[s]   in each CTA: 1 arrival, rank 0's MMA commit multicast to both;
+//   empty[s]   in each CTA: 1 arrival, rank 0's MMA commit multicast to both
+//              (both producers of a CTA wait on it);
 //   tfull[b]   in each CTA: 1 arrival, multicast commit after a tile's MMAs;
 //   tempty[b]  in rank 0: 8 arrivals, the 4 epilogue warps of each CTA.
 // Every wait is bounded as in the single-CTA kernel.
@@ -25,7 +30,7 @@ namespace dt {
 namespace gemm {
 
 template <class P>
-__global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __grid_constant__ P p) {
+__global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(const __grid_constant__ P p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + PAIR_STAGES * PAIR_STAGE_BYTES);
@@ -74,15 +79,17 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
   const long long _trace_start = clock64();
 #endif
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer (both CTAs)
+  if (warp == 0 || warp == PAIR_B_PRODUCER_WARP) {
+    // ------------------------------------------------------------ TMA producers (both CTAs)
+    // warp 0 loads this CTA's A rows (and, in rank 0, arms the stage's
+    // barrier for every byte of both CTAs); the B producer loads its B
+    // columns.  Both walk the same stages and wait on the same `empty`.
+    const bool loads_a = warp == 0;
     if (lane == 0) {
       for (int i = 0; i < p.ngroups; ++i) {
         const Group& G = p.groups[i];
-        for (int s = G.seg_begin; s < G.seg_begin + G.seg_count && s < G.seg_begin + 2; ++s) {
-          prefetch_map(&p.maps[p.segs[s].a_map]);
-          prefetch_map(&p.maps[p.segs[s].b_map]);
-        }
+        for (int s = G.seg_begin; s < G.seg_begin + G.seg_count && s < G.seg_begin + 2; ++s)
+          prefetch_map(&p.maps[loads_a ? p.segs[s].a_map : p.segs[s].b_map]);
       }
       int stage = 0;
       uint32_t phase = 0;
@@ -119,11 +126,12 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
               break;
             }
             const uint32_t full0 = mapa_shared(smem_u32(&full[stage]), 0);
-            if (rank == 0) mbar_expect_tx(&full[stage], 2 * PAIR_STAGE_BYTES);
             uint8_t* a = smem + stage * PAIR_STAGE_BYTES;
             uint8_t* b = a + PAIR_A_BYTES;
-            tma_load_2d_pair(a, &p.maps[S.a_map], kt * BK, a_row, full0);
-            if (G.b_kmajor) {
+            if (loads_a) {
+              if (rank == 0) mbar_expect_tx(&full[stage], 2 * PAIR_STAGE_BYTES);
+              tma_load_2d_pair(a, &p.maps[S.a_map], kt * BK, a_row, full0);
+            } else if (G.b_kmajor) {
               tma_load_2d_pair(b, bmap, kt * BK, b_col, full0);  // 128 N rows of 64 K
             } else {
               tma_load_2d_pair(b, bmap, b_col, kt * BK, full0);
@@ -432,12 +440,12 @@ __global__ void __launch_bounds__(THREADS, 1) tcgen05_gemm_pair_kernel(const __g
   }
 
   // ------------------------------------------------------------ teardown
-  __syncwarp();  // lanes 1..31 of warps 0 and 1 wait here for their lane 0
+  __syncwarp();  // lanes 1..31 of the producer and MMA warps wait here for their lane 0
 #ifdef DT_GEMM_TRACE
   if (threadIdx.x == 0 && p.trace) atomicAdd(&p.trace[blockIdx.x * TRACE_SLOTS + TR_TOTAL], (unsigned long long)(clock64() - _trace_start));
 #endif
   if (aborted && lane == 0) atomicOr(p.status, DT_DEV_ERR_TIMEOUT);
-  if (warp == 0 && lane == 0 && aborted) {
+  if ((warp == 0 || warp == PAIR_B_PRODUCER_WARP) && lane == 0 && aborted) {
     // copies this CTA issued count on rank 0's barrier; give them a bounded
     // time to land before the pair leaves
     const uint64_t t0 = globaltimer();
@@ -462,7 +470,7 @@ namespace {
 void pair_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int clusters, cudaStream_t stream) {
   *cfg = cudaLaunchConfig_t{};
   cfg->gridDim = dim3(2 * clusters, 1, 1);
-  cfg->blockDim = dim3(THREADS, 1, 1);
+  cfg->blockDim = dim3(PAIR_THREADS, 1, 1);
   cfg->dynamicSmemBytes = PAIR_SMEM_BYTES;
   cfg->stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;

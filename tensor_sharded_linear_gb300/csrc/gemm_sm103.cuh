@@ -295,6 +295,8 @@ constexpr int FIN_BUF_BYTES = FIN_WARP_BYTES / 2;
 constexpr int FIN_CHUNK_BYTES = 32 * 32 * 4;                        // 32 rows x 32 fp32 columns
 constexpr int FIN_MAX_PIECES = FIN_BUF_BYTES / FIN_CHUNK_BYTES;     // 6 (3 for the gated MLP)
 constexpr int PAIR_TILE_M = 2 * BM;                 // rows of one pair tile
+constexpr int PAIR_B_PRODUCER_WARP = 6;             // warps 0..5 as in the single-CTA kernel, plus this
+constexpr int PAIR_THREADS = 32 * (PAIR_B_PRODUCER_WARP + 1);
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
