@@ -949,6 +949,66 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_cublas_shapes(args):
+    """Library context, not a bench line: cuBLAS (torch.matmul, bf16 in and
+    out) on the step's dense GEMM shapes, each call after an L2 flush, CUDA
+    events, median of --steps after --warmup.  The TP MLP has no fused
+    counterpart there: gate and up run as one [T,H]x[H,2F] GEMM, SiLU(g)*u
+    as torch elementwise ops, then the down GEMM."""
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    peaks = load_peaks()
+    gen = torch.Generator(device=device).manual_seed(7)
+    bf = torch.bfloat16
+
+    def randn(*shape, std=1.0):
+        return (torch.randn(*shape, device=device, generator=gen) * std).to(bf)
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        ts = []
+        for _ in range(args.steps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize(device)
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+
+    from tensor_sharded_linear_gb300 import workloads as W
+    T, H, F = W.MLP["tokens"], W.MLP["hidden"], W.MLP["ffn"]
+    x, wgu, wd = randn(T, H), randn(H, 2 * F, std=H ** -0.5), randn(F, H, std=F ** -0.5)
+    gu, h, y = torch.empty(T, 2 * F, device=device, dtype=bf), torch.empty(T, F, device=device, dtype=bf), \
+        torch.empty(T, H, device=device, dtype=bf)
+    rows = {}
+    rows["MLP gate/up as one GEMM"] = (timed(lambda: torch.matmul(x, wgu, out=gu)), 2 * T * H * 2 * F)
+    g, u = gu[:, :F], gu[:, F:]
+    rows["MLP SiLU(g)*u, torch elementwise"] = (timed(lambda: torch.mul(torch.nn.functional.silu(g), u, out=h)), 0)
+    rows["MLP down"] = (timed(lambda: torch.matmul(h, wd, out=y)), 2 * T * F * H)
+    TA, HA = W.ATTENTION["tokens"], W.ATTENTION["hidden"]
+    xa, wqkv, wo = randn(TA, HA), randn(HA, 3 * HA, std=HA ** -0.5), randn(HA, HA, std=HA ** -0.5)
+    qkv, o = torch.empty(TA, 3 * HA, device=device, dtype=bf), torch.empty(TA, HA, device=device, dtype=bf)
+    rows["attention q/k/v as one GEMM"] = (timed(lambda: torch.matmul(xa, wqkv, out=qkv)), 2 * TA * HA * 3 * HA)
+    q = randn(TA, HA)  # contiguous, as the step's q/k/v output slots are
+    rows["attention o"] = (timed(lambda: torch.matmul(q, wo, out=o)), 2 * TA * HA * HA)
+    out = {}
+    for name, (us, flops) in rows.items():
+        out[name] = {"us": round(us, 2)}
+        if flops:
+            tf = flops / (us / 1e6) / 1e12
+            out[name].update(tflops=round(tf, 1), frac=round(tf / peaks["bf16_tflops"], 4))
+    mlp_us = sum(rows[k][0] for k in ("MLP gate/up as one GEMM", "MLP SiLU(g)*u, torch elementwise", "MLP down"))
+    print(json.dumps({"impl": "cublas-shapes", "note": "library context on the step's dense shapes, not a bench line",
+                      "rows": out, "tp_mlp_us_unfused": round(mlp_us, 2),
+                      "peak_bf16_tflops": peaks["bf16_tflops"], "steps": args.steps, "warmup": args.warmup,
+                      "l2": "256 MB written before every call"}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -958,12 +1018,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the rows timed outside the step")
+    ap.add_argument("--cublas-shapes", action="store_true",
+                    help="time cuBLAS on the step's dense GEMM shapes (library context) and exit")
     ap.add_argument("--only", default=ALL_COMPONENTS,
                     help="comma-separated subset of embedding,redistribute,mlp,attention (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.cublas_shapes:
+        run_cublas_shapes(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
