@@ -731,7 +731,7 @@ def run_ours(args):
         "metric": METRIC, "value": round(100.0 * roof_sum / step_max, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_max * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded torch CPU RNG, BASELINE shapes and distributions)",
+        "data": "synthetic (seeded torch CPU RNG, the workload shapes and distributions stated in config)",
         "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}; logical TP mesh inside each GPU",
                    "l2": "no flush: every tensor is re-read only after >2.5 GB of other traffic per step "
                          "(L2 129 MB); each kernel's inputs are >=134 MB",
