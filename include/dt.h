@@ -35,8 +35,15 @@
  *    cudaMalloc outside a stream capture; inside a capture, or when it
  *    cannot be made, every tile runs whole).  dt_clear_cache() drops the
  *    descriptors and frees the scratch.
- *  - Environment switches, read once per process: DT_GEMM_PAIR=0 selects the
- *    single-CTA GEMM kernel, DT_GEMM_SPLIT=0 turns the split tail off.
+ *  - Environment switches, read once per process:
+ *      DT_GEMM_PAIR=0   selects the single-CTA GEMM kernel;
+ *      DT_GEMM_SPLIT=0  turns the split tail off.
+ *    Two test hooks exercise the bounded-wait exit without a fault:
+ *      DT_GEMM_WAIT_LIMIT_MS=n  bounds every GEMM barrier wait at n ms
+ *                               (1..10000; default 2000);
+ *      DT_GEMM_STARVE=1         makes the GEMM producers issue no copies,
+ *                               so every wait runs out and the launch
+ *                               reports DT_DEV_ERR_TIMEOUT.
  *  - Compute calls are asynchronous on the given stream (a cudaStream_t;
  *    NULL = the legacy default stream).  Their return value covers the checks
  *    done on the host before any launch; on any error nothing is launched.
