@@ -612,6 +612,19 @@ dt_status run_groups(std::vector<HostGroup>& groups, int32_t* d_status, cudaStre
   if (live.empty()) return DT_OK;
   for (auto& g : live)
     if (g.out_ptr.size() > (size_t)MAX_OUT) return fail(DT_ERR_CAPACITY, "more than %d output row blocks", MAX_OUT);
+  // M, N and the TMA and tile coordinates are 32-bit on the device: refuse a
+  // dimension that would not fit (an [8, 2^31] bf16 activation is only
+  // 32 GB) instead of truncating it
+  constexpr int64_t DIM_LIMIT = (1ll << 31) - 512;
+  for (const auto& g : live) {
+    if (g.m > DIM_LIMIT || g.n > DIM_LIMIT)
+      return fail(DT_ERR_CAPACITY, "GEMM output %lld x %lld: each dimension must be below 2^31 - 512", (long long)g.m,
+                  (long long)g.n);
+    for (const auto& sg : g.segs)
+      if (sg.a.rows > DIM_LIMIT || sg.a.cols > DIM_LIMIT || sg.b.rows > DIM_LIMIT || sg.b.cols > DIM_LIMIT)
+        return fail(DT_ERR_CAPACITY, "GEMM operand of %lld x %lld / %lld x %lld: each dimension must be below 2^31 - 512",
+                    (long long)sg.a.rows, (long long)sg.a.cols, (long long)sg.b.rows, (long long)sg.b.cols);
+  }
   bool tc = true;
   for (const auto& g : live) {
     if (g.segs.empty()) tc = false;

@@ -113,6 +113,19 @@ struct ColumnSpec {
   const DTensor* y;
 };
 
+// The GEMM kernels keep M, N and their TMA and tile coordinates in 32 bits:
+// a dimension that would not fit is refused before anything touches the
+// device (an [8, 2^31] bf16 activation is only 32 GB).
+constexpr int64_t GEMM_DIM_LIMIT = (1ll << 31) - 512;
+dt_status check_gemm_dims(const Layout& lx, int64_t k, int64_t n) {
+  int64_t m = 1;
+  for (int d = 0; d + 1 < lx.ndim; ++d) m *= lx.gshape[d];
+  if (m > GEMM_DIM_LIMIT || k > GEMM_DIM_LIMIT || n > GEMM_DIM_LIMIT)
+    return fail(DT_ERR_CAPACITY, "GEMM of M=%lld, K=%lld, N=%lld: each must be below 2^31 - 512", (long long)m,
+                (long long)k, (long long)n);
+  return DT_OK;
+}
+
 // Checks shared by the column layers: x [.., K] Replicate on tp, w [K, N]
 // Shard(1) on tp, bias [N] Shard(0) on tp, y [.., N] Shard(-1) on tp; off tp
 // weights/bias Replicate and x, y placed alike.
@@ -132,6 +145,7 @@ dt_status check_column(const DTensor& X, const ColumnSpec& c, int tp, bool allow
   for (int d = 0; d < nd - 1; ++d)
     if (ly.gshape[d] != lx.gshape[d]) return fail(DT_ERR_SHAPE, "y leading dims differ from x");
   if (ly.gshape[nd - 1] != lw.gshape[1]) return fail(DT_ERR_SHAPE, "y last dim != w cols");
+  if (dt_status st = check_gemm_dims(lx, lw.gshape[0], lw.gshape[1]); st != DT_OK) return st;
   if (c.bias) {
     const Layout& lb = c.bias->layout;
     if (lb.ndim != 1 || lb.gshape[0] != lw.gshape[1]) return fail(DT_ERR_SHAPE, "bias must be [out]");
@@ -406,6 +420,7 @@ dt_status check_row(const Layout& lx, const Layout& lw, const Layout* lb, const 
   for (int d = 0; d < nd - 1; ++d)
     if (ly.gshape[d] != lx.gshape[d]) return fail(DT_ERR_SHAPE, "y leading dims differ from x");
   if (ly.gshape[nd - 1] != lw.gshape[1]) return fail(DT_ERR_SHAPE, "y last dim != w cols");
+  if (dt_status st = check_gemm_dims(lx, lw.gshape[0], lw.gshape[1]); st != DT_OK) return st;
   if (lb) {
     if (lb->ndim != 1 || lb->gshape[0] != lw.gshape[1]) return fail(DT_ERR_SHAPE, "bias must be [out]");
     if (lb->dtype == DT_INT32) return fail(DT_ERR_INVALID_ARG, "bias dtype");
@@ -676,6 +691,7 @@ static dt_status tp_mlp_planned(const dt_dtensor* x, const dt_dtensor* w_gate, c
   const int nd = lx.ndim;
   if (lx.gshape[nd - 1] != Wg.layout.gshape[0]) return fail(DT_ERR_SHAPE, "x last dim != w_gate rows");
   if (Wd.layout.ndim != 2 || Wd.layout.gshape[0] != Wg.layout.gshape[1]) return fail(DT_ERR_SHAPE, "w_down must be [ffn, out]");
+  if ((st = check_gemm_dims(lx, Wg.layout.gshape[0], 2 * Wg.layout.gshape[1])) != DT_OK) return st;
   MlpPlan plan;
   if ((st = mlp_plan(X, Wg, tp, &plan)) != DT_OK) return st;
   if (!workspace || workspace_bytes < plan.bytes)

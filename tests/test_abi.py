@@ -156,6 +156,28 @@ def test_host_rejections_before_launch(lib):
     assert lib.dt_tp_embedding(C.byref(ids), C.byref(table), C.byref(out), 0, None, None) == L.ERR_PLACEMENT
 
 
+def test_gemm_dimensions_beyond_32_bits_are_refused(lib):
+    """The GEMM's M, N and coordinates are 32-bit on the device: an
+    activation with 2^31 rows (32 GB in bf16, so it fits a GB300) is refused
+    on the host before anything launches, not truncated."""
+    mesh = (4,)
+    R, S1 = opl.Replicate(), opl.Shard(1)
+    big = 1 << 31
+    x = fake_desc(opl.Layout(mesh, [R], (big, 8)))
+    w = fake_desc(opl.Layout(mesh, [S1], (8, 64)))
+    y = fake_desc(opl.Layout(mesh, [S1], (big, 64)))
+    assert lib.dt_column_parallel_linear(C.byref(x), C.byref(w), None, C.byref(y), 0, None, None) == L.ERR_CAPACITY
+    assert b"2^31" in lib.dt_last_error()
+    # row-parallel with K = 2^31 (x Shard(-1), w Shard(0) on tp)
+    S0 = opl.Shard(0)
+    xr = fake_desc(opl.Layout(mesh, [S1], (8, big)))
+    wr = fake_desc(opl.Layout(mesh, [S0], (big, 64)))
+    yr = fake_desc(opl.Layout(mesh, [R], (8, 64)))
+    assert lib.dt_row_parallel_linear(C.byref(xr), C.byref(wr), None, C.byref(yr), L.TP_ALL_REDUCE, 0, None,
+                                      None) == L.ERR_CAPACITY
+    assert b"2^31" in lib.dt_last_error()
+
+
 def test_status_strings(lib):
     for s in range(8):
         assert lib.dt_status_string(s)
