@@ -32,8 +32,9 @@
  *    back to the caller's stream); per (device, stream), the split-tail
  *    scratch of the tensor-core GEMM (about 39 MB of partial accumulators
  *    and counters, made by the first linear whose last wave is split, with
- *    cudaMalloc outside a stream capture; inside a capture, or when it
- *    cannot be made, every tile runs whole).  dt_clear_cache() drops the
+ *    cudaMalloc outside a stream capture; at most 16 (device, stream) pairs
+ *    get one.  Inside a capture, past that count, or when it cannot be
+ *    made, every tile runs whole).  dt_clear_cache() drops the
  *    descriptors and frees the scratch.
  *  - Environment switches, read once per process:
  *      DT_GEMM_PAIR=0   selects the single-CTA GEMM kernel;
@@ -89,7 +90,9 @@ typedef enum dt_status {
   DT_ERR_UNSUPPORTED = 4,  /* legal in principle, not provided (e.g. Shard -> Partial) */
   DT_ERR_ALIGNMENT = 5,    /* pointer or stride alignment the kernel needs */
   DT_ERR_CUDA = 6,         /* a CUDA runtime or driver call failed */
-  DT_ERR_CAPACITY = 7      /* more slots, tasks or groups than one call plans */
+  DT_ERR_CAPACITY = 7      /* more slots, tasks or groups than one call plans, or a
+                              linear dimension at or above 2^31 - 512 (the GEMM
+                              kernels' coordinates are 32-bit) */
 } dt_status;
 
 /* Bits OR-ed into *d_status by kernels. */

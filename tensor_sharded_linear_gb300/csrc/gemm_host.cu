@@ -298,8 +298,10 @@ bool use_split_tail() {
 }
 
 // Scratch for `pieces` partial tiles and `counters` counters on this
-// device and stream; nullptr inside a NoAllocScope or when the allocation
-// fails (the launch then runs every tile whole).
+// device and stream; nullptr inside a NoAllocScope, inside a stream
+// capture, once MAX_SPLIT_STREAMS (device, stream) pairs hold one, or when
+// the allocation fails (the launch then runs every tile whole).
+constexpr size_t MAX_SPLIT_STREAMS = 16;  // ~39 MB each
 const SplitScratch* split_scratch(cudaStream_t stream, int pieces, int counters) {
   if (g_no_alloc) return nullptr;
   int dev = 0;
@@ -309,6 +311,7 @@ const SplitScratch* split_scratch(cudaStream_t stream, int pieces, int counters)
   auto it = g_split.find(key);
   if (it != g_split.end() && it->second.pieces >= pieces && it->second.counters >= counters) return &it->second;
   if (it != g_split.end()) return nullptr;  // sized once, for the largest split a launch can make
+  if (g_split.size() >= MAX_SPLIT_STREAMS) return nullptr;
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
     cudaGetLastError();
