@@ -22,23 +22,29 @@
  *  - Pointers named "device" are CUDA device pointers on the current GPU;
  *    everything else (descriptors, slot arrays, stride arrays, output
  *    scalars) is host memory that is read during the call only.
- *  - The caller owns all device memory (inputs, outputs, workspaces).  The
- *    library allocates no device memory per call.  It keeps host-side caches
- *    (TMA descriptors; redistribute launch plans keyed by the operands'
- *    layouts, slot pointers and strides, so a repeated call skips planning)
- *    and, made once and kept: per device, one auxiliary
- *    stream with two events (a redistribute call with both copies and
- *    Partial reductions runs the reductions there, forked from and joined
- *    back to the caller's stream); per (device, stream), the split-tail
- *    scratch of the tensor-core GEMM (about 39 MB of partial accumulators
- *    and counters, made by the first linear whose last wave is split, with
- *    cudaMalloc outside a stream capture; at most 16 (device, stream) pairs
- *    get one.  Inside a capture, past that count, or when it cannot be
- *    made, every tile runs whole).  dt_clear_cache() drops the
- *    descriptors and frees the scratch.
+ *  - The caller owns all device memory: inputs, outputs and workspaces.  The
+ *    library allocates no device memory, on any call.  A linear's workspace
+ *    (its size from the *_workspace_size query of that call) holds the
+ *    split tail's scratch: where the tensor-core GEMM's last wave would
+ *    leave CTA pairs idle, the remaining tiles' K range is divided over all
+ *    pairs and the pieces' fp32 partials meet in the workspace.  A call given
+ *    no workspace, or one too small, runs every tile whole: same results up
+ *    to fp32 summation order, slower where the split pays.  The workspace's
+ *    contents between calls are the caller's (the library zeroes what it
+ *    needs zeroed on the call's stream); calls whose kernels may overlap on
+ *    the GPU need separate workspaces.
+ *  - The library keeps host-side caches (TMA descriptors; launch plans keyed
+ *    by the operands' layouts, slot pointers, strides, workspace and stream,
+ *    so a repeated call skips planning) and, made once and kept, per device
+ *    one auxiliary stream with two events (a redistribute call with both
+ *    copies and Partial reductions runs the reductions there, forked from
+ *    and joined back to the caller's stream).  dt_clear_cache() drops the
+ *    caches.
  *  - Environment switches, read once per process:
- *      DT_GEMM_PAIR=0   selects the single-CTA GEMM kernel;
- *      DT_GEMM_SPLIT=0  turns the split tail off.
+ *      DT_GEMM_SPLIT=0     turns the split tail off;
+ *      DT_GEMM_BANDS=m,n   fixes the GEMM tile order's band height and block
+ *                          width (in 256 x 256 tiles) instead of the host's
+ *                          choice, to compare orders.
  *    Two test hooks exercise the bounded-wait exit without a fault:
  *      DT_GEMM_WAIT_LIMIT_MS=n  bounds every GEMM barrier wait at n ms
  *                               (1..10000; default 2000);
@@ -217,7 +223,19 @@ DT_API dt_status dt_redistribute_batch(int32_t n, const dt_dtensor* src, const d
 DT_API dt_status dt_tp_embedding(const dt_dtensor* ids, const dt_dtensor* table, const dt_dtensor* out,
                           int32_t tp_mesh_dim, int32_t* d_status, dt_stream_t stream);
 
-/* ---- linears (weights stored [in, out] as in the wineandchord reference) ---- */
+/* ---- linears (weights stored [in, out] as in the wineandchord reference) ----
+ *
+ * Every linear takes `workspace` / `workspace_bytes`: NULL (size ignored) or
+ * caller-owned device memory, 256-byte aligned, of any size.  With at least
+ * the bytes its *_workspace_size query reports, the call splits the tensor-
+ * core GEMM's last wave where that pays (see the ownership convention
+ * above); with less it runs every tile whole.  The queries take the call's
+ * operands (host descriptors only, nothing is read from the device), check
+ * them as the call would, and answer for the CURRENT device, whose number
+ * of co-resident CTA pairs decides the split; without a CUDA device they
+ * return DT_ERR_CUDA.  A call that runs on the CUDA-core kernel (fp32, or
+ * bf16 pitches TMA cannot describe) needs no workspace (0 bytes).
+ */
 
 /*
  * ColumnParallelLinear: Y_i = X W_i (+ b_i) for every tp shard i, all shards
@@ -231,11 +249,11 @@ DT_API dt_status dt_tp_embedding(const dt_dtensor* ids, const dt_dtensor* table,
  * and y are flattened and must be collapsible with unit inner stride.
  * bf16 operands run on the tcgen05 tensor-core GEMM when row pitches are
  * multiples of 16 bytes and bases 16-byte aligned; other shapes and fp32 run
- * on a CUDA-core kernel.
+ * on a CUDA-core kernel (counted by dt_cuda_core_gemm_count()).
  */
 DT_API dt_status dt_column_parallel_linear(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* bias,
-                                    const dt_dtensor* y, int32_t tp_mesh_dim, int32_t* d_status,
-                                    dt_stream_t stream);
+                                    const dt_dtensor* y, int32_t tp_mesh_dim, void* workspace,
+                                    size_t workspace_bytes, int32_t* d_status, dt_stream_t stream);
 
 /*
  * Several column-parallel linears that share one input (e.g. fused q/k/v),
@@ -245,7 +263,14 @@ DT_API dt_status dt_column_parallel_linear(const dt_dtensor* x, const dt_dtensor
  */
 DT_API dt_status dt_column_parallel_linear_multi(const dt_dtensor* x, int32_t n, const dt_dtensor* w,
                                           const dt_dtensor* bias, const dt_dtensor* y,
-                                          int32_t tp_mesh_dim, int32_t* d_status, dt_stream_t stream);
+                                          int32_t tp_mesh_dim, void* workspace, size_t workspace_bytes,
+                                          int32_t* d_status, dt_stream_t stream);
+
+/* Workspace bytes of dt_column_parallel_linear(_multi) on these operands
+ * (n = 1 for the single form; the bias does not change it). */
+DT_API dt_status dt_column_parallel_linear_workspace_size(const dt_dtensor* x, int32_t n, const dt_dtensor* w,
+                                                          const dt_dtensor* y, int32_t tp_mesh_dim,
+                                                          size_t* bytes);
 
 /*
  * RowParallelLinear: Y = sum_i X_i W_i (+ b) (wineandchord "Row parallel";
@@ -261,8 +286,12 @@ DT_API dt_status dt_column_parallel_linear_multi(const dt_dtensor* x, int32_t n,
  * fp32 tensor-core accumulator: no partial product is written to memory.
  */
 DT_API dt_status dt_row_parallel_linear(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* bias,
-                                 const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim,
-                                 int32_t* d_status, dt_stream_t stream);
+                                 const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim, void* workspace,
+                                 size_t workspace_bytes, int32_t* d_status, dt_stream_t stream);
+
+/* Workspace bytes of dt_row_parallel_linear on these operands. */
+DT_API dt_status dt_row_parallel_linear_workspace_size(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* y,
+                                                       int32_t mode, int32_t tp_mesh_dim, size_t* bytes);
 
 /*
  * Llama-style TP MLP (nanotron 5.1: the MLP follows the attention's
@@ -272,12 +301,17 @@ DT_API dt_status dt_row_parallel_linear(const dt_dtensor* x, const dt_dtensor* w
  *   Y   = row_parallel(H, Wd, mode)           down projection
  * x [M, K] Replicate, w_gate/w_up [K, F] Shard(1), w_down [F, N] Shard(0),
  * y per `mode` as in dt_row_parallel_linear.  All bf16 (y bf16 or fp32).
- * workspace: caller-owned device memory of at least
- * dt_tp_mlp_workspace_size() bytes, 256-byte aligned; it receives H as one
- * [M, F] bf16 row-major tensor (shard i = columns of chunk i).
+ * workspace: caller-owned device memory, 256-byte aligned.  It receives H
+ * at its start, as one [M, F] bf16 row-major tensor per distinct x slot
+ * (shard i = the columns of chunk i; blocks 256-byte aligned), which the
+ * call needs (DT_ERR_INVALID_ARG when the workspace is smaller); the bytes
+ * after H are the two GEMMs' split-tail scratch, as for the linears.
+ * dt_tp_mlp_workspace_size reports H plus that scratch for the current
+ * device (DT_ERR_CUDA without one).
  */
-DT_API dt_status dt_tp_mlp_workspace_size(const dt_dtensor* x, const dt_dtensor* w_gate, int32_t tp_mesh_dim,
-                                   size_t* bytes);
+DT_API dt_status dt_tp_mlp_workspace_size(const dt_dtensor* x, const dt_dtensor* w_gate, const dt_dtensor* w_up,
+                                          const dt_dtensor* w_down, const dt_dtensor* y, int32_t mode,
+                                          int32_t tp_mesh_dim, size_t* bytes);
 DT_API dt_status dt_tp_mlp(const dt_dtensor* x, const dt_dtensor* w_gate, const dt_dtensor* w_up,
                     const dt_dtensor* w_down, const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim,
                     void* workspace, size_t workspace_bytes, int32_t* d_status, dt_stream_t stream);
@@ -290,12 +324,16 @@ DT_API dt_status dt_tp_mlp(const dt_dtensor* x, const dt_dtensor* w_gate, const 
  * device array of DT_TP_MLP_STATIC_WORKSPACE_BYTES that every GPU which
  * loads the library holds until the process exits.  This entry point has no
  * counterpart in the pages; it exists for such callers only.
- *  - It allocates nothing (no cudaMalloc, no allocator of any library).
- *  - Problems whose H (dt_tp_mlp_workspace_size) exceeds the array are
- *    rejected with DT_ERR_CAPACITY.
+ *  - It allocates nothing (no cudaMalloc, no allocator of any library), and
+ *    it runs every GEMM tile whole (it has no split-tail scratch).
+ *  - Problems whose H (the [M, F] bf16 blocks described for dt_tp_mlp)
+ *    exceeds the array are rejected with DT_ERR_CAPACITY.
  *  - The first call on a device looks up the array's device address on that
- *    device (cudaGetSymbolAddress); make that first call before any stream
- *    capture.
+ *    device (cudaGetSymbolAddress).  CUDA loads the library's device code
+ *    lazily, so that first call is also when the device reserves the
+ *    array, and it fails with DT_ERR_CUDA if the device has no room left.
+ *    Make the first call on each device at start-up, before memory is
+ *    committed elsewhere and before any stream capture.
  *  - All calls share the one array: calls whose kernels overlap on the GPU
  *    (different streams, or different host threads) race on H.  H is fully
  *    rewritten by every call, so nothing needs clearing in between.
@@ -314,21 +352,22 @@ DT_API const char* dt_status_string(dt_status status);
 DT_API const char* dt_last_error(void);
 
 /* Copy the library's own device status word (used when d_status == NULL)
- * to *bits and, if clear != 0, reset it.  Synchronous on the current device.
- * When the word holds DT_DEV_ERR_TIMEOUT it also zeroes the split-tail
- * counters (a GEMM that gave up may have left them part-counted); that
- * waits for the devices to go idle. */
+ * to *bits and, if clear != 0, reset it.  Synchronous on the current device. */
 DT_API dt_status dt_read_device_status(int32_t* bits, int32_t clear);
 
-/* Drop host-side caches (TMA descriptors, redistribute plans) and free the GEMM split-tail
- * scratch (which waits for each device's work to finish).  Not to be called
- * while another thread launches, or while a captured graph that uses the
- * scratch may still run. */
+/* Drop the host-side caches (TMA descriptors, launch plans).  Not to be
+ * called while another thread launches. */
 DT_API dt_status dt_clear_cache(void);
 
 /* Number of kernels this library has launched in this process so far
  * (every successful launch on any stream counts once). */
 DT_API uint64_t dt_launch_count(void);
+
+/* Of those, the launches of the CUDA-core GEMM: linears whose operands are
+ * fp32 or whose bf16 pitches or bases TMA cannot describe (row pitch not a
+ * multiple of 16 bytes, base not 16-byte aligned) run there, an order of
+ * magnitude slower than the tensor cores. */
+DT_API uint64_t dt_cuda_core_gemm_count(void);
 
 /* Library version, as major * 10000 + minor * 100 + patch. */
 DT_API int32_t dt_version(void);

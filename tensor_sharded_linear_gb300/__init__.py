@@ -9,7 +9,8 @@ from .api import (  # noqa: F401
     ALL_REDUCE, PARTIAL, REDUCE_SCATTER, ColumnParallelLinear, ColumnParallelLinearWithReplicateInputOutput,
     ColumnParallelLinearWithReplicateOutput, DeviceMesh, DTensor, EmbeddingWithReplicateOutput, Linear, Partial,
     Replicate, ReplicateParallelLinear, RowParallelLinear, RowParallelLinearWithReplicateOutput, Shard,
-    column_parallel_linear, column_parallel_linear_multi, init_device_mesh, read_device_status, redistribute,
-    redistribute_batch,
-    row_parallel_linear, tp_attention_projections, tp_embedding, tp_mlp, tp_mlp_workspace_bytes)
+    column_parallel_linear, column_parallel_linear_multi, column_parallel_linear_workspace_bytes,
+    cuda_core_gemm_count, init_device_mesh, read_device_status, redistribute, redistribute_batch,
+    row_parallel_linear, row_parallel_linear_workspace_bytes, tp_attention_projections, tp_embedding, tp_mlp,
+    tp_mlp_output, tp_mlp_workspace_bytes)
 from ._lib import DtError  # noqa: F401

@@ -55,9 +55,10 @@ EXPORTS = [
     "dt_layout_nslots", "dt_layout_slot_of_rank", "dt_layout_slot_box", "dt_redistribute",
     "dt_redistribute_batch",
     "dt_tp_embedding", "dt_column_parallel_linear", "dt_column_parallel_linear_multi",
-    "dt_row_parallel_linear", "dt_tp_mlp_workspace_size", "dt_tp_mlp", "dt_status_string",
+    "dt_row_parallel_linear", "dt_column_parallel_linear_workspace_size", "dt_row_parallel_linear_workspace_size",
+    "dt_tp_mlp_workspace_size", "dt_tp_mlp", "dt_status_string",
     "dt_last_error", "dt_read_device_status", "dt_clear_cache", "dt_version", "dt_launch_count",
-    "dt_tp_mlp_static_workspace",
+    "dt_cuda_core_gemm_count", "dt_tp_mlp_static_workspace",
 ]
 
 _lib = None
@@ -91,10 +92,15 @@ def load(path: str = LIB_PATH) -> C.CDLL:
             "dt_redistribute": (st, [D, D, C.c_void_p, C.c_void_p]),
             "dt_redistribute_batch": (st, [C.c_int32, D, D, C.c_void_p, C.c_void_p]),
             "dt_tp_embedding": (st, [D, D, D, C.c_int32, C.c_void_p, C.c_void_p]),
-            "dt_column_parallel_linear": (st, [D, D, D, D, C.c_int32, C.c_void_p, C.c_void_p]),
-            "dt_column_parallel_linear_multi": (st, [D, C.c_int32, D, D, D, C.c_int32, C.c_void_p, C.c_void_p]),
-            "dt_row_parallel_linear": (st, [D, D, D, D, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]),
-            "dt_tp_mlp_workspace_size": (st, [D, D, C.c_int32, P(C.c_size_t)]),
+            "dt_column_parallel_linear": (st, [D, D, D, D, C.c_int32, C.c_void_p, C.c_size_t, C.c_void_p,
+                                               C.c_void_p]),
+            "dt_column_parallel_linear_multi": (st, [D, C.c_int32, D, D, D, C.c_int32, C.c_void_p, C.c_size_t,
+                                                     C.c_void_p, C.c_void_p]),
+            "dt_row_parallel_linear": (st, [D, D, D, D, C.c_int32, C.c_int32, C.c_void_p, C.c_size_t, C.c_void_p,
+                                            C.c_void_p]),
+            "dt_column_parallel_linear_workspace_size": (st, [D, C.c_int32, D, D, C.c_int32, P(C.c_size_t)]),
+            "dt_row_parallel_linear_workspace_size": (st, [D, D, D, C.c_int32, C.c_int32, P(C.c_size_t)]),
+            "dt_tp_mlp_workspace_size": (st, [D, D, D, D, D, C.c_int32, C.c_int32, P(C.c_size_t)]),
             "dt_tp_mlp": (st, [D, D, D, D, D, C.c_int32, C.c_int32, C.c_void_p, C.c_size_t, C.c_void_p, C.c_void_p]),
             "dt_status_string": (C.c_char_p, [C.c_int]),
             "dt_last_error": (C.c_char_p, []),
@@ -102,6 +108,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
             "dt_clear_cache": (st, []),
             "dt_version": (C.c_int32, []),
             "dt_launch_count": (C.c_uint64, []),
+            "dt_cuda_core_gemm_count": (C.c_uint64, []),
             "dt_tp_mlp_static_workspace": (st, [D, D, D, D, D, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]),
         }
         for name, (res, args) in sig.items():

@@ -326,29 +326,57 @@ def _col_out(x: DTensor, w: DTensor, tp: int, out_dtype, output: str = "shard") 
                          device=x.slots[0].device)
 
 
+def _ws_args(workspace: Optional[torch.Tensor]):
+    """(pointer, bytes) of a workspace tensor, or (None, 0)."""
+    if workspace is None:
+        return None, 0
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def _workspace(nbytes: int, device) -> Optional[torch.Tensor]:
+    """Device memory for a call's workspace (None when it needs none).  Torch
+    allocates it: the library itself allocates nothing."""
+    return torch.empty(nbytes, dtype=torch.uint8, device=device) if nbytes > 0 else None
+
+
+def column_parallel_linear_workspace_bytes(x: DTensor, ws: Sequence[DTensor], ys: Sequence[DTensor],
+                                           tp_dim="tp") -> int:
+    """dt_column_parallel_linear_workspace_size for the weights ``ws`` and outputs ``ys``."""
+    n = len(ws)
+    wdescs, ydescs = [w._desc() for w in ws], [y._desc() for y in ys]
+    wd, yd = (L.DTensorDesc * n)(*wdescs), (L.DTensorDesc * n)(*ydescs)
+    out = C.c_size_t()
+    L.check(L.load().dt_column_parallel_linear_workspace_size(C.byref(x._desc()), n, wd, yd,
+                                                              _tp_index(x.mesh, tp_dim), C.byref(out)),
+            "column_parallel_linear_workspace_size")
+    del wdescs, ydescs
+    return out.value
+
+
 def column_parallel_linear(x: DTensor, w: DTensor, bias: Optional[DTensor] = None, tp_dim="tp",
-                           out_dtype=None, out: Optional[DTensor] = None, output: str = "shard") -> DTensor:
+                           out_dtype=None, out: Optional[DTensor] = None, output: str = "shard",
+                           workspace: Optional[torch.Tensor] = None) -> DTensor:
     """Y_i = X W_i (+ b_i).
 
     x Replicate on tp, or Shard(0) on tp (sequence-parallel entry: the token
     shards are read in place, no gathered copy is made).  The output is
     Shard(-1) on tp, or Replicate with output="replicate" (each shard writes
-    its column block of the one Replicate tensor)."""
-    tp = _tp_index(x.mesh, tp_dim)
-    y = out if out is not None else _col_out(x, w, tp, out_dtype, output)
-    b = bias._desc() if bias is not None else None
-    L.check(L.load().dt_column_parallel_linear(C.byref(x._desc()), C.byref(w._desc()),
-                                               C.byref(b) if b is not None else None, C.byref(y._desc()), tp,
-                                               None, _stream_handle()), "column_parallel_linear")
-    return y
+    its column block of the one Replicate tensor).  ``workspace`` (a device
+    tensor of at least ``column_parallel_linear_workspace_bytes``) lets the
+    GEMM split its last wave; without one a workspace of that size is taken
+    from torch's allocator."""
+    return column_parallel_linear_multi(x, [w], [bias] if bias is not None else None, tp_dim, out_dtype,
+                                        [out] if out is not None else None, output, workspace)[0]
 
 
 def column_parallel_linear_multi(x: DTensor, ws: Sequence[DTensor], biases=None, tp_dim="tp", out_dtype=None,
-                                 outs=None, output: str = "shard"):
+                                 outs=None, output: str = "shard", workspace: Optional[torch.Tensor] = None):
     """Several column-parallel linears sharing x, in one launch (fused q/k/v)."""
     tp = _tp_index(x.mesh, tp_dim)
     ys = list(outs) if outs is not None else [_col_out(x, w, tp, out_dtype, output) for w in ws]
     n = len(ws)
+    if workspace is None:
+        workspace = _workspace(column_parallel_linear_workspace_bytes(x, ws, ys, tp_dim), x.slots[0].device)
     # the descriptors own the slot/stride arrays the copies below point at
     wdescs = [w._desc() for w in ws]
     ydescs = [y._desc() for y in ys]
@@ -356,8 +384,8 @@ def column_parallel_linear_multi(x: DTensor, ws: Sequence[DTensor], biases=None,
     wd = (L.DTensorDesc * n)(*wdescs)
     yd = (L.DTensorDesc * n)(*ydescs)
     bd = (L.DTensorDesc * n)(*bdescs) if bdescs is not None else None
-    L.check(L.load().dt_column_parallel_linear_multi(C.byref(x._desc()), n, wd, bd, yd, tp, None,
-                                                     _stream_handle()), "column_parallel_linear_multi")
+    L.check(L.load().dt_column_parallel_linear_multi(C.byref(x._desc()), n, wd, bd, yd, tp, *_ws_args(workspace),
+                                                     None, _stream_handle()), "column_parallel_linear_multi")
     del wdescs, ydescs, bdescs
     return ys
 
@@ -370,23 +398,46 @@ def _row_out(x: DTensor, w: DTensor, tp: int, mode: str, out_dtype) -> DTensor:
                          device=x.slots[0].device)
 
 
+def row_parallel_linear_workspace_bytes(x: DTensor, w: DTensor, y: DTensor, mode: str = ALL_REDUCE,
+                                        tp_dim="tp") -> int:
+    """dt_row_parallel_linear_workspace_size."""
+    out = C.c_size_t()
+    L.check(L.load().dt_row_parallel_linear_workspace_size(C.byref(x._desc()), C.byref(w._desc()),
+                                                           C.byref(y._desc()), _MODES[mode],
+                                                           _tp_index(x.mesh, tp_dim), C.byref(out)),
+            "row_parallel_linear_workspace_size")
+    return out.value
+
+
 def row_parallel_linear(x: DTensor, w: DTensor, bias: Optional[DTensor] = None, mode: str = ALL_REDUCE,
-                        tp_dim="tp", out_dtype=None, out: Optional[DTensor] = None) -> DTensor:
+                        tp_dim="tp", out_dtype=None, out: Optional[DTensor] = None,
+                        workspace: Optional[torch.Tensor] = None) -> DTensor:
     """Y = sum_i X_i W_i (+ b once): Replicate / Shard(0) / Partial on tp per ``mode``."""
     tp = _tp_index(x.mesh, tp_dim)
     y = out if out is not None else _row_out(x, w, tp, mode, out_dtype)
+    if workspace is None:
+        workspace = _workspace(row_parallel_linear_workspace_bytes(x, w, y, mode, tp_dim), x.slots[0].device)
     b = bias._desc() if bias is not None else None
     L.check(L.load().dt_row_parallel_linear(C.byref(x._desc()), C.byref(w._desc()),
                                             C.byref(b) if b is not None else None, C.byref(y._desc()),
-                                            _MODES[mode], tp, None, _stream_handle()), "row_parallel_linear")
+                                            _MODES[mode], tp, *_ws_args(workspace), None, _stream_handle()),
+            "row_parallel_linear")
     return y
 
 
-def tp_mlp_workspace_bytes(x: DTensor, w_gate: DTensor, tp_dim="tp") -> int:
+def tp_mlp_workspace_bytes(x: DTensor, w_gate: DTensor, w_up: DTensor, w_down: DTensor, y: DTensor,
+                           mode: str = ALL_REDUCE, tp_dim="tp") -> int:
+    """dt_tp_mlp_workspace_size: H plus the split tail's scratch."""
     n = C.c_size_t()
-    L.check(L.load().dt_tp_mlp_workspace_size(C.byref(x._desc()), C.byref(w_gate._desc()),
+    L.check(L.load().dt_tp_mlp_workspace_size(C.byref(x._desc()), C.byref(w_gate._desc()), C.byref(w_up._desc()),
+                                              C.byref(w_down._desc()), C.byref(y._desc()), _MODES[mode],
                                               _tp_index(x.mesh, tp_dim), C.byref(n)), "tp_mlp_workspace_size")
     return n.value
+
+
+def tp_mlp_output(x: DTensor, w_down: DTensor, mode: str = ALL_REDUCE, tp_dim="tp", out_dtype=None) -> DTensor:
+    """An empty output of ``tp_mlp`` for ``mode``."""
+    return _row_out(x, w_down, _tp_index(x.mesh, tp_dim), mode, out_dtype)
 
 
 def tp_mlp(x: DTensor, w_gate: DTensor, w_up: DTensor, w_down: DTensor, mode: str = ALL_REDUCE, tp_dim="tp",
@@ -394,14 +445,17 @@ def tp_mlp(x: DTensor, w_gate: DTensor, w_up: DTensor, w_down: DTensor, mode: st
     """H = bf16(SiLU(X Wg_i) * (X Wu_i)), then the row-parallel down projection."""
     tp = _tp_index(x.mesh, tp_dim)
     y = out if out is not None else _row_out(x, w_down, tp, mode, out_dtype)
-    need = tp_mlp_workspace_bytes(x, w_gate, tp_dim)
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=x.slots[0].device)
+        workspace = _workspace(tp_mlp_workspace_bytes(x, w_gate, w_up, w_down, y, mode, tp_dim), x.slots[0].device)
     L.check(L.load().dt_tp_mlp(C.byref(x._desc()), C.byref(w_gate._desc()), C.byref(w_up._desc()),
-                               C.byref(w_down._desc()), C.byref(y._desc()), _MODES[mode], tp,
-                               workspace.data_ptr(), workspace.numel() * workspace.element_size(), None,
-                               _stream_handle()), "tp_mlp")
+                               C.byref(w_down._desc()), C.byref(y._desc()), _MODES[mode], tp, *_ws_args(workspace),
+                               None, _stream_handle()), "tp_mlp")
     return y
+
+
+def cuda_core_gemm_count() -> int:
+    """dt_cuda_core_gemm_count: CUDA-core GEMM launches so far in this process."""
+    return int(L.load().dt_cuda_core_gemm_count())
 
 
 def mlp_hidden_view(x: DTensor, w_gate: DTensor, workspace: torch.Tensor, tp_dim="tp") -> torch.Tensor:

@@ -87,8 +87,6 @@ extern "C" dt_status dt_read_device_status(int32_t* bits, int32_t clear) {
   if (!bits) return fail(DT_ERR_INVALID_ARG, "bits is NULL");
   cudaError_t e = cudaMemcpyFromSymbol(bits, g_dt_status_word, sizeof(int32_t));
   if (e != cudaSuccess) return fail(DT_ERR_CUDA, "reading the status word: %s", cudaGetErrorString(e));
-  // a GEMM that gave up may have left split-tail tiles part-counted
-  if (*bits & DT_DEV_ERR_TIMEOUT) gemm::reset_split_counters();
   if (clear) {
     int32_t zero = 0;
     e = cudaMemcpyToSymbol(g_dt_status_word, &zero, sizeof(int32_t));

@@ -110,6 +110,10 @@ void count_launch();
 void clear_redistribute_plans();  // drop the redistribute plan cache (dt_clear_cache)
 void clear_gemm_plans();          // drop the linears' plan cache (dt_clear_cache)
 
+// Bytes of the TP MLP's H blocks for these operands (the least workspace
+// dt_tp_mlp accepts; its split tail's scratch would come on top).
+dt_status mlp_hidden_bytes(const dt_dtensor* x, const dt_dtensor* w_gate, size_t* bytes);
+
 // Append the bytes that decide a launch plan for descriptor d (its layout,
 // slot pointers and strides; a marker for NULL) to a cache key.  false: a
 // malformed descriptor, left to the planning path's checks.

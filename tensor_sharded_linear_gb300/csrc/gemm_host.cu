@@ -1,14 +1,16 @@
-// Lowering of batched GEMM groups to a launch: TMA descriptors (cached on
-// the host), tile counts, and the choice between the tcgen05 kernel and the
-// CUDA-core kernel (fp32 operands, or bf16 operands whose pitches TMA
-// cannot describe).
+// Lowering of batched GEMM groups to launches: TMA descriptors (cached on
+// the host), the packing of groups into launches, the tile order, the split
+// tail (its scratch in the caller's workspace), and the choice between the
+// tcgen05 kernel and the CUDA-core kernel (fp32 operands, or bf16 operands
+// whose pitches TMA cannot describe).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
-#include <map>
 #include <mutex>
 #include <unordered_map>
 
@@ -18,28 +20,21 @@
 namespace dt {
 namespace gemm {
 
+// One recorded step of a call: a GEMM launch (kind 0: tcgen05 pair kernel,
+// 2: CUDA-core kernel) with its exact parameter block, or (kind 3) the
+// zeroing of split-tail counters that precedes a split launch.
 struct GemmLaunch {
-  int kind = 0;  // 0 pair kernel, 1 single-CTA kernel, 2 CUDA-core kernel
+  int kind = 0;
   int grid = 0;
-  std::shared_ptr<void> params;  // a heap Params (kinds 0, 1; keeps its 128-byte alignment) or SParams
+  std::shared_ptr<void> params;  // a heap Params (keeps its 128-byte alignment) or SParams
+  void* zero_ptr = nullptr;
+  size_t zero_bytes = 0;
 };
 struct GemmRecord {
   std::vector<GemmLaunch> launches;
 };
 
 namespace {
-
-#ifdef DT_GEMM_TRACE
-__device__ unsigned long long g_trace[1024 * TRACE_SLOTS];
-unsigned long long* trace_ptr() {
-  void* ptr = nullptr;
-  if (cudaGetSymbolAddress(&ptr, g_trace) != cudaSuccess) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  return static_cast<unsigned long long*>(ptr);
-}
-#endif
 
 // ------------------------------------------------------------ TMA descriptors
 
@@ -79,21 +74,8 @@ struct MapKeyHash {
 
 std::mutex g_map_mu;
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
-
-// Split-tail scratch, one per (device, stream): the pieces' fp32 partial
-// accumulators and the tiles' arrival counters.  Made on the first split
-// launch on that stream outside a stream capture (cudaMalloc, then the
-// counters zeroed on that stream) and kept until dt_clear_cache.  Every
-// launch that completes leaves the counters at zero again.
-struct SplitScratch {
-  float* part = nullptr;
-  int32_t* count = nullptr;
-  int pieces = 0, counters = 0;
-};
-std::mutex g_split_mu;
-std::map<std::pair<int, uintptr_t>, SplitScratch> g_split;
-thread_local int g_no_alloc = 0;
 thread_local GemmRecord* g_grec = nullptr;
+std::atomic<uint64_t> g_simt_launches{0};
 
 // 2-D bf16 map over a row-major [rows, cols] matrix with pitch ld elements:
 // box of 64 columns (128 bytes, the swizzle width) by box_rows rows, 128-byte
@@ -252,12 +234,9 @@ bool out_vec_ok(const HostGroup& g) {
   return true;
 }
 
-// The CTA-pair kernel (256 x 256 tiles on tcgen05 .cta_group::2) is the
-// default; DT_GEMM_PAIR=0 in the environment selects the single-CTA kernel
-// (128 x 256 tiles), e.g. to compare the two.
 // Test hooks, read once from the environment: DT_GEMM_WAIT_LIMIT_MS bounds
 // every mbarrier wait (default 2000 ms); DT_GEMM_STARVE=1 makes the TMA
-// producers issue no loads, so the MMA waits run out and the kernels report
+// producers issue no loads, so the MMA waits run out and the kernel reports
 // DT_DEV_ERR_TIMEOUT -- it exercises the bounded-wait exit without a fault.
 unsigned long long gemm_wait_limit_ns() {
   static unsigned long long v = 0;
@@ -279,11 +258,11 @@ int gemm_starve() {
 }
 
 // What a split tail costs beyond its share of the MMAs, in 64-deep K
-// iterations of one 256 x 256 pair tile (~0.3 us each): writing the pieces'
-// partials, finishing the tiles, and the tail's operand traffic squeezed
-// into a fraction of a tile's time.  Measured on GB300 at about 20-25 us
-// per launch (the TP MLP down projection gains 15 us; 64-iteration tiles
-// lose 7-20 us).
+// iterations of one 256 x 256 pair tile (~0.3 us each): zeroing the
+// counters, writing the pieces' partials, finishing the tiles, and the
+// tail's operand traffic squeezed into a fraction of a tile's time.
+// Measured on GB300 at about 20-25 us per launch (the TP MLP down
+// projection gains 15 us; 64-iteration tiles lose 7-20 us).
 constexpr double SPLIT_OVERHEAD_ITERS = 72.0;
 
 // DT_GEMM_SPLIT=0 in the environment turns the split tail off (every tile
@@ -297,138 +276,317 @@ bool use_split_tail() {
   return v == 1;
 }
 
-// Scratch for `pieces` partial tiles and `counters` counters on this
-// device and stream; nullptr inside a NoAllocScope, inside a stream
-// capture, once MAX_SPLIT_STREAMS (device, stream) pairs hold one, or when
-// the allocation fails (the launch then runs every tile whole).
-constexpr size_t MAX_SPLIT_STREAMS = 16;  // ~39 MB each
-const SplitScratch* split_scratch(cudaStream_t stream, int pieces, int counters) {
-  if (g_no_alloc) return nullptr;
+// DT_GEMM_BANDS=m,n fixes the tile order's band height and block width (in
+// tiles) of every launch with common M tiles, e.g. to compare orders; unset,
+// the host chooses them (choose_bands).
+bool bands_override(int* m, int* n) {
+  static int vm = -1, vn = -1;
+  if (vm < 0) {
+    vm = vn = 0;
+    const char* e = getenv("DT_GEMM_BANDS");
+    int a = 0, b = 0;
+    if (e && sscanf(e, "%d,%d", &a, &b) == 2 && a > 0 && b > 0) {
+      vm = a;
+      vn = b;
+    }
+  }
+  *m = vm;
+  *n = vn;
+  return vm > 0;
+}
+
+int l2_bytes() {
+  static int cached[64] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-  std::lock_guard<std::mutex> lk(g_split_mu);
-  auto key = std::make_pair(dev, reinterpret_cast<uintptr_t>(stream));
-  auto it = g_split.find(key);
-  if (it != g_split.end() && it->second.pieces >= pieces && it->second.counters >= counters) return &it->second;
-  if (it != g_split.end()) return nullptr;  // sized once, for the largest split a launch can make
-  if (g_split.size() >= MAX_SPLIT_STREAMS) return nullptr;
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
-    cudaGetLastError();
-    return nullptr;  // no allocation inside a capture; a later uncaptured launch makes the scratch
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cached[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess || v <= 0) {
+      cudaGetLastError();
+      v = 96 << 20;
+    }
+    cached[dev] = v;
   }
-  // the largest split: fewer tail tiles than clusters, so fewer than twice
-  // the clusters pieces and eight counters per tail tile
-  const int cl = std::max(pair_max_clusters(), 1);
-  SplitScratch sc;
-  sc.pieces = std::max(pieces, 2 * cl);
-  sc.counters = std::max(counters, 8 * cl);
-  if (cudaMalloc(&sc.part, (size_t)sc.pieces * 2 * BM * BN_MAX * sizeof(float)) != cudaSuccess) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  // zeroed on the launch's own stream, so it precedes every launch that uses it
-  if (cudaMalloc(&sc.count, (size_t)sc.counters * sizeof(int32_t)) != cudaSuccess ||
-      cudaMemsetAsync(sc.count, 0, (size_t)sc.counters * sizeof(int32_t), stream) != cudaSuccess) {
-    cudaGetLastError();
-    cudaFree(sc.part);
-    if (sc.count) cudaFree(sc.count);
-    return nullptr;
-  }
-  return &(g_split[key] = sc);
+  return cached[dev];
 }
 
-bool use_pair_kernel() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("DT_GEMM_PAIR");
-    v = (e && e[0] == '0') ? 0 : 1;
-  }
-  return v == 1;
-}
+// ---- launch packing
 
-dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStream_t stream) {
-  static thread_local Params p;
-  const int sms = device_sm_count();
-  const int max_clusters = use_pair_kernel() ? pair_max_clusters() : 0;
-  const bool pair = max_clusters > 0;
-  const int tile_m = pair ? PAIR_TILE_M : BM;
-  const int ctas = pair ? max_clusters : sms;  // CTAs (single) or clusters (pair) in one wave
+MapKey key_of(const Mat& m, int box) { return MapKey{reinterpret_cast<uintptr_t>(m.ptr), m.rows, m.cols, m.ld, box}; }
+
+// Rows of a B descriptor's box: 64 K rows (MN-major B); 128 N rows per CTA
+// of a pair (K-major B).
+int b_box_rows(const HostGroup& G) { return G.segs.empty() || !G.segs[0].b.kmajor ? BK : 128; }
+
+// Split `groups` into launches: consecutive runs whose groups, K segments
+// and distinct TMA descriptors fit one parameter block.
+dt_status pack_launches(const std::vector<HostGroup>& groups, std::vector<std::pair<size_t, size_t>>* out) {
   size_t gi = 0;
   while (gi < groups.size()) {
-    // pack as many groups as fit one parameter block; descriptors of the
-    // same matrix and box (e.g. x shared by every column shard) are shared
-    auto b_rows = [&](const HostGroup& G) { return G.segs.empty() || !G.segs[0].b.kmajor ? BK : ((pair || G.dual) ? 128 : 256); };
     std::vector<MapKey> keys;
-    auto key_of = [](const Mat& m, int box) {
-      return MapKey{reinterpret_cast<uintptr_t>(m.ptr), m.rows, m.cols, m.ld, box};
-    };
-    auto count_new = [&](const HostGroup& G, std::vector<MapKey>* ks) {
-      int added = 0;
-      auto add = [&](const MapKey& k) {
-        for (const auto& e : *ks)
-          if (e == k) return;
-        ks->push_back(k);
-        ++added;
-      };
-      for (const HostSeg& s : G.segs) {
-        add(key_of(s.a, BM));
-        add(key_of(stored(s.b), b_rows(G)));
-        if (G.dual) add(key_of(stored(s.b2), b_rows(G)));
-      }
-      return added;
-    };
     size_t g_end = gi;
     int nsegs = 0;
     while (g_end < groups.size()) {
       const HostGroup& G = groups[g_end];
-      const int need_segs = (int)G.segs.size();
       std::vector<MapKey> trial = keys;
-      count_new(G, &trial);
-      if ((int)(g_end - gi) + 1 > MAX_GROUPS || nsegs + need_segs > MAX_SEGS || (int)trial.size() > MAX_MAPS) break;
+      auto add = [&](const MapKey& k) {
+        for (const auto& e : trial)
+          if (e == k) return;
+        trial.push_back(k);
+      };
+      for (const HostSeg& sg : G.segs) {
+        add(key_of(sg.a, BM));
+        add(key_of(stored(sg.b), b_box_rows(G)));
+        if (G.dual) add(key_of(stored(sg.b2), b_box_rows(G)));
+      }
+      if ((int)(g_end - gi) + 1 > MAX_GROUPS || nsegs + (int)G.segs.size() > MAX_SEGS || (int)trial.size() > MAX_MAPS)
+        break;
       keys.swap(trial);
-      nsegs += need_segs;
+      nsegs += (int)G.segs.size();
       ++g_end;
     }
     if (g_end == gi) return fail(DT_ERR_CAPACITY, "one GEMM group needs more than %d segments", MAX_SEGS);
-    // 256-column tiles: one N=256 MMA per 16-deep K step reads each A row
-    // once for 256 outputs (128-wide tiles re-read A and halve the MMA work
-    // per pipeline stage)
-    const int bn = BN_MAX;
+    out->push_back({gi, g_end});
+    gi = g_end;
+  }
+  return DT_OK;
+}
+
+// ---- the shape of one launch
+
+int group_bn(const HostGroup& G) { return G.dual ? 128 : BN_MAX; }
+int group_kiters(const HostGroup& G) {
+  int k = 0;
+  for (const HostSeg& sg : G.segs) k += (int)((sg.a.cols + BK - 1) / BK);
+  return k;
+}
+
+struct LaunchShape {
+  int tiles = 0;
+  int m_tiles = 0;   // > 0: every group has this many M tiles
+  int total_n = 0;   // N tiles over all groups
+  int kiters = 0;    // K iterations of every tile when uniform
+  bool uniform = true;
+  bool dual = false;
+};
+
+LaunchShape launch_shape(const std::vector<HostGroup>& groups, size_t b, size_t e) {
+  LaunchShape s;
+  int common_m = -1;
+  for (size_t g = b; g < e; ++g) {
+    const HostGroup& G = groups[g];
+    const int mt = (int)((G.m + PAIR_TILE_M - 1) / PAIR_TILE_M);
+    const int nt = (int)((G.n + group_bn(G) - 1) / group_bn(G));
+    s.tiles += mt * nt;
+    s.total_n += nt;
+    common_m = (common_m == -1 || common_m == mt) ? mt : -2;
+    const int k = group_kiters(G);
+    if (g == b) s.kiters = k;
+    s.uniform = s.uniform && k == s.kiters;
+    s.dual = s.dual || G.dual;
+  }
+  s.m_tiles = common_m > 0 ? common_m : 0;
+  return s;
+}
+
+// ---- split tail
+
+// When the last wave would leave clusters idle, the remaining tiles' K
+// iterations are divided over every cluster, where every tile has the same
+// K and a cluster's share plus SPLIT_OVERHEAD_ITERS is shorter than a whole
+// tile.  Finishing stages partials in shared memory, which bounds the
+// pieces of one tile.
+struct SplitPlan {
+  int sk_tiles = 0;  // 0: every tile whole
+  int kiters = 0;
+  int pieces = 0;    // partial accumulators written
+  int counters = 0;  // arrival counters (8 per tail tile: 2 CTAs x 4 row quarters)
+};
+
+SplitPlan plan_split(const LaunchShape& s, int ctas) {
+  SplitPlan sp;
+  if (s.tiles <= 0 || ctas <= 0 || !s.uniform || !use_split_tail()) return sp;
+  const int rem = s.tiles % ctas;
+  const int ki = s.kiters;
+  const int64_t share_min = (int64_t)rem * ki / ctas;  // shortest share, in K iterations
+  // most pieces one tile can have: the shares it meets
+  const int np = share_min > 0 ? (int)((ki + share_min - 1) / share_min) + 1 : 0;
+  const double split_cost = (double)rem * ki / ctas + SPLIT_OVERHEAD_ITERS;
+  // a finishing round stages one 32-column chunk of every piece (gate and
+  // up chunks for the gated MLP) in an epilogue warp's half of its quarter
+  const bool fits = np * (s.dual ? 2 : 1) <= FIN_MAX_PIECES;
+  if (rem > 0 && share_min >= 8 && fits && split_cost <= ki) {
+    sp.sk_tiles = rem;
+    sp.kiters = ki;
+    sp.pieces = rem + ctas - 1;  // every cluster boundary inside the tail adds one
+    sp.counters = 8 * rem;
+  }
+  return sp;
+}
+
+size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
+size_t split_part_bytes(const SplitPlan& sp) { return round256((size_t)sp.pieces * 2 * BM * BN_MAX * sizeof(float)); }
+size_t split_bytes(const SplitPlan& sp) {
+  return sp.sk_tiles > 0 ? split_part_bytes(sp) + round256((size_t)sp.counters * sizeof(int32_t)) : 0;
+}
+
+// ---- tile order
+
+// Estimated DRAM bytes of the operand panels of one launch in the order
+// (band_m, band_n).  Model: clusters take tiles round-robin, so tiles
+// [w C, (w + 1) C) run together as wave w and stream their K range in
+// lockstep; a wave reads each distinct A panel (an M tile's rows over all
+// of K) and B panel (an N tile's columns) once.  A panel the previous wave
+// also read is found in L2 at the points of K where the bytes streamed
+// since its last use -- about (1 - f) of the previous wave's panels plus f
+// of this wave's, f the fraction of K done -- stay within the L2.
+double order_traffic(int tiles, int ctas, int m_tiles, int total_n, const std::vector<int>& a_of_n, int n_a,
+                     double a_bytes, double b_bytes, double l2, int band_m, int band_n) {
+  std::vector<int> seen_a((size_t)n_a * m_tiles, -1), seen_b(total_n, -1);
+  std::vector<int> prev_a((size_t)n_a * m_tiles, -1), prev_b(total_n, -1);
+  double total = 0, prev_size = 0;
+  for (int w = 0; w * ctas < tiles; ++w) {
+    const int t0 = w * ctas, t1 = std::min(tiles, t0 + ctas);
+    double size = 0, shared = 0;
+    for (int t = t0; t < t1; ++t) {
+      int mi, jn;
+      band_order(t, m_tiles, total_n, band_m, band_n, &mi, &jn);
+      const size_t ka = (size_t)a_of_n[jn] * m_tiles + mi;
+      if (seen_a[ka] != w) {
+        if (seen_a[ka] == w - 1 && w > 0) shared += a_bytes;
+        prev_a[ka] = seen_a[ka];
+        seen_a[ka] = w;
+        size += a_bytes;
+      }
+      if (seen_b[jn] != w) {
+        if (seen_b[jn] == w - 1 && w > 0) shared += b_bytes;
+        prev_b[jn] = seen_b[jn];
+        seen_b[jn] = w;
+        size += b_bytes;
+      }
+    }
+    double hit = 0;  // fraction of K over which the shared panels are still in L2
+    if (w > 0) {
+      const double a = prev_size, b = size;
+      if (a <= l2 && b <= l2) hit = 1;
+      else if (a > l2 && b > l2) hit = 0;
+      else if (a <= l2) hit = (l2 - a) / (b - a);
+      else hit = (l2 - b) / (a - b);
+    }
+    total += size - shared * hit;
+    prev_size = size;
+  }
+  return total;
+}
+
+// Band height and block width of a launch with common M tiles.  The default
+// bands are a quarter of L2 of A rows, at least one wave high; the modelled
+// traffic of every other (band_m, band_n) is compared with it and a clearly
+// cheaper order (2% or more) wins.
+void choose_bands(const std::vector<HostGroup>& groups, size_t b, size_t e, const LaunchShape& s, int ctas,
+                  int* band_m, int* band_n) {
+  *band_m = 1;
+  *band_n = std::max(1, s.total_n);
+  if (s.m_tiles <= 0) return;
+  int om, on;
+  if (bands_override(&om, &on)) {
+    *band_m = std::min(om, s.m_tiles);
+    *band_n = std::min(on, s.total_n);
+    return;
+  }
+  int64_t max_k = 0;
+  for (size_t g = b; g < e; ++g) max_k = std::max<int64_t>(max_k, (int64_t)group_kiters(groups[g]) * BK);
+  const int64_t a_tile_bytes = (int64_t)PAIR_TILE_M * std::max<int64_t>(max_k, 1) * 2;
+  int band = (int)std::max<int64_t>(1, (32ll << 20) / a_tile_bytes);
+  band = std::max(band, (ctas + s.total_n - 1) / s.total_n);
+  *band_m = std::max(1, std::min(band, s.m_tiles));
+  if (ctas <= 0 || s.tiles <= ctas) return;
+  // A panels: one per distinct A matrix (groups sharing x share them) and M tile
+  std::vector<int> a_of_n;
+  std::vector<uintptr_t> a_ids;
+  for (size_t g = b; g < e; ++g) {
+    const HostGroup& G = groups[g];
+    const uintptr_t id = G.segs.empty() ? 0 : reinterpret_cast<uintptr_t>(G.segs[0].a.ptr);
+    int ai = -1;
+    for (size_t i = 0; i < a_ids.size(); ++i)
+      if (a_ids[i] == id) ai = (int)i;
+    if (ai < 0) {
+      ai = (int)a_ids.size();
+      a_ids.push_back(id);
+    }
+    const int nt = (int)((G.n + group_bn(G) - 1) / group_bn(G));
+    for (int j = 0; j < nt; ++j) a_of_n.push_back(ai);
+  }
+  const double a_bytes = (double)PAIR_TILE_M * max_k * 2, b_bytes = (double)BN_MAX * max_k * 2;
+  const double l2 = 0.8 * l2_bytes();
+  auto cost = [&](int bm, int bn) {
+    return order_traffic(s.tiles, ctas, s.m_tiles, s.total_n, a_of_n, (int)a_ids.size(), a_bytes, b_bytes, l2, bm, bn);
+  };
+  // candidate sizes: every value up to 16, then a coarser ladder
+  auto ladder = [](int n) {
+    std::vector<int> v;
+    for (int i = 1; i <= std::min(n, 16); ++i) v.push_back(i);
+    for (int i : {20, 24, 28, 32, 40, 48, 64, 80, 96, 128, 192, 256})
+      if (i < n) v.push_back(i);
+    if (n > 16) v.push_back(n);
+    return v;
+  };
+  double best = cost(*band_m, *band_n);
+  const double base = best;
+  int bm_best = *band_m, bn_best = *band_n;
+  for (int bm : ladder(s.m_tiles))
+    for (int bn : ladder(s.total_n)) {
+      const double c = cost(bm, bn);
+      if (c < best - 1e-6) {
+        best = c;
+        bm_best = bm;
+        bn_best = bn;
+      }
+    }
+  if (best <= 0.98 * base) {
+    *band_m = bm_best;
+    *band_n = bn_best;
+  }
+}
+
+// ---- launches
+
+dt_status run_tcgen05(const std::vector<HostGroup>& groups, int32_t* status, cudaStream_t stream, Workspace ws) {
+  static thread_local Params p;
+  const int ctas = pair_max_clusters();  // clusters in one wave
+  if (ctas <= 0) return fail(DT_ERR_CUDA, "the tcgen05 GEMM cannot be launched on this device");
+  std::vector<std::pair<size_t, size_t>> launches;
+  dt_status st = pack_launches(groups, &launches);
+  if (st != DT_OK) return st;
+  for (const auto& range : launches) {
+    const size_t gi = range.first, g_end = range.second;
+    const LaunchShape shape = launch_shape(groups, gi, g_end);
     int map_i = 0, seg_i = 0, tiles = 0;
     std::vector<MapKey> encoded;
     // index of the descriptor for (matrix, box rows) in this launch, encoding it once
     auto map_index = [&](const Mat& m, int box, int32_t* idx) -> dt_status {
-      const MapKey k{reinterpret_cast<uintptr_t>(m.ptr), m.rows, m.cols, m.ld, box};
+      const MapKey k = key_of(m, box);
       for (size_t i = 0; i < encoded.size(); ++i)
         if (encoded[i] == k) {
           *idx = (int32_t)i;
           return DT_OK;
         }
       if (map_i >= MAX_MAPS) return fail(DT_ERR_CAPACITY, "more than %d TMA descriptors in one launch", MAX_MAPS);
-      dt_status st = encode_map(m, box, &p.maps[map_i]);
-      if (st != DT_OK) return st;
+      dt_status e = encode_map(m, box, &p.maps[map_i]);
+      if (e != DT_OK) return e;
       encoded.push_back(k);
       *idx = map_i++;
       return DT_OK;
     };
     p.ngroups = 0;
-    int common_m = -1;
-    int64_t max_k = 0;
-    for (size_t g = gi; g < g_end; ++g) {
-      const int mt = (int)((groups[g].m + tile_m - 1) / tile_m);
-      common_m = (common_m == -1 || common_m == mt) ? mt : -2;
-      int64_t k = 0;
-      for (const HostSeg& s : groups[g].segs) k += s.a.cols;
-      max_k = std::max(max_k, k);
-    }
     for (size_t g = gi; g < g_end; ++g) {
       const HostGroup& H = groups[g];
       Group& G = p.groups[p.ngroups++];
       G.m = (int32_t)H.m;
       G.n = (int32_t)H.n;
-      G.bn = H.dual ? 128 : bn;
-      G.m_tiles = (int32_t)((H.m + tile_m - 1) / tile_m);
+      G.bn = group_bn(H);
+      G.m_tiles = (int32_t)((H.m + PAIR_TILE_M - 1) / PAIR_TILE_M);
       G.n_tiles = (int32_t)((H.n + G.bn - 1) / G.bn);
       G.tile_begin = tiles;
       tiles += G.m_tiles * G.n_tiles;
@@ -447,17 +605,13 @@ dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStrea
       G.bias_dtype = H.bias ? H.bias_dtype : -1;
       G.out_vec = out_vec_ok(H) ? 1 : 0;
       G.b_kmajor = H.segs.empty() ? 0 : (H.segs[0].b.kmajor ? 1 : 0);
-      // K-major B boxes: 128 N rows per CTA of a pair or per gated-MLP half,
-      // 256 for a plain single-CTA tile; MN-major B boxes: 64 K rows
-      const int b_box_rows = G.b_kmajor ? ((pair || H.dual) ? 128 : 256) : BK;
-      for (const HostSeg& s : H.segs) {
+      for (const HostSeg& sg : H.segs) {
         Seg& S = p.segs[seg_i++];
-        S.k_tiles = (int32_t)((s.a.cols + BK - 1) / BK);
-        dt_status st;
-        if ((st = map_index(s.a, BM, &S.a_map)) != DT_OK) return st;
-        if ((st = map_index(stored(s.b), b_box_rows, &S.b_map)) != DT_OK) return st;
+        S.k_tiles = (int32_t)((sg.a.cols + BK - 1) / BK);
+        if ((st = map_index(sg.a, BM, &S.a_map)) != DT_OK) return st;
+        if ((st = map_index(stored(sg.b), b_box_rows(H), &S.b_map)) != DT_OK) return st;
         S.b_map2 = S.b_map;
-        if (H.dual && (st = map_index(stored(s.b2), b_box_rows, &S.b_map2)) != DT_OK) return st;
+        if (H.dual && (st = map_index(stored(sg.b2), b_box_rows(H), &S.b_map2)) != DT_OK) return st;
       }
     }
     p.total_tiles = tiles;
@@ -466,77 +620,58 @@ dt_status run_tcgen05(std::vector<HostGroup>& groups, int32_t* status, cudaStrea
     p.status = status;
     p.wait_limit_ns = gemm_wait_limit_ns();
     p.starve = gemm_starve();
-#ifdef DT_GEMM_TRACE
-    p.trace = trace_ptr();
-#else
-    p.trace = nullptr;
-#endif
     p.n_tile_begin[0] = 0;
     for (int g = 0; g < p.ngroups; ++g) p.n_tile_begin[g + 1] = p.n_tile_begin[g] + p.groups[g].n_tiles;
-    p.m_tiles = common_m > 0 ? common_m : 0;
-    // band height: the band's A rows (band_m x 128 x K bf16) take about a
-    // quarter of L2, and a band holds at least one wave of tiles
-    {
-      const int64_t a_tile_bytes = (int64_t)tile_m * std::max<int64_t>(max_k, 1) * 2;
-      int band = (int)std::max<int64_t>(1, (32ll << 20) / a_tile_bytes);
-      const int total_n = std::max(1, p.n_tile_begin[p.ngroups]);
-      band = std::max(band, (ctas + total_n - 1) / total_n);
-      p.band_m = std::max(1, std::min(band, p.m_tiles > 0 ? p.m_tiles : 1));
-    }
-    // Split tail: when the last wave would leave clusters idle, divide the
-    // remaining tiles' K iterations over every cluster, where every tile has
-    // the same K and a cluster's share plus SPLIT_OVERHEAD_ITERS is shorter
-    // than a whole tile.  The finishing stages partials in shared memory,
-    // which bounds the pieces of a tile.
+    p.m_tiles = shape.m_tiles;
+    choose_bands(groups, gi, g_end, shape, ctas, &p.band_m, &p.band_n);
+    // the split tail, where the caller's workspace holds its scratch
     p.sk_tiles = 0;
     p.sk_kiters = 0;
     p.sk_part = nullptr;
     p.sk_count = nullptr;
     int grid = std::min(tiles, ctas);
-    if (pair && tiles > 0 && use_split_tail()) {
-      int ki = -1;
-      bool uniform = true;
-      for (int g = 0; g < p.ngroups; ++g) {
-        int k = 0;
-        for (int si = p.groups[g].seg_begin; si < p.groups[g].seg_begin + p.groups[g].seg_count; ++si)
-          k += p.segs[si].k_tiles;
-        if (ki < 0) ki = k;
-        uniform = uniform && k == ki;
-      }
-      bool dual = false;
-      for (int g = 0; g < p.ngroups; ++g) dual = dual || p.groups[g].dual;
-      const int rem = tiles % ctas;
-      const int64_t share_min = (int64_t)rem * ki / ctas;  // shortest share, in K iterations
-      // most pieces one tile can have: the shares it meets
-      const int np = share_min > 0 ? (int)((ki + share_min - 1) / share_min) + 1 : 0;
-      const double split_cost = (double)rem * ki / ctas + SPLIT_OVERHEAD_ITERS;
-      // a finishing round stages one 32-column chunk of every piece (gate
-      // and up chunks for the gated MLP) in an epilogue warp's half of its
-      // shared-memory quarter
-      const bool fits = np * (dual ? 2 : 1) <= FIN_MAX_PIECES;
-      if (uniform && rem > 0 && share_min >= 8 && fits && split_cost <= ki) {
-        const SplitScratch* sc = split_scratch(stream, rem + ctas - 1, 8 * rem);
-        if (sc) {
-          p.sk_tiles = rem;
-          p.sk_kiters = ki;
-          p.sk_part = sc->part;
-          p.sk_count = sc->count;
-          grid = ctas;
-        }
-      }
+    const SplitPlan sp = plan_split(shape, ctas);
+    const size_t need = split_bytes(sp);
+    int32_t* counters = nullptr;
+    if (sp.sk_tiles > 0 && ws.ptr && ws.bytes >= need) {
+      p.sk_tiles = sp.sk_tiles;
+      p.sk_kiters = sp.kiters;
+      p.sk_part = reinterpret_cast<float*>(ws.ptr);
+      counters = reinterpret_cast<int32_t*>(ws.ptr + split_part_bytes(sp));
+      p.sk_count = counters;
+      grid = ctas;
     }
     if (tiles > 0) {
-      cudaError_t e = pair ? launch_tcgen05_pair(p, grid, stream) : launch_tcgen05(p, grid, stream);
+      if (counters) {
+        // the counters start at zero in every launch: the workspace's
+        // contents are the caller's between calls
+        const size_t cbytes = (size_t)sp.counters * sizeof(int32_t);
+        cudaError_t e = cudaMemsetAsync(counters, 0, cbytes, stream);
+        if (e != cudaSuccess) return fail(DT_ERR_CUDA, "zeroing the split-tail counters: %s", cudaGetErrorString(e));
+        if (g_grec) {
+          GemmLaunch z;
+          z.kind = 3;
+          z.zero_ptr = counters;
+          z.zero_bytes = cbytes;
+          g_grec->launches.push_back(z);
+        }
+      }
+      cudaError_t e = launch_tcgen05_pair(p, grid, stream);
       if (e != cudaSuccess) return fail(DT_ERR_CUDA, "tcgen05 GEMM launch: %s", cudaGetErrorString(e));
       count_launch();
-      if (g_grec) g_grec->launches.push_back({pair ? 0 : 1, grid, std::make_shared<Params>(p)});
+      if (g_grec) {
+        GemmLaunch l;
+        l.kind = 0;
+        l.grid = grid;
+        l.params = std::make_shared<Params>(p);
+        g_grec->launches.push_back(l);
+      }
     }
-    gi = g_end;
   }
   return DT_OK;
 }
 
-dt_status run_simt(std::vector<HostGroup>& groups, cudaStream_t stream) {
+dt_status run_simt(const std::vector<HostGroup>& groups, cudaStream_t stream) {
   static thread_local SParams p;
   const int sms = device_sm_count();
   size_t gi = 0;
@@ -591,17 +726,22 @@ dt_status run_simt(std::vector<HostGroup>& groups, cudaStream_t stream) {
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return fail(DT_ERR_CUDA, "CUDA-core GEMM launch: %s", cudaGetErrorString(e));
       count_launch();
-      if (g_grec) g_grec->launches.push_back({2, grid, std::make_shared<SParams>(p)});
+      g_simt_launches.fetch_add(1, std::memory_order_relaxed);
+      if (g_grec) {
+        GemmLaunch l;
+        l.kind = 2;
+        l.grid = grid;
+        l.params = std::make_shared<SParams>(p);
+        g_grec->launches.push_back(l);
+      }
     }
     gi = g_end;
   }
   return DT_OK;
 }
 
-}  // namespace
-
-dt_status run_groups(std::vector<HostGroup>& groups, int32_t* d_status, cudaStream_t stream) {
-  // drop groups with no output; a group with no K contributes bias (or zeros)
+// Groups with output; a group with no K contributes bias (or zeros).
+std::vector<HostGroup> live_groups(std::vector<HostGroup>& groups) {
   std::vector<HostGroup> live;
   live.reserve(groups.size());
   for (auto& g : groups) {
@@ -612,7 +752,23 @@ dt_status run_groups(std::vector<HostGroup>& groups, int32_t* d_status, cudaStre
     g.segs.swap(segs);
     live.push_back(std::move(g));
   }
-  if (live.empty()) return DT_OK;
+  return live;
+}
+
+// true: the tcgen05 kernel can run every group (bf16 operands TMA can
+// describe, one B major-ness per group)
+bool tensor_core_ok(const std::vector<HostGroup>& live) {
+  for (const auto& g : live) {
+    if (g.segs.empty()) return false;
+    for (const auto& s : g.segs) {
+      if (!tma_ok(s.a) || !tma_ok(s.b) || (g.dual && !tma_ok(s.b2))) return false;
+      if (s.b.kmajor != g.segs[0].b.kmajor || (g.dual && s.b2.kmajor != s.b.kmajor)) return false;
+    }
+  }
+  return true;
+}
+
+dt_status check_limits(const std::vector<HostGroup>& live) {
   for (auto& g : live)
     if (g.out_ptr.size() > (size_t)MAX_OUT) return fail(DT_ERR_CAPACITY, "more than %d output row blocks", MAX_OUT);
   // M, N and the TMA and tile coordinates are 32-bit on the device: refuse a
@@ -628,46 +784,46 @@ dt_status run_groups(std::vector<HostGroup>& groups, int32_t* d_status, cudaStre
         return fail(DT_ERR_CAPACITY, "GEMM operand of %lld x %lld / %lld x %lld: each dimension must be below 2^31 - 512",
                     (long long)sg.a.rows, (long long)sg.a.cols, (long long)sg.b.rows, (long long)sg.b.cols);
   }
-  bool tc = true;
-  for (const auto& g : live) {
-    if (g.segs.empty()) tc = false;
-    for (const auto& s : g.segs) {
-      if (!tma_ok(s.a) || !tma_ok(s.b) || (g.dual && !tma_ok(s.b2))) tc = false;
-      // one B major-ness per group (the kernel decides it per tile)
-      if (s.b.kmajor != g.segs[0].b.kmajor || (g.dual && s.b2.kmajor != s.b.kmajor)) tc = false;
-    }
-  }
-  if (tc) {
+  return DT_OK;
+}
+
+}  // namespace
+
+dt_status run_groups(std::vector<HostGroup>& groups, int32_t* d_status, cudaStream_t stream, Workspace ws) {
+  std::vector<HostGroup> live = live_groups(groups);
+  if (live.empty()) return DT_OK;
+  dt_status st = check_limits(live);
+  if (st != DT_OK) return st;
+  if (tensor_core_ok(live)) {
     int32_t* status = device_status_word(d_status);
     if (!status) return fail(DT_ERR_CUDA, "no device status word");
-    return run_tcgen05(live, status, stream);
+    return run_tcgen05(live, status, stream, ws);
   }
   return run_simt(live, stream);
 }
 
-}  // namespace gemm
-}  // namespace dt
-
-#ifdef DT_GEMM_TRACE
-// Traced builds only: copy (and optionally clear) the per-CTA wait records.
-extern "C" __attribute__((visibility("default"))) int dt_gemm_trace_read(unsigned long long* out, int n, int clear) {
-  using dt::gemm::g_trace;
-  if (n > 1024 * dt::gemm::TRACE_SLOTS) n = 1024 * dt::gemm::TRACE_SLOTS;
-  if (cudaMemcpyFromSymbol(out, g_trace, n * sizeof(unsigned long long)) != cudaSuccess) return -1;
-  if (clear) {
-    static unsigned long long zeros[1024 * dt::gemm::TRACE_SLOTS] = {};
-    if (cudaMemcpyToSymbol(g_trace, zeros, sizeof(zeros)) != cudaSuccess) return -1;
+dt_status workspace_bytes(std::vector<HostGroup>& groups, size_t* bytes) {
+  *bytes = 0;
+  std::vector<HostGroup> live = live_groups(groups);
+  if (live.empty()) return DT_OK;
+  dt_status st = check_limits(live);
+  if (st != DT_OK) return st;
+  if (!tensor_core_ok(live)) return DT_OK;  // the CUDA-core kernel needs no scratch
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return fail(DT_ERR_CUDA, "no CUDA device: the split tail's scratch depends on the device's SM count");
   }
-  return n;
+  const int ctas = pair_max_clusters();
+  if (ctas <= 0) return fail(DT_ERR_CUDA, "the tcgen05 GEMM cannot be launched on device %d", dev);
+  std::vector<std::pair<size_t, size_t>> launches;
+  if ((st = pack_launches(live, &launches)) != DT_OK) return st;
+  for (const auto& r : launches)  // launches run one after the other: one scratch serves all
+    *bytes = std::max(*bytes, split_bytes(plan_split(launch_shape(live, r.first, r.second), ctas)));
+  return DT_OK;
 }
-#endif
 
-namespace dt {
-namespace gemm {
-
-NoAllocScope::NoAllocScope() { ++g_no_alloc; }
-NoAllocScope::~NoAllocScope() { --g_no_alloc; }
-bool gemm_no_alloc() { return g_no_alloc > 0; }
+uint64_t cuda_core_launches() { return g_simt_launches.load(std::memory_order_relaxed); }
 
 GemmRecordScope::GemmRecordScope(GemmRecord* r) { g_grec = r; }
 GemmRecordScope::~GemmRecordScope() { g_grec = nullptr; }
@@ -676,32 +832,22 @@ std::shared_ptr<GemmRecord> new_gemm_record() { return std::make_shared<GemmReco
 dt_status replay_gemm(const GemmRecord& r, cudaStream_t stream) {
   for (const GemmLaunch& l : r.launches) {
     cudaError_t e;
+    if (l.kind == 3) {
+      e = cudaMemsetAsync(l.zero_ptr, 0, l.zero_bytes, stream);
+      if (e != cudaSuccess) return fail(DT_ERR_CUDA, "zeroing the split-tail counters: %s", cudaGetErrorString(e));
+      continue;
+    }
     if (l.kind == 2) {
       simt_gemm_kernel<<<l.grid, S_THREADS, 0, stream>>>(*static_cast<const SParams*>(l.params.get()));
       e = cudaGetLastError();
+      g_simt_launches.fetch_add(1, std::memory_order_relaxed);
     } else {
-      const Params& p = *static_cast<const Params*>(l.params.get());
-      e = l.kind == 0 ? launch_tcgen05_pair(p, l.grid, stream) : launch_tcgen05(p, l.grid, stream);
+      e = launch_tcgen05_pair(*static_cast<const Params*>(l.params.get()), l.grid, stream);
     }
     if (e != cudaSuccess) return fail(DT_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
     count_launch();
   }
   return DT_OK;
-}
-
-// After a launch gave up (DT_DEV_ERR_TIMEOUT) its tiles' arrival counters
-// may be left part-counted; zero every counter so later launches start clean.
-void reset_split_counters() {
-  std::lock_guard<std::mutex> lk(g_split_mu);
-  int cur = 0;
-  cudaGetDevice(&cur);
-  for (auto& kv : g_split) {
-    cudaSetDevice(kv.first.first);
-    cudaDeviceSynchronize();  // no launch may still be counting
-    cudaMemset(kv.second.count, 0, (size_t)kv.second.counters * sizeof(int32_t));
-    cudaDeviceSynchronize();  // zero before any later launch on any stream
-  }
-  cudaSetDevice(cur);
 }
 
 }  // namespace gemm
@@ -713,16 +859,8 @@ extern "C" dt_status dt_clear_cache(void) {
     dt::gemm::g_maps.clear();
   }
   dt::clear_redistribute_plans();
-  dt::clear_gemm_plans();  // their parameters point into the scratch freed below
-  std::lock_guard<std::mutex> lk(dt::gemm::g_split_mu);
-  int cur = 0;
-  cudaGetDevice(&cur);
-  for (auto& kv : dt::gemm::g_split) {
-    cudaSetDevice(kv.first.first);
-    cudaFree(kv.second.part);  // waits for the device's work first
-    cudaFree(kv.second.count);
-  }
-  dt::gemm::g_split.clear();
-  cudaSetDevice(cur);
+  dt::clear_gemm_plans();
   return DT_OK;
 }
+
+extern "C" uint64_t dt_cuda_core_gemm_count(void) { return dt::gemm::cuda_core_launches(); }

@@ -6,21 +6,24 @@
 // B traffic into each SM and leaves room for 6 pipeline stages.
 //
 // Roles per CTA (224 threads): warp 0 TMA producer of A, warp 6 TMA producer
-// of B, warp 1 MMA issuer (rank 0 only; it owns the pair's MMAs), warps 2..5
-// epilogue.  Two producers because one thread issuing every copy capped the
-// copies alone at ~46 B/clk per SM (the issuing thread blocks ~110 cycles
-// per copy); split, the copies alone run 16-20% faster and the GEMMs ~1%.
+// of B, warp 1 MMA issuer (rank 0 only; it owns the pair's MMAs) and TMEM
+// allocator, warps 2..5 epilogue (one accumulator row per thread).  Two
+// producers because one thread issuing every copy capped the copies alone
+// at ~46 B/clk per SM (the issuing thread blocks ~110 cycles per copy);
+// split, the copies alone run 16-20% faster and the GEMMs ~1%.
 // Barriers:
 //   full[s]    in rank 0: 1 arrival (rank 0's A producer, with the byte
-//              count of both CTAs' loads) + the loads' bytes.  Every other
-//              producer only issues its loads: its bytes are its share.  (A cluster-scope release arrive from
-//              rank 1 before each stage would wait for that thread's copies
-//              still in flight and serialise rank 1's pipeline.)
+//              count of both CTAs' loads) + the loads' bytes.  Every
+//              other producer only issues its loads: its bytes are its
+//              share.  (A cluster-scope release arrive from rank 1 before
+//              each stage would wait for that thread's copies still in
+//              flight and serialise rank 1's pipeline.)
 //   empty[s]   in each CTA: 1 arrival, rank 0's MMA commit multicast to both
 //              (both producers of a CTA wait on it);
 //   tfull[b]   in each CTA: 1 arrival, multicast commit after a tile's MMAs;
 //   tempty[b]  in rank 0: 8 arrivals, the 4 epilogue warps of each CTA.
-// Every wait is bounded as in the single-CTA kernel.
+// Every wait is bounded (Params::wait_limit_ns); on expiry the role raises
+// the CTA's abort flag, the launch reports DT_DEV_ERR_TIMEOUT and unwinds.
 #include <algorithm>
 
 #include "gemm_plan.h"
@@ -42,11 +45,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // two per epilogue warp, for finishing split tiles (256 bytes past `full`)
   uint64_t* fin_bar = full + 32;
-#ifdef DT_GEMM_TRACE
-  volatile long long* t_issue = reinterpret_cast<volatile long long*>(drain + 2);   // per stage
-  volatile long long* t_commit = t_issue + PAIR_STAGES;
-  for (int i = threadIdx.x; i < 2 * PAIR_STAGES; i += blockDim.x) t_issue[i] = 0;
-#endif
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -75,9 +73,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
   const uint32_t tmem_base = *tmem_slot;
 
   bool aborted = false;
-#ifdef DT_GEMM_TRACE
-  const long long _trace_start = clock64();
-#endif
 
   if (warp == 0 || warp == PAIR_B_PRODUCER_WARP) {
     // ------------------------------------------------------------ TMA producers (both CTAs)
@@ -108,19 +103,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
           const CUtensorMap* bmap = &p.maps[(G.dual && rank == 1) ? S.b_map2 : S.b_map];
           const int kt_end = min(S.k_tiles, w.k1 - kbase);
           for (int kt = max(0, w.k0 - kbase); kt < kt_end; ++kt) {
-            bool _ok;
-            {
-              DT_TRACE_T0();
-              _ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.wait_limit_ns);
-              DT_TRACE_ADD(TR_PROD_EMPTY);
-#ifdef DT_GEMM_TRACE
-              if (p.trace && t_commit[stage] != 0)
-                atomicAdd(&p.trace[blockIdx.x * TRACE_SLOTS + TR_COMMIT_LAT],
-                          (unsigned long long)(clock64() - t_commit[stage]));
-              t_issue[stage] = clock64();
-#endif
-            }
-            if (!_ok) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.wait_limit_ns)) {
               aborted = true;
               *abort_flag = 1;
               break;
@@ -161,14 +144,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
         const Group& G = p.groups[tc.g];
         const bool bk = G.b_kmajor != 0;
         const uint32_t idesc = instr_desc(PAIR_TILE_M, G.dual ? 2 * pair_dual_half(G, tc.n0) : 256, bk);
-        bool _ok;
-        {
-          DT_TRACE_T0();
-          _ok = mbar_wait(&tempty[buf], tphase ^ 1u, abort_flag, p.wait_limit_ns);
-          DT_TRACE_ADD(TR_MMA_TEMPTY);
-        }
-        DT_TRACE_COUNT(TR_TILES);
-        if (!_ok) {
+        if (!mbar_wait(&tempty[buf], tphase ^ 1u, abort_flag, p.wait_limit_ns)) {
           aborted = true;
           *abort_flag = 1;
           break;
@@ -181,18 +157,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
           const int kts = p.segs[si].k_tiles;
           const int kt_end = min(kts, w.k1 - kbase);
           for (int kt = max(0, w.k0 - kbase); kt < kt_end; ++kt) {
-            bool _okf;
-            {
-              DT_TRACE_T0();
-              _okf = mbar_wait(&full[stage], phase, abort_flag, p.wait_limit_ns);
-              DT_TRACE_ADD(TR_MMA_FULL);
-#ifdef DT_GEMM_TRACE
-              if (p.trace) atomicAdd(&p.trace[blockIdx.x * TRACE_SLOTS + TR_TMA_LAT],
-                                     (unsigned long long)(clock64() - t_issue[stage]));
-#endif
-            }
-            DT_TRACE_COUNT(TR_STAGES);
-            if (!_okf) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_limit_ns)) {
               aborted = true;
               *abort_flag = 1;
               break;
@@ -202,17 +167,15 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
             const uint32_t b_addr = a_addr + PAIR_A_BYTES;
 #pragma unroll
             for (int j = 0; j < BK / 16; ++j) {
-              // same operand layouts as the single-CTA kernel; each CTA's
-              // B half is two 64-column chunks 8 KiB apart
+              // 16-deep K steps: A advances 32 bytes inside its 128-byte
+              // swizzle rows; an MN-major B half is two 64-column chunks
+              // 8 KiB apart, a K-major one advances like A
               const uint64_t adesc = smem_desc(a_addr + j * 32, 16, 1024);
               const uint64_t bdesc =
                   bk ? smem_desc(b_addr + j * 32, 16, 1024) : smem_desc(b_addr + j * 2048, B_CHUNK_BYTES, 1024);
               mma_bf16_pair(d_tmem, adesc, bdesc, idesc, acc);
               acc = 1;
             }
-#ifdef DT_GEMM_TRACE
-            t_commit[stage] = clock64();
-#endif
             mma_commit_pair_mc(&empty[stage], 0x3);
             if (++stage == PAIR_STAGES) {
               stage = 0;
@@ -245,11 +208,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
       const TileCoord tc = decode_tile<PAIR_TILE_M>(p, w.t);
       const Group& G = p.groups[tc.g];
       int ok = 1;
-      if (lane == 0) {
-        DT_TRACE_T0();
-        ok = mbar_wait(&tfull[buf], tphase, abort_flag, p.wait_limit_ns) ? 1 : 0;
-        if (warp == 2) DT_TRACE_ADD(TR_EPI_TFULL);
-      }
+      if (lane == 0) ok = mbar_wait(&tfull[buf], tphase, abort_flag, p.wait_limit_ns) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);  // tcgen05.ld below is warp-collective
       if (!ok) {
         aborted = true;
@@ -323,7 +282,10 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
       }
       if (w.piece >= 0) {
         // the piece whose arrival completes the tile's count finishes the
-        // tile once this CTA's MMAs are all done (see below)
+        // tile once this CTA's MMAs are all done (see below); the partials
+        // were written by generic stores and are read back by bulk copies
+        // (the async proxy), so each lane fences both before the count
+        fence_proxy_async_global();
         __threadfence();
         __syncwarp();
         int c_first = 0, c_last = 0, last = 0;
@@ -377,6 +339,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
       const int first_piece = fin_s[f] + fin_first[f];
       auto issue = [&](int rd, int b) {
         if (lane == 0) {
+          fence_proxy_async_global();  // the other pieces' partials, acquired through the count
           fence_proxy_async_smem();
           mbar_expect_tx(&fin_bar[quarter * 2 + b], static_cast<uint32_t>(np * per_round * FIN_CHUNK_BYTES));
           uint8_t* dst = fin_base + b * FIN_BUF_BYTES;
@@ -441,9 +404,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
 
   // ------------------------------------------------------------ teardown
   __syncwarp();  // lanes 1..31 of the producer and MMA warps wait here for their lane 0
-#ifdef DT_GEMM_TRACE
-  if (threadIdx.x == 0 && p.trace) atomicAdd(&p.trace[blockIdx.x * TRACE_SLOTS + TR_TOTAL], (unsigned long long)(clock64() - _trace_start));
-#endif
   if (aborted && lane == 0) atomicOr(p.status, DT_DEV_ERR_TIMEOUT);
   if ((warp == 0 || warp == PAIR_B_PRODUCER_WARP) && lane == 0 && aborted) {
     // copies this CTA issued count on rank 0's barrier; give them a bounded
@@ -532,10 +492,10 @@ cudaError_t launch_tcgen05_pair(const Params& p, int clusters, cudaStream_t stre
     ps.total_tiles = p.total_tiles;
     ps.m_tiles = p.m_tiles;
     ps.band_m = p.band_m;
+    ps.band_n = p.band_n;
     ps.starve = p.starve;
     ps.wait_limit_ns = p.wait_limit_ns;
     ps.status = p.status;
-    ps.trace = p.trace;
     ps.sk_tiles = p.sk_tiles;
     ps.sk_kiters = p.sk_kiters;
     ps.sk_part = p.sk_part;

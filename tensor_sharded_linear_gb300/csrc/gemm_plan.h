@@ -44,8 +44,23 @@ struct HostGroup {
   int bias_dtype = -1;
 };
 
-// Run every group; returns a host-detected error or DT_OK.
-dt_status run_groups(std::vector<HostGroup>& groups, int32_t* d_status, cudaStream_t stream);
+// Caller-owned device memory a call may use for the split tail's scratch
+// (256-byte aligned; null or too small: every tile runs whole).
+struct Workspace {
+  char* ptr = nullptr;
+  size_t bytes = 0;
+};
+
+// Run every group; returns a host-detected error or DT_OK.  Launches run one
+// after another on `stream`, so they share the workspace.
+dt_status run_groups(std::vector<HostGroup>& groups, int32_t* d_status, cudaStream_t stream, Workspace ws);
+
+// Workspace bytes with which run_groups on the current device splits every
+// launch's last wave that it would split (0 when none would).
+dt_status workspace_bytes(std::vector<HostGroup>& groups, size_t* bytes);
+
+// CUDA-core GEMM launches so far (operands TMA cannot describe, or fp32).
+uint64_t cuda_core_launches();
 
 // Capacities of one launch's parameter block (the device code's ParamsT).
 constexpr int MAX_MAPS = 48;
@@ -54,21 +69,8 @@ constexpr int MAX_GROUPS = 64;
 template <int NMAPS, int NSEGS, int NGROUPS>
 struct ParamsT;
 using Params = ParamsT<MAX_MAPS, MAX_SEGS, MAX_GROUPS>;
-cudaError_t launch_tcgen05(const Params& p, int grid, cudaStream_t stream);
 cudaError_t launch_tcgen05_pair(const Params& p, int clusters, cudaStream_t stream);
 int pair_max_clusters();  // co-resident clusters of the pair kernel (0: unavailable)
-
-// While one of these exists on a thread, GEMM launches from that thread
-// neither allocate nor use the split tail's scratch: every tile runs whole.
-struct NoAllocScope {
-  NoAllocScope();
-  ~NoAllocScope();
-  NoAllocScope(const NoAllocScope&) = delete;
-  NoAllocScope& operator=(const NoAllocScope&) = delete;
-};
-
-// Zero the split tail's arrival counters (after a launch reported a timeout).
-void reset_split_counters();
 
 // The launches one call made, recorded as issued so a later call with the
 // same operands replays them without planning.
@@ -79,7 +81,6 @@ struct GemmRecordScope {  // while alive, run_groups on this thread records into
 };
 std::shared_ptr<GemmRecord> new_gemm_record();
 dt_status replay_gemm(const GemmRecord& r, cudaStream_t stream);
-bool gemm_no_alloc();  // inside a NoAllocScope (plans made there differ)
 
 }  // namespace gemm
 }  // namespace dt

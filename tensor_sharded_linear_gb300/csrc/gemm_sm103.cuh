@@ -1,12 +1,6 @@
 // Device side of the tensor-parallel GEMM for sm_103a: tcgen05 MMA with the
 // accumulator in tensor memory (TMEM), operands staged in shared memory by
-// TMA, one persistent CTA per SM with warp-specialised roles.
-//
-//   warp 0      TMA producer  (one lane): fills a STAGES-deep smem ring
-//   warp 1      MMA issuer    (one lane): tcgen05.mma into a double-buffered
-//                                         TMEM accumulator; owns TMEM
-//   warps 2..5  epilogue      (128 threads, one accumulator row each):
-//                                         tcgen05.ld, bias / SiLU*mul, cast, store
+// TMA, persistent CTA pairs (clusters of two) with warp-specialised roles.
 //
 // Problem description: a list of GROUPS, each an independent output tile
 // grid, and per group a list of K SEGMENTS, each one (A, B) pair of TMA
@@ -22,8 +16,9 @@
 //                    of the accumulator and the epilogue forms SiLU(g) * u.
 //
 // Operand layouts: A is K-major (row-major [M, K] activations), B is
-// MN-major (row-major [K, N] weights, the [in, out] convention), both with
-// the 128-byte swizzle that TMA writes and the MMA reads.
+// MN-major (row-major [K, N] weights, the [in, out] convention) or K-major
+// (a transposed view of [out, in] storage), all with the 128-byte swizzle
+// that TMA writes and the MMA reads.
 #pragma once
 
 #include <cuda.h>
@@ -40,16 +35,10 @@ namespace gemm {
 constexpr int BM = 128;                       // accumulator rows = TMEM lanes
 constexpr int BN_MAX = 256;                   // accumulator columns per buffer
 constexpr int BK = 64;                        // 64 bf16 = one 128-byte swizzle row
-constexpr int STAGES = 4;
-constexpr int A_TILE_BYTES = BM * BK * 2;     // 16 KiB
 constexpr int B_CHUNK_BYTES = 64 * BK * 2;    // 8 KiB: 64 N columns x 64 K rows
-constexpr int B_TILE_BYTES = BN_MAX * BK * 2; // 32 KiB
-constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
-constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 512;                // two 256-column accumulators
 constexpr int GROUP_M = 8;                    // per-group raster: 8 M tiles per band
 constexpr int MAX_OUT = 8;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
 
 struct Seg {
@@ -68,22 +57,6 @@ struct Group {
   int64_t out_ld[MAX_OUT];  // elements
 };
 
-// Wait-time tracing (build with -DDT_GEMM_TRACE): every CTA adds the clock
-// cycles each role spends in each kind of barrier wait to its record in
-// Params::trace (TRACE_SLOTS uint64 per CTA, indexed by blockIdx.x).
-enum TraceSlot {
-  TR_TOTAL = 0,        // cycles from the first role loop to teardown (warp 0)
-  TR_PROD_EMPTY = 1,   // producer waiting for a free stage
-  TR_MMA_FULL = 2,     // MMA issuer waiting for a filled stage
-  TR_MMA_TEMPTY = 3,   // MMA issuer waiting for a drained accumulator
-  TR_EPI_TFULL = 4,    // epilogue (warp 2) waiting for a finished accumulator
-  TR_TILES = 5,        // tiles this CTA processed
-  TR_STAGES = 6,       // stages the MMA issuer consumed
-  TR_TMA_LAT = 7,      // sum over stages: stage's first TMA issued -> MMA issuer sees it full
-  TR_COMMIT_LAT = 8,   // sum over stages: MMA commit issued -> producer sees the stage empty
-  TRACE_SLOTS = 16
-};
-
 // Every launch's description travels in its parameter block.  Its size
 // costs launch time, so a launch whose tables fit the compact capacities
 // (ParamsSmall, ~8 KB) uses them and only large launches take Params (~25 KB).
@@ -98,10 +71,10 @@ struct ParamsT {  // CUtensorMap carries its own 128-byte alignment
   int32_t ngroups, total_tiles;
   int32_t m_tiles;  // > 0: every group has this many M tiles, rastered together
   int32_t band_m;   // M tiles per raster band
+  int32_t band_n;   // N tiles (across groups) per block of a band
   int32_t starve;   // test hook: producers issue no loads, so every MMA wait runs out
   unsigned long long wait_limit_ns;  // bound of every mbarrier wait
   int32_t* status;
-  unsigned long long* trace;  // TRACE_SLOTS per CTA when built with DT_GEMM_TRACE, else unused
   // Split tail (pair kernel only).  The last sk_tiles tiles are not given to
   // clusters whole: their sk_tiles * sk_kiters K iterations are divided
   // evenly over all clusters, and each (cluster, tile) piece accumulates
@@ -116,24 +89,6 @@ struct ParamsT {  // CUtensorMap carries its own 128-byte alignment
 };
 using ParamsSmall = ParamsT<24, 32, 16>;
 static_assert(sizeof(Params) <= 32000, "GEMM parameter block over the launch limit");
-
-#ifdef DT_GEMM_TRACE
-#define DT_TRACE_T0() const long long _tr0 = clock64()
-#define DT_TRACE_ADD(slot) \
-  if (p.trace) atomicAdd(&p.trace[blockIdx.x * TRACE_SLOTS + (slot)], (unsigned long long)(clock64() - _tr0))
-#define DT_TRACE_COUNT(slot) \
-  if (p.trace) atomicAdd(&p.trace[blockIdx.x * TRACE_SLOTS + (slot)], 1ull)
-#else
-#define DT_TRACE_T0() \
-  do {            \
-  } while (0)
-#define DT_TRACE_ADD(slot) \
-  do {                     \
-  } while (0)
-#define DT_TRACE_COUNT(slot) \
-  do {                       \
-  } while (0)
-#endif
 
 // ---------------------------------------------------------------- PTX helpers
 
@@ -193,49 +148,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int32_t c0, int32_t c1,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-      : "memory");
-}
-
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tmem_alloc(uint32_t* slot_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot_smem)),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem], bf16 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive on `bar` once every tcgen05 operation this thread issued so far completes.
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
 
 // 32 consecutive fp32 accumulator columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
@@ -359,6 +277,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// The same for global memory: generic-proxy stores of split-tail partials
+// before the counter update that publishes them, and, in the finishing
+// thread, the acquired counter before the bulk copies that read them.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Issued by one warp in EACH CTA of the pair.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot_smem)),
@@ -403,24 +328,40 @@ struct TileCoord {
   int g, m0, n0;
 };
 
-// Tile order.  When every group has the same M tiles (all groups of a
-// column-parallel launch share x; a row-parallel launch is one group), the
-// groups' N tiles form one sweep: a band of band_m M tiles visits every
-// (group, N tile) with M fastest, so concurrent CTAs share A rows and each
-// B panel is fetched once per band.  Otherwise each group is rastered on
-// its own in bands of GROUP_M M tiles.
+// Tile order of a launch whose groups all have the same M tiles (all groups
+// of a column-parallel launch share x; a row-parallel launch is one group):
+// the groups' N tiles form one axis of total_n tiles.  Tiles go in bands of
+// band_m M tiles; a band is cut into blocks of band_n N tiles, visited in
+// order, with M fastest inside a block; odd bands sweep N backwards, so
+// consecutive bands start on the B panels the previous one ended on.
+// Concurrent clusters then share the A rows and B columns of a compact
+// block of tiles.  Returns the M tile and the N tile across groups.
+__host__ __device__ __forceinline__ void band_order(int t, int m_tiles, int total_n, int band_m, int band_n, int* mi,
+                                                    int* jn) {
+  const int span = band_m * total_n;
+  const int mb = t / span;
+  const int first_m = mb * band_m;
+  const int gm = m_tiles - first_m < band_m ? m_tiles - first_m : band_m;
+  const int r = t - mb * span;
+  const int blk = gm * band_n;
+  const int nb = r / blk;
+  const int r2 = r - nb * blk;
+  int j = nb * band_n + r2 / gm;
+  if (mb & 1) j = total_n - 1 - j;
+  *mi = first_m + r2 % gm;
+  *jn = j;
+}
+
+// Tile t of a launch.  With common M tiles, band_order; otherwise each
+// group is rastered on its own in bands of GROUP_M M tiles.
 template <int TILE_M, class P>
 __device__ __forceinline__ TileCoord decode_tile(const P& p, int t) {
   if (p.m_tiles > 0) {
-    const int total_n = p.n_tile_begin[p.ngroups];
-    const int span = p.band_m * total_n;
-    const int first_m = (t / span) * p.band_m;
-    const int gm = min(p.band_m, p.m_tiles - first_m);
-    const int r = t % span;
-    const int jn = r / gm;  // N tile across all groups
+    int mi, jn;
+    band_order(t, p.m_tiles, p.n_tile_begin[p.ngroups], p.band_m, p.band_n, &mi, &jn);
     int g = 0;
     while (g + 1 < p.ngroups && p.n_tile_begin[g + 1] <= jn) ++g;
-    return TileCoord{g, (first_m + r % gm) * TILE_M, (jn - p.n_tile_begin[g]) * p.groups[g].bn};
+    return TileCoord{g, mi * TILE_M, (jn - p.n_tile_begin[g]) * p.groups[g].bn};
   }
   int g = 0;
   while (g + 1 < p.ngroups && p.groups[g + 1].tile_begin <= t) ++g;

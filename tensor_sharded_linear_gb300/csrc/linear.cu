@@ -252,9 +252,10 @@ dt_status add_column_groups(const DTensor& X, const ColumnSpec& c, int tp, std::
   return DT_OK;
 }
 
-dt_status column_multi(const dt_dtensor* x, int32_t n, const dt_dtensor* w, const dt_dtensor* bias,
-                       const dt_dtensor* y, int32_t tp, int32_t* d_status, dt_stream_t stream) {
-  clear_error();
+// Parse and check a (multi-)column call and lower every shard's product
+// to GEMM groups.
+dt_status column_build(const dt_dtensor* x, int32_t n, const dt_dtensor* w, const dt_dtensor* bias,
+                       const dt_dtensor* y, int32_t tp, std::vector<HostGroup>* groups) {
   if (n < 1 || !w || !y) return fail(DT_ERR_INVALID_ARG, "need n >= 1 weights and outputs");
   DTensor X;
   dt_status st = parse_dtensor(x, &X, "x");
@@ -273,16 +274,23 @@ dt_status column_multi(const dt_dtensor* x, int32_t n, const dt_dtensor* w, cons
     ColumnSpec c{&W[j], has_bias[j] ? &B[j] : nullptr, &Y[j]};
     if ((st = check_column(X, c, tp, true)) != DT_OK) return st;
   }
-  std::vector<HostGroup> groups;
   std::set<std::tuple<const void*, int, int, int>> done;
   for (int j = 0; j < n; ++j) {
     ColumnSpec c{&W[j], has_bias[j] ? &B[j] : nullptr, &Y[j]};
-    if ((st = add_column_groups(X, c, tp, &groups, &done)) != DT_OK) return st;
+    if ((st = add_column_groups(X, c, tp, groups, &done)) != DT_OK) return st;
   }
+  return DT_OK;
+}
+
+dt_status column_multi(const dt_dtensor* x, int32_t n, const dt_dtensor* w, const dt_dtensor* bias,
+                       const dt_dtensor* y, int32_t tp, gemm::Workspace ws, int32_t* d_status, dt_stream_t stream) {
+  clear_error();
+  std::vector<HostGroup> groups;
+  dt_status st = column_build(x, n, w, bias, y, tp, &groups);
+  if (st != DT_OK) return st;
   if (groups.empty()) return DT_OK;
-  const void* any = groups[0].out_ptr[0];
-  if ((st = bind_device_of(any)) != DT_OK) return st;
-  return gemm::run_groups(groups, d_status, reinterpret_cast<cudaStream_t>(stream));
+  if ((st = bind_device_of(groups[0].out_ptr[0])) != DT_OK) return st;
+  return gemm::run_groups(groups, d_status, reinterpret_cast<cudaStream_t>(stream), ws);
 }
 
 // Row-parallel groups for one (x, w, y) triple; `x_override` replaces the x
@@ -500,10 +508,20 @@ dt_status with_gemm_plan(const std::string* key, dt_stream_t stream, F&& plan_an
 }
 
 // The key's common tail: what the recorded parameters hold besides the operands.
-void finish_key(std::string* k, int32_t* d_status, dt_stream_t stream) {
+void finish_key(std::string* k, void* workspace, size_t workspace_bytes, int32_t* d_status, dt_stream_t stream) {
+  append_plan_scalar(k, workspace);
+  append_plan_scalar(k, workspace_bytes);
   append_plan_scalar(k, d_status);
   append_plan_scalar(k, stream);
-  append_plan_scalar(k, (char)(gemm::gemm_no_alloc() ? 1 : 0));
+}
+
+// A linear's workspace: null (size ignored), or 256-byte aligned device memory.
+dt_status check_workspace(void* workspace, size_t workspace_bytes, gemm::Workspace* ws) {
+  if (!workspace) return DT_OK;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256) return fail(DT_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  ws->ptr = static_cast<char*>(workspace);
+  ws->bytes = workspace_bytes;
+  return DT_OK;
 }
 
 }  // namespace
@@ -522,45 +540,47 @@ extern "C" {
 
 dt_status dt_column_parallel_linear_multi(const dt_dtensor* x, int32_t n, const dt_dtensor* w,
                                           const dt_dtensor* bias, const dt_dtensor* y, int32_t tp_mesh_dim,
-                                          int32_t* d_status, dt_stream_t stream) {
+                                          void* workspace, size_t workspace_bytes, int32_t* d_status,
+                                          dt_stream_t stream) {
+  clear_error();
+  gemm::Workspace ws;
+  if (dt_status st = check_workspace(workspace, workspace_bytes, &ws); st != DT_OK) return st;
   std::string key(1, 'c');
   bool keyed = n >= 0 && n <= 64 && (n == 0 || (w && y)) && append_plan_key(&key, x);
   for (int j = 0; j < n && keyed; ++j)
     keyed = append_plan_key(&key, &w[j]) && append_plan_key(&key, &y[j]) &&
             append_plan_key(&key, bias ? &bias[j] : nullptr);
   append_plan_scalar(&key, tp_mesh_dim);
-  finish_key(&key, d_status, stream);
+  finish_key(&key, workspace, workspace_bytes, d_status, stream);
   return with_gemm_plan(keyed ? &key : nullptr, stream,
-                        [&] { return column_multi(x, n, w, bias, y, tp_mesh_dim, d_status, stream); });
+                        [&] { return column_multi(x, n, w, bias, y, tp_mesh_dim, ws, d_status, stream); });
 }
 
 dt_status dt_column_parallel_linear(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* bias,
-                                    const dt_dtensor* y, int32_t tp_mesh_dim, int32_t* d_status,
-                                    dt_stream_t stream) {
-  return dt_column_parallel_linear_multi(x, 1, w, bias, y, tp_mesh_dim, d_status, stream);
+                                    const dt_dtensor* y, int32_t tp_mesh_dim, void* workspace,
+                                    size_t workspace_bytes, int32_t* d_status, dt_stream_t stream) {
+  return dt_column_parallel_linear_multi(x, 1, w, bias, y, tp_mesh_dim, workspace, workspace_bytes, d_status,
+                                         stream);
 }
 
-static dt_status row_parallel_planned(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* bias,
-                                      const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim, int32_t* d_status,
-                                      dt_stream_t stream);
-
-dt_status dt_row_parallel_linear(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* bias,
-                                 const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim, int32_t* d_status,
-                                 dt_stream_t stream) {
-  std::string key(1, 'r');
-  const bool keyed = append_plan_key(&key, x) && append_plan_key(&key, w) && append_plan_key(&key, bias) &&
-                     append_plan_key(&key, y);
-  append_plan_scalar(&key, mode);
-  append_plan_scalar(&key, tp_mesh_dim);
-  finish_key(&key, d_status, stream);
-  return with_gemm_plan(keyed ? &key : nullptr, stream,
-                        [&] { return row_parallel_planned(x, w, bias, y, mode, tp_mesh_dim, d_status, stream); });
-}
-
-static dt_status row_parallel_planned(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* bias,
-                                      const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim, int32_t* d_status,
-                                      dt_stream_t stream) {
+dt_status dt_column_parallel_linear_workspace_size(const dt_dtensor* x, int32_t n, const dt_dtensor* w,
+                                                   const dt_dtensor* y, int32_t tp_mesh_dim, size_t* bytes) {
   clear_error();
+  if (!bytes) return fail(DT_ERR_INVALID_ARG, "bytes is NULL");
+  std::vector<HostGroup> groups;
+  dt_status st = column_build(x, n, w, nullptr, y, tp_mesh_dim, &groups);
+  if (st != DT_OK) return st;
+  return gemm::workspace_bytes(groups, bytes);
+}
+
+}  // extern "C"
+
+namespace dt {
+namespace {
+
+// Parse and check a row call and lower it to GEMM groups.
+dt_status row_build(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* bias, const dt_dtensor* y,
+                    int32_t mode, int32_t tp, std::vector<HostGroup>* groups) {
   DTensor X, W, B, Y;
   dt_status st;
   if ((st = parse_dtensor(x, &X, "x")) != DT_OK) return st;
@@ -568,21 +588,61 @@ static dt_status row_parallel_planned(const dt_dtensor* x, const dt_dtensor* w, 
   if ((st = parse_dtensor(y, &Y, "y")) != DT_OK) return st;
   const bool has_bias = bias && bias->nslots > 0;
   if (has_bias && (st = parse_dtensor(bias, &B, "bias")) != DT_OK) return st;
-  if ((st = check_tp(tp_mesh_dim, X.layout)) != DT_OK) return st;
-  if (tp_mesh_dim < 0 && mode != DT_TP_ALL_REDUCE)
+  if ((st = check_tp(tp, X.layout)) != DT_OK) return st;
+  if (tp < 0 && mode != DT_TP_ALL_REDUCE)
     return fail(DT_ERR_INVALID_ARG, "without tp only ALL_REDUCE (a plain linear) is defined");
-  if ((st = check_row(X.layout, W.layout, has_bias ? &B.layout : nullptr, Y.layout, mode, tp_mesh_dim)) != DT_OK)
-    return st;
-  std::vector<gemm::HostGroup> groups;
-  if ((st = row_groups(X.layout, nullptr, &X, W, has_bias ? &B : nullptr, Y, mode, tp_mesh_dim, &groups)) != DT_OK)
-    return st;
+  if ((st = check_row(X.layout, W.layout, has_bias ? &B.layout : nullptr, Y.layout, mode, tp)) != DT_OK) return st;
+  return row_groups(X.layout, nullptr, &X, W, has_bias ? &B : nullptr, Y, mode, tp, groups);
+}
+
+dt_status row_parallel_planned(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* bias, const dt_dtensor* y,
+                               int32_t mode, int32_t tp, gemm::Workspace ws, int32_t* d_status, dt_stream_t stream) {
+  clear_error();
+  std::vector<HostGroup> groups;
+  dt_status st = row_build(x, w, bias, y, mode, tp, &groups);
+  if (st != DT_OK) return st;
   if (groups.empty()) return DT_OK;
   if ((st = bind_device_of(groups[0].out_ptr[0])) != DT_OK) return st;
-  return gemm::run_groups(groups, d_status, reinterpret_cast<cudaStream_t>(stream));
+  return gemm::run_groups(groups, d_status, reinterpret_cast<cudaStream_t>(stream), ws);
+}
+
+}  // namespace
+}  // namespace dt
+
+extern "C" {
+
+dt_status dt_row_parallel_linear(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* bias,
+                                 const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim, void* workspace,
+                                 size_t workspace_bytes, int32_t* d_status, dt_stream_t stream) {
+  clear_error();
+  gemm::Workspace ws;
+  if (dt_status st = check_workspace(workspace, workspace_bytes, &ws); st != DT_OK) return st;
+  std::string key(1, 'r');
+  const bool keyed = append_plan_key(&key, x) && append_plan_key(&key, w) && append_plan_key(&key, bias) &&
+                     append_plan_key(&key, y);
+  append_plan_scalar(&key, mode);
+  append_plan_scalar(&key, tp_mesh_dim);
+  finish_key(&key, workspace, workspace_bytes, d_status, stream);
+  return with_gemm_plan(keyed ? &key : nullptr, stream, [&] {
+    return row_parallel_planned(x, w, bias, y, mode, tp_mesh_dim, ws, d_status, stream);
+  });
+}
+
+dt_status dt_row_parallel_linear_workspace_size(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* y,
+                                                int32_t mode, int32_t tp_mesh_dim, size_t* bytes) {
+  clear_error();
+  if (!bytes) return fail(DT_ERR_INVALID_ARG, "bytes is NULL");
+  std::vector<HostGroup> groups;
+  dt_status st = row_build(x, w, nullptr, y, mode, tp_mesh_dim, &groups);
+  if (st != DT_OK) return st;
+  return gemm::workspace_bytes(groups, bytes);
 }
 
 // ---- TP MLP -------------------------------------------------------------
 
+}  // extern "C"
+
+namespace dt {
 namespace {
 
 struct MlpPlan {
@@ -590,12 +650,13 @@ struct MlpPlan {
   std::vector<int64_t> h_offset;   // byte offset of each H block
   std::vector<int64_t> h_rows;
   int64_t F = 0;
-  size_t bytes = 0;
+  size_t bytes = 0;                // every H block, 256-byte aligned
 };
 
-dt_status mlp_plan(const DTensor& X, const DTensor& Wg, int tp, MlpPlan* plan) {
+dt_status mlp_plan(const DTensor& X, const DTensor& Wg, MlpPlan* plan) {
   const Layout& lx = X.layout;
   if (lx.ndim < 1) return fail(DT_ERR_SHAPE, "x rank");
+  if (Wg.layout.ndim != 2) return fail(DT_ERR_SHAPE, "w_gate must be 2-D [in, ffn]");
   plan->F = Wg.layout.gshape[1];
   std::set<int> seen;
   int c[DT_MAX_MESH_DIMS];
@@ -613,51 +674,14 @@ dt_status mlp_plan(const DTensor& X, const DTensor& Wg, int tp, MlpPlan* plan) {
     off += ((size_t)rows * (size_t)plan->F * 2 + 255) & ~size_t(255);
   }
   plan->bytes = off;
-  (void)tp;
   return DT_OK;
 }
 
-}  // namespace
-
-dt_status dt_tp_mlp_workspace_size(const dt_dtensor* x, const dt_dtensor* w_gate, int32_t tp_mesh_dim,
-                                   size_t* bytes) {
-  clear_error();
-  if (!bytes) return fail(DT_ERR_INVALID_ARG, "bytes is NULL");
-  DTensor X, Wg;
-  dt_status st;
-  if ((st = parse_dtensor(x, &X, "x")) != DT_OK) return st;
-  if ((st = parse_dtensor(w_gate, &Wg, "w_gate")) != DT_OK) return st;
-  MlpPlan plan;
-  if ((st = mlp_plan(X, Wg, tp_mesh_dim, &plan)) != DT_OK) return st;
-  *bytes = plan.bytes;
-  return DT_OK;
-}
-
-static dt_status tp_mlp_planned(const dt_dtensor* x, const dt_dtensor* w_gate, const dt_dtensor* w_up,
-                                const dt_dtensor* w_down, const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim,
-                                void* workspace, size_t workspace_bytes, int32_t* d_status, dt_stream_t stream);
-
-dt_status dt_tp_mlp(const dt_dtensor* x, const dt_dtensor* w_gate, const dt_dtensor* w_up, const dt_dtensor* w_down,
-                    const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim, void* workspace, size_t workspace_bytes,
-                    int32_t* d_status, dt_stream_t stream) {
-  std::string key(1, 'm');
-  const bool keyed = append_plan_key(&key, x) && append_plan_key(&key, w_gate) && append_plan_key(&key, w_up) &&
-                     append_plan_key(&key, w_down) && append_plan_key(&key, y);
-  append_plan_scalar(&key, mode);
-  append_plan_scalar(&key, tp_mesh_dim);
-  append_plan_scalar(&key, workspace);
-  append_plan_scalar(&key, workspace_bytes);
-  finish_key(&key, d_status, stream);
-  return with_gemm_plan(keyed ? &key : nullptr, stream, [&] {
-    return tp_mlp_planned(x, w_gate, w_up, w_down, y, mode, tp_mesh_dim, workspace, workspace_bytes, d_status,
-                          stream);
-  });
-}
-
-static dt_status tp_mlp_planned(const dt_dtensor* x, const dt_dtensor* w_gate, const dt_dtensor* w_up,
-                                const dt_dtensor* w_down, const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim,
-                                void* workspace, size_t workspace_bytes, int32_t* d_status, dt_stream_t stream) {
-  clear_error();
+// Parse and check an MLP call and lower it to its two GEMM launches' groups,
+// with H at `h_base` (256-byte aligned device memory of plan->bytes).
+dt_status mlp_build(const dt_dtensor* x, const dt_dtensor* w_gate, const dt_dtensor* w_up, const dt_dtensor* w_down,
+                    const dt_dtensor* y, int32_t mode, int32_t tp, char* h_base, MlpPlan* plan,
+                    std::vector<HostGroup>* up_groups, std::vector<HostGroup>* down_groups) {
   DTensor X, Wg, Wu, Wd, Y;
   dt_status st;
   if ((st = parse_dtensor(x, &X, "x")) != DT_OK) return st;
@@ -665,7 +689,6 @@ static dt_status tp_mlp_planned(const dt_dtensor* x, const dt_dtensor* w_gate, c
   if ((st = parse_dtensor(w_up, &Wu, "w_up")) != DT_OK) return st;
   if ((st = parse_dtensor(w_down, &Wd, "w_down")) != DT_OK) return st;
   if ((st = parse_dtensor(y, &Y, "y")) != DT_OK) return st;
-  const int tp = tp_mesh_dim;
   if ((st = check_tp(tp, X.layout)) != DT_OK) return st;
   const Layout& lx = X.layout;
   if (lx.dtype != DT_BF16 || Wg.layout.dtype != DT_BF16 || Wu.layout.dtype != DT_BF16 || Wd.layout.dtype != DT_BF16)
@@ -692,12 +715,8 @@ static dt_status tp_mlp_planned(const dt_dtensor* x, const dt_dtensor* w_gate, c
   if (lx.gshape[nd - 1] != Wg.layout.gshape[0]) return fail(DT_ERR_SHAPE, "x last dim != w_gate rows");
   if (Wd.layout.ndim != 2 || Wd.layout.gshape[0] != Wg.layout.gshape[1]) return fail(DT_ERR_SHAPE, "w_down must be [ffn, out]");
   if ((st = check_gemm_dims(lx, Wg.layout.gshape[0], 2 * Wg.layout.gshape[1])) != DT_OK) return st;
-  MlpPlan plan;
-  if ((st = mlp_plan(X, Wg, tp, &plan)) != DT_OK) return st;
-  if (!workspace || workspace_bytes < plan.bytes)
-    return fail(DT_ERR_INVALID_ARG, "workspace of %zu bytes needed", plan.bytes);
-  if (reinterpret_cast<uintptr_t>(workspace) % 256) return fail(DT_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
-  const int64_t F = plan.F;
+  if ((st = mlp_plan(X, Wg, plan)) != DT_OK) return st;
+  const int64_t F = plan->F;
   if ((F * 2) % 16) return fail(DT_ERR_ALIGNMENT, "ffn width must be a multiple of 8");
 
   // H as a layout: x's placements with the last dim of size F, Shard(-1) on tp.
@@ -726,18 +745,17 @@ static dt_status tp_mlp_planned(const dt_dtensor* x, const dt_dtensor* w_gate, c
     LH.slot_coords(s, c);
     const int xs = lx.slot_of_coords(c);
     size_t bi = 0;
-    while (bi < plan.x_slots.size() && plan.x_slots[bi] != xs) ++bi;
+    while (bi < plan->x_slots.size() && plan->x_slots[bi] != xs) ++bi;
     const Box hb = LH.slot_box(s);
     Mat m;
-    m.ptr = static_cast<char*>(workspace) + plan.h_offset[bi] + hb.off[nd - 1] * 2;
-    m.rows = plan.h_rows[bi];
+    m.ptr = h_base + plan->h_offset[bi] + hb.off[nd - 1] * 2;
+    m.rows = plan->h_rows[bi];
     m.cols = hb.size[nd - 1];
     m.ld = F;
     m.dtype = DT_BF16;
     hmats[s] = m;
   }
   // 1) gate/up: one dual group per (x slot, tp shard)
-  std::vector<gemm::HostGroup> up_groups;
   std::set<int> done;
   for (int r = 0; r < lx.mesh_size; ++r) {
     lx.rank_coords(r, c);
@@ -750,26 +768,95 @@ static dt_status tp_mlp_planned(const dt_dtensor* x, const dt_dtensor* w_gate, c
     const Mat& h = hmats[hs];
     if (bg.cols != h.cols || bu.cols != h.cols || a.cols != bg.rows || a.rows != h.rows)
       return fail(DT_ERR_SHAPE, "gate/up local shapes disagree");
-    gemm::HostGroup g;
+    HostGroup g;
     g.m = h.rows;
     g.n = h.cols;
     g.dual = true;
-    g.segs.push_back(gemm::HostSeg{a, bg, bu});
+    g.segs.push_back(HostSeg{a, bg, bu});
     g.out_dtype = DT_BF16;
     g.row_begin = {0};
     g.out_ptr = {h.ptr};
     g.out_ld = {h.ld};
-    up_groups.push_back(std::move(g));
+    up_groups->push_back(std::move(g));
   }
   // 2) down: row-parallel over the H shards
   if ((st = check_row(LH, Wd.layout, nullptr, Y.layout, mode, tp)) != DT_OK) return st;
-  std::vector<gemm::HostGroup> down_groups;
-  if ((st = row_groups(LH, &hmats, nullptr, Wd, nullptr, Y, mode, tp, &down_groups)) != DT_OK) return st;
+  return row_groups(LH, &hmats, nullptr, Wd, nullptr, Y, mode, tp, down_groups);
+}
+
+dt_status tp_mlp_planned(const dt_dtensor* x, const dt_dtensor* w_gate, const dt_dtensor* w_up,
+                         const dt_dtensor* w_down, const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim,
+                         void* workspace, size_t workspace_bytes, int32_t* d_status, dt_stream_t stream) {
+  clear_error();
+  if (workspace && reinterpret_cast<uintptr_t>(workspace) % 256)
+    return fail(DT_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  MlpPlan plan;
+  std::vector<HostGroup> up_groups, down_groups;
+  dt_status st = mlp_build(x, w_gate, w_up, w_down, y, mode, tp_mesh_dim, static_cast<char*>(workspace), &plan,
+                           &up_groups, &down_groups);
+  if (st != DT_OK) return st;
+  if (!workspace || workspace_bytes < plan.bytes)
+    return fail(DT_ERR_INVALID_ARG, "workspace of at least %zu bytes (H) needed", plan.bytes);
   if (up_groups.empty()) return DT_OK;
   if ((st = bind_device_of(workspace)) != DT_OK) return st;
+  // the split tail's scratch follows H; both launches run in order on the
+  // stream, so they share it
+  gemm::Workspace split;
+  split.ptr = static_cast<char*>(workspace) + plan.bytes;
+  split.bytes = workspace_bytes - plan.bytes;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = gemm::run_groups(up_groups, d_status, s)) != DT_OK) return st;
-  return gemm::run_groups(down_groups, d_status, s);
+  if ((st = gemm::run_groups(up_groups, d_status, s, split)) != DT_OK) return st;
+  return gemm::run_groups(down_groups, d_status, s, split);
+}
+
+}  // namespace
+
+dt_status mlp_hidden_bytes(const dt_dtensor* x, const dt_dtensor* w_gate, size_t* bytes) {
+  DTensor X, Wg;
+  dt_status st;
+  if ((st = parse_dtensor(x, &X, "x")) != DT_OK) return st;
+  if ((st = parse_dtensor(w_gate, &Wg, "w_gate")) != DT_OK) return st;
+  MlpPlan plan;
+  if ((st = mlp_plan(X, Wg, &plan)) != DT_OK) return st;
+  *bytes = plan.bytes;
+  return DT_OK;
+}
+
+}  // namespace dt
+
+extern "C" {
+
+dt_status dt_tp_mlp_workspace_size(const dt_dtensor* x, const dt_dtensor* w_gate, const dt_dtensor* w_up,
+                                   const dt_dtensor* w_down, const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim,
+                                   size_t* bytes) {
+  clear_error();
+  if (!bytes) return fail(DT_ERR_INVALID_ARG, "bytes is NULL");
+  // H's place in the workspace only matters through its alignment
+  char* const h_base = reinterpret_cast<char*>(uintptr_t(256));
+  MlpPlan plan;
+  std::vector<HostGroup> up_groups, down_groups;
+  dt_status st = mlp_build(x, w_gate, w_up, w_down, y, mode, tp_mesh_dim, h_base, &plan, &up_groups, &down_groups);
+  if (st != DT_OK) return st;
+  size_t up = 0, down = 0;
+  if ((st = gemm::workspace_bytes(up_groups, &up)) != DT_OK) return st;
+  if ((st = gemm::workspace_bytes(down_groups, &down)) != DT_OK) return st;
+  *bytes = plan.bytes + std::max(up, down);
+  return DT_OK;
+}
+
+dt_status dt_tp_mlp(const dt_dtensor* x, const dt_dtensor* w_gate, const dt_dtensor* w_up, const dt_dtensor* w_down,
+                    const dt_dtensor* y, int32_t mode, int32_t tp_mesh_dim, void* workspace, size_t workspace_bytes,
+                    int32_t* d_status, dt_stream_t stream) {
+  std::string key(1, 'm');
+  const bool keyed = append_plan_key(&key, x) && append_plan_key(&key, w_gate) && append_plan_key(&key, w_up) &&
+                     append_plan_key(&key, w_down) && append_plan_key(&key, y);
+  append_plan_scalar(&key, mode);
+  append_plan_scalar(&key, tp_mesh_dim);
+  finish_key(&key, workspace, workspace_bytes, d_status, stream);
+  return with_gemm_plan(keyed ? &key : nullptr, stream, [&] {
+    return tp_mlp_planned(x, w_gate, w_up, w_down, y, mode, tp_mesh_dim, workspace, workspace_bytes, d_status,
+                          stream);
+  });
 }
 
 }  // extern "C"

@@ -9,14 +9,17 @@
 // own a device allocator at all and must not mix raw cudaMalloc with the
 // pool its framework manages.  For them this entry point keeps H in a
 // buffer that is part of the library image itself: a file-scope device
-// array, created when the library is loaded onto a GPU and held by every
-// GPU that loads the library until the process exits.
+// array.  With CUDA's lazy module loading the array is reserved on a device
+// when its address is first looked up there, i.e. by the first call on that
+// device, which can therefore fail with an out-of-memory error
+// (DT_ERR_CUDA); callers make one call at start-up, before memory is tight
+// and before any stream capture.  From then on every GPU that has run the
+// entry point holds the array until the process exits.
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "dt_internal.h"
-#include "gemm_plan.h"
 
 namespace dt {
 namespace {
@@ -60,7 +63,7 @@ extern "C" dt_status dt_tp_mlp_static_workspace(const dt_dtensor* x, const dt_dt
                                                 int32_t* d_status, dt_stream_t stream) {
   clear_error();
   size_t need = 0;
-  dt_status st = dt_tp_mlp_workspace_size(x, w_gate, tp_mesh_dim, &need);
+  dt_status st = mlp_hidden_bytes(x, w_gate, &need);
   if (st != DT_OK) return st;
   if (need > (size_t)DT_TP_MLP_STATIC_WORKSPACE_BYTES)
     return fail(DT_ERR_CAPACITY,
@@ -79,9 +82,8 @@ extern "C" dt_status dt_tp_mlp_static_workspace(const dt_dtensor* x, const dt_dt
   void* ws = nullptr;
   if ((st = static_workspace_address(&ws)) != DT_OK) return st;
   // H is written in full by the gate/up GEMM before the down GEMM reads it,
-  // so nothing in the array needs clearing between calls.  The GEMMs run
-  // every tile whole: the split tail's scratch would be an allocation.
-  gemm::NoAllocScope no_alloc;
-  return dt_tp_mlp(x, w_gate, w_up, w_down, y, mode, tp_mesh_dim, ws, (size_t)DT_TP_MLP_STATIC_WORKSPACE_BYTES,
-                   d_status, stream);
+  // so nothing in the array needs clearing between calls.  Only H's bytes
+  // are offered as workspace, so the GEMMs run every tile whole and never
+  // use split-tail scratch.
+  return dt_tp_mlp(x, w_gate, w_up, w_down, y, mode, tp_mesh_dim, ws, need, d_status, stream);
 }

@@ -130,24 +130,24 @@ def test_host_rejections_before_launch(lib):
     x = fake_desc(opl.Layout(mesh, [S1], (16, 32)))
     w = fake_desc(opl.Layout(mesh, [S1], (32, 64)))
     y = fake_desc(opl.Layout(mesh, [S1], (16, 64)))
-    assert lib.dt_column_parallel_linear(C.byref(x), C.byref(w), None, C.byref(y), 0, None, None) == L.ERR_PLACEMENT
+    assert lib.dt_column_parallel_linear(C.byref(x), C.byref(w), None, C.byref(y), 0, None, 0, None, None) == L.ERR_PLACEMENT
     assert b"Replicate" in lib.dt_last_error()
     # row-parallel input must be Shard(-1) on tp
     xr = fake_desc(opl.Layout(mesh, [R], (16, 32)))
     wr = fake_desc(opl.Layout(mesh, [S0], (32, 64)))
     yr = fake_desc(opl.Layout(mesh, [R], (16, 64)))
-    assert lib.dt_row_parallel_linear(C.byref(xr), C.byref(wr), None, C.byref(yr), L.TP_ALL_REDUCE, 0, None,
-                                      None) == L.ERR_PLACEMENT
+    assert lib.dt_row_parallel_linear(C.byref(xr), C.byref(wr), None, C.byref(yr), L.TP_ALL_REDUCE, 0, None, 0,
+                                      None, None) == L.ERR_PLACEMENT
     # REDUCE_SCATTER output must be Shard(0)
     xs = fake_desc(opl.Layout(mesh, [S1], (16, 32)))
-    assert lib.dt_row_parallel_linear(C.byref(xs), C.byref(wr), None, C.byref(yr), L.TP_REDUCE_SCATTER, 0, None,
-                                      None) == L.ERR_PLACEMENT
+    assert lib.dt_row_parallel_linear(C.byref(xs), C.byref(wr), None, C.byref(yr), L.TP_REDUCE_SCATTER, 0, None, 0,
+                                      None, None) == L.ERR_PLACEMENT
     # shape mismatch: w rows != x cols
     w_bad = fake_desc(opl.Layout(mesh, [S0], (31, 64)))
-    assert lib.dt_row_parallel_linear(C.byref(xs), C.byref(w_bad), None, C.byref(yr), L.TP_ALL_REDUCE, 0, None,
-                                      None) == L.ERR_SHAPE
+    assert lib.dt_row_parallel_linear(C.byref(xs), C.byref(w_bad), None, C.byref(yr), L.TP_ALL_REDUCE, 0, None, 0,
+                                      None, None) == L.ERR_SHAPE
     # bad mode
-    assert lib.dt_row_parallel_linear(C.byref(xs), C.byref(wr), None, C.byref(yr), 7, 0, None, None) \
+    assert lib.dt_row_parallel_linear(C.byref(xs), C.byref(wr), None, C.byref(yr), 7, 0, None, 0, None, None) \
         == L.ERR_INVALID_ARG
     # embedding: table must be Shard(1) on tp
     ids = fake_desc(opl.Layout(mesh, [R], (2, 3)), L.INT32)
@@ -166,15 +166,15 @@ def test_gemm_dimensions_beyond_32_bits_are_refused(lib):
     x = fake_desc(opl.Layout(mesh, [R], (big, 8)))
     w = fake_desc(opl.Layout(mesh, [S1], (8, 64)))
     y = fake_desc(opl.Layout(mesh, [S1], (big, 64)))
-    assert lib.dt_column_parallel_linear(C.byref(x), C.byref(w), None, C.byref(y), 0, None, None) == L.ERR_CAPACITY
+    assert lib.dt_column_parallel_linear(C.byref(x), C.byref(w), None, C.byref(y), 0, None, 0, None, None) == L.ERR_CAPACITY
     assert b"2^31" in lib.dt_last_error()
     # row-parallel with K = 2^31 (x Shard(-1), w Shard(0) on tp)
     S0 = opl.Shard(0)
     xr = fake_desc(opl.Layout(mesh, [S1], (8, big)))
     wr = fake_desc(opl.Layout(mesh, [S0], (big, 64)))
     yr = fake_desc(opl.Layout(mesh, [R], (8, 64)))
-    assert lib.dt_row_parallel_linear(C.byref(xr), C.byref(wr), None, C.byref(yr), L.TP_ALL_REDUCE, 0, None,
-                                      None) == L.ERR_CAPACITY
+    assert lib.dt_row_parallel_linear(C.byref(xr), C.byref(wr), None, C.byref(yr), L.TP_ALL_REDUCE, 0, None, 0,
+                                      None, None) == L.ERR_CAPACITY
     assert b"2^31" in lib.dt_last_error()
 
 
@@ -182,3 +182,70 @@ def test_status_strings(lib):
     for s in range(8):
         assert lib.dt_status_string(s)
     assert lib.dt_version() >= 100
+
+
+def test_workspace_queries_on_host(lib):
+    """The linears' workspace queries check their operands as the calls do,
+    before anything touches a device; the CUDA-core path (fp32) needs no
+    workspace on any device; a bf16 problem's answer depends on the device's
+    CTA pairs, so without a CUDA device it is DT_ERR_CUDA."""
+    import torch
+    mesh = (4,)
+    R, S0, S1 = opl.Replicate(), opl.Shard(0), opl.Shard(1)
+    n = C.c_size_t(123)
+    # column: x Replicate, w Shard(1), y Shard(-1)
+    x = fake_desc(opl.Layout(mesh, [R], (512, 256)))
+    w = fake_desc(opl.Layout(mesh, [S1], (256, 1024)))
+    y = fake_desc(opl.Layout(mesh, [S1], (512, 1024)))
+    assert lib.dt_column_parallel_linear_workspace_size(C.byref(x), 1, C.byref(w), C.byref(y), 0, None) \
+        == L.ERR_INVALID_ARG
+    assert lib.dt_column_parallel_linear_workspace_size(C.byref(x), 0, C.byref(w), C.byref(y), 0, C.byref(n)) \
+        == L.ERR_INVALID_ARG
+    bad_x = fake_desc(opl.Layout(mesh, [S1], (512, 256)))
+    assert lib.dt_column_parallel_linear_workspace_size(C.byref(bad_x), 1, C.byref(w), C.byref(y), 0,
+                                                        C.byref(n)) == L.ERR_PLACEMENT
+    # fp32 operands run on the CUDA-core kernel: no workspace, on any device
+    x32 = fake_desc(opl.Layout(mesh, [R], (512, 256)), L.FP32)
+    w32 = fake_desc(opl.Layout(mesh, [S1], (256, 1024)), L.FP32)
+    y32 = fake_desc(opl.Layout(mesh, [S1], (512, 1024)), L.FP32)
+    assert lib.dt_column_parallel_linear_workspace_size(C.byref(x32), 1, C.byref(w32), C.byref(y32), 0,
+                                                        C.byref(n)) == L.OK
+    assert n.value == 0
+    # row: x Shard(-1), w Shard(0), y per mode
+    xr = fake_desc(opl.Layout(mesh, [S1], (512, 1024)))
+    wr = fake_desc(opl.Layout(mesh, [S0], (1024, 256)))
+    yr = fake_desc(opl.Layout(mesh, [R], (512, 256)))
+    ys = fake_desc(opl.Layout(mesh, [S0], (512, 256)))
+    assert lib.dt_row_parallel_linear_workspace_size(C.byref(xr), C.byref(wr), C.byref(ys), L.TP_ALL_REDUCE, 0,
+                                                     C.byref(n)) == L.ERR_PLACEMENT
+    assert lib.dt_row_parallel_linear_workspace_size(C.byref(xr), C.byref(wr), C.byref(yr), 9, 0, C.byref(n)) \
+        == L.ERR_INVALID_ARG
+    # MLP: bf16 only
+    mlp = [fake_desc(opl.Layout(mesh, [R], (512, 256)), L.FP32), fake_desc(opl.Layout(mesh, [S1], (256, 1024))),
+           fake_desc(opl.Layout(mesh, [S1], (256, 1024))), fake_desc(opl.Layout(mesh, [S0], (1024, 256))),
+           fake_desc(opl.Layout(mesh, [R], (512, 256)))]
+    assert lib.dt_tp_mlp_workspace_size(*[C.byref(d) for d in mlp], L.TP_ALL_REDUCE, 0, C.byref(n)) \
+        == L.ERR_INVALID_ARG
+    if not torch.cuda.is_available():
+        assert lib.dt_column_parallel_linear_workspace_size(C.byref(x), 1, C.byref(w), C.byref(y), 0,
+                                                            C.byref(n)) == L.ERR_CUDA
+        assert b"CUDA device" in lib.dt_last_error()
+        assert lib.dt_row_parallel_linear_workspace_size(C.byref(xr), C.byref(wr), C.byref(yr), L.TP_ALL_REDUCE, 0,
+                                                         C.byref(n)) == L.ERR_CUDA
+
+
+def test_linear_workspace_alignment_checked_first(lib):
+    """A workspace must be 256-byte aligned; a misaligned one is refused before
+    any operand is read or anything launches."""
+    mesh = (4,)
+    R, S1 = opl.Replicate(), opl.Shard(1)
+    x = fake_desc(opl.Layout(mesh, [R], (16, 32)))
+    w = fake_desc(opl.Layout(mesh, [S1], (32, 64)))
+    y = fake_desc(opl.Layout(mesh, [S1], (16, 64)))
+    assert lib.dt_column_parallel_linear(C.byref(x), C.byref(w), None, C.byref(y), 0, _FAKE + 16, 1 << 20, None,
+                                         None) == L.ERR_ALIGNMENT
+    xr = fake_desc(opl.Layout(mesh, [S1], (16, 32)))
+    wr = fake_desc(opl.Layout(mesh, [opl.Shard(0)], (32, 64)))
+    yr = fake_desc(opl.Layout(mesh, [R], (16, 64)))
+    assert lib.dt_row_parallel_linear(C.byref(xr), C.byref(wr), None, C.byref(yr), L.TP_ALL_REDUCE, 0, _FAKE + 8,
+                                      1 << 20, None, None) == L.ERR_ALIGNMENT

@@ -7,8 +7,9 @@ into one CUDA graph.  Replays must reproduce the eager results bit for bit
 (same kernels, same launch plans), and, after new inputs are written into
 the same buffers, match an eager run on those inputs.  This exercises every
 piece of the runtime that capture constrains: the reduction stream forked
-from the caller's and joined back, the cached launch plans, and the GEMM
-split-tail scratch (made by the eager run; never allocated inside a capture).
+from the caller's and joined back, the cached launch plans, and the GEMM's
+split tail in the caller's workspace (its counters zeroed by a memset that
+the graph captures with the launches).
 """
 import numpy as np
 import pytest
@@ -63,7 +64,7 @@ def build_step():
     wud = tsl.DTensor([to_dev(np.ascontiguousarray(wu[:, o:o + s]), "bf16") for o, s in cols], tp8, [S1], wu.shape, bf)
     wdd = tsl.DTensor([to_dev(np.ascontiguousarray(wd[o:o + s]), "bf16") for o, s in cols], tp8, [S0], wd.shape, bf)
     ym = tsl.DTensor.empty(tp8, [R], (M, N), torch.float32, device=dev)
-    ws = torch.empty(tsl.tp_mlp_workspace_bytes(xd, wgd), dtype=torch.uint8, device=dev)
+    ws = torch.empty(tsl.tp_mlp_workspace_bytes(xd, wgd, wud, wdd, ym), dtype=torch.uint8, device=dev)
     inputs += xd.slots
     outputs += ym.slots
     calls.append(lambda: tsl.tp_mlp(xd, wgd, wud, wdd, mode=tsl.ALL_REDUCE, out=ym, workspace=ws))
@@ -109,12 +110,12 @@ def same(a, b):
 def test_step_in_a_cuda_graph(lib):
     calls, inputs, outputs, keep = build_step()
     # one stream for the eager runs and the capture: the linears' cached
-    # plans are per stream (the split-tail scratch is), so the captured calls
-    # replay exactly the eager launches
+    # plans are keyed by stream and workspace, so the captured calls replay
+    # exactly the eager launches
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
-        run(calls)  # eager: plans made, split-tail scratch made
+        run(calls)  # eager: plans made
     torch.cuda.synchronize()
     eager = snapshot(outputs)
 

@@ -103,17 +103,24 @@ def w64(bits):
 # ---------------------------------------------------------------- worked example
 
 def test_worked_example_fp32(lib):
-    """x[3, 8] @ W[8, 12], 4 parts, seed 0: column and row equal dense x @ W."""
+    """x[3, 8] @ W[8, 12], 4 parts, seed 0 ("Model parallelism", tensor-parallel
+    linear layers): the column-parallel shards and the row-parallel sum against
+    the pinned oracle (which equals dense x @ W), at the page's assert_close
+    tolerance for fp32."""
     x, w = workloads.worked_example()
     p = 4
-    xd = x_rep(x, p, "fp32")
-    y = tsl.column_parallel_linear(xd, col_dtensor(w, p, "fp32"))
-    got = np.concatenate([to_host(t, "fp32") for t in y.slots], axis=-1)
-    dense = x.astype(np.float64) @ w.astype(np.float64)
-    assert got.shape == (3, 12)
-    torch.testing.assert_close(torch.from_numpy(got), torch.from_numpy(dense.astype(np.float32)))
+    cols, rows = chunk_bounds(12, p), chunk_bounds(8, p)
+    x64, w64_ = x.astype(np.float64), w.astype(np.float64)
+    y = tsl.column_parallel_linear(x_rep(x, p, "fp32"), col_dtensor(w, p, "fp32"))
+    expect = olin.column_parallel(x64, [w64_[:, o:o + s] for o, s in cols])
+    assert [t.shape for t in y.slots] == [(3, s) for _, s in cols]
+    for t, e in zip(y.slots, expect):
+        torch.testing.assert_close(torch.from_numpy(to_host(t, "fp32")), torch.from_numpy(e.astype(np.float32)))
     yr = tsl.row_parallel_linear(x_shard(x, p, "fp32"), row_dtensor(w, p, "fp32"), mode=tsl.ALL_REDUCE)
-    torch.testing.assert_close(torch.from_numpy(to_host(yr.slots[0], "fp32")), torch.from_numpy(dense.astype(np.float32)))
+    (er,) = olin.row_parallel([x64[:, o:o + s] for o, s in rows], [w64_[o:o + s] for o, s in rows], None,
+                              olin.ALL_REDUCE)
+    assert yr.slots[0].shape == (3, 12)
+    torch.testing.assert_close(torch.from_numpy(to_host(yr.slots[0], "fp32")), torch.from_numpy(er.astype(np.float32)))
 
 
 # ---------------------------------------------------------------- column parallel
@@ -207,9 +214,10 @@ def test_tp_mlp_small(lib, M, K, F, N, p, mode):
     x, wg, wu, wd = workloads.mlp_inputs(M, K, F, seed_base=600)
     wd = workloads.randn_bf16((F, N), 604, (1.0 / F) ** 0.5)
     xd = x_rep(x, p)
-    ws = torch.empty(tsl.tp_mlp_workspace_bytes(xd, col_dtensor(wg, p)), dtype=torch.uint8, device="cuda")
-    y = tsl.tp_mlp(xd, col_dtensor(wg, p), col_dtensor(wu, p), row_dtensor(wd, p), mode=mode,
-                   out_dtype=torch.float32, workspace=ws)
+    wgd, wud, wdd = col_dtensor(wg, p), col_dtensor(wu, p), row_dtensor(wd, p)
+    y = tsl.tp_mlp_output(xd, wdd, mode=mode, out_dtype=torch.float32)
+    ws = torch.empty(tsl.tp_mlp_workspace_bytes(xd, wgd, wud, wdd, y, mode=mode), dtype=torch.uint8, device="cuda")
+    y = tsl.tp_mlp(xd, wgd, wud, wdd, mode=mode, out=y, workspace=ws)
     torch.cuda.synchronize()
     assert tsl.read_device_status() == 0
     omode = olin.ALL_REDUCE if mode == tsl.ALL_REDUCE else olin.REDUCE_SCATTER

@@ -7,10 +7,13 @@ them in K order and runs the epilogue.  The shapes below have fewer tiles
 than the 76 pairs a GB300 holds and enough K for the split to pay:
 column (bias, ragged M/N/K, fp32 and bf16 outputs), row-parallel in every
 output mode, the gated MLP (gate/up end to end, down on the oracle's H)
-and fused q/k/v.  Also: the
-split result is bit-identical from launch to launch (the partials are
-added in a fixed order and the arrival counters return to zero), two
-streams split concurrently with separate scratch, and the unsplit schedule
+and fused q/k/v.  The scratch is the caller's workspace (the Python API
+takes one of the queried size from torch's allocator): the queries report
+the library's rule, a call without enough workspace runs every tile whole,
+and a split call allocates no device memory.  Also: the split result is
+bit-identical from launch to launch (the partials are added in a fixed
+order and the counters are zeroed before every launch), two streams split
+concurrently with separate workspaces, and the unsplit schedule
 (DT_GEMM_SPLIT=0, in a child process) agrees with the oracle on the same
 shapes.  Tolerances as in the other linear tests (the MLP output: the
 relative Frobenius bound, for the reason its test gives).
@@ -41,7 +44,10 @@ def ceil_div(a, b):
     return -(-a // b)
 
 
-def split_expected(tiles, kiters, dual=False, pairs=76):
+PAIRS = 76  # CTA pairs resident on a GB300 (152 SMs)
+
+
+def split_expected(tiles, kiters, dual=False, pairs=PAIRS):
     """The library's rule: a pair's share of the tail's K iterations plus
     the split's fixed cost (72 iterations) is shorter than a tile, and a
     finishing round's partials fit the epilogue warp's buffer."""
@@ -51,6 +57,29 @@ def split_expected(tiles, kiters, dual=False, pairs=76):
         return False
     np_ = ceil_div(kiters, share_min) + 1
     return np_ * (2 if dual else 1) <= 6 and rem * kiters / pairs + 72 <= kiters
+
+
+def r256(n):
+    return (n + 255) // 256 * 256
+
+
+def split_bytes(tiles, kiters, dual=False, pairs=PAIRS):
+    """Workspace of one split launch: an fp32 [2, 128, 256] partial per piece
+    (the tail tiles plus one per pair boundary inside the tail) and 8
+    counters per tail tile, each region 256-byte aligned."""
+    if not split_expected(tiles, kiters, dual, pairs):
+        return 0
+    rem = tiles % pairs
+    return r256((rem + pairs - 1) * 2 * 128 * 256 * 4) + r256(8 * rem * 4)
+
+
+def device_pairs():
+    return torch.cuda.get_device_properties(0).multi_processor_count // 2
+
+
+def no_workspace():
+    """An empty device tensor: its data pointer is NULL, so the call gets no workspace."""
+    return torch.empty(0, dtype=torch.uint8, device="cuda")
 
 
 def column_case(seed=11):
@@ -83,7 +112,7 @@ def test_row_split(lib, mode):
     """ALL_REDUCE and REDUCE_SCATTER split (one group, 4 K segments); the
     PARTIAL launch (one group per shard) is too short to split and runs
     whole, checked all the same."""
-    M, K, N, p = 700, 4 * 2000, 1300, 4
+    M, K, N, p = 700, 4 * 2000, 1304, 4  # 1304 = 5 x 256 + 24: ragged, with a TMA-compatible pitch
     tiles = ceil_div(M, 256) * ceil_div(N, 256) * (p if mode == tsl.PARTIAL else 1)
     kiters = ceil_div(K // p, 64) * (1 if mode == tsl.PARTIAL else p)
     assert split_expected(tiles, kiters) == (mode != tsl.PARTIAL)
@@ -119,9 +148,10 @@ def test_mlp_split(lib):
     x, wg, wu, wd = workloads.mlp_inputs(M, K, F, seed_base=700)
     wd = workloads.randn_bf16((F, N), 704, (1.0 / F) ** 0.5)
     xd = x_rep(x, p)
-    ws = torch.empty(tsl.tp_mlp_workspace_bytes(xd, col_dtensor(wg, p)), dtype=torch.uint8, device="cuda")
-    y = tsl.tp_mlp(xd, col_dtensor(wg, p), col_dtensor(wu, p), row_dtensor(wd, p), mode=tsl.ALL_REDUCE,
-                   out_dtype=torch.float32, workspace=ws)
+    wgd, wud, wdd = col_dtensor(wg, p), col_dtensor(wu, p), row_dtensor(wd, p)
+    y = tsl.tp_mlp_output(xd, wdd, mode=tsl.ALL_REDUCE, out_dtype=torch.float32)
+    ws = torch.empty(tsl.tp_mlp_workspace_bytes(xd, wgd, wud, wdd, y), dtype=torch.uint8, device="cuda")
+    y = tsl.tp_mlp(xd, wgd, wud, wdd, mode=tsl.ALL_REDUCE, out=y, workspace=ws)
     torch.cuda.synchronize()
     assert tsl.read_device_status() == 0
     cols = chunk_bounds(F, p)
@@ -168,8 +198,8 @@ def test_qkv_split(lib):
 
 
 def test_split_is_deterministic(lib):
-    """Ten launches of one split GEMM give the same bits: fixed summation
-    order, and every launch leaves the arrival counters at zero."""
+    """Ten launches of one split GEMM (one workspace) give the same bits:
+    fixed summation order, and the counters are zeroed before every launch."""
     xd, wd, bd, expect = column_case(seed=21)
     out = tsl.column_parallel_linear(xd, wd, bd, out_dtype=torch.float32)
     first = [t.clone() for t in out.slots]
@@ -184,7 +214,7 @@ def test_split_is_deterministic(lib):
 
 
 def test_split_on_two_streams(lib):
-    """Two streams run split GEMMs at the same time, each with its own scratch."""
+    """Two streams run split GEMMs at the same time, each with its own workspace."""
     cases = [column_case(seed=31), column_case(seed=41)]
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
     outs = []
@@ -201,6 +231,72 @@ def test_split_on_two_streams(lib):
     for (_, _, _, expect), o in zip(cases, outs):
         for i, e in enumerate(expect):
             check_fp32(to_host(o.slots[i], "fp32"), e, f"shard {i}")
+
+
+def test_workspace_queries_follow_the_rule(lib):
+    """The size queries report the split rule's bytes (0 where a launch
+    does not split), and the MLP's query adds H's 256-byte aligned blocks."""
+    pairs = device_pairs()
+    xd, wd, _, _ = column_case()
+    ys = [tsl.DTensor.empty(xd.mesh, [tsl.Shard(1)], (300, wd.gshape[1]), torch.float32)]
+    assert tsl.column_parallel_linear_workspace_bytes(xd, [wd], ys) == split_bytes(2 * 4 * 3, 188, pairs=pairs)
+    M, K, N, p = 700, 4 * 2000, 1304, 4  # 1304 = 5 x 256 + 24: ragged, with a TMA-compatible pitch
+    xr, wr = x_shard(workloads.randn_bf16((M, K), 41), p), row_dtensor(workloads.randn_bf16((K, N), 42), p)
+    for mode, tiles, kiters in ((tsl.ALL_REDUCE, 3 * 6, 4 * 32), (tsl.REDUCE_SCATTER, 3 * 6, 4 * 32),
+                                (tsl.PARTIAL, 4 * 3 * 6, 32)):
+        y = tsl.api._row_out(xr, wr, 0, mode, torch.float32)
+        assert tsl.row_parallel_linear_workspace_bytes(xr, wr, y, mode) == split_bytes(tiles, kiters, pairs=pairs), mode
+    M, K, F, N, p = 256, 10000, 8 * 600, 384, 8
+    x, wg, wu, _ = workloads.mlp_inputs(M, K, F, seed_base=700)
+    wd = workloads.randn_bf16((F, N), 704, (1.0 / F) ** 0.5)
+    xm, wgd, wud, wdd = x_rep(x, p), col_dtensor(wg, p), col_dtensor(wu, p), row_dtensor(wd, p)
+    y = tsl.tp_mlp_output(xm, wdd)
+    h_bytes = r256(M * F * 2)
+    up = split_bytes(p * ceil_div(F // p, 128), ceil_div(K, 64), dual=True, pairs=pairs)
+    down = split_bytes(ceil_div(N, 256), p * ceil_div(F // p, 64), pairs=pairs)
+    assert tsl.tp_mlp_workspace_bytes(xm, wgd, wud, wdd, y) == h_bytes + max(up, down)
+
+
+def test_split_needs_the_workspace(lib):
+    """No workspace, or one 256 bytes short: every tile whole (both give the
+    same bits, within tolerance); the queried size: the split schedule,
+    whose fp32 sums run in another order, so some output bits differ."""
+    xd, wd, bd, expect = column_case(seed=51)
+    need = tsl.column_parallel_linear_workspace_bytes(xd, [wd], [tsl.api._col_out(xd, wd, 0, torch.float32)])
+    assert need > 0
+    runs = {}
+    for name, ws in (("none", no_workspace()),
+                     ("short", torch.empty(need - 256, dtype=torch.uint8, device="cuda")),
+                     ("full", torch.empty(need, dtype=torch.uint8, device="cuda"))):
+        runs[name] = tsl.column_parallel_linear(xd, wd, bd, out_dtype=torch.float32, workspace=ws)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    for name, y in runs.items():
+        for i, e in enumerate(expect):
+            check_fp32(to_host(y.slots[i], "fp32"), e, f"{name} shard {i}")
+    assert all(torch.equal(a, b) for a, b in zip(runs["none"].slots, runs["short"].slots))
+    assert not all(torch.equal(a, b) for a, b in zip(runs["none"].slots, runs["full"].slots))
+
+
+def test_split_call_allocates_nothing(lib):
+    """With the caller's workspace, a split launch on a stream the library
+    has never seen leaves the device's free memory unchanged."""
+    xd, wd, bd, expect = column_case(seed=61)
+    y = tsl.api._col_out(xd, wd, 0, torch.float32)
+    ws = torch.empty(tsl.column_parallel_linear_workspace_bytes(xd, [wd], [y]), dtype=torch.uint8, device="cuda")
+    tsl.column_parallel_linear(xd, wd, bd, out=y, workspace=ws)  # loads the kernels, plans, encodes descriptors
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            tsl.column_parallel_linear(xd, wd, bd, out=y, workspace=ws)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    assert tsl.read_device_status() == 0
+    for i, e in enumerate(expect):
+        check_fp32(to_host(y.slots[i], "fp32"), e, f"shard {i}")
 
 
 CHILD = r"""
