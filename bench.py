@@ -605,6 +605,26 @@ class Extras:
         self._keep5 = outs32
         self.items.append(("q/k/v, fp32 outputs", "flops", qkv_flops,
                            lambda: tsl.column_parallel_linear_multi(x_rep, ws, outs=outs32)))
+        # an unevenly split weight: [4096, 8190] over 4 leaves a 2046-column
+        # shard whose 4092-byte pitch TMA cannot read.  With the queried
+        # workspace it is copied to a padded pitch (tensor cores); with none
+        # the launch runs on the CUDA-core kernel
+        Nu = 8190
+        wu_bits = W.randn_bf16((H, Nu), 995, 1.0 / 64)
+        step = -(-Nu // P)
+        ucols = [(o, min(step, Nu - o)) for o in range(0, Nu, step)]
+        wun = DTensor([dev(np.ascontiguousarray(wu_bits[:, o:o + s])) for o, s in ucols], mesh, [tsl.Shard(1)],
+                      (H, Nu), bf)
+        yun = DTensor.empty(mesh, [tsl.Shard(1)], (T, Nu), bf, device=device)
+        wsu = torch.empty(tsl.column_parallel_linear_workspace_bytes(x_rep, [wun], [yun]), dtype=torch.uint8,
+                          device=device)
+        no_ws = torch.empty(0, dtype=torch.uint8, device=device)
+        self._keep6 = (wun, yun, wsu, no_ws)
+        self.items.append(("column linear, uneven shards [8192,4096]x[4096,8190]/4, padded in the workspace", "flops",
+                           2 * T * H * Nu,
+                           lambda: tsl.column_parallel_linear(x_rep, wun, out=yun, workspace=wsu)))
+        self.items.append(("column linear, uneven shards, no workspace (CUDA-core kernel)", "flops", 2 * T * H * Nu,
+                           lambda: tsl.column_parallel_linear(x_rep, wun, out=yun, workspace=no_ws)))
 
     def measure(self, steps, peaks):
         for _, _, _, fn in self.items:  # warm up every item (descriptor caches, first launches)
@@ -866,7 +886,8 @@ def oracle_inputs():
 def oracle_sample(inp, fraction: float):
     """Run the oracle on `fraction` of every component of one step.
 
-    Returns (seconds spent in the oracle, algorithmic work of the sample)."""
+    Returns (seconds spent in the oracle, algorithmic work of the sample,
+    per component {"seconds", "work", "kind"})."""
     from oracle import bf16 as ob
     from oracle import linear as olin
     from oracle import placement as opl
@@ -876,12 +897,21 @@ def oracle_sample(inp, fraction: float):
 
     work = {"flops": 0.0, "bytes": 0.0}
     t_total = 0.0
+    per = {}
+
+    def note(name, kind, secs, amount):
+        c = per.setdefault(name, {"seconds": 0.0, "work": 0.0, "kind": kind})
+        c["seconds"] += secs
+        c["work"] += amount
+
     # embedding: the first tokens
     ntok = max(1, int(16384 * fraction))
     t = time.perf_counter()
     oemb(inp["ids"][:ntok], inp["emb_shards"], 4096)
-    t_total += time.perf_counter() - t
+    dt_ = time.perf_counter() - t
+    t_total += dt_
     work["bytes"] += EMB_BYTES * ntok / 16384
+    note("embedding", "bytes", dt_, EMB_BYTES * ntok / 16384)
     # redistribute: the same transitions on the first rows of each tensor
     for gshape, G, g_full in inp["red"]:
         rows = max(8, int(gshape[0] * fraction))
@@ -895,8 +925,10 @@ def oracle_sample(inp, fraction: float):
         for _, a, b in transitions():
             t = time.perf_counter()
             ord_.redistribute(srcs[a], lays[a], lays[b], "bf16")
-            t_total += time.perf_counter() - t
+            dt_ = time.perf_counter() - t
+            t_total += dt_
             work["bytes"] += (5 if a == "S0P" else 2) * G * rows / gshape[0]
+            note("redistribute sweep", "bytes", dt_, (5 if a == "S0P" else 2) * G * rows / gshape[0])
     # MLP rows
     x, wg, wu, wd = inp["mlp"]
     rows = max(1, int(4096 * fraction))
@@ -904,8 +936,10 @@ def oracle_sample(inp, fraction: float):
     t = time.perf_counter()
     olin.tp_mlp(ob.widen64(x[:rows]), [ob.widen64(wg[:, o:o + s]) for o, s in cols],
                 [ob.widen64(wu[:, o:o + s]) for o, s in cols], [ob.widen64(wd[o:o + s]) for o, s in cols])
-    t_total += time.perf_counter() - t
+    dt_ = time.perf_counter() - t
+    t_total += dt_
     work["flops"] += MLP_FLOPS * rows / 4096
+    note("tp_mlp", "flops", dt_, MLP_FLOPS * rows / 4096)
     # attention rows
     x, wq, wk, wv, wo = inp["attn"]
     rows = max(1, int(8192 * fraction))
@@ -914,9 +948,11 @@ def oracle_sample(inp, fraction: float):
     olin.attention_projections(ob.widen64(x[:rows]), *[[ob.widen64(w[:, o:o + s]) for o, s in cols]
                                                         for w in (wq, wk, wv)],
                                [ob.widen64(wo[o:o + s]) for o, s in cols], olin.ALL_REDUCE)
-    t_total += time.perf_counter() - t
+    dt_ = time.perf_counter() - t
+    t_total += dt_
     work["flops"] += ATTN_FLOPS * rows / 8192
-    return t_total, work
+    note("attention", "flops", dt_, ATTN_FLOPS * rows / 8192)
+    return t_total, work, per
 
 
 def cpu_cores():
@@ -927,10 +963,16 @@ def cpu_cores():
 
 
 def cpu_baseline(peaks, fraction):
-    secs, work = oracle_sample(oracle_inputs(), fraction)
+    secs, work, per = oracle_sample(oracle_inputs(), fraction)
     roof = work["flops"] / (peaks["bf16_tflops"] * 1e12) + work["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    comps = {}
+    for name, c in per.items():  # each component's own rate, in the GPU rows' units
+        rate = c["work"] / max(c["seconds"], 1e-9)
+        comps[name] = ({"seconds": round(c["seconds"], 3), "achieved": round(rate / 1e12, 4), "unit": "TFLOP/s"}
+                       if c["kind"] == "flops" else
+                       {"seconds": round(c["seconds"], 3), "achieved": round(rate / 1e9, 3), "unit": "GB/s"})
     return {"value": round(100.0 * roof / secs, 6), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "seconds": round(secs, 3),
+            "seconds": round(secs, 3), "components": comps,
             "sample": f"{fraction:.4g} of every component of one step: the first {fraction:.4g} of the tokens / "
                       f"rows of the embedding, the 16 redistribute transitions, the MLP and the attention "
                       f"projections (numpy fp64 matmul, in-order fp32 partial sums)"}
@@ -948,7 +990,7 @@ def run_reference(args):
     secs_total = 0.0
     roof = 0.0
     for _ in range(args.steps):
-        secs, work = oracle_sample(inp, fraction)
+        secs, work, _ = oracle_sample(inp, fraction)
         secs_total += secs
         roof += work["flops"] / (peaks["bf16_tflops"] * 1e12) + work["bytes"] / (peaks["hbm_gbs"] * 1e9)
     value = round(100.0 * roof / secs_total, 6)
@@ -1024,6 +1066,67 @@ def run_cublas_shapes(args):
                       "l2": "256 MB written before every call"}), flush=True)
 
 
+def run_profile_case(args):
+    """One kernel of the step on its own, `--steps` calls after `--warmup`
+    (for ncu captures; prints no bench line).  Cases: `mlp_down` (the TP
+    MLP's down projection: H [4096, 11008] Shard(-1) over 8, Wd Shard(0),
+    ALL_REDUCE, split tail in its workspace), `qkv`, `o`, and
+    `rd:<transition>:<shape>` (one redistribute of the sweep, e.g.
+    `rd:S1->S0:8191x8190`).  GEMM inputs are random device tensors of the
+    step's shapes; redistribute inputs are the step's own."""
+    import tensor_sharded_linear_gb300 as tsl
+    from tensor_sharded_linear_gb300 import build as B
+    B.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    bf = torch.bfloat16
+    g = torch.Generator(device=dev).manual_seed(1)
+
+    def rnd(*shape, std=1.0):
+        return (torch.randn(*shape, device=dev, generator=g) * std).to(bf)
+
+    S0, S1, R = tsl.Shard(0), tsl.Shard(1), tsl.Replicate()
+    case = args.profile_case
+    if case == "mlp_down":
+        m8 = tsl.DeviceMesh((8,), ("tp",))
+        h = tsl.DTensor([rnd(4096, 1376) for _ in range(8)], m8, [S1], (4096, 11008), bf)
+        wd = tsl.DTensor([rnd(1376, 4096, std=0.0095) for _ in range(8)], m8, [S0], (11008, 4096), bf)
+        y = tsl.DTensor.empty(m8, [R], (4096, 4096), bf)
+        ws = torch.empty(max(1, tsl.row_parallel_linear_workspace_bytes(h, wd, y)), dtype=torch.uint8, device=dev)
+        fn = lambda: tsl.row_parallel_linear(h, wd, out=y, workspace=ws)  # noqa: E731
+    elif case in ("qkv", "o"):
+        m4 = tsl.DeviceMesh((4,), ("tp",))
+        x = tsl.DTensor([rnd(8192, 4096)], m4, [R], (8192, 4096), bf)
+        wq = [tsl.DTensor([rnd(4096, 1024, std=1 / 64) for _ in range(4)], m4, [S1], (4096, 4096), bf)
+              for _ in range(3)]
+        qkv = [tsl.DTensor.empty(m4, [S1], (8192, 4096), bf) for _ in range(3)]
+        wo = tsl.DTensor([rnd(1024, 4096, std=1 / 64) for _ in range(4)], m4, [S0], (4096, 4096), bf)
+        od = tsl.DTensor.empty(m4, [S0], (8192, 4096), bf)
+        none = torch.empty(0, dtype=torch.uint8, device=dev)
+        tsl.column_parallel_linear_multi(x, wq, outs=qkv, workspace=none)
+        if case == "qkv":
+            fn = lambda: tsl.column_parallel_linear_multi(x, wq, outs=qkv, workspace=none)  # noqa: E731
+        else:
+            fn = lambda: tsl.row_parallel_linear(qkv[0], wo, mode=tsl.REDUCE_SCATTER, out=od, workspace=none)  # noqa
+    elif case.startswith("rd:"):
+        _, name, shape = case.split(":")
+        blk = Block(dev, only=("redistribute",))
+        tag = f"redistribute {name} {shape}"
+        hits = [(a, b) for n, _, a, b in blk.sweep if n == tag]
+        if not hits:
+            raise SystemExit(f"no sweep transition {tag!r}")
+        a, b = hits[0]
+        fn = lambda: tsl.redistribute(a, b)  # noqa: E731
+    else:
+        raise SystemExit(f"unknown --profile-case {case!r}")
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    if tsl.read_device_status() != 0:
+        raise SystemExit("device status set")
+    print(f"profile case {case}: {args.warmup} + {args.steps} calls", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -1037,10 +1140,14 @@ def main():
                     help="time cuBLAS on the step's dense GEMM shapes (library context) and exit")
     ap.add_argument("--only", default=ALL_COMPONENTS,
                     help="comma-separated subset of embedding,redistribute,mlp,attention (profiling)")
+    ap.add_argument("--profile-case", default=None,
+                    help="run one kernel of the step alone for a profiler and exit (see run_profile_case)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.cublas_shapes:
+    if args.profile_case:
+        run_profile_case(args)
+    elif args.cublas_shapes:
         run_cublas_shapes(args)
     elif args.impl == "reference":
         run_reference(args)

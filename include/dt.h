@@ -233,8 +233,15 @@ DT_API dt_status dt_tp_embedding(const dt_dtensor* ids, const dt_dtensor* table,
  * operands (host descriptors only, nothing is read from the device), check
  * them as the call would, and answer for the CURRENT device, whose number
  * of co-resident CTA pairs decides the split; without a CUDA device they
- * return DT_ERR_CUDA.  A call that runs on the CUDA-core kernel (fp32, or
- * bf16 pitches TMA cannot describe) needs no workspace (0 bytes).
+ * return DT_ERR_CUDA.
+ * bf16 operands whose row pitch is not a multiple of 16 bytes, or whose base
+ * is not 16-byte aligned (the shards of a dim that torch.chunk splits
+ * unevenly, e.g. 8190 columns over 4), cannot be read by TMA.  With enough
+ * workspace (the query counts it) the call copies each such operand into
+ * the workspace with a padded pitch and runs on the tensor cores; with less
+ * it runs on a CUDA-core kernel, an order of magnitude slower, and
+ * dt_cuda_core_gemm_count() counts the launch.  fp32 linears always run on
+ * the CUDA-core kernel and need no workspace (0 bytes).
  */
 
 /*
@@ -247,9 +254,9 @@ DT_API dt_status dt_tp_embedding(const dt_dtensor* ids, const dt_dtensor* table,
  * On other mesh dims w and bias must be Replicate and x, y must agree.
  * tp_mesh_dim < 0 means no TP (ReplicateParallelLinear).  Leading dims of x
  * and y are flattened and must be collapsible with unit inner stride.
- * bf16 operands run on the tcgen05 tensor-core GEMM when row pitches are
- * multiples of 16 bytes and bases 16-byte aligned; other shapes and fp32 run
- * on a CUDA-core kernel (counted by dt_cuda_core_gemm_count()).
+ * bf16 operands run on the tcgen05 tensor-core GEMM (operands whose pitch
+ * TMA cannot describe through a padded copy in the workspace, see above);
+ * fp32 runs on a CUDA-core kernel.
  */
 DT_API dt_status dt_column_parallel_linear(const dt_dtensor* x, const dt_dtensor* w, const dt_dtensor* bias,
                                     const dt_dtensor* y, int32_t tp_mesh_dim, void* workspace,

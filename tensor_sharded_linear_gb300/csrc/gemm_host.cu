@@ -20,15 +20,25 @@
 namespace dt {
 namespace gemm {
 
+// A bf16 matrix copied into the workspace with a row pitch TMA can describe.
+struct PitchCopy {
+  char* dst;
+  const char* src;
+  int64_t dst_ld, src_ld, rows, cols;  // elements
+  int grid_x, grid_y;
+};
+
 // One recorded step of a call: a GEMM launch (kind 0: tcgen05 pair kernel,
-// 2: CUDA-core kernel) with its exact parameter block, or (kind 3) the
-// zeroing of split-tail counters that precedes a split launch.
+// 2: CUDA-core kernel) with its exact parameter block, (kind 3) the zeroing
+// of split-tail counters that precedes a split launch, or (kind 4) the copy
+// of an operand into a TMA-compatible pitch.
 struct GemmLaunch {
   int kind = 0;
   int grid = 0;
   std::shared_ptr<void> params;  // a heap Params (keeps its 128-byte alignment) or SParams
   void* zero_ptr = nullptr;
   size_t zero_bytes = 0;
+  PitchCopy pc{};
 };
 struct GemmRecord {
   std::vector<GemmLaunch> launches;
@@ -223,6 +233,37 @@ __global__ void __launch_bounds__(S_THREADS) simt_gemm_kernel(const __grid_const
   }
 }
 
+// ------------------------------------------------------------ pitch copies
+
+// Copy a [rows, cols] bf16 matrix (any element-aligned base and pitch) to a
+// destination whose base is 16-byte aligned and whose pitch is a multiple of
+// 8 elements: thread x of the row grid moves elements [8x, 8x + 8) of rows
+// blockIdx.y, blockIdx.y + gridDim.y, ...; reads are element-wise (the
+// source may sit at any alignment), writes whole 16-byte vectors.
+__global__ void __launch_bounds__(256) pitch_copy_kernel(PitchCopy c) {
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t c0 = g * 8;
+  if (c0 >= c.cols) return;
+  const int n = c.cols - c0 < 8 ? static_cast<int>(c.cols - c0) : 8;
+  for (int64_t r = blockIdx.y; r < c.rows; r += gridDim.y) {
+    const uint16_t* s = reinterpret_cast<const uint16_t*>(c.src) + r * c.src_ld + c0;
+    uint16_t* d = reinterpret_cast<uint16_t*>(c.dst) + r * c.dst_ld + c0;
+    if (n == 8) {
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) w[k] = static_cast<uint32_t>(s[2 * k]) | (static_cast<uint32_t>(s[2 * k + 1]) << 16);
+      *reinterpret_cast<uint4*>(d) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      for (int k = 0; k < n; ++k) d[k] = s[k];
+    }
+  }
+}
+
+cudaError_t launch_pitch_copy(const PitchCopy& c, cudaStream_t stream) {
+  pitch_copy_kernel<<<dim3(c.grid_x, c.grid_y), 256, 0, stream>>>(c);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------ lowering
 
 bool out_vec_ok(const HostGroup& g) {
@@ -293,22 +334,6 @@ bool bands_override(int* m, int* n) {
   *m = vm;
   *n = vn;
   return vm > 0;
-}
-
-int l2_bytes() {
-  static int cached[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (!cached[dev]) {
-    int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess || v <= 0) {
-      cudaGetLastError();
-      v = 96 << 20;
-    }
-    cached[dev] = v;
-  }
-  return cached[dev];
 }
 
 // ---- launch packing
@@ -433,57 +458,17 @@ size_t split_bytes(const SplitPlan& sp) {
 
 // ---- tile order
 
-// Estimated DRAM bytes of the operand panels of one launch in the order
-// (band_m, band_n).  Model: clusters take tiles round-robin, so tiles
-// [w C, (w + 1) C) run together as wave w and stream their K range in
-// lockstep; a wave reads each distinct A panel (an M tile's rows over all
-// of K) and B panel (an N tile's columns) once.  A panel the previous wave
-// also read is found in L2 at the points of K where the bytes streamed
-// since its last use -- about (1 - f) of the previous wave's panels plus f
-// of this wave's, f the fraction of K done -- stay within the L2.
-double order_traffic(int tiles, int ctas, int m_tiles, int total_n, const std::vector<int>& a_of_n, int n_a,
-                     double a_bytes, double b_bytes, double l2, int band_m, int band_n) {
-  std::vector<int> seen_a((size_t)n_a * m_tiles, -1), seen_b(total_n, -1);
-  std::vector<int> prev_a((size_t)n_a * m_tiles, -1), prev_b(total_n, -1);
-  double total = 0, prev_size = 0;
-  for (int w = 0; w * ctas < tiles; ++w) {
-    const int t0 = w * ctas, t1 = std::min(tiles, t0 + ctas);
-    double size = 0, shared = 0;
-    for (int t = t0; t < t1; ++t) {
-      int mi, jn;
-      band_order(t, m_tiles, total_n, band_m, band_n, &mi, &jn);
-      const size_t ka = (size_t)a_of_n[jn] * m_tiles + mi;
-      if (seen_a[ka] != w) {
-        if (seen_a[ka] == w - 1 && w > 0) shared += a_bytes;
-        prev_a[ka] = seen_a[ka];
-        seen_a[ka] = w;
-        size += a_bytes;
-      }
-      if (seen_b[jn] != w) {
-        if (seen_b[jn] == w - 1 && w > 0) shared += b_bytes;
-        prev_b[jn] = seen_b[jn];
-        seen_b[jn] = w;
-        size += b_bytes;
-      }
-    }
-    double hit = 0;  // fraction of K over which the shared panels are still in L2
-    if (w > 0) {
-      const double a = prev_size, b = size;
-      if (a <= l2 && b <= l2) hit = 1;
-      else if (a > l2 && b > l2) hit = 0;
-      else if (a <= l2) hit = (l2 - a) / (b - a);
-      else hit = (l2 - b) / (a - b);
-    }
-    total += size - shared * hit;
-    prev_size = size;
-  }
-  return total;
-}
-
-// Band height and block width of a launch with common M tiles.  The default
-// bands are a quarter of L2 of A rows, at least one wave high; the modelled
-// traffic of every other (band_m, band_n) is compared with it and a clearly
-// cheaper order (2% or more) wins.
+// Band height and block width of a launch with common M tiles: bands whose
+// A rows take about a quarter of L2, at least one wave high, each sweeping
+// every N tile (band_n = total_n) in snake order; for long K (8192 and more,
+// where one tile's A rows or B columns pass 4 MB) blocks of 8 M x 4 N tiles.
+// Measured on GB300 with DT_GEMM_BANDS over 13 orders (blocks of 1..32 M
+// tiles by 1..48 N tiles): the fused q/k/v ran fastest with 16-tile bands
+// and lost 4-10% with 32-tile or 1-tile bands; the o projection gained 2.5%
+// with 1-tile bands; the MLP down projection (K = 11008) moved by about 1%
+// whatever the order, but 8 x 4 blocks cut its DRAM reads from 520 to 401 MB
+// (ncu), so long-K launches take them.  No simple traffic model ranked the
+// orders' times correctly.
 void choose_bands(const std::vector<HostGroup>& groups, size_t b, size_t e, const LaunchShape& s, int ctas,
                   int* band_m, int* band_n) {
   *band_m = 1;
@@ -498,56 +483,14 @@ void choose_bands(const std::vector<HostGroup>& groups, size_t b, size_t e, cons
   int64_t max_k = 0;
   for (size_t g = b; g < e; ++g) max_k = std::max<int64_t>(max_k, (int64_t)group_kiters(groups[g]) * BK);
   const int64_t a_tile_bytes = (int64_t)PAIR_TILE_M * std::max<int64_t>(max_k, 1) * 2;
+  if (max_k >= 8192) {
+    *band_m = std::min(8, s.m_tiles);
+    *band_n = std::min(4, *band_n);
+    return;
+  }
   int band = (int)std::max<int64_t>(1, (32ll << 20) / a_tile_bytes);
   band = std::max(band, (ctas + s.total_n - 1) / s.total_n);
   *band_m = std::max(1, std::min(band, s.m_tiles));
-  if (ctas <= 0 || s.tiles <= ctas) return;
-  // A panels: one per distinct A matrix (groups sharing x share them) and M tile
-  std::vector<int> a_of_n;
-  std::vector<uintptr_t> a_ids;
-  for (size_t g = b; g < e; ++g) {
-    const HostGroup& G = groups[g];
-    const uintptr_t id = G.segs.empty() ? 0 : reinterpret_cast<uintptr_t>(G.segs[0].a.ptr);
-    int ai = -1;
-    for (size_t i = 0; i < a_ids.size(); ++i)
-      if (a_ids[i] == id) ai = (int)i;
-    if (ai < 0) {
-      ai = (int)a_ids.size();
-      a_ids.push_back(id);
-    }
-    const int nt = (int)((G.n + group_bn(G) - 1) / group_bn(G));
-    for (int j = 0; j < nt; ++j) a_of_n.push_back(ai);
-  }
-  const double a_bytes = (double)PAIR_TILE_M * max_k * 2, b_bytes = (double)BN_MAX * max_k * 2;
-  const double l2 = 0.8 * l2_bytes();
-  auto cost = [&](int bm, int bn) {
-    return order_traffic(s.tiles, ctas, s.m_tiles, s.total_n, a_of_n, (int)a_ids.size(), a_bytes, b_bytes, l2, bm, bn);
-  };
-  // candidate sizes: every value up to 16, then a coarser ladder
-  auto ladder = [](int n) {
-    std::vector<int> v;
-    for (int i = 1; i <= std::min(n, 16); ++i) v.push_back(i);
-    for (int i : {20, 24, 28, 32, 40, 48, 64, 80, 96, 128, 192, 256})
-      if (i < n) v.push_back(i);
-    if (n > 16) v.push_back(n);
-    return v;
-  };
-  double best = cost(*band_m, *band_n);
-  const double base = best;
-  int bm_best = *band_m, bn_best = *band_n;
-  for (int bm : ladder(s.m_tiles))
-    for (int bn : ladder(s.total_n)) {
-      const double c = cost(bm, bn);
-      if (c < best - 1e-6) {
-        best = c;
-        bm_best = bm;
-        bn_best = bn;
-      }
-    }
-  if (best <= 0.98 * base) {
-    *band_m = bm_best;
-    *band_n = bn_best;
-  }
 }
 
 // ---- launches
@@ -789,12 +732,98 @@ dt_status check_limits(const std::vector<HostGroup>& live) {
 
 }  // namespace
 
+namespace {
+
+// Operands TMA cannot describe (bf16 with a row pitch that is not a multiple
+// of 16 bytes, or a base that is not 16-byte aligned: the shards of a dim
+// torch.chunk splits unevenly), each given a copy in the workspace.
+struct PadPlan {
+  std::vector<PitchCopy> copies;
+  size_t bytes = 0;  // the copies' share of the workspace (each 256-byte aligned)
+  bool possible = true;  // every group could run on the tensor cores after padding
+};
+
+PadPlan plan_padding(std::vector<HostGroup>& live, char* base) {
+  PadPlan pp;
+  std::vector<std::pair<MapKey, Mat>> done;  // stored matrix -> its padded copy
+  auto pad = [&](Mat& m) {
+    if (tma_ok(m)) return;
+    const Mat st = stored(m);
+    if (st.dtype != DT_BF16 || st.rows <= 0 || st.cols <= 0 || st.ld < st.cols) {
+      pp.possible = false;
+      return;
+    }
+    const MapKey k = key_of(st, 0);
+    for (const auto& e : done)
+      if (e.first == k) {
+        m.ptr = e.second.ptr;
+        m.ld = e.second.ld;
+        return;
+      }
+    PitchCopy c{};
+    c.src = st.ptr;
+    c.src_ld = st.ld;
+    c.rows = st.rows;
+    c.cols = st.cols;
+    c.dst_ld = (st.cols + 7) & ~int64_t(7);
+    c.dst = base + pp.bytes;
+    pp.bytes += round256((size_t)c.rows * (size_t)c.dst_ld * 2);
+    const int64_t gx = (st.cols + 8 * 256 - 1) / (8 * 256);
+    c.grid_x = (int)gx;
+    c.grid_y = (int)std::max<int64_t>(1, std::min<int64_t>(st.rows, std::max<int64_t>(1, 4096 / gx)));
+    pp.copies.push_back(c);
+    Mat padded = m;
+    padded.ptr = c.dst;
+    padded.ld = c.dst_ld;
+    done.push_back({k, padded});
+    m.ptr = c.dst;
+    m.ld = c.dst_ld;
+  };
+  for (auto& g : live) {
+    for (auto& sg : g.segs) {
+      if (sg.a.kmajor) pp.possible = false;
+      pad(sg.a);
+      pad(sg.b);
+      if (g.dual) pad(sg.b2);
+      if (sg.b.kmajor != g.segs[0].b.kmajor || (g.dual && sg.b2.kmajor != sg.b.kmajor)) pp.possible = false;
+    }
+    if (g.segs.empty()) pp.possible = false;
+  }
+  return pp;
+}
+
+}  // namespace
+
 dt_status run_groups(std::vector<HostGroup>& groups, int32_t* d_status, cudaStream_t stream, Workspace ws) {
   std::vector<HostGroup> live = live_groups(groups);
   if (live.empty()) return DT_OK;
   dt_status st = check_limits(live);
   if (st != DT_OK) return st;
-  if (tensor_core_ok(live)) {
+  bool tc = tensor_core_ok(live);
+  if (!tc && ws.ptr) {
+    // bf16 operands with pitches TMA cannot describe: copy them into the
+    // workspace with one it can, when the workspace holds the copies
+    std::vector<HostGroup> padded = live;
+    const PadPlan pp = plan_padding(padded, ws.ptr);
+    if (pp.possible && pp.bytes <= ws.bytes && tensor_core_ok(padded)) {
+      for (const PitchCopy& c : pp.copies) {
+        cudaError_t e = launch_pitch_copy(c, stream);
+        if (e != cudaSuccess) return fail(DT_ERR_CUDA, "operand copy: %s", cudaGetErrorString(e));
+        count_launch();
+        if (g_grec) {
+          GemmLaunch l;
+          l.kind = 4;
+          l.pc = c;
+          g_grec->launches.push_back(l);
+        }
+      }
+      live.swap(padded);
+      ws.ptr += pp.bytes;
+      ws.bytes -= pp.bytes;
+      tc = true;
+    }
+  }
+  if (tc) {
     int32_t* status = device_status_word(d_status);
     if (!status) return fail(DT_ERR_CUDA, "no device status word");
     return run_tcgen05(live, status, stream, ws);
@@ -808,7 +837,13 @@ dt_status workspace_bytes(std::vector<HostGroup>& groups, size_t* bytes) {
   if (live.empty()) return DT_OK;
   dt_status st = check_limits(live);
   if (st != DT_OK) return st;
-  if (!tensor_core_ok(live)) return DT_OK;  // the CUDA-core kernel needs no scratch
+  size_t pad_bytes = 0;
+  if (!tensor_core_ok(live)) {
+    // the padded copies, placed from a 256-aligned base (only their sizes matter here)
+    const PadPlan pp = plan_padding(live, reinterpret_cast<char*>(uintptr_t(256)));
+    if (!pp.possible || !tensor_core_ok(live)) return DT_OK;  // the CUDA-core kernel needs no workspace
+    pad_bytes = pp.bytes;
+  }
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
     cudaGetLastError();
@@ -818,8 +853,10 @@ dt_status workspace_bytes(std::vector<HostGroup>& groups, size_t* bytes) {
   if (ctas <= 0) return fail(DT_ERR_CUDA, "the tcgen05 GEMM cannot be launched on device %d", dev);
   std::vector<std::pair<size_t, size_t>> launches;
   if ((st = pack_launches(live, &launches)) != DT_OK) return st;
+  size_t split = 0;
   for (const auto& r : launches)  // launches run one after the other: one scratch serves all
-    *bytes = std::max(*bytes, split_bytes(plan_split(launch_shape(live, r.first, r.second), ctas)));
+    split = std::max(split, split_bytes(plan_split(launch_shape(live, r.first, r.second), ctas)));
+  *bytes = pad_bytes + split;
   return DT_OK;
 }
 
@@ -835,6 +872,12 @@ dt_status replay_gemm(const GemmRecord& r, cudaStream_t stream) {
     if (l.kind == 3) {
       e = cudaMemsetAsync(l.zero_ptr, 0, l.zero_bytes, stream);
       if (e != cudaSuccess) return fail(DT_ERR_CUDA, "zeroing the split-tail counters: %s", cudaGetErrorString(e));
+      continue;
+    }
+    if (l.kind == 4) {
+      e = launch_pitch_copy(l.pc, stream);
+      if (e != cudaSuccess) return fail(DT_ERR_CUDA, "operand copy: %s", cudaGetErrorString(e));
+      count_launch();
       continue;
     }
     if (l.kind == 2) {

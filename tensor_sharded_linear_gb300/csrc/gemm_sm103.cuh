@@ -28,6 +28,7 @@
 
 #include "../../include/dt.h"
 #include "gemm_plan.h"  // Params and its capacities
+#include "ptx_sm103.cuh"
 
 namespace dt {
 namespace gemm {
@@ -39,7 +40,6 @@ constexpr int B_CHUNK_BYTES = 64 * BK * 2;    // 8 KiB: 64 N columns x 64 K rows
 constexpr int TMEM_COLS = 512;                // two 256-column accumulators
 constexpr int GROUP_M = 8;                    // per-group raster: 8 M tiles per band
 constexpr int MAX_OUT = 8;
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
 
 struct Seg {
   int32_t a_map, b_map, b_map2, k_tiles;
@@ -90,63 +90,7 @@ struct ParamsT {  // CUtensorMap carries its own 128-byte alignment
 using ParamsSmall = ParamsT<24, 32, 16>;
 static_assert(sizeof(Params) <= 32000, "GEMM parameter block over the launch limit");
 
-// ---------------------------------------------------------------- PTX helpers
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait for the phase of parity `parity` to complete.  Gives up (and
-// returns false) when another role has raised the CTA's abort flag or after
-// WAIT_LIMIT_NS; the caller then records DT_DEV_ERR_TIMEOUT and unwinds.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned long long limit_ns = WAIT_LIMIT_NS) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  uint32_t spins = 0;
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((++spins & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > limit_ns) return false;
-    }
-  }
-}
+// ---------------------------------------------------------------- tcgen05 helpers
 
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -202,7 +146,7 @@ constexpr int PAIR_STAGES = 6;
 constexpr int PAIR_A_BYTES = BM * BK * 2;           // this CTA's 128 rows of A: 16 KiB
 constexpr int PAIR_B_BYTES = 128 * BK * 2;          // this CTA's 128 columns of B: 16 KiB
 constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
-constexpr int PAIR_BAR_BYTES = 512;  // barriers, flags and (traced builds) timestamps
+constexpr int PAIR_BAR_BYTES = 512;  // barriers and flags
 constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + 1024 + PAIR_BAR_BYTES;
 // Split-tail finishing reuses the operand ring once a CTA's MMAs are all
 // done: each epilogue warp stages pieces' partials in its own quarter of
@@ -213,7 +157,7 @@ constexpr int FIN_BUF_BYTES = FIN_WARP_BYTES / 2;
 constexpr int FIN_CHUNK_BYTES = 32 * 32 * 4;                        // 32 rows x 32 fp32 columns
 constexpr int FIN_MAX_PIECES = FIN_BUF_BYTES / FIN_CHUNK_BYTES;     // 6 (3 for the gated MLP)
 constexpr int PAIR_TILE_M = 2 * BM;                 // rows of one pair tile
-constexpr int PAIR_B_PRODUCER_WARP = 6;             // warps 0..5 as in the single-CTA kernel, plus this
+constexpr int PAIR_B_PRODUCER_WARP = 6;             // after warps 0 (A), 1 (MMA), 2..5 (epilogue)
 constexpr int PAIR_THREADS = 32 * (PAIR_B_PRODUCER_WARP + 1);
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -258,30 +202,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
           smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
-}
-
-// Untiled bulk copy global -> this CTA's shared memory, completion counted
-// on `bar` (addresses 16-byte aligned, size a multiple of 16).
-__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
-  uint64_t g;
-  asm volatile("cvta.to.global.u64 %0, %1;" : "=l"(g) : "l"(gsrc));
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_u32(smem_dst)),
-               "l"(g), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
-
-// Order this thread's earlier generic-proxy shared-memory accesses before
-// later async-proxy ones (a bulk copy overwriting what was just read).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// The same for global memory: generic-proxy stores of split-tail partials
-// before the counter update that publishes them, and, in the finishing
-// thread, the acquired counter before the bulk copies that read them.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // Issued by one warp in EACH CTA of the pair.

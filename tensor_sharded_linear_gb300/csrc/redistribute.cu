@@ -28,6 +28,7 @@
 #include <vector>
 
 #include "dt_internal.h"
+#include "ptx_sm103.cuh"
 
 namespace dt {
 namespace {
@@ -48,6 +49,9 @@ namespace {
 #endif
 #ifndef RD_SUM_CTAS
 #define RD_SUM_CTAS 2
+#endif
+#ifndef RD_BULK_DEFAULT
+#define RD_BULK_DEFAULT 1
 #endif
 
 constexpr int RD_MAX_TASKS = 192;
@@ -81,6 +85,7 @@ struct RdTask {
   int8_t dmap[4];     // slot stride used for each padded position (dims merged on the host)
   int8_t nextra;      // copies: further destination slots receiving the same box
   int8_t extra16;     // 1: every further destination is a multiple of 16 bytes from the first
+  int16_t rows_per_item;  // bulk copies: whole rows per work item (1: one segment of a row)
 };
 
 struct RdRef {
@@ -105,6 +110,7 @@ struct RdParamsT {
   int32_t dtype;  // one dtype, element size and reduce op per launch
   int32_t esize;
   int32_t op;
+  int32_t* status;  // DT_DEV_* bits (the bulk copy kernel's bounded waits)
 };
 using RdParams = RdParamsT<RD_MAX_LAUNCH_SLOTS, RD_MAX_TASKS, RD_MAX_REFS>;
 using RdParamsSmall = RdParamsT<32, 48, 64>;
@@ -166,16 +172,18 @@ __device__ __forceinline__ void copy_vec_realign(uint4* dv, const char* s, int64
   const uint4 z = make_uint4(0, 0, 0, 0);
   for (int64_t base = 0; base < nvec; base += RD_REALIGN_UNROLL * 32) {
     uint4 a[RD_REALIGN_UNROLL], b[RD_REALIGN_UNROLL];
+    // lane 31's next vector (the one its neighbour would hold) is loaded with
+    // the others, so a pass costs one memory round trip, not two
 #pragma unroll
     for (int u = 0; u < RD_REALIGN_UNROLL; ++u) {
       const int64_t j = base + 32 * u + lane;
       a[u] = j <= nvec ? ld_stream(sa + j) : z;
+      b[u] = (lane == 31 && j + 1 <= nvec) ? ld_stream(sa + j + 1) : z;
     }
 #pragma unroll
     for (int u = 0; u < RD_REALIGN_UNROLL; ++u) {
-      const int64_t j = base + 32 * u + lane;
-      b[u] = shfl_down_vec(a[u]);
-      if (lane == 31) b[u] = j + 1 <= nvec ? ld_stream(sa + j + 1) : z;
+      const uint4 next = shfl_down_vec(a[u]);
+      if (lane != 31) b[u] = next;
     }
 #pragma unroll
     for (int u = 0; u < RD_REALIGN_UNROLL; ++u) {
@@ -527,6 +535,173 @@ __global__ void __launch_bounds__(RD_THREADS, SUM ? RD_SUM_CTAS : RD_COPY_CTAS) 
   }
 }
 
+// ---------------------------------------------------------------- bulk (TMA) copies
+//
+// Copies whose every row starts on a 16-byte boundary in source and
+// destination and is a multiple of 16 bytes long (the aligned shapes:
+// Shard <-> Shard / Replicate of [8192, 8192] bf16 and the like) can run
+// entirely on the bulk-copy (TMA) engine: global -> shared memory with
+// cp.async.bulk, completion counted on an mbarrier, then shared -> global
+// with the bulk store, its reads of shared memory tracked by bulk groups.
+// No thread touches the data.  Four pipelines per CTA (lane 0 of warps
+// 0..3), each with RDT_STAGES stages of RDT_STAGE_BYTES, walk disjoint work
+// items: item i of pipeline q of CTA b is q + 4 b + i * 4 G.  A work item is
+// a run of whole rows, or one segment of a longer row, of at most one stage.
+constexpr int RDT_PIPES = 4;
+constexpr int RDT_STAGES = 3;
+constexpr int RDT_STAGE_BYTES = 16384;
+constexpr int RDT_THREADS = 32 * RDT_PIPES;
+constexpr int RDT_SMEM_BYTES = RDT_PIPES * RDT_STAGES * RDT_STAGE_BYTES + RDT_PIPES * RDT_STAGES * 8 + 16;
+constexpr int RDT_LAG = 1;  // a stage is stored this many items after it was loaded
+
+// The rows of work item `it`: task t (advanced from the caller's hint), first
+// row r0, nrows rows, elements [e0, e0 + n) of each.  Bulk launches keep row
+// and item counts below 2^31 (rows of at least 16 bytes in a tensor below
+// 32 GB), so the index arithmetic is 32-bit.
+template <class P>
+__device__ __forceinline__ void rdt_item(const P& p, int64_t it, int* t, uint32_t* r0, int* nrows, int64_t* e0,
+                                         int64_t* n) {
+  while (*t + 1 < p.ntasks && p.task[*t + 1].item_begin <= it) ++*t;
+  const RdTask& T = p.task[*t];
+  const uint32_t local = static_cast<uint32_t>(it - T.item_begin);
+  if (T.rows_per_item > 1) {
+    const uint32_t rows = static_cast<uint32_t>(T.ext[0] * T.ext[1] * T.ext[2]);
+    *r0 = local * static_cast<uint32_t>(T.rows_per_item);
+    *nrows = static_cast<int>(min(static_cast<uint32_t>(T.rows_per_item), rows - *r0));
+    *e0 = 0;
+    *n = T.ext[3];
+  } else {
+    const uint32_t spr = static_cast<uint32_t>(T.segs_per_row);
+    *r0 = local / spr;
+    *nrows = 1;
+    *e0 = static_cast<int64_t>(local - *r0 * spr) * T.seg_elems;
+    *n = min(T.ext[3] - *e0, static_cast<int64_t>(T.seg_elems));
+  }
+}
+
+// Consecutive rows of a task: the (i0, i1, i2) index of the three outer
+// (padded) dims, advanced like an odometer, and the row's two addresses.
+struct RdtRows {
+  uint32_t i0, i1, i2, e1, e2;
+  __device__ __forceinline__ RdtRows(const RdTask& T, uint32_t r) {
+    e1 = static_cast<uint32_t>(T.ext[1]);
+    e2 = static_cast<uint32_t>(T.ext[2]);
+    i2 = r % e2;
+    const uint32_t q = r / e2;
+    i1 = q % e1;
+    i0 = q / e1;
+  }
+  __device__ __forceinline__ void next() {
+    if (++i2 == e2) {
+      i2 = 0;
+      if (++i1 == e1) {
+        i1 = 0;
+        ++i0;
+      }
+    }
+  }
+  template <class P>
+  __device__ __forceinline__ void at(const P& p, const RdTask& T, int64_t e0, char** d, const char** s) const {
+    const RdSlot& D = p.dst[T.dst_slot];
+    const RdRef& R = p.ref[T.ref_begin];
+    const RdSlot& S = p.src[R.slot];
+    const int m0 = T.dmap[0], m1 = T.dmap[1], m2 = T.dmap[2];
+    *d = D.ptr + (T.dst_off + i0 * D.stride[m0] + i1 * D.stride[m1] + i2 * D.stride[m2] + e0) * p.esize;
+    *s = S.ptr + (R.off + i0 * S.stride[m0] + i1 * S.stride[m1] + i2 * S.stride[m2] + e0) * p.esize;
+  }
+};
+
+__device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uint32_t bytes) {
+  uint64_t g;
+  asm volatile("cvta.to.global.u64 %0, %1;" : "=l"(g) : "l"(gdst));
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(g), "r"(smem_u32(smem_src)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+template <class P>
+__global__ void __launch_bounds__(RDT_THREADS, 1) rd_tma_kernel(const __grid_constant__ P p) {
+  extern __shared__ __align__(128) uint8_t rdt_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint64_t* full = reinterpret_cast<uint64_t*>(rdt_smem + RDT_PIPES * RDT_STAGES * RDT_STAGE_BYTES) + warp * RDT_STAGES;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(reinterpret_cast<uint64_t*>(
+                                 rdt_smem + RDT_PIPES * RDT_STAGES * RDT_STAGE_BYTES) + RDT_PIPES * RDT_STAGES);
+  if (lane == 0)
+    for (int s = 0; s < RDT_STAGES; ++s) mbar_init(&full[s], 1);
+  if (threadIdx.x == 0) *abort_flag = 0;
+  fence_mbar_init();
+  __syncthreads();
+  if (lane != 0) return;
+  uint8_t* ring = rdt_smem + warp * RDT_STAGES * RDT_STAGE_BYTES;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * RDT_PIPES + warp;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * RDT_PIPES;
+  const int64_t count = first < p.nitems ? (p.nitems - 1 - first) / step + 1 : 0;
+  int t_load = 0, t_store = 0;
+  bool aborted = false;
+  // iteration k loads item k (if any) and stores item k - RDT_LAG (if any)
+  for (int64_t k = 0; k < count + RDT_LAG && !aborted; ++k) {
+    if (k < count) {
+      const int stage = static_cast<int>(k % RDT_STAGES);
+      // the store that last read this stage (item k - RDT_STAGES) is done reading
+      if (k >= RDT_STAGES) bulk_wait_read<RDT_STAGES - 1 - RDT_LAG>();
+      uint32_t r0;
+      int64_t e0, n;
+      int nrows;
+      rdt_item(p, first + k * step, &t_load, &r0, &nrows, &e0, &n);
+      const RdTask& T = p.task[t_load];
+      const uint32_t nbytes = static_cast<uint32_t>(n * p.esize);
+      mbar_expect_tx(&full[stage], nbytes * static_cast<uint32_t>(nrows));
+      uint8_t* dst = ring + stage * RDT_STAGE_BYTES;
+      RdtRows rows(T, r0);
+      for (int j = 0; j < nrows; ++j, rows.next(), dst += nbytes) {
+        char* d;
+        const char* src;
+        rows.at(p, T, e0, &d, &src);
+        bulk_load(dst, src, nbytes, &full[stage]);
+      }
+    }
+    if (k >= RDT_LAG) {
+      const int64_t ks = k - RDT_LAG;
+      const int stage = static_cast<int>(ks % RDT_STAGES);
+      if (!mbar_wait(&full[stage], static_cast<uint32_t>((ks / RDT_STAGES) & 1), abort_flag)) {
+        aborted = true;
+        break;
+      }
+      uint32_t r0;
+      int64_t e0, n;
+      int nrows;
+      rdt_item(p, first + ks * step, &t_store, &r0, &nrows, &e0, &n);
+      const RdTask& T = p.task[t_store];
+      const uint32_t nbytes = static_cast<uint32_t>(n * p.esize);
+      const uint8_t* src = ring + stage * RDT_STAGE_BYTES;
+      RdtRows rows(T, r0);
+      for (int j = 0; j < nrows; ++j, rows.next(), src += nbytes) {
+        char* d;
+        const char* s;
+        rows.at(p, T, e0, &d, &s);
+        bulk_store(d, src, nbytes);
+      }
+      bulk_commit();
+    }
+  }
+  if (aborted) {
+    *abort_flag = 1;
+    atomicOr(p.status, DT_DEV_ERR_TIMEOUT);
+    // loads issued before the wait gave up: a bounded time to land
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 20000000ull) {
+    }
+  }
+  bulk_wait_all();  // every store has read its stage and written global memory
+}
+
 // ---------------------------------------------------------------- host
 
 struct HostTask {
@@ -765,22 +940,85 @@ dt_status plan_pair(const dt_dtensor* src, const dt_dtensor* dst, PairPlan* pp) 
 // few launches as the parameter block holds.
 enum RdKind { RD_COPY = 0, RD_SUM = 1, RD_COPY_REPL = 2 };
 
+// The bulk copy kernel's shared memory, opted in once per parameter-block size.
 template <class P>
-void launch_rd(const P& p, int kind, int grid, cudaStream_t stream) {
+bool rdt_ready() {
+  static int ok = -1;
+  if (ok < 0) {
+    ok = cudaFuncSetAttribute(rd_tma_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, RDT_SMEM_BYTES) ==
+                 cudaSuccess
+             ? 1
+             : 0;
+    if (!ok) cudaGetLastError();
+  }
+  return ok == 1;
+}
+
+template <class P>
+void launch_rd(const P& p, int kind, bool bulk, int grid, cudaStream_t stream) {
   if (kind == RD_SUM)
     rd_kernel<true, false, P><<<grid, RD_THREADS, 0, stream>>>(p);
   else if (kind == RD_COPY_REPL)
     rd_kernel<false, true, P><<<grid, RD_THREADS, 0, stream>>>(p);
+  else if (bulk)
+    rd_tma_kernel<P><<<grid, RDT_THREADS, RDT_SMEM_BYTES, stream>>>(p);
   else
     rd_kernel<false, false, P><<<grid, RD_THREADS, 0, stream>>>(p);
 }
 
-// A call's launches, recorded as issued (kind, grid and the exact parameter
-// block) so a later call with the same operands can replay them without
-// planning again.
+// DT_RD_BULK=0 / 1 in the environment turns the bulk (TMA) copy kernel off
+// or on for the copy launches it can run (every row 16-byte aligned on both
+// sides), e.g. to compare the two copy kernels; unset, the default applies.
+int bulk_copies() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("DT_RD_BULK");
+    v = (e && e[0] == '0') ? 0 : (e && e[0] == '1') ? 1 : RD_BULK_DEFAULT;
+  }
+  return v;
+}
+
+// Whole rows per bulk work item (1: a long row is cut into segments of one
+// stage).
+void bulk_partition(RdTask* t, int esize) {
+  const int64_t row_bytes = t->ext[3] * esize;
+  const int64_t rows = t->ext[0] * t->ext[1] * t->ext[2];
+  if (row_bytes <= RDT_STAGE_BYTES / 2) {
+    t->rows_per_item = (int16_t)std::min<int64_t>(RDT_STAGE_BYTES / row_bytes, rows);
+    t->seg_elems = (int32_t)t->ext[3];
+    t->segs_per_row = 1;
+  } else {
+    t->rows_per_item = 1;
+    t->seg_elems = (int32_t)(RDT_STAGE_BYTES / esize);
+    t->segs_per_row = (int32_t)((t->ext[3] + t->seg_elems - 1) / t->seg_elems);
+  }
+}
+
+int64_t bulk_items(const RdTask& t) {
+  const int64_t rows = t.ext[0] * t.ext[1] * t.ext[2];
+  return t.rows_per_item > 1 ? (rows + t.rows_per_item - 1) / t.rows_per_item : rows * t.segs_per_row;
+}
+
+// Every row of the task starts on a 16-byte boundary in both slots and is
+// a multiple of 16 bytes long.
+bool bulk_task_ok(const RdTask& t, const RdSlot& D, const RdSlot& S, int64_t src_off, int esize) {
+  if (t.nsrc != 1 || t.nextra != 0) return false;
+  if (D.stride[t.dmap[3]] != 1 || S.stride[t.dmap[3]] != 1) return false;
+  if ((t.ext[3] * esize) % 16) return false;
+  if ((reinterpret_cast<uintptr_t>(D.ptr) + (uintptr_t)(t.dst_off * esize)) % 16) return false;
+  if ((reinterpret_cast<uintptr_t>(S.ptr) + (uintptr_t)(src_off * esize)) % 16) return false;
+  for (int q = 0; q < 3; ++q)
+    if (t.ext[q] > 1 && ((D.stride[t.dmap[q]] * esize) % 16 || (S.stride[t.dmap[q]] * esize) % 16)) return false;
+  return t.ext[0] * t.ext[1] * t.ext[2] < (1ll << 31);
+}
+
+// A call's launches, recorded as issued (kind, kernel, grid and the exact
+// parameter block) so a later call with the same operands can replay them
+// without planning again.
 struct RecordedLaunch {
   int kind = 0;
   bool small = false;
+  bool bulk = false;
   int grid = 0;
   std::vector<uint8_t> params;
 };
@@ -790,22 +1028,39 @@ struct RecordedPlan {
 };
 thread_local RecordedPlan* g_recording = nullptr;
 
-dt_status launch_kind(std::vector<PairPlan>& plans, int kind, cudaStream_t stream) {
+dt_status launch_kind(std::vector<PairPlan>& plans, int kind, int32_t* status, cudaStream_t stream) {
   const bool sum = kind == RD_SUM;
   static thread_local RdParams p;  // ~28 KB: off the stack
   static thread_local RdParamsSmall ps;
   const int sms = device_sm_count();
   int nd_slots = 0, ns_slots = 0, nt = 0, nref = 0;
   int64_t items = 0;
+  // every copy task so far can run on the bulk copy kernel (rows aligned on both sides)
+  bool aligned = kind == RD_COPY && bulk_copies() == 1;
   auto flush = [&]() -> dt_status {
     if (nt == 0) return DT_OK;
+    const bool small = nd_slots <= ps.kSlots && ns_slots <= ps.kSlots && nt <= ps.kTasks && nref <= ps.kRefs;
+    const bool bulk = aligned && (small ? rdt_ready<RdParamsSmall>() : rdt_ready<RdParams>());
+    int grid;
+    if (bulk) {  // the bulk kernel's work items: whole rows or row segments of one stage
+      items = 0;
+      for (int i = 0; i < nt; ++i) {
+        bulk_partition(&p.task[i], p.esize);
+        p.task[i].item_begin = items;
+        items += bulk_items(p.task[i]);
+      }
+      // one CTA (four pipelines) per SM
+      grid = (int)std::min<int64_t>((items + RDT_PIPES - 1) / RDT_PIPES, (int64_t)sms);
+    } else {
+      // one wave of resident CTAs, grid-stride over items
+      const int64_t blocks = (items + RD_WARPS - 1) / RD_WARPS;
+      grid = (int)std::min<int64_t>(blocks, (int64_t)sms * (sum ? RD_SUM_CTAS : RD_COPY_CTAS));
+    }
     p.ntasks = nt;
     p.nitems = items;
-    const int64_t blocks = (items + RD_WARPS - 1) / RD_WARPS;
-    // one wave of resident CTAs, grid-stride over items
-    const int grid = (int)std::min<int64_t>(blocks, (int64_t)sms * (sum ? RD_SUM_CTAS : RD_COPY_CTAS));
+    p.status = status;
     if (grid > 0) {
-      if (nd_slots <= ps.kSlots && ns_slots <= ps.kSlots && nt <= ps.kTasks && nref <= ps.kRefs) {
+      if (small) {
         std::copy(p.dst, p.dst + nd_slots, ps.dst);
         std::copy(p.src, p.src + ns_slots, ps.src);
         std::copy(p.task, p.task + nt, ps.task);
@@ -815,16 +1070,17 @@ dt_status launch_kind(std::vector<PairPlan>& plans, int kind, cudaStream_t strea
         ps.dtype = p.dtype;
         ps.esize = p.esize;
         ps.op = p.op;
-        launch_rd(ps, kind, grid, stream);
+        ps.status = p.status;
+        launch_rd(ps, kind, bulk, grid, stream);
         if (g_recording) {
           const uint8_t* b = reinterpret_cast<const uint8_t*>(&ps);
-          g_recording->launches.push_back({kind, true, grid, std::vector<uint8_t>(b, b + sizeof(ps))});
+          g_recording->launches.push_back({kind, true, bulk, grid, std::vector<uint8_t>(b, b + sizeof(ps))});
         }
       } else {
-        launch_rd(p, kind, grid, stream);
+        launch_rd(p, kind, bulk, grid, stream);
         if (g_recording) {
           const uint8_t* b = reinterpret_cast<const uint8_t*>(&p);
-          g_recording->launches.push_back({kind, false, grid, std::vector<uint8_t>(b, b + sizeof(p))});
+          g_recording->launches.push_back({kind, false, bulk, grid, std::vector<uint8_t>(b, b + sizeof(p))});
         }
       }
       cudaError_t e = cudaGetLastError();
@@ -833,6 +1089,7 @@ dt_status launch_kind(std::vector<PairPlan>& plans, int kind, cudaStream_t strea
     }
     nd_slots = ns_slots = nt = nref = 0;
     items = 0;
+    aligned = kind == RD_COPY && bulk_copies() == 1;
     return DT_OK;
   };
   dt_status st;
@@ -901,7 +1158,11 @@ dt_status launch_kind(std::vector<PairPlan>& plans, int kind, cudaStream_t strea
       if (spr > (1ll << 30)) return fail(DT_ERR_CAPACITY, "row of %lld elements", (long long)t.ext[3]);
       t.segs_per_row = (int32_t)spr;
       t.item_begin = items;
+      t.rows_per_item = 1;
       items += t.ext[0] * t.ext[1] * t.ext[2] * spr;
+      if (aligned)
+        aligned = t.nsrc == 1 && bulk_task_ok(t, p.dst[t.dst_slot], p.src[p.ref[t.ref_begin].slot],
+                                              p.ref[t.ref_begin].off, ls.esize);
       ++nt;
     }
   }
@@ -955,12 +1216,12 @@ dt_status launch_forked(Launch&& launch, cudaStream_t s) {
   return st;
 }
 
-dt_status redistribute_planned(int32_t n, const dt_dtensor* src, const dt_dtensor* dst, cudaStream_t s,
-                               RecordedPlan* rec);
+dt_status redistribute_planned(int32_t n, const dt_dtensor* src, const dt_dtensor* dst, int32_t* status,
+                               cudaStream_t s, RecordedPlan* rec);
 
 template <class P>
 dt_status replay_one(const RecordedLaunch& r, cudaStream_t s) {
-  launch_rd(*reinterpret_cast<const P*>(r.params.data()), r.kind, r.grid, s);
+  launch_rd(*reinterpret_cast<const P*>(r.params.data()), r.kind, r.bulk, r.grid, s);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(DT_ERR_CUDA, "redistribute launch: %s", cudaGetErrorString(e));
   count_launch();
@@ -992,13 +1253,15 @@ dt_status replay(const RecordedPlan& rp, cudaStream_t s) {
   return DT_OK;
 }
 
-dt_status redistribute_many(int32_t n, const dt_dtensor* src, const dt_dtensor* dst, dt_stream_t stream) {
+dt_status redistribute_many(int32_t n, const dt_dtensor* src, const dt_dtensor* dst, int32_t* d_status,
+                            dt_stream_t stream) {
   clear_error();
   if (n < 0 || (n > 0 && (!src || !dst))) return fail(DT_ERR_INVALID_ARG, "need n >= 0 and src/dst arrays");
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   std::string key;
   bool keyed = true;
   for (int i = 0; i < n && keyed; ++i) keyed = append_plan_key(&key, &src[i]) && append_plan_key(&key, &dst[i]);
+  append_plan_scalar(&key, d_status);  // the recorded parameters hold the status word
   if (keyed && n > 0) {
     std::shared_ptr<const RecordedPlan> hit;
     {
@@ -1019,7 +1282,7 @@ dt_status redistribute_many(int32_t n, const dt_dtensor* src, const dt_dtensor* 
     }
   }
   auto rec = std::make_shared<RecordedPlan>();
-  dt_status st = redistribute_planned(n, src, dst, cs, rec.get());
+  dt_status st = redistribute_planned(n, src, dst, d_status, cs, rec.get());
   if (st == DT_OK && keyed && n > 0) {
     std::lock_guard<std::mutex> lk(g_plan_mu);
     if (g_plans.size() >= RD_PLAN_CACHE) g_plans.clear();
@@ -1028,8 +1291,8 @@ dt_status redistribute_many(int32_t n, const dt_dtensor* src, const dt_dtensor* 
   return st;
 }
 
-dt_status redistribute_planned(int32_t n, const dt_dtensor* src, const dt_dtensor* dst, cudaStream_t s,
-                               RecordedPlan* rec) {
+dt_status redistribute_planned(int32_t n, const dt_dtensor* src, const dt_dtensor* dst, int32_t* d_status,
+                               cudaStream_t s, RecordedPlan* rec) {
   std::vector<PairPlan> plans(n);
   const void* any = nullptr;
   dt_status st;
@@ -1054,7 +1317,9 @@ dt_status redistribute_planned(int32_t n, const dt_dtensor* src, const dt_dtenso
     ~Recording() { g_recording = nullptr; }
   } recording(rec);
   rec->forked = copies && sums;
-  auto launch = [&](int kind, cudaStream_t stream) { return launch_kind(plans, kind, stream); };
+  int32_t* status = device_status_word(d_status);
+  if (!status) return fail(DT_ERR_CUDA, "no device status word");
+  auto launch = [&](int kind, cudaStream_t stream) { return launch_kind(plans, kind, status, stream); };
   if (rec->forked) return launch_forked(launch, s);
   for (int k : {RD_COPY, RD_COPY_REPL, RD_SUM})
     if ((st = launch(k, s)) != DT_OK) return st;
@@ -1072,12 +1337,10 @@ void clear_redistribute_plans() {
 
 extern "C" dt_status dt_redistribute(const dt_dtensor* src, const dt_dtensor* dst, int32_t* d_status,
                                      dt_stream_t stream) {
-  (void)d_status;  // data movement reports no device-side errors
-  return dt::redistribute_many(1, src, dst, stream);
+  return dt::redistribute_many(1, src, dst, d_status, stream);
 }
 
 extern "C" dt_status dt_redistribute_batch(int32_t n, const dt_dtensor* src, const dt_dtensor* dst,
                                            int32_t* d_status, dt_stream_t stream) {
-  (void)d_status;
-  return dt::redistribute_many(n, src, dst, stream);
+  return dt::redistribute_many(n, src, dst, d_status, stream);
 }

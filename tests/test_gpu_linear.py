@@ -294,3 +294,46 @@ def test_unaligned_kmajor_weights_use_cuda_cores(lib):
     expect = olin.column_parallel(w64(x), [w64(w[:, o:o + s]) for o, s in chunk_bounds(N, p)])
     for i in range(p):
         check_fp32(to_host(y.slots[i], "fp32"), expect[i], f"shard {i}")
+
+
+# ---------------------------------------------------------------- uneven shards
+
+def test_uneven_shards_run_on_tensor_cores_with_workspace(lib):
+    """[512, 1024] x [1024, 8190] over 4: the last column shard is 2046 wide,
+    a 4092-byte pitch TMA cannot read.  With the queried workspace the shard
+    is copied to a padded pitch and the launch runs on the tensor cores; with
+    none it runs on the CUDA-core kernel (counted).  Both match the oracle.
+    The row-parallel layer on the same split (x shards [512, 2046]) likewise."""
+    M, K, N, p = 512, 1024, 8190, 4
+    x = workloads.randn_bf16((M, K), 961)
+    w = workloads.randn_bf16((K, N), 962, (1.0 / K) ** 0.5)
+    xd, wd = x_rep(x, p), col_dtensor(w, p)
+    y = tsl.api._col_out(xd, wd, 0, torch.float32)
+    need = tsl.column_parallel_linear_workspace_bytes(xd, [wd], [y])
+    assert need >= 1024 * 2048 * 2  # at least the padded 2046-column shard
+    expect = olin.column_parallel(w64(x), [w64(w[:, o:o + s]) for o, s in chunk_bounds(N, p)])
+    c0 = tsl.cuda_core_gemm_count()
+    tsl.column_parallel_linear(xd, wd, out=y, workspace=torch.empty(need, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert tsl.cuda_core_gemm_count() == c0
+    for i, e in enumerate(expect):
+        check_fp32(to_host(y.slots[i], "fp32"), e, f"padded, shard {i}")
+    tsl.column_parallel_linear(xd, wd, out=y, workspace=torch.empty(0, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert tsl.cuda_core_gemm_count() > c0
+    assert tsl.read_device_status() == 0
+    for i, e in enumerate(expect):
+        check_fp32(to_host(y.slots[i], "fp32"), e, f"CUDA-core, shard {i}")
+    # row parallel: K = 8190 over 4, x shards [512, 2046]
+    xr = workloads.randn_bf16((M, N), 963)
+    wr = workloads.randn_bf16((N, 768), 964, (1.0 / N) ** 0.5)
+    xrd, wrd = x_shard(xr, p), row_dtensor(wr, p)
+    yr = tsl.api._row_out(xrd, wrd, 0, tsl.ALL_REDUCE, torch.float32)
+    c1 = tsl.cuda_core_gemm_count()
+    tsl.row_parallel_linear(xrd, wrd, out=yr)  # the Python API passes the queried workspace
+    torch.cuda.synchronize()
+    assert tsl.cuda_core_gemm_count() == c1
+    assert tsl.read_device_status() == 0
+    (er,) = olin.row_parallel([w64(xr[:, o:o + s]) for o, s in chunk_bounds(N, p)],
+                              [w64(wr[o:o + s]) for o, s in chunk_bounds(N, p)], None, olin.ALL_REDUCE)
+    check_fp32(to_host(yr.slots[0], "fp32"), er, "row, padded x shards")
