@@ -53,7 +53,7 @@ G_ODD = 8191 * 8190 * 2
 EMB_BYTES = 4 * 4096 * 4096 * 2 * 2 + 4 * 4096 * 4
 MLP_FLOPS = 3 * 2 * 4096 * 4096 * 11008
 ATTN_FLOPS = 4 * 2 * 8192 * 4096 * 4096
-GEMM_SOURCES = ["gemm_sm103.cuh", "gemm_pair_kernel.cu", "gemm_host.cu"]
+GEMM_SOURCES = ["ptx_sm103.cuh", "gemm_sm103.cuh", "gemm_pair_kernel.cu", "gemm_host.cu"]
 ALL_COMPONENTS = "embedding,redistribute,mlp,attention"
 
 
@@ -1067,8 +1067,9 @@ def run_cublas_shapes(args):
 
 
 def run_profile_case(args):
-    """One kernel of the step on its own, `--steps` calls after `--warmup`
-    (for ncu captures; prints no bench line).  Cases: `mlp_down` (the TP
+    """One kernel of the step on its own, `--steps` calls after `--warmup`,
+    each timed with CUDA events after a 512 MB write that flushes L2 (for ncu
+    captures and A/B timing; prints one small JSON line, not a bench line).  Cases: `mlp_down` (the TP
     MLP's down projection: H [4096, 11008] Shard(-1) over 8, Wd Shard(0),
     ALL_REDUCE, split tail in its workspace), `qkv`, `o`, and
     `rd:<transition>:<shape>` (one redistribute of the sweep, e.g.
@@ -1102,12 +1103,15 @@ def run_profile_case(args):
         qkv = [tsl.DTensor.empty(m4, [S1], (8192, 4096), bf) for _ in range(3)]
         wo = tsl.DTensor([rnd(1024, 4096, std=1 / 64) for _ in range(4)], m4, [S0], (4096, 4096), bf)
         od = tsl.DTensor.empty(m4, [S0], (8192, 4096), bf)
-        none = torch.empty(0, dtype=torch.uint8, device=dev)
-        tsl.column_parallel_linear_multi(x, wq, outs=qkv, workspace=none)
+        wsq = torch.empty(max(1, tsl.column_parallel_linear_workspace_bytes(x, wq, qkv)), dtype=torch.uint8,
+                          device=dev)
+        wso = torch.empty(max(1, tsl.row_parallel_linear_workspace_bytes(qkv[0], wo, od, tsl.REDUCE_SCATTER)),
+                          dtype=torch.uint8, device=dev)
+        tsl.column_parallel_linear_multi(x, wq, outs=qkv, workspace=wsq)
         if case == "qkv":
-            fn = lambda: tsl.column_parallel_linear_multi(x, wq, outs=qkv, workspace=none)  # noqa: E731
+            fn = lambda: tsl.column_parallel_linear_multi(x, wq, outs=qkv, workspace=wsq)  # noqa: E731
         else:
-            fn = lambda: tsl.row_parallel_linear(qkv[0], wo, mode=tsl.REDUCE_SCATTER, out=od, workspace=none)  # noqa
+            fn = lambda: tsl.row_parallel_linear(qkv[0], wo, mode=tsl.REDUCE_SCATTER, out=od, workspace=wso)  # noqa
     elif case.startswith("rd:"):
         _, name, shape = case.split(":")
         blk = Block(dev, only=("redistribute",))
@@ -1119,12 +1123,24 @@ def run_profile_case(args):
         fn = lambda: tsl.redistribute(a, b)  # noqa: E731
     else:
         raise SystemExit(f"unknown --profile-case {case!r}")
-    for _ in range(args.warmup + args.steps):
+    for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)  # > L2: every call starts L2-cold
+    times = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3)
     if tsl.read_device_status() != 0:
         raise SystemExit("device status set")
-    print(f"profile case {case}: {args.warmup} + {args.steps} calls", flush=True)
+    print(json.dumps({"profile_case": case, "warmup": args.warmup, "steps": args.steps,
+                      "us_median": round(statistics.median(times), 2),
+                      "bands": os.environ.get("DT_GEMM_BANDS", "default")}), flush=True)
 
 
 def main():

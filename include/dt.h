@@ -41,7 +41,9 @@
  *    and joined back to the caller's stream).  dt_clear_cache() drops the
  *    caches.
  *  - Environment switches, read once per process:
- *      DT_GEMM_SPLIT=0     turns the split tail off;
+ *      DT_GEMM_SPLIT=0     turns the split tail off; =2 splits every last
+ *                          wave the finishing can take, whether or not the
+ *                          cost model expects a gain (to compare schedules);
  *      DT_GEMM_BANDS=m,n   fixes the GEMM tile order's band height and block
  *                          width (in 256 x 256 tiles) instead of the host's
  *                          choice, to compare orders.

@@ -307,14 +307,15 @@ int gemm_starve() {
 constexpr double SPLIT_OVERHEAD_ITERS = 72.0;
 
 // DT_GEMM_SPLIT=0 in the environment turns the split tail off (every tile
-// whole), e.g. to compare the two schedules.
-bool use_split_tail() {
+// whole), DT_GEMM_SPLIT=2 splits every last wave the finishing can take
+// whatever the cost model says, e.g. to compare the schedules.
+int split_mode() {
   static int v = -1;
   if (v < 0) {
     const char* e = getenv("DT_GEMM_SPLIT");
-    v = (e && e[0] == '0') ? 0 : 1;
+    v = (e && e[0] == '0') ? 0 : (e && e[0] == '2') ? 2 : 1;
   }
-  return v == 1;
+  return v;
 }
 
 // DT_GEMM_BANDS=m,n fixes the tile order's band height and block width (in
@@ -431,7 +432,7 @@ struct SplitPlan {
 
 SplitPlan plan_split(const LaunchShape& s, int ctas) {
   SplitPlan sp;
-  if (s.tiles <= 0 || ctas <= 0 || !s.uniform || !use_split_tail()) return sp;
+  if (s.tiles <= 0 || ctas <= 0 || !s.uniform || split_mode() == 0) return sp;
   const int rem = s.tiles % ctas;
   const int ki = s.kiters;
   const int64_t share_min = (int64_t)rem * ki / ctas;  // shortest share, in K iterations
@@ -441,7 +442,7 @@ SplitPlan plan_split(const LaunchShape& s, int ctas) {
   // a finishing round stages one 32-column chunk of every piece (gate and
   // up chunks for the gated MLP) in an epilogue warp's half of its quarter
   const bool fits = np * (s.dual ? 2 : 1) <= FIN_MAX_PIECES;
-  if (rem > 0 && share_min >= 8 && fits && split_cost <= ki) {
+  if (rem > 0 && share_min >= 8 && fits && (split_cost <= ki || split_mode() == 2)) {
     sp.sk_tiles = rem;
     sp.kiters = ki;
     sp.pieces = rem + ctas - 1;  // every cluster boundary inside the tail adds one

@@ -398,6 +398,40 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Store the NW words w (a run of 4 * NW bytes, elements of ES bytes) at
+// address `a`, which is ES-aligned and H bytes short of a 16-byte boundary:
+// the first H bytes element by element, then whole 16-byte vectors shifted
+// out of the words, then the remaining elements.  Output rows whose pitch is
+// not a multiple of 16 bytes (an uneven shard of a column layer) get 16-byte
+// stores this way instead of one store per element.
+template <int ES, int NW, int H>
+__device__ __forceinline__ void store_words_at(char* a, const uint32_t (&w)[NW]) {
+  constexpr int NB = NW * 4;
+  constexpr int NV = (NB - H) / 16;
+  auto elem = [&](int b) -> uint32_t {  // the element at byte b of the run
+    return ES == 4 ? w[b >> 2] : (w[b >> 2] >> ((b & 3) * 8)) & 0xffffu;
+  };
+#pragma unroll
+  for (int b = 0; b < H; b += ES) {
+    if (ES == 4) *reinterpret_cast<uint32_t*>(a + b) = elem(b);
+    else *reinterpret_cast<uint16_t*>(a + b) = static_cast<uint16_t>(elem(b));
+  }
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const int b = H + 16 * j;
+    const int q = b >> 2, sh = (b & 3) * 8;
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = sh ? __funnelshift_r(w[q + k], w[q + k + 1], sh) : w[q + k];
+    *reinterpret_cast<uint4*>(a + b) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+#pragma unroll
+  for (int b = H + 16 * NV; b < NB; b += ES) {
+    if (ES == 4) *reinterpret_cast<uint32_t*>(a + b) = elem(b);
+    else *reinterpret_cast<uint16_t*>(a + b) = static_cast<uint16_t>(elem(b));
+  }
+}
+
 // Store 32 fp32 values of one output row at columns [col0, col0 + 32).
 __device__ __forceinline__ void store_row32(const Group& G, char* row_ptr, int col0, const float (&v)[32]) {
   const int valid = min(32, G.n - col0);
@@ -410,6 +444,21 @@ __device__ __forceinline__ void store_row32(const Group& G, char* row_ptr, int c
       for (int q = 0; q < 4; ++q)
         o4[q] = make_uint4(pack2(v[8 * q + 0], v[8 * q + 1]), pack2(v[8 * q + 2], v[8 * q + 3]),
                            pack2(v[8 * q + 4], v[8 * q + 5]), pack2(v[8 * q + 6], v[8 * q + 7]));
+    } else if (valid == 32) {
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) w[i] = pack2(v[2 * i], v[2 * i + 1]);
+      char* a = reinterpret_cast<char*>(o);
+      switch ((16 - (reinterpret_cast<uintptr_t>(a) & 15)) & 15) {
+        case 0: store_words_at<2, 16, 0>(a, w); break;
+        case 2: store_words_at<2, 16, 2>(a, w); break;
+        case 4: store_words_at<2, 16, 4>(a, w); break;
+        case 6: store_words_at<2, 16, 6>(a, w); break;
+        case 8: store_words_at<2, 16, 8>(a, w); break;
+        case 10: store_words_at<2, 16, 10>(a, w); break;
+        case 12: store_words_at<2, 16, 12>(a, w); break;
+        default: store_words_at<2, 16, 14>(a, w); break;
+      }
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
@@ -421,6 +470,17 @@ __device__ __forceinline__ void store_row32(const Group& G, char* row_ptr, int c
       float4* o4 = reinterpret_cast<float4*>(o);
 #pragma unroll
       for (int q = 0; q < 8; ++q) o4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else if (valid == 32) {
+      uint32_t w[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i]);
+      char* a = reinterpret_cast<char*>(o);
+      switch ((16 - (reinterpret_cast<uintptr_t>(a) & 15)) & 15) {
+        case 0: store_words_at<4, 32, 0>(a, w); break;
+        case 4: store_words_at<4, 32, 4>(a, w); break;
+        case 8: store_words_at<4, 32, 8>(a, w); break;
+        default: store_words_at<4, 32, 12>(a, w); break;
+      }
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i)

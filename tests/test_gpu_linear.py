@@ -159,15 +159,25 @@ def test_column_parallel_multi_qkv_small(lib):
             check_fp32(to_host(ys[j].slots[i], "fp32"), expect[i], f"w{j} shard {i}")
 
 
-def test_unaligned_shapes_use_cuda_cores(lib):
-    """Shard pitches TMA cannot describe (odd widths) run on the CUDA-core kernel."""
+@pytest.mark.parametrize("k_major", [False, True])
+def test_unaligned_shapes(lib, k_major):
+    """Shard pitches TMA cannot describe (odd widths): without a workspace
+    the launch runs on the CUDA-core kernel (counted), with the queried one
+    the operands are copied to padded pitches and it runs on the tensor
+    cores; both against the oracle."""
     M, K, N, p = 33, 50, 30, 4
-    x = workloads.randn_bf16((M, K), 31)
-    w = workloads.randn_bf16((K, N), 32, (1.0 / K) ** 0.5)
-    y = tsl.column_parallel_linear(x_rep(x, p), col_dtensor(w, p), out_dtype=torch.float32)
+    x = workloads.randn_bf16((M, K), 31 if not k_major else 81)
+    w = workloads.randn_bf16((K, N), 32 if not k_major else 82, (1.0 / K) ** 0.5)
+    xd, wd = x_rep(x, p), col_dtensor(w, p, k_major=k_major)
     expect = olin.column_parallel(w64(x), [w64(w[:, o:o + s]) for o, s in chunk_bounds(N, p)])
-    for i in range(p):
-        check_fp32(to_host(y.slots[i], "fp32"), expect[i], f"shard {i}")
+    for ws, cuda_cores in ((torch.empty(0, dtype=torch.uint8, device="cuda"), True), (None, False)):
+        c0 = tsl.cuda_core_gemm_count()
+        y = tsl.column_parallel_linear(xd, wd, out_dtype=torch.float32, workspace=ws)
+        torch.cuda.synchronize()
+        assert (tsl.cuda_core_gemm_count() > c0) == cuda_cores
+        assert tsl.read_device_status() == 0
+        for i in range(p):
+            check_fp32(to_host(y.slots[i], "fp32"), expect[i], f"cuda_cores={cuda_cores} shard {i}")
 
 
 # ---------------------------------------------------------------- row parallel
@@ -284,16 +294,6 @@ def test_tp_mlp_kmajor_weights(lib):
     (expect,), _ = olin.tp_mlp(w64(x), [w64(wg[:, o:o + s]) for o, s in cols], [w64(wu[:, o:o + s]) for o, s in cols],
                                [w64(wd[o:o + s]) for o, s in cols])
     check_fp32(to_host(y.slots[0], "fp32"), expect, "mlp")
-
-
-def test_unaligned_kmajor_weights_use_cuda_cores(lib):
-    M, K, N, p = 33, 50, 30, 4
-    x = workloads.randn_bf16((M, K), 81)
-    w = workloads.randn_bf16((K, N), 82, (1.0 / K) ** 0.5)
-    y = tsl.column_parallel_linear(x_rep(x, p), col_dtensor(w, p, k_major=True), out_dtype=torch.float32)
-    expect = olin.column_parallel(w64(x), [w64(w[:, o:o + s]) for o, s in chunk_bounds(N, p)])
-    for i in range(p):
-        check_fp32(to_host(y.slots[i], "fp32"), expect[i], f"shard {i}")
 
 
 # ---------------------------------------------------------------- uneven shards

@@ -5,8 +5,10 @@ Each case draws M, K, N and the part count P, so shards are ragged
 TMA's out-of-bounds fill is exercised; bias on or off, bf16 and fp32
 outputs, weights stored [in, out] or as [out, in] views, and every
 row-parallel mode.  K a multiple of 8 keeps bf16 row pitches 16-byte
-aligned (the tcgen05 path); other K take the CUDA-core kernel.  Tolerances
-as in the other linear tests.
+aligned (the tcgen05 path); other K give pitches TMA cannot read, which the
+calls copy to padded pitches in their workspace (the Python API passes the
+queried size) and run on the tcgen05 path too; the CUDA-core kernel is
+tested in test_gpu_linear.py.  Tolerances as in the other linear tests.
 """
 import random
 
