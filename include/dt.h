@@ -105,7 +105,7 @@ typedef enum dt_status {
 
 /* Bits OR-ed into *d_status by kernels. */
 #define DT_DEV_ERR_INDEX 0x1   /* an embedding id was outside [0, vocab): its row was zero-filled */
-#define DT_DEV_ERR_TIMEOUT 0x2 /* a bounded wait in a GEMM gave up; its outputs are not valid */
+#define DT_DEV_ERR_TIMEOUT 0x2 /* a bounded wait (GEMM or bulk copy kernel) gave up; its outputs are not valid */
 
 typedef enum dt_dtype { DT_BF16 = 0, DT_FP32 = 1, DT_INT32 = 2 } dt_dtype;
 
@@ -192,6 +192,10 @@ DT_API dt_status dt_layout_slot_box(const dt_layout* layout, int32_t slot, int64
  * and round a bf16 result once, to nearest even: results are bit-exact and
  * independent of the launch shape.  Shard -> Partial returns
  * DT_ERR_UNSUPPORTED; dtypes must match; int32 supports no Partial.
+ * Copies whose rows are all 16-byte aligned on both sides run on the bulk
+ * (TMA) copy engine, the others on a warp copy kernel; only the bulk kernel
+ * waits (bounded), and a wait that gives up sets DT_DEV_ERR_TIMEOUT in
+ * *d_status (NULL: the library's status word).
  */
 DT_API dt_status dt_redistribute(const dt_dtensor* src, const dt_dtensor* dst, int32_t* d_status,
                           dt_stream_t stream);
