@@ -2,7 +2,9 @@
 
 One small step (embedding gather, a batched redistribute with copies and
 Partial reductions, a TP MLP whose down projection splits its tail, fused
-q/k/v and the o projection) runs eagerly, then the same calls are captured
+q/k/v and the o projection, an aligned move on the bulk-copy kernel and an
+unevenly split column layer whose shard is copied to a padded pitch in its
+workspace) runs eagerly, then the same calls are captured
 into one CUDA graph.  Replays must reproduce the eager results bit for bit
 (same kernels, same launch plans), and, after new inputs are written into
 the same buffers, match an eager run on those inputs.  This exercises every
@@ -85,7 +87,27 @@ def build_step():
     outputs += od.slots
     calls.append(lambda: tsl.column_parallel_linear_multi(xa, wqkv, outs=qkv))
     calls.append(lambda: tsl.row_parallel_linear(qkv[0], wod, mode=tsl.REDUCE_SCATTER, out=od))
-    keep = (tdt, idt, emb, src, part, o1, o2, xd, wgd, wud, wdd, ym, ws, xa, wqkv, wod, qkv, od)
+
+    # an aligned move on its own (the bulk-copy kernel) and an unevenly split
+    # column layer with its workspace (operand copy to a padded pitch, and
+    # output rows at every alignment)
+    g2 = (256, 2048)
+    src2 = tsl.DTensor.distribute_tensor(to_dev(workloads.randn_bf16(g2, 95), "bf16"), tp4, [S0])
+    o3 = tsl.DTensor.empty(tp4, [S1], g2, bf, device=dev)
+    inputs += src2.slots
+    outputs += o3.slots
+    calls.append(lambda: tsl.redistribute(src2, o3))
+    Nu = 1022  # over 4: 256, 256, 256, 254 columns
+    wun = workloads.randn_bf16((H, Nu), 96, 1.0 / 23)
+    wud_u = tsl.DTensor([to_dev(np.ascontiguousarray(wun[:, o:o + s]), "bf16") for o, s in chunk_bounds(Nu, 4)],
+                        tp4, [S1], (H, Nu), bf)
+    yu = tsl.DTensor.empty(tp4, [S1], (T, Nu), bf, device=dev)
+    wsu = torch.empty(tsl.column_parallel_linear_workspace_bytes(xa, [wud_u], [yu]), dtype=torch.uint8, device=dev)
+    assert wsu.numel() > 0
+    outputs += yu.slots
+    calls.append(lambda: tsl.column_parallel_linear(xa, wud_u, out=yu, workspace=wsu))
+    keep = (tdt, idt, emb, src, part, o1, o2, xd, wgd, wud, wdd, ym, ws, xa, wqkv, wod, qkv, od, src2, o3, wud_u, yu,
+            wsu)
     return calls, inputs, outputs, keep
 
 
