@@ -249,3 +249,19 @@ def test_linear_workspace_alignment_checked_first(lib):
     yr = fake_desc(opl.Layout(mesh, [R], (16, 64)))
     assert lib.dt_row_parallel_linear(C.byref(xr), C.byref(wr), None, C.byref(yr), L.TP_ALL_REDUCE, 0, _FAKE + 8,
                                       1 << 20, None, None) == L.ERR_ALIGNMENT
+
+
+def test_mlp_workspace_checked_before_launch(lib):
+    """dt_tp_mlp needs at least H's bytes of 256-byte aligned workspace; a
+    missing, short or misaligned one is refused on the host."""
+    mesh = (4,)
+    R, S0, S1 = opl.Replicate(), opl.Shard(0), opl.Shard(1)
+    descs = [fake_desc(opl.Layout(mesh, [R], (512, 256))), fake_desc(opl.Layout(mesh, [S1], (256, 1024))),
+             fake_desc(opl.Layout(mesh, [S1], (256, 1024))), fake_desc(opl.Layout(mesh, [S0], (1024, 256))),
+             fake_desc(opl.Layout(mesh, [R], (512, 256)))]
+    args = [C.byref(d) for d in descs] + [L.TP_ALL_REDUCE, 0]
+    h_bytes = 512 * 1024 * 2
+    assert lib.dt_tp_mlp(*args, None, 0, None, None) == L.ERR_INVALID_ARG
+    assert str(h_bytes).encode() in lib.dt_last_error()
+    assert lib.dt_tp_mlp(*args, _FAKE, h_bytes - 256, None, None) == L.ERR_INVALID_ARG
+    assert lib.dt_tp_mlp(*args, _FAKE + 128, h_bytes, None, None) == L.ERR_ALIGNMENT
