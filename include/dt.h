@@ -53,6 +53,8 @@
  *      DT_GEMM_STARVE=1         makes the GEMM producers issue no copies,
  *                               so every wait runs out and the launch
  *                               reports DT_DEV_ERR_TIMEOUT.
+ *      DT_RD_WAIT_LIMIT_MS=n,   the same two hooks for the bulk (TMA) copy
+ *      DT_RD_STARVE=1           kernel of dt_redistribute.
  *  - Compute calls are asynchronous on the given stream (a cudaStream_t;
  *    NULL = the legacy default stream).  Their return value covers the checks
  *    done on the host before any launch; on any error nothing is launched.

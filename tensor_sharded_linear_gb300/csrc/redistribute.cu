@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <map>
 #include <memory>
 #include <mutex>
@@ -111,6 +112,8 @@ struct RdParamsT {
   int32_t esize;
   int32_t op;
   int32_t* status;  // DT_DEV_* bits (the bulk copy kernel's bounded waits)
+  unsigned long long wait_limit_ns;  // bound of the bulk copy kernel's waits
+  int32_t starve;                    // test hook: the bulk kernel issues no loads, so its waits run out
 };
 using RdParams = RdParamsT<RD_MAX_LAUNCH_SLOTS, RD_MAX_TASKS, RD_MAX_REFS>;
 using RdParamsSmall = RdParamsT<32, 48, 64>;
@@ -664,13 +667,13 @@ __global__ void __launch_bounds__(RDT_THREADS, 1) rd_tma_kernel(const __grid_con
         char* d;
         const char* src;
         rows.at(p, T, e0, &d, &src);
-        bulk_load(dst, src, nbytes, &full[stage]);
+        if (!p.starve) bulk_load(dst, src, nbytes, &full[stage]);
       }
     }
     if (k >= RDT_LAG) {
       const int64_t ks = k - RDT_LAG;
       const int stage = static_cast<int>(ks % RDT_STAGES);
-      if (!mbar_wait(&full[stage], static_cast<uint32_t>((ks / RDT_STAGES) & 1), abort_flag)) {
+      if (!mbar_wait(&full[stage], static_cast<uint32_t>((ks / RDT_STAGES) & 1), abort_flag, p.wait_limit_ns)) {
         aborted = true;
         break;
       }
@@ -978,6 +981,29 @@ int bulk_copies() {
   return v;
 }
 
+// Test hooks, read once from the environment: DT_RD_WAIT_LIMIT_MS bounds
+// the bulk copy kernel's waits (default 2000 ms); DT_RD_STARVE=1 makes it
+// issue no loads, so its waits run out and the call reports
+// DT_DEV_ERR_TIMEOUT -- the bounded-wait exit, exercised without a fault.
+unsigned long long rd_wait_limit_ns() {
+  static unsigned long long v = 0;
+  if (!v) {
+    const char* e = getenv("DT_RD_WAIT_LIMIT_MS");
+    const long ms = e ? atol(e) : 0;
+    v = (ms > 0 && ms <= 10000) ? (unsigned long long)ms * 1000000ull : WAIT_LIMIT_NS;
+  }
+  return v;
+}
+
+int rd_starve() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("DT_RD_STARVE");
+    v = (e && e[0] == '1') ? 1 : 0;
+  }
+  return v;
+}
+
 // Whole rows per bulk work item (1: a long row is cut into segments of one
 // stage).
 void bulk_partition(RdTask* t, int esize) {
@@ -1059,6 +1085,8 @@ dt_status launch_kind(std::vector<PairPlan>& plans, int kind, int32_t* status, c
     p.ntasks = nt;
     p.nitems = items;
     p.status = status;
+    p.wait_limit_ns = rd_wait_limit_ns();
+    p.starve = rd_starve();
     if (grid > 0) {
       if (small) {
         std::copy(p.dst, p.dst + nd_slots, ps.dst);
@@ -1071,6 +1099,8 @@ dt_status launch_kind(std::vector<PairPlan>& plans, int kind, int32_t* status, c
         ps.esize = p.esize;
         ps.op = p.op;
         ps.status = p.status;
+        ps.wait_limit_ns = p.wait_limit_ns;
+        ps.starve = p.starve;
         launch_rd(ps, kind, bulk, grid, stream);
         if (g_recording) {
           const uint8_t* b = reinterpret_cast<const uint8_t*>(&ps);
