@@ -7,7 +7,11 @@
 //
 // Roles per CTA (224 threads): warp 0 TMA producer of A, warp 6 TMA producer
 // of B, warp 1 MMA issuer (rank 0 only; it owns the pair's MMAs) and TMEM
-// allocator, warps 2..5 epilogue (one accumulator row per thread).  Two
+// allocator, warps 2..5 epilogue (one accumulator row per thread).  The
+// producer and MMA warps run their loops with all 32 lanes, waits included,
+// and one elected lane issues the copies, MMAs and commits: the same loops
+// run by lane 0 alone, inside a branch on the lane, took 5-7% longer (the
+// issuing thread's time between stages shows up as tensor-pipe idle time).  Two
 // producers because one thread issuing every copy capped the copies alone
 // at ~46 B/clk per SM (the issuing thread blocks ~110 cycles per copy);
 // split, the copies alone run 16-20% faster and the GEMMs ~1%.
@@ -71,6 +75,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
   cluster_sync();  // barriers of both CTAs initialised, TMEM of both allocated
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const bool leader = elect_one();
 
   bool aborted = false;
 
@@ -80,8 +85,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
     // barrier for every byte of both CTAs); the B producer loads its B
     // columns.  Both walk the same stages and wait on the same `empty`.
     const bool loads_a = warp == 0;
-    if (lane == 0) {
-      for (int i = 0; i < p.ngroups; ++i) {
+    {
+      for (int i = 0; leader && i < p.ngroups; ++i) {
         const Group& G = p.groups[i];
         for (int s = G.seg_begin; s < G.seg_begin + G.seg_count && s < G.seg_begin + 2; ++s)
           prefetch_map(&p.maps[loads_a ? p.segs[s].a_map : p.segs[s].b_map]);
@@ -103,7 +108,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
           const CUtensorMap* bmap = &p.maps[(G.dual && rank == 1) ? S.b_map2 : S.b_map];
           const int kt_end = min(S.k_tiles, w.k1 - kbase);
           for (int kt = max(0, w.k0 - kbase); kt < kt_end; ++kt) {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.wait_limit_ns)) {
+            if (!mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag, p.wait_limit_ns)) {
               aborted = true;
               *abort_flag = 1;
               break;
@@ -111,14 +116,16 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
             const uint32_t full0 = mapa_shared(smem_u32(&full[stage]), 0);
             uint8_t* a = smem + stage * PAIR_STAGE_BYTES;
             uint8_t* b = a + PAIR_A_BYTES;
-            if (loads_a) {
-              if (rank == 0) mbar_expect_tx(&full[stage], 2 * PAIR_STAGE_BYTES);
-              tma_load_2d_pair(a, &p.maps[S.a_map], kt * BK, a_row, full0);
-            } else if (G.b_kmajor) {
-              tma_load_2d_pair(b, bmap, kt * BK, b_col, full0);  // 128 N rows of 64 K
-            } else {
-              tma_load_2d_pair(b, bmap, b_col, kt * BK, full0);
-              tma_load_2d_pair(b + B_CHUNK_BYTES, bmap, b_col + 64, kt * BK, full0);
+            if (leader) {
+              if (loads_a) {
+                if (rank == 0) mbar_expect_tx(&full[stage], 2 * PAIR_STAGE_BYTES);
+                tma_load_2d_pair(a, &p.maps[S.a_map], kt * BK, a_row, full0);
+              } else if (G.b_kmajor) {
+                tma_load_2d_pair(b, bmap, kt * BK, b_col, full0);  // 128 N rows of 64 K
+              } else {
+                tma_load_2d_pair(b, bmap, b_col, kt * BK, full0);
+                tma_load_2d_pair(b + B_CHUNK_BYTES, bmap, b_col + 64, kt * BK, full0);
+              }
             }
             if (++stage == PAIR_STAGES) {
               stage = 0;
@@ -131,7 +138,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (rank 0)
-    if (lane == 0 && rank == 0) {
+    if (rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int buf = 0;
@@ -144,7 +151,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
         const Group& G = p.groups[tc.g];
         const bool bk = G.b_kmajor != 0;
         const uint32_t idesc = instr_desc(PAIR_TILE_M, G.dual ? 2 * pair_dual_half(G, tc.n0) : 256, bk);
-        if (!mbar_wait(&tempty[buf], tphase ^ 1u, abort_flag, p.wait_limit_ns)) {
+        if (!mbar_wait_warp(&tempty[buf], tphase ^ 1u, abort_flag, p.wait_limit_ns)) {
           aborted = true;
           *abort_flag = 1;
           break;
@@ -157,7 +164,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
           const int kts = p.segs[si].k_tiles;
           const int kt_end = min(kts, w.k1 - kbase);
           for (int kt = max(0, w.k0 - kbase); kt < kt_end; ++kt) {
-            if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_limit_ns)) {
+            if (!mbar_wait_warp(&full[stage], phase, abort_flag, p.wait_limit_ns)) {
               aborted = true;
               *abort_flag = 1;
               break;
@@ -165,18 +172,20 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
             tc_fence_after();
             const uint32_t a_addr = a_base + stage * PAIR_STAGE_BYTES;
             const uint32_t b_addr = a_addr + PAIR_A_BYTES;
+            if (leader) {
 #pragma unroll
-            for (int j = 0; j < BK / 16; ++j) {
-              // 16-deep K steps: A advances 32 bytes inside its 128-byte
-              // swizzle rows; an MN-major B half is two 64-column chunks
-              // 8 KiB apart, a K-major one advances like A
-              const uint64_t adesc = smem_desc(a_addr + j * 32, 16, 1024);
-              const uint64_t bdesc =
-                  bk ? smem_desc(b_addr + j * 32, 16, 1024) : smem_desc(b_addr + j * 2048, B_CHUNK_BYTES, 1024);
-              mma_bf16_pair(d_tmem, adesc, bdesc, idesc, acc);
-              acc = 1;
+              for (int j = 0; j < BK / 16; ++j) {
+                // 16-deep K steps: A advances 32 bytes inside its 128-byte
+                // swizzle rows; an MN-major B half is two 64-column chunks
+                // 8 KiB apart, a K-major one advances like A
+                const uint64_t adesc = smem_desc(a_addr + j * 32, 16, 1024);
+                const uint64_t bdesc =
+                    bk ? smem_desc(b_addr + j * 32, 16, 1024) : smem_desc(b_addr + j * 2048, B_CHUNK_BYTES, 1024);
+                mma_bf16_pair(d_tmem, adesc, bdesc, idesc, acc | static_cast<uint32_t>(j));
+              }
+              mma_commit_pair_mc(&empty[stage], 0x3);
             }
-            mma_commit_pair_mc(&empty[stage], 0x3);
+            acc = 1;
             if (++stage == PAIR_STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -185,7 +194,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
           kbase += kts;
         }
         if (aborted) break;
-        mma_commit_pair_mc(&tfull[buf], 0x3);
+        if (leader) mma_commit_pair_mc(&tfull[buf], 0x3);
         if (++buf == 2) {
           buf = 0;
           tphase ^= 1u;
@@ -207,10 +216,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
     while (wi.next(&w)) {
       const TileCoord tc = decode_tile<PAIR_TILE_M>(p, w.t);
       const Group& G = p.groups[tc.g];
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(&tfull[buf], tphase, abort_flag, p.wait_limit_ns) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);  // tcgen05.ld below is warp-collective
-      if (!ok) {
+      // the whole warp waits: tcgen05.ld below is warp-collective
+      if (!mbar_wait_warp(&tfull[buf], tphase, abort_flag, p.wait_limit_ns)) {
         aborted = true;
         *abort_flag = 1;
         break;
@@ -356,10 +363,9 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
       for (int rd = 0; rd < nrounds; ++rd) {
         const int b = rd & 1;
         if (rd + 1 < nrounds) issue(rd + 1, b ^ 1);  // buffer b^1 was last read in round rd - 1
-        int ok = 1;
-        if (lane == 0) ok = mbar_wait(&fin_bar[quarter * 2 + b], (fin_phase >> b) & 1u, abort_flag, p.wait_limit_ns) ? 1 : 0;
+        const bool ok = mbar_wait_warp(&fin_bar[quarter * 2 + b], (fin_phase >> b) & 1u, abort_flag, p.wait_limit_ns);
         fin_phase ^= 1u << b;
-        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        if (!ok) {
           aborted = true;
           *abort_flag = 1;
           if (lane == 0) {  // let this warp's copies still in flight land before the CTA leaves
@@ -403,16 +409,16 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
   }
 
   // ------------------------------------------------------------ teardown
-  __syncwarp();  // lanes 1..31 of the producer and MMA warps wait here for their lane 0
+  __syncwarp();
   if (aborted && lane == 0) atomicOr(p.status, DT_DEV_ERR_TIMEOUT);
-  if ((warp == 0 || warp == PAIR_B_PRODUCER_WARP) && lane == 0 && aborted) {
+  if ((warp == 0 || warp == PAIR_B_PRODUCER_WARP) && leader && aborted) {
     // copies this CTA issued count on rank 0's barrier; give them a bounded
     // time to land before the pair leaves
     const uint64_t t0 = globaltimer();
     while (globaltimer() - t0 < 20000000ull) {
     }
   }
-  if (warp == 1 && lane == 0 && rank == 0) {
+  if (warp == 1 && leader && rank == 0) {
     // every MMA of the pair has completed before either CTA frees TMEM
     mma_commit_pair(drain);
     const uint64_t t0 = globaltimer();

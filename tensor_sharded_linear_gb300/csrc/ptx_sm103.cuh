@@ -67,6 +67,37 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// One thread of a converged warp: the leader issues what one thread must
+// issue (copies, MMAs, commits) while the whole warp walks the loop, so the
+// loop's values stay warp-uniform.  Taken once per warp and kept: every
+// commit must come from the thread that issued the MMAs it tracks.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// mbar_wait for a whole converged warp: every lane tests the barrier and the
+// warp leaves together (a phase, once seen complete, stays complete until
+// the warp itself lets the barrier move on).  Bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                               unsigned long long limit_ns = WAIT_LIMIT_NS) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = globaltimer();
+  uint32_t spins = 0;
+  while (true) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    if ((++spins & 255u) == 0) {
+      const int give_up = (*abort_flag != 0) || (globaltimer() - t0 > limit_ns);
+      if (__any_sync(0xffffffffu, give_up)) return false;
+    }
+  }
+}
+
 // Untiled bulk copy global -> this CTA's shared memory, completion counted
 // on `bar` (addresses 16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
