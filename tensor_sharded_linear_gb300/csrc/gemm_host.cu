@@ -439,9 +439,8 @@ SplitPlan plan_split(const LaunchShape& s, int ctas) {
   // most pieces one tile can have: the shares it meets
   const int np = share_min > 0 ? (int)((ki + share_min - 1) / share_min) + 1 : 0;
   const double split_cost = (double)rem * ki / ctas + SPLIT_OVERHEAD_ITERS;
-  // a finishing round stages one 32-column chunk of every piece (gate and
-  // up chunks for the gated MLP) in an epilogue warp's half of its quarter
-  const bool fits = np * (s.dual ? 2 : 1) <= FIN_MAX_PIECES;
+  // the warp that finishes a tile reads every piece's partial back
+  const bool fits = np <= FIN_MAX_PIECES;
   if (rem > 0 && share_min >= 8 && fits && (split_cost <= ki || split_mode() == 2)) {
     sp.sk_tiles = rem;
     sp.kiters = ki;

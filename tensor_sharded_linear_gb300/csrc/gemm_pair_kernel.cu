@@ -47,8 +47,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  // two per epilogue warp, for finishing split tiles (256 bytes past `full`)
-  uint64_t* fin_bar = full + 32;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -66,7 +64,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
       mbar_init(&tempty[b], 8);
     }
     mbar_init(drain, 1);
-    for (int i = 0; i < 8; ++i) mbar_init(&fin_bar[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -208,9 +205,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
     const uint32_t tempty0[2] = {mapa_shared(smem_u32(&tempty[0]), 0), mapa_shared(smem_u32(&tempty[1]), 0)};
     int buf = 0;
     uint32_t tphase = 0;
-    // split tiles this warp finishes at the end (a cluster holds at most two pieces)
-    int fin_t[2], fin_s[2], fin_first[2], fin_last[2];
-    int nfin = 0;
     WorkIter wi(p, cid, ncl);
     Work w;
     while (wi.next(&w)) {
@@ -288,122 +282,22 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
         tphase ^= 1u;
       }
       if (w.piece >= 0) {
-        // the piece whose arrival completes the tile's count finishes the
-        // tile once this CTA's MMAs are all done (see below); the partials
-        // were written by generic stores and are read back by bulk copies
-        // (the async proxy), so each lane fences both before the count
-        fence_proxy_async_global();
-        __threadfence();
+        // the warp whose arrival completes this tile's count (its CTA and
+        // row quarter) finishes the tile now, while the pair's MMAs move on
+        __threadfence();  // this lane's partial before the count
         __syncwarp();
         int c_first = 0, c_last = 0, last = 0;
         if (lane == 0) {
           sk_tile_clusters(p, ncl, w.s, &c_first, &c_last);
           int* cnt = p.sk_count + (w.s * 2 + static_cast<int>(rank)) * 4 + quarter;
-          if (atomicAdd(cnt, 1) == c_last - c_first) {
-            last = 1;
-            atomicExch(cnt, 0);  // ready for the next launch
-            __threadfence();
-          }
+          last = atomicAdd(cnt, 1) == c_last - c_first ? 1 : 0;
         }
-        if (__shfl_sync(0xffffffffu, last, 0) && nfin == 2) {  // the host never gives a pair three pieces
-          if (lane == 0) atomicOr(p.status, DT_DEV_ERR_INDEX);
-        } else if (__shfl_sync(0xffffffffu, last, 0)) {
-          fin_t[nfin] = w.t;
-          fin_s[nfin] = w.s;
-          fin_first[nfin] = __shfl_sync(0xffffffffu, c_first, 0);
-          fin_last[nfin] = __shfl_sync(0xffffffffu, c_last, 0);
-          ++nfin;
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+          __threadfence();  // every piece's partial after the count
+          const int first_piece = w.s + __shfl_sync(0xffffffffu, c_first, 0);
+          const int np = __shfl_sync(0xffffffffu, c_last, 0) - __shfl_sync(0xffffffffu, c_first, 0) + 1;
+          finish_split_tile(p, G, tc, row_ptr, first_piece, np, rank, quarter, lane);
         }
-      }
-    }
-
-    // Finish the split tiles this warp completed.  Every MMA of the pair has
-    // finished (the last tfull wait above), so the operand ring is idle:
-    // this warp streams the pieces' partials for its 32 rows into its
-    // quarter of the ring with bulk copies, two rounds in flight, and adds
-    // them in K order from shared memory.
-    uint8_t* fin_base = smem + quarter * FIN_WARP_BYTES;
-    uint32_t fin_phase = 0;  // bit b: parity of the next completion of fin_bar[quarter * 2 + b]
-    for (int f = 0; f < nfin && !aborted; ++f) {
-      const TileCoord tc = decode_tile<PAIR_TILE_M>(p, fin_t[f]);
-      const Group& G = p.groups[tc.g];
-      const int64_t r = tc.m0 + static_cast<int>(rank) * BM + row_in_tile;
-      char* row_ptr = nullptr;
-      if (r < G.m) {
-        int j = 0;
-        while (j + 1 < G.nout && G.out_row_begin[j + 1] <= r) ++j;
-        const int esize = G.out_dtype == DT_BF16 ? 2 : 4;
-        row_ptr = G.out_ptr[j] + (r - G.out_row_begin[j]) * G.out_ld[j] * esize;
-      }
-      const int np = fin_last[f] - fin_first[f] + 1;
-      const int per_round = G.dual ? 2 : 1;  // 32-column chunks per round (gate and up)
-      if (np * per_round > FIN_MAX_PIECES) {  // the host never splits this finely
-        if (lane == 0) atomicOr(p.status, DT_DEV_ERR_INDEX);
-        continue;
-      }
-      const int hh = G.dual ? pair_dual_half(G, tc.n0) : 0;
-      const int nrounds = G.dual ? hh >> 5 : min(8, (G.n - tc.n0 + 31) >> 5);
-      const int first_piece = fin_s[f] + fin_first[f];
-      auto issue = [&](int rd, int b) {
-        if (lane == 0) {
-          fence_proxy_async_global();  // the other pieces' partials, acquired through the count
-          fence_proxy_async_smem();
-          mbar_expect_tx(&fin_bar[quarter * 2 + b], static_cast<uint32_t>(np * per_round * FIN_CHUNK_BYTES));
-          uint8_t* dst = fin_base + b * FIN_BUF_BYTES;
-          for (int q = 0; q < np; ++q)
-            for (int j = 0; j < per_round; ++j) {
-              const int chunk = rd + j * (hh >> 5);  // gated MLP: up starts hh columns after gate
-              bulk_load(dst + (q * per_round + j) * FIN_CHUNK_BYTES,
-                        sk_slot(p, first_piece + q, rank, quarter) + chunk * 8 * 32, FIN_CHUNK_BYTES,
-                        &fin_bar[quarter * 2 + b]);
-            }
-        }
-      };
-      issue(0, 0);
-      for (int rd = 0; rd < nrounds; ++rd) {
-        const int b = rd & 1;
-        if (rd + 1 < nrounds) issue(rd + 1, b ^ 1);  // buffer b^1 was last read in round rd - 1
-        const bool ok = mbar_wait_warp(&fin_bar[quarter * 2 + b], (fin_phase >> b) & 1u, abort_flag, p.wait_limit_ns);
-        fin_phase ^= 1u << b;
-        if (!ok) {
-          aborted = true;
-          *abort_flag = 1;
-          if (lane == 0) {  // let this warp's copies still in flight land before the CTA leaves
-            const uint64_t t0 = globaltimer();
-            while (globaltimer() - t0 < 20000000ull) {
-            }
-          }
-          break;
-        }
-        const float4* buf = reinterpret_cast<const float4*>(fin_base + b * FIN_BUF_BYTES);
-        float v[2][32];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          if (j >= per_round) break;
-          for (int q = 0; q < np; ++q) {
-            const float4* src = buf + (q * per_round + j) * (FIN_CHUNK_BYTES / 16) + lane;
-#pragma unroll
-            for (int qv = 0; qv < 8; ++qv) {
-              const float4 x = src[qv * 32];
-              if (q == 0) {
-                v[j][4 * qv] = x.x;
-                v[j][4 * qv + 1] = x.y;
-                v[j][4 * qv + 2] = x.z;
-                v[j][4 * qv + 3] = x.w;
-              } else {
-                v[j][4 * qv] += x.x;
-                v[j][4 * qv + 1] += x.y;
-                v[j][4 * qv + 2] += x.z;
-                v[j][4 * qv + 3] += x.w;
-              }
-            }
-          }
-        }
-        if (row_ptr) {
-          if (G.dual) finish_dual(G, row_ptr, tc.n0 + rd * 32, v[0], v[1]);
-          else finish_chunk(G, row_ptr, tc.n0 + rd * 32, v[0]);
-        }
-        __syncwarp();  // every lane is done with buffer b before it is refilled
       }
     }
   }

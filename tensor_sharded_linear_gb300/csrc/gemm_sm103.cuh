@@ -79,9 +79,10 @@ struct ParamsT {  // CUtensorMap carries its own 128-byte alignment
   // clusters whole: their sk_tiles * sk_kiters K iterations are divided
   // evenly over all clusters, and each (cluster, tile) piece accumulates
   // its K range on its own.  Every piece writes its fp32 accumulator to
-  // sk_part; the piece whose arrival completes a tile's count (sk_count,
-  // one counter per tile, CTA and 32-row quarter, left at zero) adds all
-  // pieces in K order and runs the tile's epilogue.
+  // sk_part; the warp whose arrival completes a tile's count (sk_count,
+  // one counter per tile, CTA and 32-row quarter, zeroed before the launch)
+  // reads every piece's partial back, adds them in K order and runs the
+  // tile's epilogue for its 32 rows.
   int32_t sk_tiles;   // 0: every tile whole
   int32_t sk_kiters;  // K iterations of every tile (uniform when sk_tiles > 0)
   float* sk_part;     // [piece][2 CTAs][128 rows][256 columns]
@@ -148,14 +149,9 @@ constexpr int PAIR_B_BYTES = 128 * BK * 2;          // this CTA's 128 columns of
 constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
 constexpr int PAIR_BAR_BYTES = 512;  // barriers and flags
 constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + 1024 + PAIR_BAR_BYTES;
-// Split-tail finishing reuses the operand ring once a CTA's MMAs are all
-// done: each epilogue warp stages pieces' partials in its own quarter of
-// it, double-buffered.  A round moves one 32-column chunk (two, gate and up,
-// for the gated MLP) of every piece: 4 KiB per chunk per piece.
-constexpr int FIN_WARP_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES / 4;  // 48 KiB
-constexpr int FIN_BUF_BYTES = FIN_WARP_BYTES / 2;
-constexpr int FIN_CHUNK_BYTES = 32 * 32 * 4;                        // 32 rows x 32 fp32 columns
-constexpr int FIN_MAX_PIECES = FIN_BUF_BYTES / FIN_CHUNK_BYTES;     // 6 (3 for the gated MLP)
+// Most pieces a split tile may have: the warp that finishes it reads every
+// piece's partial from L2, so this bounds the finishing time.
+constexpr int FIN_MAX_PIECES = 8;
 constexpr int PAIR_TILE_M = 2 * BM;                 // rows of one pair tile
 constexpr int PAIR_B_PRODUCER_WARP = 6;             // after warps 0 (A), 1 (MMA), 2..5 (epilogue)
 constexpr int PAIR_THREADS = 32 * (PAIR_B_PRODUCER_WARP + 1);
@@ -295,9 +291,9 @@ __device__ __forceinline__ TileCoord decode_tile(const P& p, int t) {
 }
 
 // ---------------------------------------------------------------- work list
-// What one cluster does, in order: whole tiles cid, cid + ncl, ... below
-// the split tail, then its share [b(cid), b(cid + 1)) of the tail's K
-// iterations, b(c) = c * I / ncl, I = sk_tiles * sk_kiters.  The host only
+// What one cluster does, in order: its share [b(cid), b(cid + 1)) of the
+// split tail's K iterations, b(c) = c * I / ncl, I = sk_tiles * sk_kiters,
+// then whole tiles cid, cid + ncl, ... below the tail.  The host only
 // splits when a share is shorter than a tile, so a share covers the end of
 // one tail tile and the start of the next at most: one piece each.  The
 // piece of tail tile s done by cluster c has id s + c, unique because both
@@ -323,7 +319,23 @@ struct WorkIter {
     it = p.sk_tiles > 0 ? sk_bound(cid, total, ncl) : 0;
     it_end = p.sk_tiles > 0 ? sk_bound(cid + 1, total, ncl) : 0;
   }
+  // The cluster's pieces of the split tail come first, then its whole
+  // tiles: a tail tile is complete early in the launch, and the warp that
+  // finishes it does so while its pair's MMAs run the whole tiles.
   __device__ bool next(Work* w) {
+    if (it < it_end) {
+      const int s = (int)(it / kiters);
+      const int k0 = (int)(it - (int64_t)s * kiters);
+      const int64_t k1_wide = k0 + (it_end - it);
+      const int k1 = k1_wide < kiters ? (int)k1_wide : kiters;
+      w->t = dp_end + s;
+      w->k0 = k0;
+      w->k1 = k1;
+      w->piece = s + cid;
+      w->s = s;
+      it += k1 - k0;
+      return true;
+    }
     if (t_dp < dp_end) {
       w->t = t_dp;
       w->k0 = 0;
@@ -333,18 +345,7 @@ struct WorkIter {
       t_dp += ncl;
       return true;
     }
-    if (it >= it_end) return false;
-    const int s = (int)(it / kiters);
-    const int k0 = (int)(it - (int64_t)s * kiters);
-    const int64_t k1_wide = k0 + (it_end - it);
-    const int k1 = k1_wide < kiters ? (int)k1_wide : kiters;
-    w->t = dp_end + s;
-    w->k0 = k0;
-    w->k1 = k1;
-    w->piece = s + cid;
-    w->s = s;
-    it += k1 - k0;
-    return true;
+    return false;
   }
 };
 
@@ -508,6 +509,78 @@ __device__ __forceinline__ void finish_dual(const Group& G, char* row_ptr, int c
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
   store_row32(G, row_ptr, col0, v);
+}
+
+// ---------------------------------------------------------------- split tiles
+// A piece's partial in sk_part, as seen by one lane: 8 float4 (32 columns of
+// its row) 32 float4 apart; consecutive pieces' partials SK_PIECE_F4 apart.
+constexpr size_t SK_PIECE_F4 = 2 * 4 * 8 * 8 * 32;
+
+// v = the sum, in piece (K) order, of np pieces' 32 columns for this lane's
+// row, read from L2 (the pieces were written by other SMs) two pieces at a
+// time, so 16 loads are in flight per lane.
+__device__ __forceinline__ void sum_pieces(const float4* src, int np, float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 x = __ldcg(src + i * 32);
+    v[4 * i] = x.x;
+    v[4 * i + 1] = x.y;
+    v[4 * i + 2] = x.z;
+    v[4 * i + 3] = x.w;
+  }
+  for (int q = 1; q < np; q += 2) {
+    const float4* a = src + q * SK_PIECE_F4;
+    const bool two = q + 1 < np;
+    float4 xa[8], xb[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) xa[i] = __ldcg(a + i * 32);
+    if (two) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xb[i] = __ldcg(a + SK_PIECE_F4 + i * 32);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[4 * i] += xa[i].x;
+      v[4 * i + 1] += xa[i].y;
+      v[4 * i + 2] += xa[i].z;
+      v[4 * i + 3] += xa[i].w;
+    }
+    if (two) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[4 * i] += xb[i].x;
+        v[4 * i + 1] += xb[i].y;
+        v[4 * i + 2] += xb[i].z;
+        v[4 * i + 3] += xb[i].w;
+      }
+    }
+  }
+}
+
+// Finishes split tile tc for one epilogue warp's 32 rows (this lane's row
+// at row_ptr, null when past the last row): the np pieces first_piece ...
+// are added in K order and the sums take the tile's normal epilogue.
+template <class P>
+__device__ __noinline__ void finish_split_tile(const P& p, const Group& G, const TileCoord& tc, char* row_ptr,
+                                               int first_piece, int np, uint32_t rank, int quarter, int lane) {
+  const float4* src = sk_slot(p, first_piece, rank, quarter) + lane;
+  if (!G.dual) {
+    const int nrounds = min(8, (G.n - tc.n0 + 31) >> 5);
+    for (int rd = 0; rd < nrounds; ++rd) {
+      float v[32];
+      sum_pieces(src + rd * 8 * 32, np, v);
+      if (row_ptr) finish_chunk(G, row_ptr, tc.n0 + rd * 32, v);
+    }
+  } else {
+    // gate in accumulator columns [0, hh), up in [hh, 2 hh)
+    const int hc = pair_dual_half(G, tc.n0) >> 5;
+    for (int rd = 0; rd < hc; ++rd) {
+      float g[32], u[32];
+      sum_pieces(src + rd * 8 * 32, np, g);
+      sum_pieces(src + (rd + hc) * 8 * 32, np, u);
+      if (row_ptr) finish_dual(G, row_ptr, tc.n0 + rd * 32, g, u);
+    }
+  }
 }
 
 }  // namespace gemm

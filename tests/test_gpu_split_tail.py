@@ -49,14 +49,15 @@ PAIRS = 76  # CTA pairs resident on a GB300 (152 SMs)
 
 def split_expected(tiles, kiters, dual=False, pairs=PAIRS):
     """The library's rule: a pair's share of the tail's K iterations plus
-    the split's fixed cost (72 iterations) is shorter than a tile, and a
-    finishing round's partials fit the epilogue warp's buffer."""
+    the split's fixed cost (72 iterations) is shorter than a tile, and no
+    tail tile has more than 8 pieces (the finishing warp reads them all).
+    `dual` (the gated MLP) does not change the rule."""
     rem = tiles % pairs
     share_min = rem * kiters // pairs
     if rem == 0 or share_min < 8:
         return False
     np_ = ceil_div(kiters, share_min) + 1
-    return np_ * (2 if dual else 1) <= 6 and rem * kiters / pairs + 72 <= kiters
+    return np_ <= 8 and rem * kiters / pairs + 72 <= kiters
 
 
 def r256(n):
@@ -134,16 +135,22 @@ def test_row_split(lib, mode):
         check_bf16(to_host(y16.slots[i], "bf16"), f, e, f"{mode} out {i}")
 
 
-def test_mlp_split(lib):
-    """The fused MLP with its gated gate/up GEMM split (40 dual tiles, 157 K
-    iterations, each shard's last tile 96 columns of gate and up).  The split GEMM's output, H, is checked per element; the
+MLP_SPLIT_SHAPES = [
+    (256, 10000, 8 * 600, 384, 8),  # 40 dual tiles, 157 K iterations: 3 pieces per tail tile
+    (256, 8000, 5 * 600, 384, 5),   # 25 dual tiles, 125 K iterations: 5 pieces per tail tile
+]
+
+
+@pytest.mark.parametrize("M,K,F,N,p", MLP_SPLIT_SHAPES)
+def test_mlp_split(lib, M, K, F, N, p):
+    """The fused MLP with its gated gate/up GEMM split (each shard's last
+    tile 88 columns of gate and up; 600 = 4 x 128 + 88).  The split GEMM's output, H, is checked per element; the
     MLP output with the relative Frobenius bound.  (Its max-abs error also
     carries H's bf16 rounding: where the kernel's fp32 SiLU(g)*u and the
     oracle's fp64 one round to neighbouring bf16 values, each such element
     moves outputs by one bf16 ulp of H times a weight, which at this K can
     pass 2e-3 on a few outputs with either schedule.  The down GEMM's split
     is test_mlp_down_split, on the oracle's H.)"""
-    M, K, F, N, p = 256, 10000, 8 * 600, 384, 8  # 600 = 4 x 128 + 88: a short last tile per shard
     assert split_expected(ceil_div(M, 256) * p * ceil_div(F // p, 128), ceil_div(K, 64), dual=True)
     x, wg, wu, wd = workloads.mlp_inputs(M, K, F, seed_base=700)
     wd = workloads.randn_bf16((F, N), 704, (1.0 / F) ** 0.5)
@@ -305,7 +312,8 @@ sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
 import test_gpu_split_tail as T
 T.test_column_split(None)
 T.test_row_split(None, T.tsl.ALL_REDUCE)
-T.test_mlp_split(None)
+for shape in T.MLP_SPLIT_SHAPES:
+    T.test_mlp_split(None, *shape)
 T.test_mlp_down_split(None)
 print("OK")
 """
