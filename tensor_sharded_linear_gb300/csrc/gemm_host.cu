@@ -391,7 +391,8 @@ int group_kiters(const HostGroup& G) {
 struct LaunchShape {
   int tiles = 0;
   int m_tiles = 0;   // > 0: every group has this many M tiles
-  int total_n = 0;   // N tiles over all groups
+  int m_blocks = 1;  // row blocks (runs of groups with one N structure)
+  int total_n = 0;   // N tiles over the groups of one row block
   int kiters = 0;    // K iterations of every tile when uniform
   bool uniform = true;
   bool dual = false;
@@ -413,6 +414,26 @@ LaunchShape launch_shape(const std::vector<HostGroup>& groups, size_t b, size_t 
     s.dual = s.dual || G.dual;
   }
   s.m_tiles = common_m > 0 ? common_m : 0;
+  // row blocks: equal runs of groups by m_block whose N tiles match
+  // position by position; then the M axis is the blocks end to end
+  const size_t n = e - b;
+  size_t run = 1;
+  while (run < n && groups[b + run].m_block == groups[b].m_block) ++run;
+  if (s.m_tiles > 0 && run < n && n % run == 0) {
+    bool ok = true;
+    for (size_t i = run; i < n && ok; ++i) {
+      const HostGroup& G = groups[b + i];
+      const HostGroup& F = groups[b + i % run];
+      const HostGroup& P = groups[b + i - 1];
+      ok = G.n == F.n && group_bn(G) == group_bn(F) && G.dual == F.dual &&
+           (i % run == 0 ? G.m_block != P.m_block : G.m_block == P.m_block);
+    }
+    if (ok) {
+      s.m_blocks = (int)(n / run);
+      s.total_n = 0;
+      for (size_t i = 0; i < run; ++i) s.total_n += (int)((groups[b + i].n + group_bn(groups[b + i]) - 1) / group_bn(groups[b + i]));
+    }
+  }
   return s;
 }
 
@@ -474,9 +495,10 @@ void choose_bands(const std::vector<HostGroup>& groups, size_t b, size_t e, cons
   *band_m = 1;
   *band_n = std::max(1, s.total_n);
   if (s.m_tiles <= 0) return;
+  const int m_all = s.m_tiles * s.m_blocks;
   int om, on;
   if (bands_override(&om, &on)) {
-    *band_m = std::min(om, s.m_tiles);
+    *band_m = std::min(om, m_all);
     *band_n = std::min(on, s.total_n);
     return;
   }
@@ -484,13 +506,13 @@ void choose_bands(const std::vector<HostGroup>& groups, size_t b, size_t e, cons
   for (size_t g = b; g < e; ++g) max_k = std::max<int64_t>(max_k, (int64_t)group_kiters(groups[g]) * BK);
   const int64_t a_tile_bytes = (int64_t)PAIR_TILE_M * std::max<int64_t>(max_k, 1) * 2;
   if (max_k >= 8192) {
-    *band_m = std::min(8, s.m_tiles);
+    *band_m = std::min(8, m_all);
     *band_n = std::min(4, *band_n);
     return;
   }
   int band = (int)std::max<int64_t>(1, (32ll << 20) / a_tile_bytes);
   band = std::max(band, (ctas + s.total_n - 1) / s.total_n);
-  *band_m = std::max(1, std::min(band, s.m_tiles));
+  *band_m = std::max(1, std::min(band, m_all));
 }
 
 // ---- launches
@@ -563,8 +585,11 @@ dt_status run_tcgen05(const std::vector<HostGroup>& groups, int32_t* status, cud
     p.status = status;
     p.wait_limit_ns = gemm_wait_limit_ns();
     p.starve = gemm_starve();
+    // N tile prefix sums over one row block's groups (all groups when the
+    // launch is one block)
+    p.m_blocks = shape.m_blocks;
     p.n_tile_begin[0] = 0;
-    for (int g = 0; g < p.ngroups; ++g) p.n_tile_begin[g + 1] = p.n_tile_begin[g] + p.groups[g].n_tiles;
+    for (int g = 0; g < p.ngroups / p.m_blocks; ++g) p.n_tile_begin[g + 1] = p.n_tile_begin[g] + p.groups[g].n_tiles;
     p.m_tiles = shape.m_tiles;
     choose_bands(groups, gi, g_end, shape, ctas, &p.band_m, &p.band_n);
     // the split tail, where the caller's workspace holds its scratch

@@ -391,6 +391,7 @@ cudaError_t launch_tcgen05_pair(const Params& p, int clusters, cudaStream_t stre
     ps.ngroups = p.ngroups;
     ps.total_tiles = p.total_tiles;
     ps.m_tiles = p.m_tiles;
+    ps.m_blocks = p.m_blocks;
     ps.band_m = p.band_m;
     ps.band_n = p.band_n;
     ps.starve = p.starve;

@@ -42,6 +42,9 @@ struct HostGroup {
   std::vector<int64_t> out_ld;
   const void* bias = nullptr;  // [n], added before the cast
   int bias_dtype = -1;
+  // row block of x the group reads, when x is split by rows into several
+  // slots (token shards); groups come ordered by it
+  int m_block = 0;
 };
 
 // Caller-owned device memory a call may use for the split tail's scratch

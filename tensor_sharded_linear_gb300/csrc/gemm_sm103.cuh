@@ -70,6 +70,7 @@ struct ParamsT {  // CUtensorMap carries its own 128-byte alignment
   int32_t nmaps, nsegs;               // entries of maps and segs in use
   int32_t ngroups, total_tiles;
   int32_t m_tiles;  // > 0: every group has this many M tiles, rastered together
+  int32_t m_blocks; // row blocks: groups [b * ngroups / m_blocks, ...) hold rows block b
   int32_t band_m;   // M tiles per raster band
   int32_t band_n;   // N tiles (across groups) per block of a band
   int32_t starve;   // test hook: producers issue no loads, so every MMA wait runs out
@@ -246,7 +247,11 @@ struct TileCoord {
 
 // Tile order of a launch whose groups all have the same M tiles (all groups
 // of a column-parallel launch share x; a row-parallel launch is one group):
-// the groups' N tiles form one axis of total_n tiles.  Tiles go in bands of
+// the groups' N tiles form one axis of total_n tiles.  When x is split into
+// row blocks (a token-sharded input: one group per (row block, weight
+// shard)), the launch holds m_blocks runs of groups with the same N
+// structure, and the M axis is the blocks' M tiles end to end: the tiles
+// form the same grid as the one GEMM they are parts of.  Tiles go in bands of
 // band_m M tiles; a band is cut into blocks of band_n N tiles, visited in
 // order, with M fastest inside a block; odd bands sweep N backwards, so
 // consecutive bands start on the B panels the previous one ended on.
@@ -273,14 +278,28 @@ __host__ __device__ __forceinline__ void band_order(int t, int m_tiles, int tota
 template <int TILE_M, class P>
 __device__ __forceinline__ TileCoord decode_tile(const P& p, int t) {
   if (p.m_tiles > 0) {
+    const int gpb = p.ngroups / p.m_blocks;  // groups per row block
     int mi, jn;
-    band_order(t, p.m_tiles, p.n_tile_begin[p.ngroups], p.band_m, p.band_n, &mi, &jn);
-    int g = 0;
-    while (g + 1 < p.ngroups && p.n_tile_begin[g + 1] <= jn) ++g;
-    return TileCoord{g, mi * TILE_M, (jn - p.n_tile_begin[g]) * p.groups[g].bn};
+    band_order(t, p.m_tiles * p.m_blocks, p.n_tile_begin[gpb], p.band_m, p.band_n, &mi, &jn);
+    const int mb = mi / p.m_tiles;
+    // the group holding N tile jn: binary search of the prefix sums (a
+    // launch may hold 48 groups, e.g. sequence-parallel q/k/v)
+    int lo = 0, hi = gpb - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.n_tile_begin[mid] <= jn) lo = mid;
+      else hi = mid - 1;
+    }
+    const int g = mb * gpb + lo;
+    return TileCoord{g, (mi - mb * p.m_tiles) * TILE_M, (jn - p.n_tile_begin[lo]) * p.groups[g].bn};
   }
-  int g = 0;
-  while (g + 1 < p.ngroups && p.groups[g + 1].tile_begin <= t) ++g;
+  int lo = 0, hi = p.ngroups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.groups[mid].tile_begin <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  const int g = lo;
   const Group& G = p.groups[g];
   const int local = t - G.tile_begin;
   const int span = GROUP_M * G.n_tiles;

@@ -233,6 +233,7 @@ dt_status add_column_groups(const DTensor& X, const ColumnSpec& c, int tp, std::
       HostGroup g;
       g.m = a.rows;
       g.n = b.cols;
+      g.m_block = x_seq ? j : 0;
       g.segs.push_back(HostSeg{a, b, Mat()});
       g.out_dtype = ly.dtype;
       const int esize = dtype_size(ly.dtype);
@@ -279,6 +280,10 @@ dt_status column_build(const dt_dtensor* x, int32_t n, const dt_dtensor* w, cons
     ColumnSpec c{&W[j], has_bias[j] ? &B[j] : nullptr, &Y[j]};
     if ((st = add_column_groups(X, c, tp, groups, &done)) != DT_OK) return st;
   }
+  // a token-sharded x: each token shard's groups together, in weight order,
+  // so a launch can order its tiles as the one GEMM of which they are parts
+  std::stable_sort(groups->begin(), groups->end(),
+                   [](const HostGroup& a, const HostGroup& b) { return a.m_block < b.m_block; });
   return DT_OK;
 }
 
