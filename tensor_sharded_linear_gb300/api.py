@@ -144,6 +144,7 @@ class DTensor:
             if t.dtype != dtype:
                 raise ValueError("slot dtype")
         self.slots = list(slots)
+        self._layout_key = bytes(self._layout)
 
     # -- layout queries (host only)
     @property
@@ -254,19 +255,27 @@ class DTensor:
         return len(self.gshape)
 
     # -- ABI descriptor
+    def _key(self):
+        """What the descriptor is made of: each slot's address and strides."""
+        return tuple((t.data_ptr() if t.numel() else 0, t.stride()) for t in self.slots)
+
     def _desc(self):
-        ptrs = (C.c_void_p * max(1, self.nslots))(*[t.data_ptr() if t.numel() else None for t in self.slots])
-        nd = len(self.gshape)
-        strides = (C.c_int64 * max(1, self.nslots * nd))()
-        for s, t in enumerate(self.slots):
-            for d in range(nd):
-                strides[s * nd + d] = t.stride(d)
+        """The C descriptor (dt_dtensor) of this tensor.  Built once and kept
+        while the slots' addresses and strides stay the same."""
+        key = self._key()
+        cached = getattr(self, "_desc_cache", None)
+        if cached is not None and cached[0] == key:
+            return cached[1]
+        n = max(1, self.nslots)
+        ptrs = (C.c_void_p * n)(*[p or None for p, _ in key])
+        strides = (C.c_int64 * max(1, self.nslots * len(self.gshape)))(*[d for _, st in key for d in st])
         desc = L.DTensorDesc()
         desc.layout = self._layout
         desc.nslots = self.nslots
         desc.slots = C.cast(ptrs, C.POINTER(C.c_void_p))
         desc.strides = C.cast(strides, C.POINTER(C.c_int64))
         desc._keep = (ptrs, strides)  # keep the arrays alive with the descriptor
+        self._desc_cache = (key, desc)
         return desc
 
     def __repr__(self):
@@ -333,6 +342,26 @@ def _ws_args(workspace: Optional[torch.Tensor]):
     return workspace.data_ptr(), workspace.numel() * workspace.element_size()
 
 
+_WS_SIZES: dict = {}
+
+
+def _op_key(op, tensors, *args):
+    """Everything a workspace size depends on: the operands' layouts,
+    addresses and strides, the call's other arguments and the device."""
+    return (op, tensors[0].slots[0].device if tensors[0].slots else None,
+            tuple((t._layout_key, t._key()) for t in tensors), args)
+
+
+def _ws_size(key, query):
+    """A workspace-size query's answer, kept per operand set (see _op_key)."""
+    v = _WS_SIZES.get(key)
+    if v is None:
+        if len(_WS_SIZES) >= 256:
+            _WS_SIZES.clear()
+        v = _WS_SIZES[key] = query()
+    return v
+
+
 def _workspace(nbytes: int, device) -> Optional[torch.Tensor]:
     """Device memory for a call's workspace (None when it needs none).  Torch
     allocates it: the library itself allocates nothing."""
@@ -343,14 +372,17 @@ def column_parallel_linear_workspace_bytes(x: DTensor, ws: Sequence[DTensor], ys
                                            tp_dim="tp") -> int:
     """dt_column_parallel_linear_workspace_size for the weights ``ws`` and outputs ``ys``."""
     n = len(ws)
-    wdescs, ydescs = [w._desc() for w in ws], [y._desc() for y in ys]
-    wd, yd = (L.DTensorDesc * n)(*wdescs), (L.DTensorDesc * n)(*ydescs)
-    out = C.c_size_t()
-    L.check(L.load().dt_column_parallel_linear_workspace_size(C.byref(x._desc()), n, wd, yd,
-                                                              _tp_index(x.mesh, tp_dim), C.byref(out)),
-            "column_parallel_linear_workspace_size")
-    del wdescs, ydescs
-    return out.value
+    tp = _tp_index(x.mesh, tp_dim)
+
+    def query():
+        wdescs, ydescs = [w._desc() for w in ws], [y._desc() for y in ys]
+        wd, yd = (L.DTensorDesc * n)(*wdescs), (L.DTensorDesc * n)(*ydescs)
+        out = C.c_size_t()
+        L.check(L.load().dt_column_parallel_linear_workspace_size(C.byref(x._desc()), n, wd, yd, tp, C.byref(out)),
+                "column_parallel_linear_workspace_size")
+        return out.value
+
+    return _ws_size(_op_key("column", [x, *ws, *ys], n, tp), query)
 
 
 def column_parallel_linear(x: DTensor, w: DTensor, bias: Optional[DTensor] = None, tp_dim="tp",
@@ -401,12 +433,16 @@ def _row_out(x: DTensor, w: DTensor, tp: int, mode: str, out_dtype) -> DTensor:
 def row_parallel_linear_workspace_bytes(x: DTensor, w: DTensor, y: DTensor, mode: str = ALL_REDUCE,
                                         tp_dim="tp") -> int:
     """dt_row_parallel_linear_workspace_size."""
-    out = C.c_size_t()
-    L.check(L.load().dt_row_parallel_linear_workspace_size(C.byref(x._desc()), C.byref(w._desc()),
-                                                           C.byref(y._desc()), _MODES[mode],
-                                                           _tp_index(x.mesh, tp_dim), C.byref(out)),
-            "row_parallel_linear_workspace_size")
-    return out.value
+    tp = _tp_index(x.mesh, tp_dim)
+
+    def query():
+        out = C.c_size_t()
+        L.check(L.load().dt_row_parallel_linear_workspace_size(C.byref(x._desc()), C.byref(w._desc()),
+                                                               C.byref(y._desc()), _MODES[mode], tp, C.byref(out)),
+                "row_parallel_linear_workspace_size")
+        return out.value
+
+    return _ws_size(_op_key("row", [x, w, y], mode, tp), query)
 
 
 def row_parallel_linear(x: DTensor, w: DTensor, bias: Optional[DTensor] = None, mode: str = ALL_REDUCE,
@@ -428,11 +464,16 @@ def row_parallel_linear(x: DTensor, w: DTensor, bias: Optional[DTensor] = None, 
 def tp_mlp_workspace_bytes(x: DTensor, w_gate: DTensor, w_up: DTensor, w_down: DTensor, y: DTensor,
                            mode: str = ALL_REDUCE, tp_dim="tp") -> int:
     """dt_tp_mlp_workspace_size: H plus the split tail's scratch."""
-    n = C.c_size_t()
-    L.check(L.load().dt_tp_mlp_workspace_size(C.byref(x._desc()), C.byref(w_gate._desc()), C.byref(w_up._desc()),
-                                              C.byref(w_down._desc()), C.byref(y._desc()), _MODES[mode],
-                                              _tp_index(x.mesh, tp_dim), C.byref(n)), "tp_mlp_workspace_size")
-    return n.value
+    tp = _tp_index(x.mesh, tp_dim)
+
+    def query():
+        n = C.c_size_t()
+        L.check(L.load().dt_tp_mlp_workspace_size(C.byref(x._desc()), C.byref(w_gate._desc()), C.byref(w_up._desc()),
+                                                  C.byref(w_down._desc()), C.byref(y._desc()), _MODES[mode], tp,
+                                                  C.byref(n)), "tp_mlp_workspace_size")
+        return n.value
+
+    return _ws_size(_op_key("mlp", [x, w_gate, w_up, w_down, y], mode, tp), query)
 
 
 def tp_mlp_output(x: DTensor, w_down: DTensor, mode: str = ALL_REDUCE, tp_dim="tp", out_dtype=None) -> DTensor:
