@@ -28,6 +28,12 @@
 //   tempty[b]  in rank 0: 8 arrivals, the 4 epilogue warps of each CTA.
 // Every wait is bounded (Params::wait_limit_ns); on expiry the role raises
 // the CTA's abort flag, the launch reports DT_DEV_ERR_TIMEOUT and unwinds.
+// Split tail (Params::sk_tiles > 0): a cluster runs its pieces of the tail
+// tiles first, then its whole tiles; a piece's epilogue writes its fp32
+// partial to the workspace and counts it, and the warp whose count completes
+// a tail tile adds every piece's partial (read from L2, in K order) and runs
+// the tile's epilogue, while the pair's MMAs move on.  No wait involves
+// another cluster.
 #include <algorithm>
 
 #include "gemm_plan.h"
