@@ -690,6 +690,9 @@ __global__ void __launch_bounds__(RDT_THREADS, 1) rd_tma_kernel(const __grid_con
         const char* s;
         rows.at(p, T, e0, &d, &s);
         bulk_store(d, src, nbytes);
+        // the replicas of a materialised Replicate layout: the same row,
+        // stored again from the same stage a fixed byte distance away
+        for (int x = 1; x <= T.nextra; ++x) bulk_store(d + p.ref[T.ref_begin + x].off, src, nbytes);
       }
       bulk_commit();
     }
@@ -961,10 +964,10 @@ template <class P>
 void launch_rd(const P& p, int kind, bool bulk, int grid, cudaStream_t stream) {
   if (kind == RD_SUM)
     rd_kernel<true, false, P><<<grid, RD_THREADS, 0, stream>>>(p);
+  else if (bulk)  // copies, to replicas too
+    rd_tma_kernel<P><<<grid, RDT_THREADS, RDT_SMEM_BYTES, stream>>>(p);
   else if (kind == RD_COPY_REPL)
     rd_kernel<false, true, P><<<grid, RD_THREADS, 0, stream>>>(p);
-  else if (bulk)
-    rd_tma_kernel<P><<<grid, RDT_THREADS, RDT_SMEM_BYTES, stream>>>(p);
   else
     rd_kernel<false, false, P><<<grid, RD_THREADS, 0, stream>>>(p);
 }
@@ -1026,9 +1029,10 @@ int64_t bulk_items(const RdTask& t) {
 }
 
 // Every row of the task starts on a 16-byte boundary in both slots and is
-// a multiple of 16 bytes long.
+// a multiple of 16 bytes long; replicas (if any) sit a multiple of 16 bytes
+// from the first destination.
 bool bulk_task_ok(const RdTask& t, const RdSlot& D, const RdSlot& S, int64_t src_off, int esize) {
-  if (t.nsrc != 1 || t.nextra != 0) return false;
+  if (t.nsrc != 1 || (t.nextra != 0 && !t.extra16)) return false;
   if (D.stride[t.dmap[3]] != 1 || S.stride[t.dmap[3]] != 1) return false;
   if ((t.ext[3] * esize) % 16) return false;
   if ((reinterpret_cast<uintptr_t>(D.ptr) + (uintptr_t)(t.dst_off * esize)) % 16) return false;
@@ -1061,8 +1065,9 @@ dt_status launch_kind(std::vector<PairPlan>& plans, int kind, int32_t* status, c
   const int sms = device_sm_count();
   int nd_slots = 0, ns_slots = 0, nt = 0, nref = 0;
   int64_t items = 0;
-  // every copy task so far can run on the bulk copy kernel (rows aligned on both sides)
-  bool aligned = kind == RD_COPY && bulk_copies() == 1;
+  // every copy task so far can run on the bulk copy kernel (rows aligned on
+  // both sides, replicas a multiple of 16 bytes apart)
+  bool aligned = (kind == RD_COPY || kind == RD_COPY_REPL) && bulk_copies() == 1;
   auto flush = [&]() -> dt_status {
     if (nt == 0) return DT_OK;
     const bool small = nd_slots <= ps.kSlots && ns_slots <= ps.kSlots && nt <= ps.kTasks && nref <= ps.kRefs;

@@ -8,7 +8,8 @@ bulk kernel: rows packed several to a work item and long rows cut into
 segments, bf16 / fp32 / int32, three- and four-dimensional boxes whose rows
 wrap the outer indices inside one work item, slots that are views of
 parent buffers at 16-byte aligned offsets with padded pitches, batches of
-several pairs, and a launch that mixes an aligned and an unaligned pair (it
+several pairs, copies to materialised replicas (one staged row stored to
+every replica), and a launch that mixes an aligned and an unaligned pair (it
 takes the other kernel).  The same cases run with the bulk kernel turned
 off (DT_RD_BULK=0, in a child process).
 """
@@ -110,6 +111,23 @@ def test_views_in_parent_buffers(lib, offset, pad):
         np.testing.assert_array_equal(to_host(t, "bf16"), e, err_msg=f"slot {s}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("gshape", [(64, 1024), (12, 24576), (40, 2056)])
+def test_materialised_replicas(lib, dtype, gshape):
+    """Copies to a materialised Replicate layout (a slot per rank): each
+    source row is staged once and stored to every replica.  Rows packed
+    several to an item, long rows cut into segments, and (40, 2056) whose
+    S(1) shards are 514 elements: bf16 rows of 1028 bytes are not 16-byte
+    multiples (the other kernel), fp32 rows of 2056 bytes are."""
+    nrng = np.random.default_rng(sum(gshape) + len(dtype))
+    mesh = (2, 4)
+    for sp, dp, smat, dmat in (([S(0), S(0)], [S(0), R], False, True), ([S(0), S(1)], [R, R], False, True),
+                               ([S(0), R], [R, R], True, True), ([R, S(1)], [S(0), R], False, True)):
+        src, dst = opl.Layout(mesh, sp, gshape, smat), opl.Layout(mesh, dp, gshape, dmat)
+        g = random_values(gshape, dtype, nrng)
+        run(ord_.distribute(g, src, dtype), src, dst, dtype)
+
+
 def test_batches(lib):
     """Several aligned pairs in one launch; then the same with one unaligned pair added."""
     rng = random.Random(3)
@@ -149,6 +167,9 @@ for args in [((6, 40, 512), [T.S(1), T.S(2)], [T.S(2), T.S(1)]), ((3, 7, 11, 256
 for off, pad in ((8, 8), (3, 5)):
     T.test_views_in_parent_buffers(None, off, pad)
 T.test_batches(None)
+for dt in ("bf16", "fp32"):
+    for g in [(64, 1024), (12, 24576), (40, 2056)]:
+        T.test_materialised_replicas(None, dt, g)
 print("OK")
 """
 
