@@ -1,6 +1,7 @@
 // Inline-PTX helpers for sm_103a shared by the GEMM and the data-movement
-// kernels: mbarriers with bounded waits, the untiled bulk (TMA) copy from
-// global to shared memory, and proxy fences.
+// kernels: mbarriers with bounded waits (per thread and per converged warp),
+// warp leader election, and the untiled bulk (TMA) copy from global to
+// shared memory.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -107,19 +108,6 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
                    smem_u32(smem_dst)),
                "l"(g), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
-}
-
-// Order this thread's earlier generic-proxy shared-memory accesses before
-// later async-proxy ones (a bulk copy overwriting what was just read).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// The same for global memory: generic-proxy stores of split-tail partials
-// before the counter update that publishes them, and, in the finishing
-// thread, the acquired counter before the bulk copies that read them.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 }  // namespace dt
