@@ -266,6 +266,17 @@ cudaError_t launch_pitch_copy(const PitchCopy& c, cudaStream_t stream) {
 
 // ------------------------------------------------------------ lowering
 
+// Every output block starts on a 32-byte boundary and its pitch is a
+// multiple of 32 bytes: the epilogue may store whole 32-byte sectors.
+bool out_vec32_ok(const HostGroup& g) {
+  const int esize = g.out_dtype == DT_BF16 ? 2 : 4;
+  for (size_t j = 0; j < g.out_ptr.size(); ++j) {
+    if (reinterpret_cast<uintptr_t>(g.out_ptr[j]) % 32) return false;
+    if ((g.out_ld[j] * esize) % 32) return false;
+  }
+  return true;
+}
+
 bool out_vec_ok(const HostGroup& g) {
   const int esize = g.out_dtype == DT_BF16 ? 2 : 4;
   for (size_t j = 0; j < g.out_ptr.size(); ++j) {
@@ -569,6 +580,7 @@ dt_status run_tcgen05(const std::vector<HostGroup>& groups, int32_t* status, cud
       G.bias = H.bias;
       G.bias_dtype = H.bias ? H.bias_dtype : -1;
       G.out_vec = out_vec_ok(H) ? 1 : 0;
+      G.out_vec32 = out_vec32_ok(H) ? 1 : 0;
       G.b_kmajor = H.segs.empty() ? 0 : (H.segs[0].b.kmajor ? 1 : 0);
       for (const HostSeg& sg : H.segs) {
         Seg& S = p.segs[seg_i++];
