@@ -585,6 +585,7 @@ dt_status run_tcgen05(const std::vector<HostGroup>& groups, int32_t* status, cud
       for (const HostSeg& sg : H.segs) {
         Seg& S = p.segs[seg_i++];
         S.k_tiles = (int32_t)((sg.a.cols + BK - 1) / BK);
+        S.last_steps = (int32_t)((sg.a.cols - (int64_t)(S.k_tiles - 1) * BK + 15) / 16);
         if ((st = map_index(sg.a, BM, &S.a_map)) != DT_OK) return st;
         if ((st = map_index(stored(sg.b), b_box_rows(H), &S.b_map)) != DT_OK) return st;
         S.b_map2 = S.b_map;

@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
         int kbase = 0;
         for (int si = G.seg_begin; si < G.seg_begin + G.seg_count && !aborted; ++si) {
           const int kts = p.segs[si].k_tiles;
+          const int last_steps = p.segs[si].last_steps;
           const int kt_end = min(kts, w.k1 - kbase);
           for (int kt = max(0, w.k0 - kbase); kt < kt_end; ++kt) {
             if (!mbar_wait_warp(&full[stage], phase, abort_flag, p.wait_limit_ns)) {
@@ -175,9 +176,11 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) tcgen05_gemm_pair_kernel(cons
             tc_fence_after();
             const uint32_t a_addr = a_base + stage * PAIR_STAGE_BYTES;
             const uint32_t b_addr = a_addr + PAIR_A_BYTES;
+            const int nsteps = kt == kts - 1 ? last_steps : BK / 16;  // the K tail past the data is zero fill
             if (leader) {
 #pragma unroll
               for (int j = 0; j < BK / 16; ++j) {
+                if (j >= nsteps) break;
                 // 16-deep K steps: A advances 32 bytes inside its 128-byte
                 // swizzle rows; an MN-major B half is two 64-column chunks
                 // 8 KiB apart, a K-major one advances like A

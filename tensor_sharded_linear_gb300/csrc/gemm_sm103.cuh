@@ -43,6 +43,7 @@ constexpr int MAX_OUT = 8;
 
 struct Seg {
   int32_t a_map, b_map, b_map2, k_tiles;
+  int32_t last_steps;  // 16-deep MMA steps of the last K tile that hold data (1..4)
 };
 
 struct Group {
