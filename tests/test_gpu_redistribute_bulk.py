@@ -128,6 +128,30 @@ def test_materialised_replicas(lib, dtype, gshape):
         run(ord_.distribute(g, src, dtype), src, dst, dtype)
 
 
+@pytest.mark.parametrize("shift", [8, 4])
+def test_replicas_at_any_distance(lib, shift):
+    """Materialised replicas that are views of one parent buffer, `shift`
+    elements apart from 16-byte boundaries: 8 bf16 (16 bytes) keeps every
+    replica a multiple of 16 bytes from the first (bulk kernel), 4 (8 bytes)
+    does not (the other kernel).  Bit-exact either way."""
+    gshape = (64, 2048)
+    g = random_values(gshape, "bf16", np.random.default_rng(shift))
+    src_l = opl.Layout((4,), [S(0)], gshape)
+    locals_ = ord_.distribute(g, src_l, "bf16")
+    src = dtensor_from_locals(locals_, src_l, "bf16")
+    n = gshape[0] * gshape[1]
+    parent = torch.zeros(4 * n + 4 * shift + 64, dtype=torch.bfloat16, device="cuda")
+    # replica k starts k * (n + shift) elements in: 16-byte aligned for k = 0
+    slots = [parent[k * (n + shift):k * (n + shift) + n].view(gshape) for k in range(4)]
+    dst = tsl.DTensor(slots, tsl.DeviceMesh((4,)), [tsl.Replicate()], gshape, torch.bfloat16,
+                      materialize_replicas=True)
+    tsl.redistribute(src, dst)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    for k, t in enumerate(dst.slots):
+        np.testing.assert_array_equal(to_host(t, "bf16"), g, err_msg=f"shift {shift} replica {k}")
+
+
 def test_batches(lib):
     """Several aligned pairs in one launch; then the same with one unaligned pair added."""
     rng = random.Random(3)
@@ -170,6 +194,8 @@ T.test_batches(None)
 for dt in ("bf16", "fp32"):
     for g in [(64, 1024), (12, 24576), (40, 2056)]:
         T.test_materialised_replicas(None, dt, g)
+for shift in (8, 4):
+    T.test_replicas_at_any_distance(None, shift)
 print("OK")
 """
 
