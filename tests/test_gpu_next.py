@@ -1,4 +1,4 @@
-"""GPU parity of the rows built after the hot path (the survey's NEXT list):
+"""GPU parity of the layers and moves built beside the hot path:
 
 * the sequence-parallel column entry (nanotron 5.1's REDUCE_SCATTER-mode
   column layer: x sharded over tokens, all-gathered, then the column GEMM) --
