@@ -33,7 +33,11 @@ def x_tokens(x_bits, p):
     return tsl.DTensor(slots, mesh1(p), [tsl.Shard(0)], x_bits.shape, torch.bfloat16)
 
 
-@pytest.mark.parametrize("T,K,N,p", [(384, 256, 1056, 4), (301, 200, 8 * 136, 8), (1024, 512, 512, 4)])
+@pytest.mark.parametrize("T,K,N,p", [
+    (384, 256, 1056, 4), (301, 200, 8 * 136, 8), (1024, 512, 512, 4),
+    (1300, 256, 520, 4),  # two M tiles per token shard, the second ragged: row blocks
+    (1030, 256, 520, 4),  # shards of 258, 258, 258, 256 rows: 2, 2, 2, 1 M tiles, no row blocks
+])
 def test_sequence_parallel_column_entry(lib, T, K, N, p):
     x = workloads.randn_bf16((T, K), 91)
     w = workloads.randn_bf16((K, N), 92, (1.0 / K) ** 0.5)
