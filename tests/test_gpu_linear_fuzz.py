@@ -4,7 +4,8 @@ Each case draws M, K, N and the part count P, so shards are ragged
 (torch.chunk, empty tails included), tiles are ragged in M, N and K, and
 TMA's out-of-bounds fill is exercised; bias on or off, bf16 and fp32
 outputs, weights stored [in, out] or as [out, in] views, and every
-row-parallel mode.  K a multiple of 8 keeps bf16 row pitches 16-byte
+row-parallel mode; token-sharded inputs into fused column layers (the
+sequence-parallel entry).  K a multiple of 8 keeps bf16 row pitches 16-byte
 aligned (the tcgen05 path); other K give pitches TMA cannot read, which the
 calls copy to padded pitches in their workspace (the Python API passes the
 queried size) and run on the tcgen05 path too; the CUDA-core kernel is
@@ -157,3 +158,33 @@ def test_column_variants_fuzz(lib, seed):
             expect = olin.column_parallel_seq(xs, shards) if seq else olin.column_parallel(w64(x), shards)
             for i, e in enumerate(expect):
                 check_fp32(to_host(ys[j].slots[i], "fp32"), e, f"{what} weight {j} shard {i}")
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_sequence_parallel_fuzz(lib, seed):
+    """Token-sharded x (Shard(0)) into 1 to 3 fused column layers: each token
+    shard is one block of the GEMM's rows, read in place.  Token counts give
+    one or several M tiles per shard, equal or not (the launch orders its
+    tiles as row blocks of one GEMM when every shard has the same M tiles)."""
+    rng = random.Random(6000 + seed)
+    P = rng.choice([2, 3, 4, 8])
+    T = rng.choice([5, 300, 1030, 1300, 2100, 2600])
+    K = rng.choice([64, 136, 512, 1368])
+    N = rng.choice([40, 264, 520, 1032])
+    nw = rng.choice([1, 2, 3])
+    x = workloads.randn_bf16((T, K), 6100 + seed)
+    ws = [workloads.randn_bf16((K, N), 6200 + 10 * seed + j, (1.0 / K) ** 0.5) for j in range(nw)]
+    toks = chunk_bounds(T, P)
+    xd = tsl.DTensor([to_dev(np.ascontiguousarray(x[o:o + s]), "bf16") for o, s in toks], mesh1(P),
+                     [tsl.Shard(0)], x.shape, torch.bfloat16)
+    wds = [col_dtensor(w, P) for w in ws]
+    outs = [tsl.DTensor.empty(mesh1(P), [tsl.Shard(1)], (T, N), torch.float32) for _ in ws]
+    tsl.column_parallel_linear_multi(xd, wds, outs=outs)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    xs = [w64(x[o:o + s]) for o, s in toks]
+    cols = chunk_bounds(N, P)
+    for j, w in enumerate(ws):
+        expect = olin.column_parallel_seq(xs, [w64(w[:, o:o + s]) for o, s in cols])
+        for i, e in enumerate(expect):
+            check_fp32(to_host(outs[j].slots[i], "fp32"), e, f"T={T} K={K} N={N} P={P} weight {j} shard {i}")
