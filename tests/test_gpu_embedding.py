@@ -48,8 +48,9 @@ def test_fp32_and_materialised_output(lib):
     assert status == 0
 
 
-def test_out_of_range_ids_set_status(lib):
-    table, ids = workloads.embedding_inputs(vocab=100, dim=64, ids_shape=(2, 9), seed_base=760)
+@pytest.mark.parametrize("dim", [64, 4096])  # 4096 over 8: 1 KiB rows, the two-rows-in-flight path
+def test_out_of_range_ids_set_status(lib, dim):
+    table, ids = workloads.embedding_inputs(vocab=100, dim=dim, ids_shape=(2, 9), seed_base=760)
     ids = ids.copy()
     ids[0, 3] = 100
     ids[1, 0] = -5
