@@ -400,15 +400,6 @@ __device__ __forceinline__ int pair_dual_half(const Group& G, int n0) {
   return r < 128 ? r : 128;
 }
 
-// MMA width of a tile: the gated MLP always uses both 128-column halves;
-// otherwise the tile's remaining columns rounded up to the MMA's N step of 16.
-__device__ __forceinline__ int tile_mma_n(const Group& G, int n0) {
-  if (G.dual) return 256;
-  int rem = G.n - n0;
-  rem = (rem + 15) & ~15;
-  return rem < G.bn ? rem : G.bn;
-}
-
 __device__ __forceinline__ float bias_at(const Group& G, int col) {
   if (G.bias_dtype == DT_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(G.bias)[col]);
   return reinterpret_cast<const float*>(G.bias)[col];
