@@ -805,7 +805,7 @@ dt_status plan(const DTensor& S, const DTensor& D, std::vector<HostTask>* tasks)
     for (int m = 0; m < nm; ++m)
       if (zeroed[m] && cd[m] != 0) zero = true;
     if (zero) {
-      tasks->push_back(HostTask{bd, ds, {}});
+      tasks->push_back(HostTask{bd, ds, {}, {}});
       continue;
     }
     for (int sc = 0; sc < nshard_combos; ++sc) {
