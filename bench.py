@@ -1071,7 +1071,8 @@ def run_profile_case(args):
     each timed with CUDA events after a 512 MB write that flushes L2 (for ncu
     captures and A/B timing; prints one small JSON line, not a bench line).  Cases: `mlp_down` (the TP
     MLP's down projection: H [4096, 11008] Shard(-1) over 8, Wd Shard(0),
-    ALL_REDUCE, split tail in its workspace), `qkv`, `o`, and
+    ALL_REDUCE, split tail in its workspace), `qkv`, `o`, `sp_qkv` (q/k/v
+    from the same x as 4 token shards, the sequence-parallel entry), and
     `rd:<transition>:<shape>` (one redistribute of the sweep, e.g.
     `rd:S1->S0:8191x8190`).  GEMM inputs are random device tensors of the
     step's shapes; redistribute inputs are the step's own."""
@@ -1095,9 +1096,12 @@ def run_profile_case(args):
         y = tsl.DTensor.empty(m8, [R], (4096, 4096), bf)
         ws = torch.empty(max(1, tsl.row_parallel_linear_workspace_bytes(h, wd, y)), dtype=torch.uint8, device=dev)
         fn = lambda: tsl.row_parallel_linear(h, wd, out=y, workspace=ws)  # noqa: E731
-    elif case in ("qkv", "o"):
+    elif case in ("qkv", "o", "sp_qkv"):
         m4 = tsl.DeviceMesh((4,), ("tp",))
-        x = tsl.DTensor([rnd(8192, 4096)], m4, [R], (8192, 4096), bf)
+        xt = rnd(8192, 4096)
+        x = tsl.DTensor([xt], m4, [R], (8192, 4096), bf)
+        # the same tokens as 4 token shards (the sequence-parallel entry)
+        x_tok = tsl.DTensor([xt[i * 2048:(i + 1) * 2048].contiguous() for i in range(4)], m4, [S0], (8192, 4096), bf)
         wq = [tsl.DTensor([rnd(4096, 1024, std=1 / 64) for _ in range(4)], m4, [S1], (4096, 4096), bf)
               for _ in range(3)]
         qkv = [tsl.DTensor.empty(m4, [S1], (8192, 4096), bf) for _ in range(3)]
@@ -1110,6 +1114,8 @@ def run_profile_case(args):
         tsl.column_parallel_linear_multi(x, wq, outs=qkv, workspace=wsq)
         if case == "qkv":
             fn = lambda: tsl.column_parallel_linear_multi(x, wq, outs=qkv, workspace=wsq)  # noqa: E731
+        elif case == "sp_qkv":
+            fn = lambda: tsl.column_parallel_linear_multi(x_tok, wq, outs=qkv)  # noqa: E731
         else:
             fn = lambda: tsl.row_parallel_linear(qkv[0], wo, mode=tsl.REDUCE_SCATTER, out=od, workspace=wso)  # noqa
     elif case.startswith("rd:"):
