@@ -164,6 +164,11 @@ extern "C" dt_status dt_tp_embedding(const dt_dtensor* ids, const dt_dtensor* ta
   for (int d = 0; d < li.ndim; ++d)
     if (lo.gshape[d] != li.gshape[d]) return fail(DT_ERR_SHAPE, "out leading dims must equal ids dims");
   if (lo.gshape[lo.ndim - 1] != lt.gshape[1]) return fail(DT_ERR_SHAPE, "out last dim must be the embedding dim");
+  // no tokens or an empty embedding dim: nothing to gather (and the slots'
+  // strides, which torch leaves arbitrary on empty dims, are not checked)
+  int64_t ntok = 1;
+  for (int d = 0; d < li.ndim; ++d) ntok *= li.gshape[d];
+  if (ntok == 0 || lt.gshape[1] == 0) return DT_OK;
 
   // ids: one contiguous slot (replica 0)
   const SlotView& iv = I.slots[0];

@@ -41,6 +41,11 @@ dt_status slot_matrix(const SlotView& v, int ndim, int dtype, Mat* out, const ch
   m.cols = v.shape[ndim - 1];
   m.rows = 1;
   for (int d = 0; d < ndim - 1; ++d) m.rows *= v.shape[d];
+  if (m.rows == 0 || m.cols == 0) {  // no elements: strides mean nothing (torch leaves them arbitrary)
+    m.ld = m.cols;
+    *out = m;
+    return DT_OK;
+  }
   if (m.cols > 1 && v.stride[ndim - 1] != 1) return fail(DT_ERR_UNSUPPORTED, "%s: inner stride must be 1", what);
   if (ndim >= 2) {
     m.ld = v.stride[ndim - 2];
@@ -117,6 +122,15 @@ struct ColumnSpec {
 // a dimension that would not fit is refused before anything touches the
 // device (an [8, 2^31] bf16 activation is only 32 GB).
 constexpr int64_t GEMM_DIM_LIMIT = (1ll << 31) - 512;
+// The first output of a group that writes anything, or nullptr when none
+// does (no tokens, or no output columns): the device the call binds to.
+// A REDUCE_SCATTER group over no rows has no output blocks at all.
+const void* first_output(const std::vector<HostGroup>& groups) {
+  for (const auto& g : groups)
+    if (g.m > 0 && g.n > 0 && !g.out_ptr.empty()) return g.out_ptr[0];
+  return nullptr;
+}
+
 dt_status check_gemm_dims(const Layout& lx, int64_t k, int64_t n) {
   int64_t m = 1;
   for (int d = 0; d + 1 < lx.ndim; ++d) m *= lx.gshape[d];
@@ -293,8 +307,9 @@ dt_status column_multi(const dt_dtensor* x, int32_t n, const dt_dtensor* w, cons
   std::vector<HostGroup> groups;
   dt_status st = column_build(x, n, w, bias, y, tp, &groups);
   if (st != DT_OK) return st;
-  if (groups.empty()) return DT_OK;
-  if ((st = bind_device_of(groups[0].out_ptr[0])) != DT_OK) return st;
+  const void* out = first_output(groups);
+  if (!out) return DT_OK;
+  if ((st = bind_device_of(out)) != DT_OK) return st;
   return gemm::run_groups(groups, d_status, reinterpret_cast<cudaStream_t>(stream), ws);
 }
 
@@ -606,8 +621,9 @@ dt_status row_parallel_planned(const dt_dtensor* x, const dt_dtensor* w, const d
   std::vector<HostGroup> groups;
   dt_status st = row_build(x, w, bias, y, mode, tp, &groups);
   if (st != DT_OK) return st;
-  if (groups.empty()) return DT_OK;
-  if ((st = bind_device_of(groups[0].out_ptr[0])) != DT_OK) return st;
+  const void* out = first_output(groups);
+  if (!out) return DT_OK;
+  if ((st = bind_device_of(out)) != DT_OK) return st;
   return gemm::run_groups(groups, d_status, reinterpret_cast<cudaStream_t>(stream), ws);
 }
 
@@ -800,15 +816,18 @@ dt_status tp_mlp_planned(const dt_dtensor* x, const dt_dtensor* w_gate, const dt
   dt_status st = mlp_build(x, w_gate, w_up, w_down, y, mode, tp_mesh_dim, static_cast<char*>(workspace), &plan,
                            &up_groups, &down_groups);
   if (st != DT_OK) return st;
-  if (!workspace || workspace_bytes < plan.bytes)
+  if (plan.bytes > 0 && (!workspace || workspace_bytes < plan.bytes))
     return fail(DT_ERR_INVALID_ARG, "workspace of at least %zu bytes (H) needed", plan.bytes);
-  if (up_groups.empty()) return DT_OK;
-  if ((st = bind_device_of(workspace)) != DT_OK) return st;
+  // H is empty with no tokens or no ffn columns: then the launches write Y
+  // alone (zeros and nothing else when the ffn width is 0), or nothing
+  const void* anchor = workspace ? workspace : first_output(down_groups);
+  if (!anchor) return DT_OK;
+  if ((st = bind_device_of(anchor)) != DT_OK) return st;
   // the split tail's scratch follows H; both launches run in order on the
   // stream, so they share it
   gemm::Workspace split;
-  split.ptr = static_cast<char*>(workspace) + plan.bytes;
-  split.bytes = workspace_bytes - plan.bytes;
+  split.ptr = workspace ? static_cast<char*>(workspace) + plan.bytes : nullptr;
+  split.bytes = workspace ? workspace_bytes - plan.bytes : 0;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = gemm::run_groups(up_groups, d_status, s, split)) != DT_OK) return st;
   return gemm::run_groups(down_groups, d_status, s, split);

@@ -48,7 +48,7 @@ def test_fp32_and_materialised_output(lib):
     assert status == 0
 
 
-@pytest.mark.parametrize("dim", [64, 4096])  # 4096 over 8: 1 KiB rows, the two-rows-in-flight path
+@pytest.mark.parametrize("dim", [64, 4096])  # 4096 over 8: 1 KiB rows (one row per warp at 18 tokens)
 def test_out_of_range_ids_set_status(lib, dim):
     table, ids = workloads.embedding_inputs(vocab=100, dim=dim, ids_shape=(2, 9), seed_base=760)
     ids = ids.copy()
@@ -63,3 +63,26 @@ def test_full_size_config(lib):
     table, ids = workloads.embedding_inputs()
     status, bad = run(table, ids, workloads.EMBEDDING["parts"])
     assert status == 0 and not bad
+
+
+def test_out_of_range_ids_two_rows_in_flight(lib):
+    """16384 tokens x 8 shards of 1 KiB rows: more items than warps, so each warp
+    copies its rows two at a time, and some of those rows have bad ids."""
+    table, ids = workloads.embedding_inputs(vocab=1000, dim=4096, ids_shape=(4, 4096), seed_base=780)
+    ids = ids.copy()
+    rng = np.random.default_rng(781)
+    flat = ids.reshape(-1)
+    pos = rng.choice(flat.size, 64, replace=False)
+    flat[pos[:32]] = 1000 + rng.integers(0, 50, 32)
+    flat[pos[32:]] = -1 - rng.integers(0, 50, 32)
+    status, bad = run(table, ids, 8)
+    assert bad and status & tsl._lib.DEV_ERR_INDEX
+
+
+def test_no_tokens(lib):
+    """Empty ids: OK, no launch, an empty output."""
+    table, _ = workloads.embedding_inputs(vocab=100, dim=512, ids_shape=(1, 1), seed_base=790)
+    n0 = lib.dt_launch_count()
+    status, bad = run(table, np.zeros((2, 0), dtype=np.int32), 8)
+    assert status == 0 and not bad
+    assert lib.dt_launch_count() == n0

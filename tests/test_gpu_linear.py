@@ -337,3 +337,95 @@ def test_uneven_shards_run_on_tensor_cores_with_workspace(lib):
     (er,) = olin.row_parallel([w64(xr[:, o:o + s]) for o, s in chunk_bounds(N, p)],
                               [w64(wr[o:o + s]) for o, s in chunk_bounds(N, p)], None, olin.ALL_REDUCE)
     check_fp32(to_host(yr.slots[0], "fp32"), er, "row, padded x shards")
+
+
+# ---------------------------------------------------------------- degenerate sizes
+
+ROW_MODES = [tsl.ALL_REDUCE, tsl.REDUCE_SCATTER, tsl.PARTIAL]
+OMODE = {tsl.ALL_REDUCE: olin.ALL_REDUCE, tsl.REDUCE_SCATTER: olin.REDUCE_SCATTER, tsl.PARTIAL: olin.PARTIAL}
+
+
+def test_zero_tokens(lib):
+    """x with no rows: every layer returns OK, launches nothing and gives empty outputs."""
+    K, N, F, p = 256, 192, 4 * 96, 4
+    x = workloads.randn_bf16((0, K), 61)
+    w = workloads.randn_bf16((K, N), 62, (1.0 / K) ** 0.5)
+    wg = workloads.randn_bf16((K, F), 63, (1.0 / K) ** 0.5)
+    wu = workloads.randn_bf16((K, F), 64, (1.0 / K) ** 0.5)
+    wd = workloads.randn_bf16((F, N), 65, (1.0 / F) ** 0.5)
+    torch.cuda.synchronize()
+    tsl.read_device_status(clear=True)
+    n0 = lib.dt_launch_count()
+    y = tsl.column_parallel_linear(x_rep(x, p), col_dtensor(w, p))
+    assert [tuple(t.shape) for t in y.slots] == [(0, s) for _, s in chunk_bounds(N, p)]
+    for mode in ROW_MODES:
+        yr = tsl.row_parallel_linear(x_shard(x, p), row_dtensor(w, p), mode=mode, out_dtype=torch.float32)
+        assert yr.slots and all(t.numel() == 0 for t in yr.slots)
+    for mode in (tsl.ALL_REDUCE, tsl.REDUCE_SCATTER):
+        xd = x_rep(x, p)
+        ym = tsl.tp_mlp(xd, col_dtensor(wg, p), col_dtensor(wu, p), row_dtensor(wd, p), mode=mode)
+        assert ym.slots and all(t.numel() == 0 for t in ym.slots)
+    torch.cuda.synchronize()
+    assert lib.dt_launch_count() == n0
+    assert tsl.read_device_status() == 0
+
+
+def test_zero_inner_dim_column(lib):
+    """K = 0: X W is the zero matrix, so the column layer writes its bias."""
+    M, N, p = 130, 200, 4
+    x = workloads.randn_bf16((M, 0), 71)
+    w = workloads.randn_bf16((0, N), 72)
+    b = workloads.randn_bf16((N,), 73, 0.5)
+    cols = chunk_bounds(N, p)
+    bd = tsl.DTensor([to_dev(np.ascontiguousarray(b[o:o + s]), "bf16") for o, s in cols], mesh1(p), [tsl.Shard(0)],
+                     (N,), torch.bfloat16)
+    xd, wd = x_rep(x, p), col_dtensor(w, p)
+    y32 = tsl.column_parallel_linear(xd, wd, bd, out_dtype=torch.float32)
+    y16 = tsl.column_parallel_linear(xd, wd, bd)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    expect = olin.column_parallel(w64(x), [w64(w[:, o:o + s]) for o, s in cols], [w64(b[o:o + s]) for o, s in cols])
+    for i, e in enumerate(expect):
+        f = to_host(y32.slots[i], "fp32")
+        np.testing.assert_array_equal(f, e, err_msg=f"shard {i}")  # the bias itself, exactly
+        check_bf16(to_host(y16.slots[i], "bf16"), f, e, f"shard {i}")
+
+
+@pytest.mark.parametrize("mode", ROW_MODES)
+def test_zero_inner_dim_row(lib, mode):
+    """K = 0 over p empty shards: the output is the bias, added once (PARTIAL: on part 0)."""
+    M, N, p = 130, 200, 4
+    x = workloads.randn_bf16((M, 0), 74)
+    w = workloads.randn_bf16((0, N), 75)
+    b = workloads.randn_bf16((N,), 76, 0.5)
+    bd = tsl.DTensor([to_dev(b, "bf16")], mesh1(p), [tsl.Replicate()], (N,), torch.bfloat16)
+    y = tsl.row_parallel_linear(x_shard(x, p), row_dtensor(w, p), bd, mode=mode, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    expect = olin.row_parallel([w64(x[:, o:o + s]) for o, s in chunk_bounds(0, p)],
+                               [w64(w[o:o + s]) for o, s in chunk_bounds(0, p)], w64(b), OMODE[mode], parts=p)
+    assert len(expect) == len(y.slots)
+    for i, e in enumerate(expect):
+        np.testing.assert_array_equal(to_host(y.slots[i], "fp32"), e, err_msg=f"{mode} out {i}")
+
+
+@pytest.mark.parametrize("mode", [tsl.ALL_REDUCE, tsl.REDUCE_SCATTER])
+def test_zero_ffn_width(lib, mode):
+    """An MLP with no ffn columns: H is empty and Y = 0 (SiLU and the product never run)."""
+    M, K, N, p = 130, 256, 200, 4
+    x = workloads.randn_bf16((M, K), 77)
+    wg, wu = workloads.randn_bf16((K, 0), 78), workloads.randn_bf16((K, 0), 79)
+    wd = workloads.randn_bf16((0, N), 80)
+    xd = x_rep(x, p)
+    y = tsl.tp_mlp_output(xd, row_dtensor(wd, p), mode=mode, out_dtype=torch.float32)
+    for t in y.slots:
+        t.fill_(7.0)
+    tsl.tp_mlp(xd, col_dtensor(wg, p), col_dtensor(wu, p), row_dtensor(wd, p), mode=mode, out=y)
+    torch.cuda.synchronize()
+    assert tsl.read_device_status() == 0
+    cols = chunk_bounds(0, p)
+    expect, _ = olin.tp_mlp(w64(x), [w64(wg[:, o:o + s]) for o, s in cols], [w64(wu[:, o:o + s]) for o, s in cols],
+                            [w64(wd[o:o + s]) for o, s in cols], OMODE[mode])
+    for i, e in enumerate(expect):
+        assert not e.any()
+        np.testing.assert_array_equal(to_host(y.slots[i], "fp32"), e, err_msg=f"{mode} out {i}")
