@@ -63,6 +63,10 @@
  *    trap.  d_status may be NULL: the bits then go to a status word inside
  *    the library, read and cleared by dt_read_device_status().
  *  - Inputs and outputs must not overlap.
+ *  - Empty tensors are valid operands.  A slot with no elements may have a
+ *    NULL pointer and any strides.  A call with nothing to write (no tokens,
+ *    no output columns) returns DT_OK without launching or calling CUDA.  A
+ *    linear whose inner dim K is 0 writes its bias, or zeros.
  *  - dt_last_error() returns a human-readable reason for the last non-OK
  *    status returned on the calling thread.
  */
