@@ -23,6 +23,8 @@ pytestmark = pytest.mark.gpu
 
 ABS_TOL = 2e-3
 REL_FRO_TOL = 1e-3
+ROW_MODES = [tsl.ALL_REDUCE, tsl.REDUCE_SCATTER, tsl.PARTIAL]
+OMODE = {tsl.ALL_REDUCE: olin.ALL_REDUCE, tsl.REDUCE_SCATTER: olin.REDUCE_SCATTER, tsl.PARTIAL: olin.PARTIAL}
 
 
 def check_fp32(got: np.ndarray, expect: np.ndarray, what=""):
@@ -194,7 +196,7 @@ def test_row_parallel(lib, mode, M, K, N, p):
     y16 = tsl.row_parallel_linear(xd, wd, bd, mode=mode)
     torch.cuda.synchronize()
     assert tsl.read_device_status() == 0
-    omode = {tsl.ALL_REDUCE: olin.ALL_REDUCE, tsl.REDUCE_SCATTER: olin.REDUCE_SCATTER, tsl.PARTIAL: olin.PARTIAL}[mode]
+    omode = OMODE[mode]
     expect = olin.row_parallel([w64(x[:, o:o + s]) for o, s in chunk_bounds(K, p)],
                                [w64(w[o:o + s]) for o, s in chunk_bounds(K, p)], w64(b), omode, parts=p)
     assert len(expect) == len(y32.slots)
@@ -219,7 +221,8 @@ def test_row_parallel_3d_reduce_scatter_on_batch(lib):
 # ---------------------------------------------------------------- MLP / attention
 
 @pytest.mark.parametrize("M,K,F,N,p,mode", [(256, 256, 8 * 136, 384, 8, tsl.ALL_REDUCE),
-                                            (200, 192, 4 * 96, 320, 4, tsl.REDUCE_SCATTER)])
+                                            (200, 192, 4 * 96, 320, 4, tsl.REDUCE_SCATTER),
+                                            (192, 256, 4 * 136, 264, 4, tsl.PARTIAL)])
 def test_tp_mlp_small(lib, M, K, F, N, p, mode):
     x, wg, wu, wd = workloads.mlp_inputs(M, K, F, seed_base=600)
     wd = workloads.randn_bf16((F, N), 604, (1.0 / F) ** 0.5)
@@ -230,7 +233,7 @@ def test_tp_mlp_small(lib, M, K, F, N, p, mode):
     y = tsl.tp_mlp(xd, wgd, wud, wdd, mode=mode, out=y, workspace=ws)
     torch.cuda.synchronize()
     assert tsl.read_device_status() == 0
-    omode = olin.ALL_REDUCE if mode == tsl.ALL_REDUCE else olin.REDUCE_SCATTER
+    omode = OMODE[mode]
     cols = chunk_bounds(F, p)
     expect, hs = olin.tp_mlp(w64(x), [w64(wg[:, o:o + s]) for o, s in cols], [w64(wu[:, o:o + s]) for o, s in cols],
                              [w64(wd[o:o + s]) for o, s in cols], omode)
@@ -340,9 +343,6 @@ def test_uneven_shards_run_on_tensor_cores_with_workspace(lib):
 
 
 # ---------------------------------------------------------------- degenerate sizes
-
-ROW_MODES = [tsl.ALL_REDUCE, tsl.REDUCE_SCATTER, tsl.PARTIAL]
-OMODE = {tsl.ALL_REDUCE: olin.ALL_REDUCE, tsl.REDUCE_SCATTER: olin.REDUCE_SCATTER, tsl.PARTIAL: olin.PARTIAL}
 
 
 def test_zero_tokens(lib):

@@ -23,7 +23,7 @@ from oracle.placement import chunk_bounds
 from tensor_sharded_linear_gb300 import workloads
 
 from helpers import to_dev, to_host
-from test_gpu_linear import check_bf16, check_fp32, col_dtensor, mesh1, row_dtensor, w64, x_rep, x_shard
+from test_gpu_linear import OMODE, check_bf16, check_fp32, col_dtensor, mesh1, row_dtensor, w64, x_rep, x_shard
 
 pytestmark = pytest.mark.gpu
 
@@ -84,7 +84,7 @@ def test_row_fuzz(lib, seed):
     y16 = tsl.row_parallel_linear(xd, wd, bd, mode=mode)
     torch.cuda.synchronize()
     assert tsl.read_device_status() == 0
-    omode = {tsl.ALL_REDUCE: olin.ALL_REDUCE, tsl.REDUCE_SCATTER: olin.REDUCE_SCATTER, tsl.PARTIAL: olin.PARTIAL}[mode]
+    omode = OMODE[mode]
     rows = chunk_bounds(K, P)
     expect = olin.row_parallel([w64(x[:, o:o + s]) for o, s in rows], [w64(w[o:o + s]) for o, s in rows],
                                w64(b) if use_bias else None, omode, parts=P)
@@ -104,7 +104,7 @@ def test_mlp_fuzz(lib, seed):
     P = rng.choice([1, 2, 4, 8])
     F = P * rng.choice([8, 64, 96, 136])
     N = rng.choice([8, 200, 384])
-    mode = tsl.ALL_REDUCE if seed % 2 == 0 else tsl.REDUCE_SCATTER
+    mode = [tsl.ALL_REDUCE, tsl.REDUCE_SCATTER, tsl.PARTIAL][seed % 3]
     x, wg, wu, _ = workloads.mlp_inputs(M, K, F, seed_base=5100 + 10 * seed)
     wd = workloads.randn_bf16((F, N), 5200 + seed, (1.0 / F) ** 0.5)
     xd = x_rep(x, P)
@@ -114,8 +114,7 @@ def test_mlp_fuzz(lib, seed):
     assert tsl.read_device_status() == 0
     cols = chunk_bounds(F, P)
     expect, _ = olin.tp_mlp(w64(x), [w64(wg[:, o:o + s]) for o, s in cols], [w64(wu[:, o:o + s]) for o, s in cols],
-                            [w64(wd[o:o + s]) for o, s in cols],
-                            olin.ALL_REDUCE if mode == tsl.ALL_REDUCE else olin.REDUCE_SCATTER)
+                            [w64(wd[o:o + s]) for o, s in cols], OMODE[mode])
     what = f"M={M} K={K} F={F} N={N} P={P} mode={mode}"
     assert len(expect) == len(y.slots)
     for i, e in enumerate(expect):
