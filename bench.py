@@ -1011,7 +1011,13 @@ def run_cublas_shapes(args):
     out) on the step's dense GEMM shapes, each call after an L2 flush, CUDA
     events, median of --steps after --warmup.  The TP MLP has no fused
     counterpart there: gate and up run as one [T,H]x[H,2F] GEMM, SiLU(g)*u
-    as torch elementwise ops, then the down GEMM."""
+    as torch elementwise ops, then the down GEMM.  The embedding gather is
+    timed back to back three ways that move the same bytes: torch's
+    index_select (the gather F.embedding runs) on the unsharded
+    [128256, 4096] table (8 KiB rows); torch's index_select on each of the 8
+    Shard(1) slots (1 KiB rows, 8 launches, outputs left unassembled); and
+    this library's one-launch gather from the 8 slots into the Replicate
+    output."""
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     peaks = load_peaks()
@@ -1053,17 +1059,68 @@ def run_cublas_shapes(args):
     rows["attention q/k/v as one GEMM"] = (timed(lambda: torch.matmul(xa, wqkv, out=qkv)), 2 * TA * HA * 3 * HA)
     q = randn(TA, HA)  # contiguous, as the step's q/k/v output slots are
     rows["attention o"] = (timed(lambda: torch.matmul(q, wo, out=o)), 2 * TA * HA * HA)
+    del x, wgu, wd, gu, h, y, xa, wqkv, wo, qkv, o, q
+    import tensor_sharded_linear_gb300 as tsl
+    from tensor_sharded_linear_gb300 import build as B
+    B.build()
+    E = W.EMBEDDING
+    V, D, P = E["vocab"], E["dim"], E["parts"]
+    ids = torch.randint(0, V, E["ids"], device=device, generator=gen, dtype=torch.int32)
+    table = randn(V, D, std=E["std"])
+    emb = torch.empty(*E["ids"], D, device=device, dtype=bf)
+    ids64 = ids.long()
+
+    def back_to_back(fn):
+        """HBM-bound rows: --steps calls back to back between two events, as
+        the bench times the step (a flush by writes would leave up to 129 MB
+        of dirty lines for the timed call to write back)."""
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) * 1e3 / args.steps
+
+    # int64 ids: 64 KiB more than the int32 ids the library reads
+    gathered = torch.empty_like(emb)
+    brows = {"embedding, torch index_select (F.embedding's gather), unsharded table": (back_to_back(
+        lambda: torch.index_select(table, 0, ids64.view(-1), out=gathered.view(-1, D))), EMB_BYTES + 4 * ids.numel())}
+    tp = tsl.DeviceMesh((P,), ("tp",))
+    shards = [t.contiguous() for t in table.chunk(P, dim=1)]
+    del table
+    tdt = tsl.DTensor(shards, tp, [tsl.Shard(1)], (V, D), bf)
+    idt = tsl.DTensor([ids], tp, [tsl.Replicate()], tuple(E["ids"]), torch.int32)
+    odt = tsl.DTensor([emb], tp, [tsl.Replicate()], tuple(E["ids"]) + (D,), bf)
+    parts = [torch.empty(ids.numel(), t.shape[1], device=device, dtype=bf) for t in shards]
+
+    def per_shard():
+        for t, o in zip(shards, parts):
+            torch.index_select(t, 0, ids64.view(-1), out=o)
+
+    brows["embedding, torch index_select per Shard(1) slot (8 launches)"] = (back_to_back(per_shard),
+                                                                              EMB_BYTES + (8 * P - 4) * ids.numel())
+    brows["embedding, this library (8 Shard(1) slots -> Replicate)"] = (back_to_back(
+        lambda: tsl.tp_embedding(idt, tdt, out=odt)), EMB_BYTES)
     out = {}
     for name, (us, flops) in rows.items():
         out[name] = {"us": round(us, 2)}
         if flops:
             tf = flops / (us / 1e6) / 1e12
             out[name].update(tflops=round(tf, 1), frac=round(tf / peaks["bf16_tflops"], 4))
+    for name, (us, nbytes) in brows.items():
+        gbs = nbytes / (us / 1e6) / 1e9
+        out[name] = {"us": round(us, 2), "bytes": int(nbytes), "gbs": round(gbs, 1),
+                     "frac": round(gbs / peaks["hbm_gbs"], 4)}
     mlp_us = sum(rows[k][0] for k in ("MLP gate/up as one GEMM", "MLP SiLU(g)*u, torch elementwise", "MLP down"))
     print(json.dumps({"impl": "cublas-shapes", "note": "library context on the step's dense shapes, not a bench line",
                       "rows": out, "tp_mlp_us_unfused": round(mlp_us, 2),
                       "peak_bf16_tflops": peaks["bf16_tflops"], "steps": args.steps, "warmup": args.warmup,
-                      "l2": "256 MB written before every call"}), flush=True)
+                      "l2": "GEMM rows: 256 MB written before every call; embedding rows: back to back"}),
+          flush=True)
 
 
 def run_profile_case(args):
