@@ -310,12 +310,15 @@ int gemm_starve() {
 }
 
 // What a split tail costs beyond its share of the MMAs, in 64-deep K
-// iterations of one 256 x 256 pair tile (~0.3 us each): zeroing the
+// iterations of one 256 x 256 pair tile (~0.33 us each): zeroing the
 // counters, writing the pieces' partials, finishing the tiles, and the
 // tail's operand traffic squeezed into a fraction of a tile's time.
-// Measured on GB300 at about 20-25 us per launch (the TP MLP down
-// projection gains 15 us; 64-iteration tiles lose 7-20 us).
-constexpr double SPLIT_OVERHEAD_ITERS = 72.0;
+// Measured on GB300 with the pieces first and the tiles finished from L2,
+// forcing the split on 64-iteration launches: fused q/k/v (1536 tiles, a
+// 16-tile tail) went from 418-421 to 413-415 us, the o projection (512
+// tiles, a 56-tile tail) from 146-147 to 153-154 us.  Both put the cost
+// at 35-40 iterations.
+constexpr double SPLIT_OVERHEAD_ITERS = 40.0;
 
 // DT_GEMM_SPLIT=0 in the environment turns the split tail off (every tile
 // whole), DT_GEMM_SPLIT=2 splits every last wave the finishing can take
