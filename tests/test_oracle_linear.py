@@ -181,3 +181,54 @@ def test_sequence_parallel_entry_and_replicate_output():
     np.testing.assert_allclose(np.concatenate(seq, -1), dense, atol=1e-12, rtol=0)
     assert all(y.shape[0] == 11 for y in seq)
     np.testing.assert_allclose(ol.column_parallel_replicate(x, col_shards(w, p)), dense, atol=1e-12, rtol=0)
+
+
+def test_mlp_modes_agree():
+    """The MLP's PARTIAL parts sum to its ALL_REDUCE output, and its
+    REDUCE_SCATTER row blocks (torch.chunk of the tokens) tile it; that
+    output is the brute-force product of the bf16 H and the down weight."""
+    rng = np.random.default_rng(14)
+    p = 3
+    x = bf16.widen64(bf16.round_rne(rng.standard_normal((7, 12))))
+    wg = bf16.widen64(bf16.round_rne(rng.standard_normal((12, 9)) / 4))
+    wu = bf16.widen64(bf16.round_rne(rng.standard_normal((12, 9)) / 4))
+    wd = bf16.widen64(bf16.round_rne(rng.standard_normal((9, 5)) / 4))
+    args = (x, col_shards(wg, p), col_shards(wu, p), row_shards(wd, p))
+    (full,), hs = ol.tp_mlp(*args, ol.ALL_REDUCE)
+    np.testing.assert_allclose(full, brute_matmul(bf16.widen64(np.concatenate(hs, -1)), wd), atol=1e-12, rtol=0)
+    parts, _ = ol.tp_mlp(*args, ol.PARTIAL)
+    assert len(parts) == p
+    np.testing.assert_allclose(sum(parts), full, atol=1e-12, rtol=0)
+    for i, (o, s) in enumerate(chunk_bounds(9, p)):  # part i is H_i times its rows of the down weight
+        np.testing.assert_allclose(parts[i], brute_matmul(bf16.widen64(hs[i]), wd[o:o + s]), atol=1e-12, rtol=0)
+    blocks, _ = ol.tp_mlp(*args, ol.REDUCE_SCATTER)
+    assert [b.shape[0] for b in blocks] == [3, 3, 1]
+    np.testing.assert_array_equal(np.concatenate(blocks, 0), full)
+
+
+def test_degenerate_sizes():
+    """Closed forms of the empty cases: with K = 0 the product is the zero
+    matrix, so a row layer's output is its bias (PARTIAL: on part 0 only) and
+    a column layer's is its bias shards; an MLP with no ffn columns gives 0;
+    no tokens give empty outputs of the right widths."""
+    rng = np.random.default_rng(16)
+    M, N, p = 5, 7, 3
+    b = rng.standard_normal(N)
+    xs = [np.zeros((M, 0)) for _ in range(p)]
+    ws = [np.zeros((0, N)) for _ in range(p)]
+    (y,) = ol.row_parallel(xs, ws, b, ol.ALL_REDUCE)
+    np.testing.assert_array_equal(y, np.broadcast_to(b, (M, N)))
+    parts = ol.row_parallel(xs, ws, b, ol.PARTIAL)
+    np.testing.assert_array_equal(parts[0], np.broadcast_to(b, (M, N)))
+    assert all(not q.any() for q in parts[1:])
+    blocks = ol.row_parallel(xs, ws, b, ol.REDUCE_SCATTER, parts=p)
+    assert [blk.shape for blk in blocks] == [(2, N), (2, N), (1, N)]
+    np.testing.assert_array_equal(np.concatenate(blocks, 0), np.broadcast_to(b, (M, N)))
+    bs = [b[o:o + s] for o, s in chunk_bounds(N, p)]
+    cols = ol.column_parallel(np.zeros((M, 0)), [np.zeros((0, s)) for _, s in chunk_bounds(N, p)], bs)
+    np.testing.assert_array_equal(np.concatenate(cols, -1), np.broadcast_to(b, (M, N)))
+    x = rng.standard_normal((M, 4))
+    (ym,), hs = ol.tp_mlp(x, [np.zeros((4, 0))] * p, [np.zeros((4, 0))] * p, [np.zeros((0, N))] * p, ol.ALL_REDUCE)
+    assert ym.shape == (M, N) and not ym.any() and all(h.size == 0 for h in hs)
+    cols = ol.column_parallel(np.zeros((0, 4)), col_shards(rng.standard_normal((4, N)), p))
+    assert [c.shape for c in cols] == [(0, s) for _, s in chunk_bounds(N, p)]
