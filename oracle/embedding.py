@@ -29,11 +29,9 @@ def tp_embedding(ids: np.ndarray, table_shards, dim: int):
     vocab = table_shards[0].shape[0]
     out = np.zeros(ids.shape + (dim,), dtype=table_shards[0].dtype)
     valid = (ids >= 0) & (ids < vocab)
-    safe = np.where(valid, ids, 0)
     for i, (o, d) in enumerate(chunk_bounds(dim, parts)):
         t = table_shards[i]
         assert t.shape == (vocab, d)
-        rows = t[safe]                       # row gather
-        rows[~valid] = 0
-        out[..., o:o + d] = rows
+        block = out[..., o:o + d]             # zeros where the id is invalid
+        block[valid] = t[ids[valid]]          # row gather of the valid ids
     return out, bool((~valid).any())

@@ -34,3 +34,15 @@ def test_out_of_range_ids_give_zero_rows():
     assert bad
     assert not out[0, 1].any() and not out[1, 3].any()
     np.testing.assert_array_equal(out[0, 0], table[ids[0, 0]])
+
+
+def test_no_tokens_and_no_vocabulary():
+    """Empty ids give an empty [.., dim] output and no index error; with an
+    empty vocabulary every id is out of range, so every row is zero."""
+    table, _ = workloads.embedding_inputs(vocab=40, dim=12, ids_shape=(1, 1), seed_base=995)
+    shards = [np.ascontiguousarray(table[:, o:o + s]) for o, s in chunk_bounds(12, 4)]
+    out, bad = tp_embedding(np.zeros((2, 0), dtype=np.int32), shards, 12)
+    assert out.shape == (2, 0, 12) and not bad
+    empty = [np.zeros((0, s), dtype=table.dtype) for _, s in chunk_bounds(12, 4)]
+    out, bad = tp_embedding(np.array([[0, 3]], dtype=np.int32), empty, 12)
+    assert bad and out.shape == (1, 2, 12) and not out.any()
