@@ -230,7 +230,9 @@ DT_API dt_status dt_redistribute_batch(int32_t n, const dt_dtensor* src, const d
  * of the embedding dim), ids int32 Replicate on tp, out Replicate on tp with
  * shape ids.shape + [dim].  out[t, o_i:o_i+d_i] = table_i[ids[t], :]; an id
  * outside [0, vocab) zero-fills that row and sets DT_DEV_ERR_INDEX.
- * Other mesh dims must be Replicate for all three.
+ * Other mesh dims must be Replicate for all three.  With no tokens (or an
+ * empty embedding dim) the call returns DT_OK without launching; a table of
+ * no rows with tokens to gather is refused with DT_ERR_SHAPE.
  */
 DT_API dt_status dt_tp_embedding(const dt_dtensor* ids, const dt_dtensor* table, const dt_dtensor* out,
                           int32_t tp_mesh_dim, int32_t* d_status, dt_stream_t stream);

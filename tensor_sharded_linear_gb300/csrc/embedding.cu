@@ -169,6 +169,9 @@ extern "C" dt_status dt_tp_embedding(const dt_dtensor* ids, const dt_dtensor* ta
   int64_t ntok = 1;
   for (int d = 0; d < li.ndim; ++d) ntok *= li.gshape[d];
   if (ntok == 0 || lt.gshape[1] == 0) return DT_OK;
+  // an empty vocabulary has no row to gather for any id: refused here rather
+  // than launched on slots without memory
+  if (lt.gshape[0] == 0) return fail(DT_ERR_SHAPE, "table has no rows: every id would be out of range");
 
   // ids: one contiguous slot (replica 0)
   const SlotView& iv = I.slots[0];

@@ -89,3 +89,16 @@ def test_embedding_nothing_to_gather(lib, ids_shape, dim):
     out = tsl.DTensor.empty(mesh, [tsl.Replicate()], ids_shape + (dim,), BF, device="cpu")
     no_launch(lib, lambda: lib.dt_tp_embedding(C.byref(ids._desc()), C.byref(table._desc()), C.byref(out._desc()), 0,
                                                None, None))
+
+
+def test_embedding_empty_vocabulary_refused(lib):
+    """A table of no rows with tokens to gather: refused before any launch
+    (every id would be out of range, and the slots hold no memory)."""
+    mesh = tsl.DeviceMesh((8,), ("tp",))
+    table = shard((0, 512), 1, mesh, zero_strides=True)
+    ids = replicate((2, 3), torch.int32, mesh)
+    out = tsl.DTensor.empty(mesh, [tsl.Replicate()], (2, 3, 512), BF, device="cpu")
+    n0 = lib.dt_launch_count()
+    st = lib.dt_tp_embedding(C.byref(ids._desc()), C.byref(table._desc()), C.byref(out._desc()), 0, None, None)
+    assert st == L.ERR_SHAPE and b"no rows" in lib.dt_last_error()
+    assert lib.dt_launch_count() == n0
