@@ -1216,7 +1216,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the rows timed outside the step")
     ap.add_argument("--cublas-shapes", action="store_true",
-                    help="time cuBLAS on the step's dense GEMM shapes (library context) and exit")
+                    help="time cuBLAS on the step's dense GEMM shapes and torch's embedding gather (library context) and exit")
     ap.add_argument("--only", default=ALL_COMPONENTS,
                     help="comma-separated subset of embedding,redistribute,mlp,attention (profiling)")
     ap.add_argument("--profile-case", default=None,
